@@ -1,0 +1,458 @@
+#!/usr/bin/env python
+"""Benchmark of one paged-KV decode step on GB300.
+
+A step is one pass of the whole hot path over one batch: append each
+sequence's new K/V token through ``slot_mapping``, then decode attention over
+the paged cache (with the split-K log-sum-exp merge when the plan splits).
+Inputs are seeded synthetic caches (see ``workloads``) already resident in
+HBM; the KV cache of every workload is larger than the 129 MB L2, so no L2
+flush is needed between steps.
+
+Prints ONE JSON line on rank 0.  ``value`` is achieved HBM bandwidth over the
+step's algorithmic bytes (K+V of every context token, counted once per
+physical slot, + Q + O + block-table entries + context lengths + the append's
+reads and writes), in GB/s, summed over ranks.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--config c2]
+  python bench.py --impl reference ...   # the fp64 CPU oracle on the same workload
+
+Multi-GPU (N > 1, one process per GPU under torch.distributed.run): every rank
+runs an independent replica of the workload (its own seed); there is no
+collective on the data path, only a barrier and a max-reduction of the timing.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "paged decode-attn achieved HBM GB/s (% of GB300 peak); decode tokens/s, 1 GPU"
+FALLBACK_HBM_GBS = 6800.0
+
+WORKLOAD_TEXT = {
+    "c1": "tiny paged decode: B=2, context {37,50}+1, bs16, 4q/2kv heads, d64, fp16",
+    "c2": "Llama-7B-shaped MHA layer: B=64, 32q/32kv heads, d128, bs16, context U[512,4096], fp16",
+    "c3": "Llama-70B-shaped GQA-8 layer: B=32, 64q/8kv heads, d128, bs16, context 4096, bf16",
+    "c4": "long-context split-K: B=8, 64q/8kv heads, d128, bs16, context U[32768,131072], bf16",
+    "c5": "continuous-batching mix: B=256, 32q/8kv heads, d128, bs16, 2048-token shared prefix "
+          "in 4 groups + lognormal suffix, bf16",
+    "c5_bs32": "continuous-batching mix, bs32 variant",
+}
+
+# DRAM bytes (read + write) per launch of the decode path measured by ncu
+# (profiles/), keyed by workload; valid only for the kernel sources they were
+# measured on (digest of csrc/), else reported as null.
+NCU_TRAFFIC = {}
+
+
+def _kernel_digest() -> str:
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "paged_kv_cache_164_gb300", "csrc")
+    for f in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, f), "rb") as fh:
+            h.update(f.encode())
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def _peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def step_bytes(w) -> dict:
+    """Algorithmic bytes of one step of workload ``w`` (all 16-bit values: 2 bytes)."""
+    import torch
+    e = 2
+    s = w.spec
+    lens = w.context_lens.cpu().long()
+    bt = w.block_tables.cpu().long()
+    bs = s.block_size
+    row = s.num_kv_heads * s.head_dim * e            # one token's K (or V) row
+    logical_tokens = int(lens.sum())
+    # unique physical slots read (shared prefix pages count once per step)
+    slots = []
+    for b in range(s.num_seqs):
+        n = int(lens[b])
+        t = torch.arange(n)
+        slots.append(bt[b, t // bs] * bs + t % bs)
+    unique_tokens = int(torch.unique(torch.cat(slots)).numel()) if slots else 0
+    pages = int(((lens + bs - 1) // bs).sum())
+    qo = 2 * s.num_seqs * s.num_q_heads * s.head_dim * e
+    meta = pages * 4 + s.num_seqs * 4
+    decode = 2 * unique_tokens * row + qo + meta
+    decode_logical = 2 * logical_tokens * row + qo + meta
+    append = 4 * s.num_seqs * row + 8 * s.num_seqs   # read k_new, v_new; write both; slots
+    flops = 4 * logical_tokens * s.num_q_heads * s.head_dim
+    return dict(decode=decode, decode_logical=decode_logical, append=append,
+                step=decode + append, kv_unique=2 * unique_tokens * row, flops=flops,
+                tokens=s.num_seqs)
+
+
+class ClockSampler:
+    """Samples SM clocks and throttle reasons with nvidia-smi while it runs."""
+
+    FIELDS = ("timestamp,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int, period_ms: int = 100):
+        self.lines = []
+        self.proc = None
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(gpu_index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", f"-lms={period_ms}"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append((time.time(), line.strip()))
+
+    def wait_first(self, timeout=3.0):
+        t0 = time.time()
+        while self.proc is not None and not self.lines and time.time() - t0 < timeout:
+            time.sleep(0.02)
+
+    def stop(self):
+        if self.proc is not None:
+            time.sleep(0.25)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self, t_begin: float, t_end: float) -> dict:
+        if self.proc is None or not self.lines:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        inside = [l for (t, l) in self.lines if t_begin <= t <= t_end + 0.15]
+        note = None
+        if not inside:
+            # the region was shorter than the sampling period: take the nearest sample
+            nearest = min(self.lines, key=lambda tl: abs(tl[0] - (t_begin + t_end) / 2))
+            inside = [nearest[1]]
+            note = "timed region shorter than the sampling period; nearest sample used"
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for l in inside:
+            p = [x.strip() for x in l.split(",")]
+            try:
+                sm.append(float(p[1]))
+                smax.append(float(p[2]))
+            except (ValueError, IndexError):
+                continue
+            for name, flag in zip(names, p[5:9]):
+                if flag.lower() == "active":
+                    reasons.add(name)
+        out = {"sm_mhz": statistics.median(sm) if sm else None,
+               "sm_max_mhz": max(smax) if smax else None, "reasons": sorted(reasons),
+               "samples": len(inside)}
+        if note:
+            out["note"] = note
+        return out
+
+
+def _dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def reduce_over_ranks(value: float, op: str, device=None) -> float:
+    """max or sum of a scalar over ranks (identity without torch.distributed)."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()):
+        return value
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX if op == "max" else dist.ReduceOp.SUM)
+    return float(t.item())
+
+
+def barrier(device=None):
+    import torch.distributed as dist
+    if dist.is_available() and dist.is_initialized():
+        if device is not None and dist.get_backend() == "nccl":
+            dist.barrier(device_ids=[device.index])
+        else:
+            dist.barrier()
+
+
+def oracle_sample_rate(w, budget_s: float, seqs=None):
+    """Times the fp64 oracle on a bounded sample of ``w``'s sequences.
+
+    Returns (GB/s over the sample's algorithmic bytes, seconds, sample description,
+    threads).  The sample is the first k sequences, k sized from a one-sequence
+    calibration so the timed call takes about ``budget_s`` seconds.
+    """
+    import numpy as np
+    import oracle
+    from workloads import bits
+    kc, vc = bits(w.k_cache).copy(), bits(w.v_cache).copy()
+    oracle.append(kc, vc, bits(w.k_new), bits(w.v_new), w.slot_mapping.cpu().numpy())
+    q = bits(w.q)
+    bt = w.block_tables.cpu().numpy()
+    cl = w.context_lens.cpu().numpy()
+    s = w.spec
+    row = s.num_kv_heads * s.head_dim * 2
+
+    def run(idx):
+        t0 = time.perf_counter()
+        oracle.decode_attention(q[idx], kc, vc, bt[idx], cl[idx], w.scale, s.dtype)
+        return time.perf_counter() - t0
+
+    if seqs is None:
+        t1 = run(np.arange(1))
+        per_seq = max(t1, 1e-4)
+        k = int(max(1, min(s.num_seqs, budget_s / per_seq)))
+        seqs = np.arange(k)
+    secs = run(seqs)
+    toks = int(cl[seqs].sum())
+    nbytes = 2 * toks * row + 2 * len(seqs) * s.num_q_heads * s.head_dim * 2
+    desc = (f"oracle decode attention on the first {len(seqs)} of {s.num_seqs} sequences "
+            f"({toks} context tokens) of the same workload")
+    return nbytes / secs / 1e9, secs, desc, oracle.num_threads(), seqs
+
+
+def run_reference(args):
+    """The fp64 CPU oracle timed as the reference arm (rank 0 only)."""
+    ws, rank, _ = _dist_env()
+    if rank != 0:
+        return
+    import torch
+    from workloads import make_workload
+    dev = "cuda" if torch.cuda.is_available() else "cpu"
+    w = make_workload(args.config, device=dev).to("cpu")
+    per_step = max(0.5, min(10.0, 150.0 / max(1, args.steps + args.warmup)))
+    seqs = None
+    for _ in range(args.warmup):
+        _, _, _, _, seqs = oracle_sample_rate(w, per_step, seqs)
+    rates, secs_all = [], []
+    desc, threads = "", 1
+    for _ in range(args.steps):
+        r, secs, desc, threads, seqs = oracle_sample_rate(w, per_step, seqs)
+        rates.append(r)
+        secs_all.append(secs)
+    value = statistics.median(rates) if rates else 0.0
+    line = {"impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s",
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(1e3 * statistics.median(secs_all), 3) if secs_all else None,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "f64", "data": "synthetic",
+            "config": {"workload": args.config, "description": WORKLOAD_TEXT[args.config]},
+            "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": threads,
+                             "kind": "oracle", "sample": desc},
+            "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def run_gpu(args):
+    import torch
+    import torch.distributed as dist
+
+    import paged_kv_cache_164_gb300 as pkv
+    from workloads import make_workload
+
+    ws, rank, local = _dist_env()
+    if ws > 1:
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    device = torch.device("cuda", local if ws > 1 else 0)
+    torch.cuda.set_device(device)
+    pkv.load()
+
+    if ws > 1:  # an independent replica per rank
+        from workloads import SPECS
+        w = make_workload(args.config, device=device, seed=SPECS[args.config].seed + 1000 * rank)
+    else:
+        w = make_workload(args.config, device=device)
+    s = w.spec
+    nbytes = step_bytes(w)
+    mcl = w.max_context_len
+    splits = pkv.decode_num_splits(s.num_seqs, s.num_q_heads, s.num_kv_heads, s.head_dim,
+                                   s.block_size, mcl, args.splits)
+    ws_bytes = pkv.workspace_size(s.num_seqs, s.num_q_heads, s.num_kv_heads, s.head_dim,
+                                  s.block_size, mcl, args.splits)
+    workspace = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device=device)
+    out = torch.empty_like(w.q)
+    flag = pkv.new_error_flag(device)
+    launches_per_step = 2 + (1 if splits > 1 else 0)
+
+    def step():
+        pkv.append(w.k_new, w.v_new, w.k_cache, w.v_cache, w.slot_mapping, err_flag=flag)
+        pkv.decode_attention(w.q, w.k_cache, w.v_cache, w.block_tables, w.context_lens, mcl,
+                             scale=w.scale, num_splits=args.splits, out=out,
+                             workspace=workspace, err_flag=flag)
+
+    for _ in range(args.warmup):
+        step()
+    if pkv.check_error(flag) != 0:
+        raise RuntimeError("device error flag set during warm-up")
+
+    stream = torch.cuda.current_stream(device)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
+           torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    sampler = ClockSampler(device.index) if rank == 0 else None
+    if sampler:
+        sampler.wait_first()
+    barrier(device)
+    torch.cuda.synchronize(device)
+    t_begin = time.time()
+    for i in range(args.steps):
+        ev[i][0].record(stream)
+        pkv.append(w.k_new, w.v_new, w.k_cache, w.v_cache, w.slot_mapping, err_flag=flag)
+        ev[i][1].record(stream)
+        pkv.decode_attention(w.q, w.k_cache, w.v_cache, w.block_tables, w.context_lens, mcl,
+                             scale=w.scale, num_splits=args.splits, out=out,
+                             workspace=workspace, err_flag=flag)
+        ev[i][2].record(stream)
+    torch.cuda.synchronize(device)
+    t_end = time.time()
+    barrier(device)
+    if sampler:
+        sampler.stop()
+    total_ms = ev[0][0].elapsed_time(ev[-1][2])
+    decode_ms = statistics.mean(ev[i][1].elapsed_time(ev[i][2]) for i in range(args.steps))
+    append_ms = statistics.mean(ev[i][0].elapsed_time(ev[i][1]) for i in range(args.steps))
+    ms_local = total_ms / args.steps
+    ms_step = reduce_over_ranks(ms_local, "max", device)
+    bytes_all = reduce_over_ranks(float(nbytes["step"]), "sum", device)
+    tokens_all = reduce_over_ranks(float(nbytes["tokens"]), "sum", device)
+    if pkv.check_error(flag) != 0:
+        raise RuntimeError("device error flag set during the timed steps")
+
+    # ---- end to end through the public API: pinned host inputs -> device -> host output
+    host = {k: getattr(w, k).cpu().pin_memory() for k in
+            ("q", "k_new", "v_new", "slot_mapping", "block_tables", "context_lens")}
+    dev_in = {k: torch.empty_like(getattr(w, k)) for k in host}
+    out_h = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in host.values())
+    d2h = out_h.numel() * out_h.element_size()
+
+    def e2e_step():
+        for k, t in host.items():
+            dev_in[k].copy_(t, non_blocking=True)
+        pkv.append(dev_in["k_new"], dev_in["v_new"], w.k_cache, w.v_cache,
+                   dev_in["slot_mapping"], err_flag=flag)
+        pkv.decode_attention(dev_in["q"], w.k_cache, w.v_cache, dev_in["block_tables"],
+                             dev_in["context_lens"], mcl, scale=w.scale,
+                             num_splits=args.splits, out=out, workspace=workspace,
+                             err_flag=flag)
+        out_h.copy_(out, non_blocking=True)
+
+    for _ in range(max(3, args.warmup // 2)):
+        e2e_step()
+    torch.cuda.synchronize(device)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    barrier(device)
+    e0.record(stream)
+    for _ in range(args.steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize(device)
+    e2e_ms = reduce_over_ranks(e0.elapsed_time(e1) / args.steps, "max", device)
+    if not torch.equal(out_h.to(device), out):
+        raise RuntimeError("end-to-end output differs from the device output")
+
+    if rank != 0:
+        if ws > 1:
+            dist.destroy_process_group()
+        return
+
+    peak, peak_src = _peaks()
+    value = bytes_all / (ms_step * 1e-3) / 1e9
+    decode_gbs = nbytes["decode"] / (decode_ms * 1e-3) / 1e9
+    clocks = sampler.summary(t_begin, t_end) if sampler else None
+    traffic = None
+    rec = NCU_TRAFFIC.get(args.config)
+    if rec and rec.get("digest") == _kernel_digest() and rec.get("splits") == splits:
+        traffic = rec["bytes"]
+
+    cpu = None
+    if args.cpu_baseline:
+        w_host = w.to("cpu")
+        gbs, secs, desc, threads, _ = oracle_sample_rate(w_host, args.cpu_seconds)
+        cpu = {"value": round(gbs, 4), "unit": "GB/s", "cores": threads, "kind": "oracle",
+               "sample": desc, "seconds": round(secs, 3)}
+
+    line = {
+        "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": ws,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 5),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": s.dtype, "data": "synthetic",
+        "config": {"workload": args.config, "description": WORKLOAD_TEXT[args.config],
+                   "num_seqs": s.num_seqs, "num_q_heads": s.num_q_heads,
+                   "num_kv_heads": s.num_kv_heads, "head_dim": s.head_dim,
+                   "block_size": s.block_size, "context_tokens": int(w.context_lens.sum()),
+                   "max_context_len": mcl, "num_splits": splits, "accumulate": "fp32",
+                   "kv_bytes_unique": nbytes["kv_unique"],
+                   "decode_bytes_per_step": nbytes["decode"],
+                   "decode_bytes_logical": nbytes["decode_logical"],
+                   "append_bytes_per_step": nbytes["append"],
+                   "l2": "no flush: KV inputs larger than the 129 MB L2",
+                   "parallelism": f"replicas x{ws}" if ws > 1 else "1 GPU"},
+        "pct_of_peak": round(100.0 * value / (peak * ws), 2),
+        "tokens_per_s": round(tokens_all / (ms_step * 1e-3), 1),
+        "decode_ms": round(decode_ms, 5), "append_ms": round(append_ms, 5),
+        "roofline": {"bound": "hbm", "achieved": round(decode_gbs, 2), "peak": peak,
+                     "unit": "GB/s", "frac": round(decode_gbs / peak, 4),
+                     "traffic": traffic, "kernel": "decode attention (+ split merge)",
+                     "peak_source": f"{peak_src} hbm_gbs"},
+        "cpu_baseline": cpu,
+        "e2e": {"value": round(bytes_all / (e2e_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
+                "ms_per_step": round(e2e_ms, 5), "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h},
+        "gpu_launches": launches_per_step * args.steps,
+        "clocks": clocks,
+    }
+    print(json.dumps(line), flush=True)
+    if ws > 1:
+        dist.destroy_process_group()
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=300)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["mine", "reference"], default="mine")
+    ap.add_argument("--config", default="c2", choices=sorted(WORKLOAD_TEXT))
+    ap.add_argument("--splits", type=int, default=0, help="KV partitions (0 = automatic)")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--no-cpu-baseline", dest="cpu_baseline", action="store_false")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("at least 3 warm-up steps")
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_gpu(args)
+
+
+if __name__ == "__main__":
+    main()

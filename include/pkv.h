@@ -1,0 +1,191 @@
+/*
+ * pkv — decode-phase attention over a paged KV cache, for NVIDIA GB300 (sm_103a).
+ *
+ * Sources, cited below by short name:
+ *   [inference]  LLM-101-CN, "推理优化" (engineering/inference.html)
+ *   [essay]      gsyq.cn essay on the three dimensions of LLM inference
+ *   [vllm-06]    "Deep dive into vLLM 06: GPU execution, kernels and graphs"
+ *   [chapter12]  tutorial chapter "12-推理优化" (docs.yz520gzy.top)
+ *
+ * Conventions shared by every call:
+ *   - All tensors are dense, row-major (C order), in device memory owned by the
+ *     caller.  The library allocates nothing on the device, keeps no per-call
+ *     state, and every call is asynchronous on `stream` (a cudaStream_t; NULL
+ *     is the legacy default stream).  Only pkv_check_error synchronises.
+ *   - Device pointers must be 16-byte aligned.
+ *   - 16-bit element types: PKV_FP16 (IEEE binary16) or PKV_BF16 (bfloat16).
+ *   - Cache layout, "organised by page" ([inference] "PagedAttention 内核实现"):
+ *       k_cache, v_cache: [num_blocks][block_size][num_kv_heads][head_dim]
+ *   - Argument errors are found on the host before any launch: the call
+ *     returns a status and launches nothing.
+ *   - Bad indices found on the device (a block id outside [0, num_blocks), a
+ *     slot beyond the pool, a context longer than the block table or than
+ *     max_context_len) never fault: the offending token is skipped and a bit
+ *     is OR-ed into the optional device word *err_flag (PKV_EFLAG_*), which
+ *     the caller zero-initialises and reads back with pkv_check_error.
+ *   - Supported sizes: head_dim in {64, 128}; block_size in {16, 32};
+ *     num_q_heads a multiple of num_kv_heads with at most 16 query heads per
+ *     KV head.
+ */
+#ifndef PKV_H
+#define PKV_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    PKV_OK = 0,
+    PKV_ERR_INVALID_ARG = 1,    /* null pointer, bad size, misaligned pointer */
+    PKV_ERR_UNSUPPORTED = 2,    /* valid but not implemented (head_dim, block_size, group) */
+    PKV_ERR_WORKSPACE = 3,      /* workspace missing or smaller than required */
+    PKV_ERR_CUDA = 4,           /* a CUDA runtime call failed (launch, query, copy) */
+    PKV_ERR_DEVICE_INDEX = 5,   /* pkv_check_error: a kernel skipped an out-of-range index */
+    PKV_ERR_DEVICE_TIMEOUT = 6  /* pkv_check_error: a bounded in-kernel wait gave up */
+} pkv_status;
+
+typedef enum { PKV_FP16 = 0, PKV_BF16 = 1 } pkv_dtype;
+
+/* Bits OR-ed into *err_flag by the kernels. */
+#define PKV_EFLAG_BLOCK_ID      0x1  /* block id outside [0, num_blocks) */
+#define PKV_EFLAG_SLOT          0x2  /* slot >= num_blocks * block_size */
+#define PKV_EFLAG_CONTEXT_LEN   0x4  /* context_len > max_blocks_per_seq * block_size,
+                                        > max_context_len, or negative */
+#define PKV_EFLAG_TIMEOUT       0x8  /* a bounded wait inside a kernel expired */
+
+#define PKV_MAX_SPLITS 1024           /* upper bound on split-K partitions per sequence */
+
+/*
+ * Append (scatter) each step's new K/V token into its slot.
+ *
+ * For every i < num_tokens with s = slot_mapping[i] >= 0:
+ *     k_cache[s / block_size][s % block_size][:][:] = k_new[i][:][:]   (same for V)
+ * The block/offset split of a slot follows the token-to-page addressing of
+ * [essay] §三.2 (get_kv_cache) and [chapter12] PagedKVCache.update; writing
+ * the new token at the current page and offset follows [inference]
+ * KVCachePool.write_tokens.  A negative slot is padding and is skipped.  The
+ * copy is bit-exact.
+ *
+ *   k_new, v_new   [num_tokens][num_kv_heads][head_dim] (read)
+ *   k_cache, v_cache                                    (written at the slots only)
+ *   slot_mapping   int64 [num_tokens]; slots must be distinct within one call
+ *   err_flag       nullable; PKV_EFLAG_SLOT if a slot lies beyond the pool
+ */
+pkv_status pkv_append(const void* k_new, const void* v_new, void* k_cache, void* v_cache,
+                      const int64_t* slot_mapping, int num_tokens, int num_blocks,
+                      int block_size, int num_kv_heads, int head_dim, pkv_dtype dtype,
+                      int32_t* err_flag, void* stream);
+
+/*
+ * Bytes of device workspace pkv_decode_attention needs for these arguments on
+ * the current device (the split-K plan depends on the device's SM count).
+ * Returns 0 when no workspace is needed and SIZE_MAX when the arguments are
+ * invalid or the device cannot be queried.
+ */
+size_t pkv_decode_workspace_size(int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
+                                 int block_size, int max_context_len, int num_splits);
+
+/*
+ * The number of KV partitions per sequence (split-K) pkv_decode_attention
+ * uses for these arguments on the current device: >= 1, or -1 when the
+ * arguments are invalid or the device cannot be queried.  num_splits as in
+ * pkv_decode_attention (0 = automatic).
+ */
+int pkv_decode_num_splits(int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
+                          int block_size, int max_context_len, int num_splits);
+
+/*
+ * Decode attention: one query token per sequence against its paged context.
+ *
+ * For sequence b, query head h, KV head g = h / (num_q_heads / num_kv_heads)
+ * (contiguous GQA groups, [essay] §三.6) and n = context_lens[b]:
+ *     K_t = k_cache[block_tables[b][t / block_size]][t % block_size][g][:]   t < n
+ *     s_t = scale * <q[b][h], K_t>            (scale = 1/sqrt(head_dim) normally,
+ *                                              [inference] chunked prefill, NPUAttention)
+ *     out[b][h] = sum_t softmax(s)_t V_t      ([chapter12] Attention(Q_t, K_1:t, V_1:t))
+ * computed in fp32 with an online softmax ([vllm-06] FlashAttention, online
+ * softmax) and, for long contexts, split over the KV length into partitions
+ * merged by log-sum-exp ([vllm-06] Flash-Decoding; [inference] combine_result).
+ * Tokens at positions >= n are never read.  n == 0 gives a zero row.
+ *
+ *   out            [num_seqs][num_q_heads][head_dim] (written), dtype
+ *   q              [num_seqs][num_q_heads][head_dim] (read), dtype
+ *   block_tables   int32 [num_seqs][max_blocks_per_seq]; entries past the
+ *                  context are never read
+ *   context_lens   int32 [num_seqs], in device memory
+ *   max_context_len  host-side upper bound of context_lens, used to plan the
+ *                  split; a longer context is truncated and flagged
+ *   num_splits     0 = automatic, else the requested number of KV partitions
+ *                  per sequence (1 .. PKV_MAX_SPLITS; fewer are used when the
+ *                  context has fewer pages)
+ *   workspace      device scratch of at least pkv_decode_workspace_size(...)
+ *                  bytes (may be NULL when that size is 0); its contents on
+ *                  entry do not matter and are clobbered
+ *   err_flag       nullable; PKV_EFLAG_BLOCK_ID / PKV_EFLAG_CONTEXT_LEN /
+ *                  PKV_EFLAG_TIMEOUT
+ */
+pkv_status pkv_decode_attention(void* out, const void* q, const void* k_cache,
+                                const void* v_cache, const int32_t* block_tables,
+                                int max_blocks_per_seq, const int32_t* context_lens,
+                                int max_context_len, int num_seqs, int num_blocks,
+                                int block_size, int num_q_heads, int num_kv_heads, int head_dim,
+                                float scale, int num_splits, void* workspace,
+                                size_t workspace_bytes, pkv_dtype dtype, int32_t* err_flag,
+                                void* stream);
+
+/*
+ * Log-sum-exp merge of split-K partials ([inference] combine_result and the
+ * exactness remark after it; [vllm-06] Flash-Decoding merges with the same
+ * m / l rescale rule).  Each partial is stored normalised with its
+ * log-sum-exp lse_p = M_p + ln L_p; since exp(M_p - M*) L_p = exp(lse_p - M*),
+ *     lse* = max_p lse_p,  w_p = exp(lse_p - lse*),  out = sum_p w_p O_p / sum_p w_p
+ * is the pages' combine.  lse_p = -inf marks an empty partition (weight 0);
+ * a row whose partitions are all empty becomes 0.
+ *
+ *   out          [num_seqs][num_q_heads][head_dim] (written), dtype
+ *   partial_o    float32 [num_seqs][num_q_heads][num_splits][head_dim]
+ *   partial_lse  float32 [num_seqs][num_q_heads][num_splits], natural log
+ */
+pkv_status pkv_merge(void* out, const float* partial_o, const float* partial_lse, int num_seqs,
+                     int num_q_heads, int num_splits, int head_dim, pkv_dtype dtype,
+                     void* stream);
+
+/*
+ * Block-table gather: copies each sequence's cached K and V rows, in token
+ * order, into contiguous buffers ([essay] §三.2 get_kv_cache;
+ * [chapter12] PagedKVCache.get):
+ *     k_out[b][t][:][:] = k_cache[block_tables[b][t / block_size]][t % block_size][:][:]
+ * for t < min(context_lens[b], max_context_len); rows t >= that are left
+ * untouched.  Bit-exact.
+ *
+ *   k_out, v_out   [num_seqs][max_context_len][num_kv_heads][head_dim] (written)
+ *   err_flag       nullable; PKV_EFLAG_BLOCK_ID / PKV_EFLAG_CONTEXT_LEN
+ */
+pkv_status pkv_gather(void* k_out, void* v_out, const void* k_cache, const void* v_cache,
+                      const int32_t* block_tables, int max_blocks_per_seq,
+                      const int32_t* context_lens, int max_context_len, int num_seqs,
+                      int num_blocks, int block_size, int num_kv_heads, int head_dim,
+                      pkv_dtype dtype, int32_t* err_flag, void* stream);
+
+/*
+ * Synchronises `stream`, then reads the device error word.  Returns PKV_OK
+ * when it is 0, PKV_ERR_DEVICE_TIMEOUT when PKV_EFLAG_TIMEOUT is set,
+ * PKV_ERR_DEVICE_INDEX for any other bit, PKV_ERR_CUDA if the copy fails.
+ * When flags_out is not NULL it receives the word.  The word is not cleared.
+ */
+pkv_status pkv_check_error(const int32_t* err_flag, void* stream, int32_t* flags_out);
+
+/* A static, human-readable name for a status. */
+const char* pkv_status_string(pkv_status status);
+
+/* Number of query heads one CTA of the decode kernel serves at most. */
+int pkv_max_group_size(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PKV_H */

@@ -1,0 +1,102 @@
+"""The C-ABI library loads, exports every declared symbol, and validates on the host (CPU)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import paged_kv_cache_164_gb300 as pkv
+from paged_kv_cache_164_gb300 import build as pkv_build
+
+HEADER = os.path.join(os.path.dirname(os.path.dirname(__file__)), "include", "pkv.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    pkv_build.build()
+    return pkv.load()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(pkv_[a-z_0-9]+)\s*\(", text)))
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = declared_functions()
+    assert {"pkv_append", "pkv_decode_attention", "pkv_merge"} <= set(names)
+    for name in names:
+        assert hasattr(lib, name), name
+
+
+def test_status_strings(lib):
+    for code in range(7):
+        assert pkv.status_string(code) != "unknown status"
+    assert pkv.status_string(99) == "unknown status"
+    assert lib.pkv_max_group_size() == 16
+
+
+NULL = ctypes.c_void_p(0)
+
+
+def test_append_rejects_bad_arguments_without_launching(lib):
+    ok_args = dict(nt=4, nb=8, bs=16, h=2, d=64, dt=0)
+    # null pointers
+    assert lib.pkv_append(NULL, NULL, NULL, NULL, NULL, 4, 8, 16, 2, 64, 0, NULL, NULL) == 1
+    # negative sizes, bad dtype
+    assert lib.pkv_append(NULL, NULL, NULL, NULL, NULL, -1, 8, 16, 2, 64, 0, NULL, NULL) == 1
+    assert lib.pkv_append(NULL, NULL, NULL, NULL, NULL, 4, 8, 16, 2, 64, 7, NULL, NULL) == 1
+    # zero tokens is a no-op
+    assert lib.pkv_append(NULL, NULL, NULL, NULL, NULL, 0, 8, 16, 2, 64, 0, NULL, NULL) == 0
+    assert ok_args
+
+
+def _decode(lib, **kw):
+    a = dict(out=NULL, q=NULL, k=NULL, v=NULL, bt=NULL, mb=4, cl=NULL, mcl=64, B=2, nb=8, bs=16,
+             hq=4, hkv=2, d=64, scale=0.125, splits=0, ws=NULL, wsb=0, dt=0, err=NULL,
+             stream=NULL)
+    a.update(kw)
+    return lib.pkv_decode_attention(a["out"], a["q"], a["k"], a["v"], a["bt"], a["mb"], a["cl"],
+                                    a["mcl"], a["B"], a["nb"], a["bs"], a["hq"], a["hkv"],
+                                    a["d"], a["scale"], a["splits"], a["ws"], a["wsb"], a["dt"],
+                                    a["err"], a["stream"])
+
+
+def test_decode_rejects_bad_arguments_without_launching(lib):
+    assert _decode(lib) == 1                      # null pointers
+    assert _decode(lib, hq=5, hkv=2) == 1         # heads not a multiple
+    assert _decode(lib, d=96) == 2                # unsupported head_dim
+    assert _decode(lib, bs=8) == 2                # unsupported block_size
+    assert _decode(lib, hq=34, hkv=2) == 2        # group of 17 > 16
+    assert _decode(lib, splits=-1) == 1
+    assert _decode(lib, splits=5000) == 1
+    assert _decode(lib, dt=3) == 1
+    assert _decode(lib, scale=float("nan")) == 1
+    assert _decode(lib, B=0) == 0                 # empty batch is a no-op
+
+
+def test_workspace_size_rejects_bad_arguments(lib):
+    assert lib.pkv_decode_workspace_size(2, 5, 2, 64, 16, 64, 0) == pkv.SIZE_MAX
+    assert lib.pkv_decode_workspace_size(2, 4, 2, 96, 16, 64, 1) == pkv.SIZE_MAX
+    # an explicit single partition needs no workspace and no device query
+    assert lib.pkv_decode_workspace_size(2, 4, 2, 64, 16, 64, 1) == 0
+    assert lib.pkv_decode_num_splits(2, 4, 2, 64, 16, 64, 1) == 1
+    assert lib.pkv_decode_num_splits(2, 4, 2, 64, 16, 64, 3) == 3   # 4 pages -> chunks of 2 pages
+    assert lib.pkv_decode_num_splits(2, 4, 2, 64, 16, 64, 2000) == -1
+    assert lib.pkv_decode_num_splits(2, 4, 2, 64, 16, 64, 8) == 4     # no more than the pages
+
+
+def test_merge_and_gather_reject_bad_arguments(lib):
+    assert lib.pkv_merge(NULL, NULL, NULL, 2, 4, 3, 64, 0, NULL) == 1
+    assert lib.pkv_merge(NULL, NULL, NULL, 2, 4, 0, 64, 0, NULL) == 1
+    assert lib.pkv_gather(NULL, NULL, NULL, NULL, NULL, 4, NULL, 64, 2, 8, 16, 2, 64, 0, NULL,
+                          NULL) == 1
+    assert lib.pkv_check_error(NULL, NULL, None) == 1
+
+
+def test_binding_refuses_cpu_tensors(lib):
+    import torch
+    k = torch.zeros(4, 16, 2, 64, dtype=torch.float16)
+    with pytest.raises(ValueError, match="CUDA"):
+        pkv.append(k[:1, 0], k[:1, 0], k, k, torch.zeros(1, dtype=torch.int64))
