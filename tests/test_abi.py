@@ -82,7 +82,7 @@ def test_workspace_size_rejects_bad_arguments(lib):
     # an explicit single partition needs no workspace and no device query
     assert lib.pkv_decode_workspace_size(2, 4, 2, 64, 16, 64, 1) == 0
     assert lib.pkv_decode_num_splits(2, 4, 2, 64, 16, 64, 1) == 1
-    assert lib.pkv_decode_num_splits(2, 4, 2, 64, 16, 64, 3) == 3   # 4 pages -> chunks of 2 pages
+    assert lib.pkv_decode_num_splits(2, 4, 2, 64, 16, 64, 3) == 2   # 4 pages -> 2 chunks of 2
     assert lib.pkv_decode_num_splits(2, 4, 2, 64, 16, 64, 2000) == -1
     assert lib.pkv_decode_num_splits(2, 4, 2, 64, 16, 64, 8) == 4     # no more than the pages
 
