@@ -137,6 +137,42 @@ pkv_status pkv_decode_attention(void* out, const void* q, const void* k_cache,
                                 void* stream);
 
 /*
+ * Decode attention for callers that cannot allocate device memory.
+ *
+ * The paper has no counterpart to this call; it exists for integration.  Some
+ * callers have no way to provide the workspace pkv_decode_attention needs:
+ * plain-C hosts with no device allocator of their own, plug-ins living inside
+ * another runtime whose memory pool they must not bypass, and latency-bound
+ * decode loops that cannot afford cudaMalloc / cudaFree (both may synchronise
+ * the whole device).  This entry point takes the same arguments minus the
+ * workspace and computes the same result with the same kernels, using instead
+ * a fixed scratch array of PKV_NOALLOC_SCRATCH_BYTES that lives in the
+ * library's own device memory.  It calls no allocating routine.
+ *
+ *   - The array is reserved on every GPU that loads the library and stays
+ *     reserved until the process exits.
+ *   - The first call on each device (with that device current) looks up the
+ *     array's device address; make that first call before any stream capture.
+ *   - All calls share the one array, which keeps the previous call's contents.
+ *     The kernels overwrite every scratch entry they read, so nothing has to be
+ *     cleared, but calls that may run at the same time on the GPU (for
+ *     example on two streams without ordering between them) race on it and
+ *     corrupt each other's results.  Order them on one stream.
+ *   - Returns PKV_ERR_WORKSPACE, launching nothing, when the split plan for
+ *     these arguments needs more than PKV_NOALLOC_SCRATCH_BYTES; pass a
+ *     smaller num_splits, or use pkv_decode_attention.
+ */
+#define PKV_NOALLOC_SCRATCH_BYTES (8u << 20)
+
+pkv_status pkv_decode_attention_noalloc(void* out, const void* q, const void* k_cache,
+                                        const void* v_cache, const int32_t* block_tables,
+                                        int max_blocks_per_seq, const int32_t* context_lens,
+                                        int max_context_len, int num_seqs, int num_blocks,
+                                        int block_size, int num_q_heads, int num_kv_heads,
+                                        int head_dim, float scale, int num_splits,
+                                        pkv_dtype dtype, int32_t* err_flag, void* stream);
+
+/*
  * Log-sum-exp merge of split-K partials ([inference] combine_result and the
  * exactness remark after it; [vllm-06] Flash-Decoding merges with the same
  * m / l rescale rule).  Each partial is stored normalised with its

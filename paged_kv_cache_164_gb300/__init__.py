@@ -63,13 +63,16 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.pkv_decode_num_splits.restype = i
     lib.pkv_decode_attention.argtypes = [p, p, p, p, p, i, p, i, i, i, i, i, i, i, f, i, p, sz,
                                          i, p, p]
+    lib.pkv_decode_attention_noalloc.argtypes = [p, p, p, p, p, i, p, i, i, i, i, i, i, i, f,
+                                                 i, i, p, p]
     lib.pkv_merge.argtypes = [p, p, p, i, i, i, i, i, p]
     lib.pkv_gather.argtypes = [p, p, p, p, p, i, p, i, i, i, i, i, i, i, p, p]
     lib.pkv_check_error.argtypes = [p, p, ctypes.POINTER(ctypes.c_int32)]
     lib.pkv_status_string.argtypes = [i]
     lib.pkv_status_string.restype = ctypes.c_char_p
     lib.pkv_max_group_size.argtypes = []
-    for name in ("pkv_append", "pkv_decode_attention", "pkv_merge", "pkv_gather",
+    for name in ("pkv_append", "pkv_decode_attention", "pkv_decode_attention_noalloc",
+                 "pkv_merge", "pkv_gather",
                  "pkv_check_error", "pkv_max_group_size"):
         getattr(lib, name).restype = i
     _lib = lib
@@ -186,6 +189,42 @@ def decode_attention(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tens
         int(max_context_len), b, nb, bs, h_q, h_kv, d, float(scale), int(num_splits), ws_ptr,
         ws_bytes, _kv_dtype(k_cache), _opt(err_flag, "err_flag"), _stream(stream, q.device))
     _check(st, "pkv_decode_attention")
+    return out
+
+
+NOALLOC_SCRATCH_BYTES = 8 << 20
+
+
+def decode_attention_noalloc(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
+                             block_tables: torch.Tensor, context_lens: torch.Tensor,
+                             max_context_len: int, out: torch.Tensor,
+                             scale: Optional[float] = None, num_splits: int = 0,
+                             err_flag: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """``decode_attention`` for callers that cannot allocate device memory.
+
+    Same result, but the split-K scratch is a fixed 8 MiB array inside the
+    library (reserved per GPU for the life of the process) and the caller
+    passes ``out``, so the call allocates nothing.  Calls share that array:
+    keep calls that use it ordered on one stream.  Make the first call on each
+    device before any stream capture.  Plans needing more scratch than the
+    array holds are rejected (PKV_ERR_WORKSPACE); ask for fewer splits then.
+    """
+    lib = load()
+    b, h_q, d = q.shape
+    nb, bs, h_kv, d2 = k_cache.shape
+    if d2 != d or v_cache.shape != k_cache.shape or block_tables.dim() != 2 or \
+            block_tables.shape[0] != b or context_lens.shape != (b,) or out.shape != q.shape:
+        raise ValueError("inconsistent decode shapes")
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    dt = k_cache.dtype
+    st = lib.pkv_decode_attention_noalloc(
+        _dev(out, "out", dt), _dev(q, "q", dt), _dev(k_cache, "k_cache", dt),
+        _dev(v_cache, "v_cache", dt), _dev(block_tables, "block_tables", torch.int32),
+        block_tables.shape[1], _dev(context_lens, "context_lens", torch.int32),
+        int(max_context_len), b, nb, bs, h_q, h_kv, d, float(scale), int(num_splits),
+        _kv_dtype(k_cache), _opt(err_flag, "err_flag"), _stream(stream, q.device))
+    _check(st, "pkv_decode_attention_noalloc")
     return out
 
 
