@@ -1,27 +1,66 @@
 // Decode attention over a paged KV cache, split-K partitions and their
-// log-sum-exp merge.
+// log-sum-exp merge, for sm_103a.
 //
 // The math: for one query token, s_t = scale * <q, K_t>, out = softmax(s) V
 // (tutorial chapter 12, Attention(Q_t, K_1:t, V_1:t)), with the streaming
-// online softmax m_new = max(m, s), l = e^(m - m_new) l + e^(s - m_new),
-// O = e^(m - m_new) O + e^(s - m_new) V, one division at the end (vLLM deep
-// dive 06, FlashAttention ③).  Long contexts are cut into KV partitions that
-// run on different SMs and are merged with the same rescale rule
-// (Flash-Decoding, ⑥; LLM-101-CN "推理优化" combine_result).
+// online softmax m_new = max(m, rowmax S), l = e^(m - m_new) l + rowsum P,
+// O = e^(m - m_new) O + P V, one division at the end (vLLM deep dive 06,
+// FlashAttention ③).  Long contexts are cut into KV partitions that run on
+// different SMs and are merged with the same rescale rule (Flash-Decoding, ⑥;
+// LLM-101-CN "推理优化" combine_result).
+//
+// Kernel design (GB300):
+//  * One CTA per (partition, KV head, sequence).  Warp 4 is the producer: one
+//    lane issues 4-D TMA tensor loads of 16-token tiles of K and V straight
+//    from the paged cache, the physical block id from the block table being
+//    the outermost coordinate, into a ring of shared-memory stages guarded by
+//    mbarriers.  Warps 0-3 consume stage i = w (mod 4) each.
+//  * Per 16-token stage a consumer computes S^T = K Q^T on the tensor cores
+//    (mma.sync m16n8k16, M = 16 tokens, N = 8 query heads of the GQA group,
+//    K = 16 dims), the online-softmax update in fp32, and O^T += V^T P^T
+//    (M = 16 dims, N = 8 heads, K = 16 tokens).  P enters the second product
+//    as two 16-bit terms (hi + lo) so the weights keep ~16 significant bits;
+//    a single 16-bit P would break the attention tolerance for short contexts.
+//    movmatrix turns the S^T fragments into P^T operand fragments in registers.
+//  * Every wait on an mbarrier is bounded by %globaltimer: on expiry the CTA
+//    flags PKV_EFLAG_TIMEOUT, drains its own TMA copies and returns.
+//  * Bad block ids are flagged and their tokens skipped; tokens at or past the
+//    context length are masked (their scores are -inf and their V rows are
+//    zeroed in registers, so garbage in unused slots never reaches the output).
 #include <algorithm>
 #include <atomic>
 #include <climits>
 #include <cmath>
+#include <mutex>
+
+#include <cudaTypedefs.h>
 
 #include "pkv_common.cuh"
+#include "pkv_ptx.cuh"
 
 namespace pkv {
+
+constexpr int kStageTokens = 16;      // tokens per pipeline stage
+constexpr int kConsumerWarps = 4;
+constexpr int kThreads = (kConsumerWarps + 1) * 32;
+constexpr int kMaxChunkPages = 64;    // pages per partition (block-table slice in smem)
+constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s per wait before giving up
+
+template <int D>
+struct Tile {
+    static constexpr int kRegions = D / 64;                   // 64-dim (128-byte) column blocks
+    static constexpr int kRegionBytes = kStageTokens * 128;   // 16 rows of 128 bytes, swizzled
+    static constexpr int kHalfBytes = kRegions * kRegionBytes;  // K (or V) of one stage
+    static constexpr int kStageBytes = 2 * kHalfBytes;
+    static constexpr int kStages = D == 128 ? 8 : 16;         // ring depth: 64 KB either way
+    static constexpr int kRingBytes = kStages * kStageBytes;
+    static constexpr int kSmemBytes = 1024 /*align*/ + kRingBytes + 2 * kStages * 8 +
+                                      kMaxChunkPages * 4 + 16;
+};
 
 struct DecodeParams {
     void* out;
     const void* q;
-    const void* k_cache;
-    const void* v_cache;
     const int32_t* block_tables;
     const int32_t* context_lens;
     float* partial_o;    // [B][H_q][num_splits][D] when num_splits > 1
@@ -31,175 +70,455 @@ struct DecodeParams {
     int num_blocks;
     int block_size;
     int num_q_heads;
-    int num_kv_heads;
     int group;           // query heads per KV head
     int num_splits;
-    int chunk_tokens;    // tokens per partition (a multiple of block_size)
+    int chunk_tokens;    // tokens per partition (a multiple of block_size and of 16)
     int max_context_len;
     float scale_log2;    // scale * log2(e)
 };
 
-constexpr int kDecodeWarps = 4;
+// Context length of sequence b as the kernels use it: negative or too long
+// values are clamped (and flagged by the decode kernel).
+__device__ __forceinline__ int clamped_len(int n, int cap) { return n < 0 ? 0 : (n > cap ? cap : n); }
 
-// One CTA per (partition, KV head, sequence); its warps take the partition's
-// pages round-robin and keep their own running (m, l, O) for every query head
-// of the GQA group; the warps' states are combined at the end.  Lane j owns
-// dimensions [j * D/32, (j + 1) * D/32).
-template <typename T, int D, int GMAX>
-__global__ void __launch_bounds__(kDecodeWarps * 32)
-decode_simple_kernel(DecodeParams p) {
-    constexpr int VPT = D / 32;
-    const int split = blockIdx.x;
-    const int g = blockIdx.y;
-    const int b = blockIdx.z;
-    const int warp = threadIdx.x / 32;
-    const int lane = threadIdx.x % 32;
-    const int G = p.group;
-    const int bs = p.block_size;
+__device__ __forceinline__ uint32_t pack2(float lo, float hi, __nv_bfloat16) {
+    __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&v);
+}
+__device__ __forceinline__ uint32_t pack2(float lo, float hi, __half) {
+    __half2 v = __floats2half2_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&v);
+}
+__device__ __forceinline__ float2 unpack2(uint32_t x, __nv_bfloat16) {
+    return __bfloat1622float2(*reinterpret_cast<__nv_bfloat162*>(&x));
+}
+__device__ __forceinline__ float2 unpack2(uint32_t x, __half) {
+    return __half22float2(*reinterpret_cast<__half2*>(&x));
+}
 
-    int n = __ldg(p.context_lens + b);
-    const int cap = min(p.max_blocks_per_seq * bs, p.max_context_len);
-    if (n < 0 || n > cap) {
-        if (split == 0 && threadIdx.x == 0) flag_error(p.err_flag, PKV_EFLAG_CONTEXT_LEN);
-        n = n < 0 ? 0 : cap;
-    }
-    const int t_begin = split * p.chunk_tokens;
-    const int t_end = min(n, t_begin + p.chunk_tokens);
-
-    const T* q = static_cast<const T*>(p.q);
-    float qf[GMAX][VPT];
-#pragma unroll
-    for (int h = 0; h < GMAX; ++h) {
-        if (h < G) {
-            const T* qrow = q + ((int64_t)b * p.num_q_heads + g * G + h) * D + lane * VPT;
-            load_as_float<T, VPT>(qrow, qf[h]);
-#pragma unroll
-            for (int i = 0; i < VPT; ++i) qf[h][i] *= p.scale_log2;
-        } else {
-#pragma unroll
-            for (int i = 0; i < VPT; ++i) qf[h][i] = 0.f;
+// Bounded wait on an mbarrier phase.  Returns false (after raising the CTA's
+// abort flag and the device error bit on expiry) if the phase did not complete.
+__device__ __forceinline__ bool wait_phase(uint32_t bar, uint32_t parity, volatile int* abort_flag,
+                                           int32_t* err_flag) {
+    if (ptx::mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = ptx::globaltimer();
+    while (true) {
+        if (ptx::mbar_try_wait(bar, parity)) return true;
+        if (*abort_flag) return false;
+        if (ptx::globaltimer() - t0 > kWaitLimitNs) {
+            *abort_flag = 1;
+            flag_error(err_flag, PKV_EFLAG_TIMEOUT);
+            return false;
         }
     }
+}
 
-    float m[GMAX], l[GMAX], o[GMAX][VPT];
-#pragma unroll
-    for (int h = 0; h < GMAX; ++h) {
-        m[h] = -INFINITY;
-        l[h] = 0.f;
-#pragma unroll
-        for (int i = 0; i < VPT; ++i) o[h][i] = 0.f;
+// NT = number of 8-head groups (1: G <= 8, 2: G <= 16).
+template <typename T, int D, int NT>
+__global__ void __launch_bounds__(kThreads, 3)
+decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
+              const DecodeParams p) {
+    using Cfg = Tile<D>;
+    constexpr int S = Cfg::kStages;
+    constexpr int KSTEPS = D / 16;   // k-steps of S^T = K Q^T, also m-tiles of O^T
+
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                               ~uintptr_t(1023));
+    uint8_t* ring = smem;
+    uint64_t* full_bar = reinterpret_cast<uint64_t*>(ring + Cfg::kRingBytes);
+    uint64_t* empty_bar = full_bar + S;
+    int* table = reinterpret_cast<int*>(empty_bar + S);
+    volatile int* abort_flag = table + kMaxChunkPages;
+
+    const int split = blockIdx.x;
+    const int g = blockIdx.y;   // KV head
+    const int b = blockIdx.z;   // sequence
+    const int tid = threadIdx.x;
+    const int warp = tid >> 5;
+    const int lane = tid & 31;
+    const int bs = p.block_size;
+
+    // Let the merge kernel (launched as a programmatic dependent) get scheduled
+    // as soon as every CTA of this grid has started; it waits for our results.
+    ptx::launch_dependents();
+    // Inputs may come from the previous kernel on the stream (the append).
+    ptx::grid_dependency_wait();
+
+    const int cap = min(p.max_blocks_per_seq * bs, p.max_context_len);
+    const int n_raw = __ldg(p.context_lens + b);
+    if ((n_raw < 0 || n_raw > cap) && split == 0 && g == 0 && tid == 0)
+        flag_error(p.err_flag, PKV_EFLAG_CONTEXT_LEN);
+    const int n = clamped_len(n_raw, cap);
+    const int nsplit = max(1, (n + p.chunk_tokens - 1) / p.chunk_tokens);
+    if (split >= nsplit) return;
+    const int t_begin = split * p.chunk_tokens;
+    const int t_end = min(n, t_begin + p.chunk_tokens);
+    const int nstages = t_end > t_begin ? (t_end - t_begin + kStageTokens - 1) / kStageTokens : 0;
+    const int page0 = t_begin / bs;
+
+    if (tid == 0) {
+        for (int s = 0; s < S; ++s) {
+            ptx::mbar_init(ptx::smem_addr(&full_bar[s]), 1);
+            ptx::mbar_init(ptx::smem_addr(&empty_bar[s]), 1);
+        }
+        *abort_flag = 0;
+        ptx::fence_barrier_init();
     }
-
-    const T* kc = static_cast<const T*>(p.k_cache);
-    const T* vc = static_cast<const T*>(p.v_cache);
-    if (t_begin < t_end) {
-        const int page_begin = t_begin / bs;
-        const int page_end = (t_end + bs - 1) / bs;
-        for (int pg = page_begin + warp; pg < page_end; pg += kDecodeWarps) {
-            const int blk = __ldg(p.block_tables + (int64_t)b * p.max_blocks_per_seq + pg);
+    if (warp == kConsumerWarps) {
+        // Stage this partition's slice of the block table, validating each id.
+        const int npages = t_end > t_begin ? (t_end + bs - 1) / bs - page0 : 0;
+        const int32_t* row = p.block_tables + (int64_t)b * p.max_blocks_per_seq + page0;
+        for (int i = lane; i < npages; i += 32) {
+            int blk = __ldg(row + i);
             if (blk < 0 || blk >= p.num_blocks) {
-                if (lane == 0) flag_error(p.err_flag, PKV_EFLAG_BLOCK_ID);
-                continue;
+                flag_error(p.err_flag, PKV_EFLAG_BLOCK_ID);
+                blk = -1;
             }
-            const int tb = max(pg * bs, t_begin);
-            const int te = min(pg * bs + bs, t_end);
-            for (int t = tb; t < te; ++t) {
-                const int64_t row =
-                    (((int64_t)blk * bs + (t - pg * bs)) * p.num_kv_heads + g) * D + lane * VPT;
-                float kf[VPT], vf[VPT];
-                load_as_float<T, VPT>(kc + row, kf);
-                load_as_float<T, VPT>(vc + row, vf);
+            table[i] = blk;
+        }
+        if (lane == 0) {
+            ptx::prefetch_tensormap(&tm_k);
+            ptx::prefetch_tensormap(&tm_v);
+        }
+    }
+    __syncthreads();
+
+    const uint32_t ring_addr = ptx::smem_addr(ring);
+
+    // ---------------------------------------------------------------- producer
+    if (warp == kConsumerWarps) {
+        if (lane == 0) {
+            const uint64_t policy = ptx::l2_policy_evict_first();
+            int issued = 0;
+            for (int i = 0; i < nstages; ++i) {
+                const int slot = i % S;
+                if (i >= S &&
+                    !wait_phase(ptx::smem_addr(&empty_bar[slot]), ((i / S) - 1) & 1, abort_flag,
+                                p.err_flag))
+                    break;
+                const int tok0 = t_begin + i * kStageTokens;
+                const int blk = table[tok0 / bs - page0];
+                const uint32_t fb = ptx::smem_addr(&full_bar[slot]);
+                if (blk >= 0) {
+                    const int toff = tok0 % bs;
+                    const uint32_t kdst = ring_addr + slot * Cfg::kStageBytes;
+                    ptx::mbar_arrive_expect_tx(fb, Cfg::kStageBytes);
 #pragma unroll
-                for (int h = 0; h < GMAX; ++h) {
-                    if (h >= G) break;
-                    float s = 0.f;
-#pragma unroll
-                    for (int i = 0; i < VPT; ++i) s = fmaf(qf[h][i], kf[i], s);
-#pragma unroll
-                    for (int off = 16; off > 0; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
-                    const float m_new = fmaxf(m[h], s);
-                    const float alpha = exp2f(m[h] - m_new);  // 0 when m was -inf
-                    const float e = exp2f(s - m_new);
-                    l[h] = l[h] * alpha + e;
-#pragma unroll
-                    for (int i = 0; i < VPT; ++i) o[h][i] = fmaf(o[h][i], alpha, e * vf[i]);
-                    m[h] = m_new;
+                    for (int r = 0; r < Cfg::kRegions; ++r) {
+                        ptx::tma_load_4d(kdst + r * Cfg::kRegionBytes, &tm_k, fb, r * 64, g, toff,
+                                         blk, policy);
+                        ptx::tma_load_4d(kdst + Cfg::kHalfBytes + r * Cfg::kRegionBytes, &tm_v, fb,
+                                         r * 64, g, toff, blk, policy);
+                    }
+                } else {
+                    ptx::mbar_arrive(fb);  // nothing to load: the consumer masks the stage
+                }
+                issued = i + 1;
+            }
+            if (*abort_flag) {
+                // Wait (bounded) for this CTA's copies still in flight before leaving.
+                for (int i = max(0, issued - S); i < issued; ++i) {
+                    const uint32_t fb = ptx::smem_addr(&full_bar[i % S]);
+                    const uint64_t t0 = ptx::globaltimer();
+                    while (!ptx::mbar_try_wait(fb, (i / S) & 1) &&
+                           ptx::globaltimer() - t0 < kWaitLimitNs) {
+                    }
                 }
             }
         }
     }
 
-    // Combine the warps' (m, l, O) per query head.
-    __shared__ float sm_m[kDecodeWarps][GMAX];
-    __shared__ float sm_l[kDecodeWarps][GMAX];
-    __shared__ float sm_o[kDecodeWarps][GMAX][D];
+    // ---------------------------------------------------------------- consumers
+    const int gq = lane >> 2;  // fragment row group
+    const int tq = lane & 3;   // fragment column pair
+    float o[NT][KSTEPS][4];    // O^T tiles: 16 dims x 8 heads each
+    float m0[NT], m1[NT], l0[NT], l1[NT];  // heads 2tq and 2tq+1 of each 8-head group
+    if (warp < kConsumerWarps) {
+        // Q^T operand fragments (B of S^T = K Q^T): head nt*8 + gq, dims 2tq.. of each k-step.
+        uint32_t qb[NT][KSTEPS][2];
+        const T* qbase = static_cast<const T*>(p.q) + ((int64_t)b * p.num_q_heads + g * p.group) * D;
 #pragma unroll
-    for (int h = 0; h < GMAX; ++h) {
-        if (lane == 0) {
-            sm_m[warp][h] = m[h];
-            sm_l[warp][h] = l[h];
+        for (int nt = 0; nt < NT; ++nt) {
+            const int head = nt * 8 + gq;
+            const uint32_t* qrow = reinterpret_cast<const uint32_t*>(qbase + head * D);
+#pragma unroll
+            for (int ks = 0; ks < KSTEPS; ++ks) {
+                const bool ok = head < p.group;
+                qb[nt][ks][0] = ok ? __ldg(qrow + (ks * 16 + 2 * tq) / 2) : 0u;
+                qb[nt][ks][1] = ok ? __ldg(qrow + (ks * 16 + 8 + 2 * tq) / 2) : 0u;
+            }
+            m0[nt] = m1[nt] = -INFINITY;
+            l0[nt] = l1[nt] = 0.f;
+#pragma unroll
+            for (int mt = 0; mt < KSTEPS; ++mt)
+#pragma unroll
+                for (int c = 0; c < 4; ++c) o[nt][mt][c] = 0.f;
         }
-#pragma unroll
-        for (int i = 0; i < VPT; ++i) sm_o[warp][h][lane * VPT + i] = o[h][i];
-    }
-    __syncthreads();
 
-    for (int idx = threadIdx.x; idx < G * D; idx += blockDim.x) {
-        const int h = idx / D;
-        const int j = idx % D;
-        float mx = -INFINITY;
+        // Per-lane ldmatrix row offsets (the 128-byte swizzle XORs the 16-byte
+        // chunk index with the row index mod 8; rows here are tokens).
+        const int mi = lane >> 3;
+        const int r8 = lane & 7;
+        const int k_tok = (mi & 1) * 8 + r8;    // K: matrices (t0-7,c), (t8-15,c), (t0-7,c+1), (t8-15,c+1)
+        const int k_csel = mi >> 1;
+        const int v_tok = (mi >> 1) * 8 + r8;   // V: matrices (t0-7,c), (t0-7,c+1), (t8-15,c), (t8-15,c+1)
+        const int v_csel = mi & 1;
+
+        for (int i = warp; i < nstages; i += kConsumerWarps) {
+            const int slot = i % S;
+            if (!wait_phase(ptx::smem_addr(&full_bar[slot]), (i / S) & 1, abort_flag, p.err_flag))
+                break;
+            const int tok0 = t_begin + i * kStageTokens;
+            const int blk = table[tok0 / bs - page0];
+            const int nvalid = blk >= 0 ? min(kStageTokens, t_end - tok0) : 0;
+            if (nvalid > 0) {
+                const uint32_t kbase = ring_addr + slot * Cfg::kStageBytes;
+                const uint32_t vbase = kbase + Cfg::kHalfBytes;
+
+                // S^T = K Q^T
+                float s[NT][4];
 #pragma unroll
-        for (int w = 0; w < kDecodeWarps; ++w) mx = fmaxf(mx, sm_m[w][h]);
-        float acc = 0.f, den = 0.f;
-        if (mx != -INFINITY) {
+                for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
-            for (int w = 0; w < kDecodeWarps; ++w) {
-                const float mw = sm_m[w][h];
-                if (mw == -INFINITY) continue;
-                const float c = exp2f(mw - mx);
-                den = fmaf(sm_l[w][h], c, den);
-                acc = fmaf(sm_o[w][h][j], c, acc);
+                    for (int c = 0; c < 4; ++c) s[nt][c] = 0.f;
+#pragma unroll
+                for (int ks = 0; ks < KSTEPS; ++ks) {
+                    const int chunk = ks * 2 + k_csel;
+                    const uint32_t addr = kbase + (chunk >> 3) * Cfg::kRegionBytes + k_tok * 128 +
+                                          (((chunk & 7) ^ r8) << 4);
+                    uint32_t a[4];
+                    ptx::ldmatrix_x4(a, addr);
+#pragma unroll
+                    for (int nt = 0; nt < NT; ++nt)
+                        ptx::mma_16816<T>(s[nt], a, qb[nt][ks][0], qb[nt][ks][1]);
+                }
+
+                // Online softmax in base 2.  s[nt][0]: (token gq, head 2tq), [1]: (gq, 2tq+1),
+                // [2]: (gq+8, 2tq), [3]: (gq+8, 2tq+1).
+                const bool lo_ok = gq < nvalid;
+                const bool hi_ok = gq + 8 < nvalid;
+                uint32_t pb_hi[NT][2], pb_lo[NT][2];
+                float alpha0[NT], alpha1[NT];
+#pragma unroll
+                for (int nt = 0; nt < NT; ++nt) {
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) s[nt][c] *= p.scale_log2;
+                    if (!lo_ok) s[nt][0] = s[nt][1] = -INFINITY;
+                    if (!hi_ok) s[nt][2] = s[nt][3] = -INFINITY;
+                    float mx0 = fmaxf(s[nt][0], s[nt][2]);
+                    float mx1 = fmaxf(s[nt][1], s[nt][3]);
+#pragma unroll
+                    for (int off = 4; off < 32; off <<= 1) {
+                        mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
+                        mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
+                    }
+                    const float mn0 = fmaxf(m0[nt], mx0);
+                    const float mn1 = fmaxf(m1[nt], mx1);
+                    const float ref0 = mn0 == -INFINITY ? 0.f : mn0;
+                    const float ref1 = mn1 == -INFINITY ? 0.f : mn1;
+                    alpha0[nt] = exp2f(m0[nt] - ref0);
+                    alpha1[nt] = exp2f(m1[nt] - ref1);
+                    m0[nt] = mn0;
+                    m1[nt] = mn1;
+                    const float p0 = exp2f(s[nt][0] - ref0);
+                    const float p1 = exp2f(s[nt][1] - ref1);
+                    const float p2 = exp2f(s[nt][2] - ref0);
+                    const float p3 = exp2f(s[nt][3] - ref1);
+                    l0[nt] = l0[nt] * alpha0[nt] + (p0 + p2);
+                    l1[nt] = l1[nt] * alpha1[nt] + (p1 + p3);
+                    // P as hi + lo 16-bit terms, transposed into P^T operand fragments.
+                    const uint32_t h01 = pack2(p0, p1, T());
+                    const uint32_t h23 = pack2(p2, p3, T());
+                    const float2 r01 = unpack2(h01, T());
+                    const float2 r23 = unpack2(h23, T());
+                    const uint32_t l01 = pack2(p0 - r01.x, p1 - r01.y, T());
+                    const uint32_t l23 = pack2(p2 - r23.x, p3 - r23.y, T());
+                    pb_hi[nt][0] = ptx::movmatrix_trans(h01);
+                    pb_hi[nt][1] = ptx::movmatrix_trans(h23);
+                    pb_lo[nt][0] = ptx::movmatrix_trans(l01);
+                    pb_lo[nt][1] = ptx::movmatrix_trans(l23);
+                }
+
+                // O^T = alpha * O^T + V^T P^T
+                uint32_t vmask_lo = 0xffffffffu, vmask_hi = 0xffffffffu;
+                if (nvalid < kStageTokens) {
+                    // A fragments of V^T hold tokens 2tq, 2tq+1 (a0, a1) and 2tq+8, 2tq+9 (a2, a3)
+                    vmask_lo = (2 * tq < nvalid ? 0x0000ffffu : 0u) |
+                               (2 * tq + 1 < nvalid ? 0xffff0000u : 0u);
+                    vmask_hi = (2 * tq + 8 < nvalid ? 0x0000ffffu : 0u) |
+                               (2 * tq + 9 < nvalid ? 0xffff0000u : 0u);
+                }
+#pragma unroll
+                for (int mt = 0; mt < KSTEPS; ++mt) {
+                    const int chunk = mt * 2 + v_csel;
+                    const uint32_t addr = vbase + (chunk >> 3) * Cfg::kRegionBytes + v_tok * 128 +
+                                          (((chunk & 7) ^ r8) << 4);
+                    uint32_t a[4];
+                    ptx::ldmatrix_x4_trans(a, addr);
+                    a[0] &= vmask_lo;
+                    a[1] &= vmask_lo;
+                    a[2] &= vmask_hi;
+                    a[3] &= vmask_hi;
+#pragma unroll
+                    for (int nt = 0; nt < NT; ++nt) {
+                        o[nt][mt][0] *= alpha0[nt];
+                        o[nt][mt][1] *= alpha1[nt];
+                        o[nt][mt][2] *= alpha0[nt];
+                        o[nt][mt][3] *= alpha1[nt];
+                        ptx::mma_16816<T>(o[nt][mt], a, pb_hi[nt][0], pb_hi[nt][1]);
+                        ptx::mma_16816<T>(o[nt][mt], a, pb_lo[nt][0], pb_lo[nt][1]);
+                    }
+                }
+            }
+            __syncwarp();
+            if (lane == 0) ptx::mbar_arrive(ptx::smem_addr(&empty_bar[slot]));
+        }
+    }
+
+    __syncthreads();
+    if (*abort_flag) return;
+
+    // ---------------------------------------------------------------- combine the warps
+    // Reuses the ring (every copy has landed and been consumed).
+    constexpr int HP = NT * 8;        // heads per warp state
+    constexpr int OSTRIDE = D + 4;    // padded row of the per-warp O tile (conflict-free writes)
+    float* sm_o = reinterpret_cast<float*>(ring);                 // [warps][HP][OSTRIDE]
+    float* sm_m = sm_o + kConsumerWarps * HP * OSTRIDE;           // [warps][HP]
+    float* sm_l = sm_m + kConsumerWarps * HP;                     // [warps][HP]
+    if (warp < kConsumerWarps) {
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+            float a = l0[nt], c = l1[nt];
+#pragma unroll
+            for (int off = 4; off < 32; off <<= 1) {
+                a += __shfl_xor_sync(0xffffffffu, a, off);
+                c += __shfl_xor_sync(0xffffffffu, c, off);
+            }
+            const int h0 = nt * 8 + 2 * tq;
+            if (gq == 0) {
+                sm_m[warp * HP + h0] = m0[nt];
+                sm_m[warp * HP + h0 + 1] = m1[nt];
+                sm_l[warp * HP + h0] = a;
+                sm_l[warp * HP + h0 + 1] = c;
+            }
+            float* w0 = sm_o + (warp * HP + h0) * OSTRIDE;
+            float* w1 = w0 + OSTRIDE;
+#pragma unroll
+            for (int mt = 0; mt < KSTEPS; ++mt) {
+                w0[mt * 16 + gq] = o[nt][mt][0];
+                w1[mt * 16 + gq] = o[nt][mt][1];
+                w0[mt * 16 + gq + 8] = o[nt][mt][2];
+                w1[mt * 16 + gq + 8] = o[nt][mt][3];
             }
         }
-        const float val = den > 0.f ? acc / den : 0.f;
-        const int hq = g * G + h;
-        if (p.num_splits == 1) {
-            T* out = static_cast<T*>(p.out);
-            out[((int64_t)b * p.num_q_heads + hq) * D + j] = from_float(val, T());
-        } else {
-            const int64_t row = ((int64_t)b * p.num_q_heads + hq) * p.num_splits + split;
-            p.partial_o[row * D + j] = val;
-            if (j == 0) p.partial_lse[row] = den > 0.f ? (mx + log2f(den)) * kLn2 : -INFINITY;
+        ptx::named_barrier_sync(1, kConsumerWarps * 32);
+
+        const int G = p.group;
+        for (int idx = tid; idx < G * D; idx += kConsumerWarps * 32) {
+            const int h = idx / D;
+            const int j = idx - h * D;
+            float mx = -INFINITY;
+#pragma unroll
+            for (int w = 0; w < kConsumerWarps; ++w) mx = fmaxf(mx, sm_m[w * HP + h]);
+            float acc = 0.f, den = 0.f;
+            if (mx != -INFINITY) {
+#pragma unroll
+                for (int w = 0; w < kConsumerWarps; ++w) {
+                    const float mw = sm_m[w * HP + h];
+                    if (mw == -INFINITY) continue;
+                    const float c = exp2f(mw - mx);
+                    den = fmaf(sm_l[w * HP + h], c, den);
+                    acc = fmaf(sm_o[(w * HP + h) * OSTRIDE + j], c, acc);
+                }
+            }
+            const float val = den > 0.f ? acc / den : 0.f;
+            const int hq = g * G + h;
+            if (nsplit == 1) {
+                T* out = static_cast<T*>(p.out);
+                out[((int64_t)b * p.num_q_heads + hq) * D + j] = from_float(val, T());
+            } else {
+                const int64_t prow = ((int64_t)b * p.num_q_heads + hq) * p.num_splits + split;
+                p.partial_o[prow * D + j] = val;
+                if (j == 0) p.partial_lse[prow] = den > 0.f ? (mx + log2f(den)) * kLn2 : -INFINITY;
+            }
         }
     }
 }
 
-// Merge: one CTA per (sequence, query head); thread j produces dimension j.
+// Merge of split partials: one CTA per (query head, sequence).  With
+// context_lens given, a sequence whose context fits one partition was written
+// directly by the decode kernel and is skipped, and only its first
+// ceil(n / chunk_tokens) partials are read; without, all num_splits are merged.
+struct MergeParams {
+    void* out;
+    const float* partial_o;
+    const float* partial_lse;
+    const int32_t* context_lens;  // nullable
+    int num_q_heads;
+    int num_splits;
+    int head_dim;
+    int chunk_tokens;
+    int cap;                      // context clamp, as in the decode kernel
+};
+
+constexpr int kMergeThreads = 128;
+
 template <typename T>
-__global__ void __launch_bounds__(128)
-merge_kernel(T* __restrict__ out, const float* __restrict__ partial_o,
-             const float* __restrict__ partial_lse, int num_splits, int head_dim) {
-    const int64_t row = blockIdx.x;  // b * H_q + h
-    const float* lse = partial_lse + row * num_splits;
+__global__ void __launch_bounds__(kMergeThreads)
+merge_kernel(const MergeParams p) {
+    __shared__ float w_s[PKV_MAX_SPLITS];
+    __shared__ float red[kMergeThreads / 32];
+    const int h = blockIdx.x;
+    const int b = blockIdx.y;
+    ptx::grid_dependency_wait();
+    int ns = p.num_splits;
+    if (p.context_lens != nullptr) {
+        const int n = clamped_len(__ldg(p.context_lens + b), p.cap);
+        ns = max(1, (n + p.chunk_tokens - 1) / p.chunk_tokens);
+        if (ns <= 1) return;
+    }
+    const int64_t row = (int64_t)b * p.num_q_heads + h;
+    const float* lse = p.partial_lse + row * p.num_splits;
     float mx = -INFINITY;
-    for (int s = 0; s < num_splits; ++s) mx = fmaxf(mx, __ldg(lse + s));
-    for (int j = threadIdx.x; j < head_dim; j += blockDim.x) {
-        float acc = 0.f, den = 0.f;
-        if (mx != -INFINITY) {
-            for (int s = 0; s < num_splits; ++s) {
-                const float ls = __ldg(lse + s);
-                if (ls == -INFINITY) continue;
-                const float w = expf(ls - mx);
-                den += w;
-                acc = fmaf(w, __ldg(partial_o + (row * num_splits + s) * head_dim + j), acc);
-            }
+    for (int s = threadIdx.x; s < ns; s += kMergeThreads) mx = fmaxf(mx, lse[s]);
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = mx;
+    __syncthreads();
+    mx = red[0];
+#pragma unroll
+    for (int w = 1; w < kMergeThreads / 32; ++w) mx = fmaxf(mx, red[w]);
+    __syncthreads();
+    float den = 0.f;
+    for (int s = threadIdx.x; s < ns; s += kMergeThreads) {
+        const float ls = lse[s];
+        const float w = (mx == -INFINITY || ls == -INFINITY) ? 0.f : expf(ls - mx);
+        w_s[s] = w;
+        den += w;
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) den += __shfl_xor_sync(0xffffffffu, den, off);
+    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = den;
+    __syncthreads();
+    den = 0.f;
+#pragma unroll
+    for (int w = 0; w < kMergeThreads / 32; ++w) den += red[w];
+    const float inv = den > 0.f ? 1.f / den : 0.f;
+    const float* po = p.partial_o + row * p.num_splits * p.head_dim;
+    T* out = static_cast<T*>(p.out) + row * p.head_dim;
+    for (int j = threadIdx.x; j < p.head_dim; j += kMergeThreads) {
+        float acc = 0.f;
+        for (int s = 0; s < ns; ++s) {
+            const float w = w_s[s];
+            if (w != 0.f) acc = fmaf(w, po[(int64_t)s * p.head_dim + j], acc);
         }
-        out[row * head_dim + j] = from_float(den > 0.f ? acc / den : 0.f, T());
+        out[j] = from_float(acc * inv, T());
     }
 }
 
 // ---------------------------------------------------------------------------
-// Host side: split planning, dispatch
+// Host side: split planning, tensor maps, launches
 // ---------------------------------------------------------------------------
 
 static int current_sm_count() {
@@ -240,25 +559,31 @@ static pkv_status check_shapes(int num_seqs, int num_q_heads, int num_kv_heads, 
     return PKV_OK;
 }
 
+// Partitions: each is a whole number of pages, at most kMaxChunkPages; the
+// automatic plan aims at several waves of CTAs over the SMs so ragged lengths
+// balance, without cutting partitions below 256 tokens.
 static pkv_status make_plan(int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
                             int block_size, int max_context_len, int num_splits, Plan* plan) {
     pkv_status st = check_shapes(num_seqs, num_q_heads, num_kv_heads, head_dim, block_size,
                                  max_context_len, num_splits);
     if (st != PKV_OK) return st;
-    const int max_pages = max(1, (max_context_len + block_size - 1) / block_size);
-    int splits = num_splits;
-    if (splits == 0) {
+    const int max_pages = std::max(1, (max_context_len + block_size - 1) / block_size);
+    int chunk_pages;
+    if (num_splits == 0) {
         const int sms = current_sm_count();
         if (sms <= 0) return PKV_ERR_CUDA;
-        const int64_t units = (int64_t)max(1, num_seqs) * num_kv_heads;
-        const int64_t target = 4LL * sms;
-        splits = (int)std::min<int64_t>(PKV_MAX_SPLITS, (target + units - 1) / units);
-        // keep at least 8 pages per partition
-        splits = min(splits, max(1, max_pages / 8));
+        const int64_t units = (int64_t)std::max(1, num_seqs) * num_kv_heads;
+        const int64_t target = 4LL * 3 * sms;  // four waves of three resident CTAs per SM
+        const int64_t want = std::max<int64_t>(1, (target + units - 1) / units);
+        chunk_pages = (int)((max_pages + want - 1) / want);
+        const int min_pages = std::max(1, 256 / block_size);
+        chunk_pages = std::max(chunk_pages, min_pages);
+    } else {
+        chunk_pages = (max_pages + num_splits - 1) / num_splits;
     }
-    splits = max(1, min(splits, max_pages));
-    const int chunk_pages = (max_pages + splits - 1) / splits;
-    splits = (max_pages + chunk_pages - 1) / chunk_pages;
+    chunk_pages = std::min(std::max(chunk_pages, 1), kMaxChunkPages);
+    int splits = (max_pages + chunk_pages - 1) / chunk_pages;
+    if (splits > PKV_MAX_SPLITS) return PKV_ERR_UNSUPPORTED;  // context too long for the plan
     plan->num_splits = splits;
     plan->chunk_tokens = chunk_pages * block_size;
     plan->workspace_bytes =
@@ -267,27 +592,94 @@ static pkv_status make_plan(int num_seqs, int num_q_heads, int num_kv_heads, int
     return PKV_OK;
 }
 
-template <typename T, int D>
-static void launch_decode_d(const DecodeParams& p, dim3 grid, cudaStream_t stream) {
-    const int G = p.group;
-    if (G == 1)
-        decode_simple_kernel<T, D, 1><<<grid, kDecodeWarps * 32, 0, stream>>>(p);
-    else if (G == 2)
-        decode_simple_kernel<T, D, 2><<<grid, kDecodeWarps * 32, 0, stream>>>(p);
-    else if (G <= 4)
-        decode_simple_kernel<T, D, 4><<<grid, kDecodeWarps * 32, 0, stream>>>(p);
-    else if (G <= 8)
-        decode_simple_kernel<T, D, 8><<<grid, kDecodeWarps * 32, 0, stream>>>(p);
-    else
-        decode_simple_kernel<T, D, 16><<<grid, kDecodeWarps * 32, 0, stream>>>(p);
+static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* ptr = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000,
+                                             cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+        else
+            cudaGetLastError();
+    });
+    return fn;
+}
+
+// Tensor map over a cache [num_blocks][block_size][H_kv][D]: dims (innermost
+// first) D, H_kv, block_size, num_blocks; box 64 dims x 1 head x 16 tokens x
+// 1 block, 128-byte swizzle.
+static bool make_cache_map(CUtensorMap* map, const void* base, pkv_dtype dtype, int num_blocks,
+                           int block_size, int num_kv_heads, int head_dim) {
+    PFN_cuTensorMapEncodeTiled_v12000 fn = encode_fn();
+    if (fn == nullptr) return false;
+    const cuuint64_t e = 2;
+    cuuint64_t dims[4] = {(cuuint64_t)head_dim, (cuuint64_t)num_kv_heads, (cuuint64_t)block_size,
+                          (cuuint64_t)num_blocks};
+    cuuint64_t strides[3] = {(cuuint64_t)head_dim * e, (cuuint64_t)num_kv_heads * head_dim * e,
+                             (cuuint64_t)block_size * num_kv_heads * head_dim * e};
+    cuuint32_t box[4] = {64, 1, (cuuint32_t)kStageTokens, 1};
+    cuuint32_t estr[4] = {1, 1, 1, 1};
+    CUresult r = fn(map, dtype == PKV_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                           : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
+                    4, const_cast<void*>(base), dims, strides, box, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+template <typename T, int D, int NT>
+static cudaError_t launch_decode_t(const CUtensorMap& mk, const CUtensorMap& mv,
+                                   const DecodeParams& p, dim3 grid, cudaStream_t stream) {
+    auto kern = decode_kernel<T, D, NT>;
+    static std::once_flag once;
+    static cudaError_t attr_err = cudaSuccess;
+    std::call_once(once, [&] {
+        attr_err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                        Tile<D>::kSmemBytes);
+    });
+    if (attr_err != cudaSuccess) return attr_err;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = Tile<D>::kSmemBytes;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, mk, mv, p);
 }
 
 template <typename T>
-static void launch_decode(const DecodeParams& p, int head_dim, dim3 grid, cudaStream_t stream) {
+static cudaError_t launch_decode(const CUtensorMap& mk, const CUtensorMap& mv,
+                                 const DecodeParams& p, int head_dim, dim3 grid,
+                                 cudaStream_t stream) {
+    const bool wide = p.group > 8;
     if (head_dim == 64)
-        launch_decode_d<T, 64>(p, grid, stream);
-    else
-        launch_decode_d<T, 128>(p, grid, stream);
+        return wide ? launch_decode_t<T, 64, 2>(mk, mv, p, grid, stream)
+                    : launch_decode_t<T, 64, 1>(mk, mv, p, grid, stream);
+    return wide ? launch_decode_t<T, 128, 2>(mk, mv, p, grid, stream)
+                : launch_decode_t<T, 128, 1>(mk, mv, p, grid, stream);
+}
+
+template <typename T>
+static cudaError_t launch_merge(const MergeParams& p, int rows_h, int rows_b,
+                                cudaStream_t stream) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(rows_h, rows_b);
+    cfg.blockDim = dim3(kMergeThreads);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, merge_kernel<T>, p);
 }
 
 }  // namespace pkv
@@ -335,6 +727,7 @@ extern "C" pkv_status pkv_decode_attention(void* out, const void* q, const void*
         (reinterpret_cast<uintptr_t>(block_tables) & 3u) ||
         (reinterpret_cast<uintptr_t>(context_lens) & 3u))
         return PKV_ERR_INVALID_ARG;
+    if ((int64_t)max_blocks_per_seq * block_size > INT_MAX) return PKV_ERR_UNSUPPORTED;
     Plan plan;
     st = make_plan(num_seqs, num_q_heads, num_kv_heads, head_dim, block_size, max_context_len,
                    num_splits, &plan);
@@ -343,11 +736,14 @@ extern "C" pkv_status pkv_decode_attention(void* out, const void* q, const void*
         return PKV_ERR_WORKSPACE;
     if (workspace != nullptr && !aligned16(workspace)) return PKV_ERR_INVALID_ARG;
 
+    CUtensorMap mk, mv;
+    if (!make_cache_map(&mk, k_cache, dtype, num_blocks, block_size, num_kv_heads, head_dim) ||
+        !make_cache_map(&mv, v_cache, dtype, num_blocks, block_size, num_kv_heads, head_dim))
+        return PKV_ERR_CUDA;
+
     DecodeParams p;
     p.out = out;
     p.q = q;
-    p.k_cache = k_cache;
-    p.v_cache = v_cache;
     p.block_tables = block_tables;
     p.context_lens = context_lens;
     p.err_flag = err_flag;
@@ -355,7 +751,6 @@ extern "C" pkv_status pkv_decode_attention(void* out, const void* q, const void*
     p.num_blocks = num_blocks;
     p.block_size = block_size;
     p.num_q_heads = num_q_heads;
-    p.num_kv_heads = num_kv_heads;
     p.group = num_q_heads / num_kv_heads;
     p.num_splits = plan.num_splits;
     p.chunk_tokens = plan.chunk_tokens;
@@ -369,21 +764,29 @@ extern "C" pkv_status pkv_decode_attention(void* out, const void* q, const void*
     }
     cudaStream_t s = (cudaStream_t)stream;
     dim3 grid(plan.num_splits, num_kv_heads, num_seqs);
-    if (dtype == PKV_FP16)
-        launch_decode<__half>(p, head_dim, grid, s);
-    else
-        launch_decode<__nv_bfloat16>(p, head_dim, grid, s);
-    if (cudaGetLastError() != cudaSuccess) return PKV_ERR_CUDA;
+    cudaError_t e = dtype == PKV_FP16 ? launch_decode<__half>(mk, mv, p, head_dim, grid, s)
+                                      : launch_decode<__nv_bfloat16>(mk, mv, p, head_dim, grid, s);
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return PKV_ERR_CUDA;
+    }
     if (plan.num_splits > 1) {
-        const int rows = num_seqs * num_q_heads;
-        if (dtype == PKV_FP16)
-            merge_kernel<__half><<<rows, 128, 0, s>>>(static_cast<__half*>(out), p.partial_o,
-                                                      p.partial_lse, plan.num_splits, head_dim);
-        else
-            merge_kernel<__nv_bfloat16><<<rows, 128, 0, s>>>(static_cast<__nv_bfloat16*>(out),
-                                                             p.partial_o, p.partial_lse,
-                                                             plan.num_splits, head_dim);
-        if (cudaGetLastError() != cudaSuccess) return PKV_ERR_CUDA;
+        MergeParams mp;
+        mp.out = out;
+        mp.partial_o = p.partial_o;
+        mp.partial_lse = p.partial_lse;
+        mp.context_lens = context_lens;
+        mp.num_q_heads = num_q_heads;
+        mp.num_splits = plan.num_splits;
+        mp.head_dim = head_dim;
+        mp.chunk_tokens = plan.chunk_tokens;
+        mp.cap = std::min(max_blocks_per_seq * block_size, max_context_len);
+        e = dtype == PKV_FP16 ? launch_merge<__half>(mp, num_q_heads, num_seqs, s)
+                              : launch_merge<__nv_bfloat16>(mp, num_q_heads, num_seqs, s);
+        if (e != cudaSuccess) {
+            cudaGetLastError();
+            return PKV_ERR_CUDA;
+        }
     }
     return PKV_OK;
 }
@@ -391,22 +794,31 @@ extern "C" pkv_status pkv_decode_attention(void* out, const void* q, const void*
 extern "C" pkv_status pkv_merge(void* out, const float* partial_o, const float* partial_lse,
                                 int num_seqs, int num_q_heads, int num_splits, int head_dim,
                                 pkv_dtype dtype, void* stream) {
-    if (num_seqs < 0 || num_q_heads <= 0 || num_splits <= 0 || head_dim <= 0 ||
-        (dtype != PKV_FP16 && dtype != PKV_BF16))
+    if (num_seqs < 0 || num_q_heads <= 0 || num_splits <= 0 || num_splits > PKV_MAX_SPLITS ||
+        head_dim <= 0 || (dtype != PKV_FP16 && dtype != PKV_BF16))
         return PKV_ERR_INVALID_ARG;
     if (num_seqs == 0) return PKV_OK;
     if (!out || !partial_o || !partial_lse) return PKV_ERR_INVALID_ARG;
     if ((reinterpret_cast<uintptr_t>(out) & 1u) || (reinterpret_cast<uintptr_t>(partial_o) & 3u) ||
         (reinterpret_cast<uintptr_t>(partial_lse) & 3u))
         return PKV_ERR_INVALID_ARG;
-    const int64_t rows = (int64_t)num_seqs * num_q_heads;
-    if (rows > INT_MAX) return PKV_ERR_UNSUPPORTED;
+    if (num_seqs > 65535) return PKV_ERR_UNSUPPORTED;
+    MergeParams mp;
+    mp.out = out;
+    mp.partial_o = partial_o;
+    mp.partial_lse = partial_lse;
+    mp.context_lens = nullptr;
+    mp.num_q_heads = num_q_heads;
+    mp.num_splits = num_splits;
+    mp.head_dim = head_dim;
+    mp.chunk_tokens = 1;
+    mp.cap = 0;
     cudaStream_t s = (cudaStream_t)stream;
-    if (dtype == PKV_FP16)
-        merge_kernel<__half><<<(int)rows, 128, 0, s>>>(static_cast<__half*>(out), partial_o,
-                                                       partial_lse, num_splits, head_dim);
-    else
-        merge_kernel<__nv_bfloat16><<<(int)rows, 128, 0, s>>>(
-            static_cast<__nv_bfloat16*>(out), partial_o, partial_lse, num_splits, head_dim);
-    return cudaGetLastError() == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
+    cudaError_t e = dtype == PKV_FP16 ? launch_merge<__half>(mp, num_q_heads, num_seqs, s)
+                                      : launch_merge<__nv_bfloat16>(mp, num_q_heads, num_seqs, s);
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return PKV_ERR_CUDA;
+    }
+    return PKV_OK;
 }
