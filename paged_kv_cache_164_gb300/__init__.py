@@ -25,7 +25,8 @@ from typing import Optional
 import torch
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
-LIB_PATH = os.path.join(_HERE, "_build", "libpkv.so")
+# The in-tree build; PKV_LIBRARY may point at another build of the same library.
+LIB_PATH = os.environ.get("PKV_LIBRARY") or os.path.join(_HERE, "_build", "libpkv.so")
 
 PKV_OK = 0
 STATUS_NAMES = {0: "PKV_OK", 1: "PKV_ERR_INVALID_ARG", 2: "PKV_ERR_UNSUPPORTED",

@@ -10,7 +10,7 @@
 // LLM-101-CN "推理优化" combine_result).
 //
 // Kernel design (GB300):
-//  * One CTA per (partition, KV head, sequence).  Warp 4 is the producer: one
+//  * One CTA per (KV head, sequence, partition).  Warp 4 is the producer: one
 //    lane issues 4-D TMA tensor loads of 16-token tiles of K and V straight
 //    from the paged cache, the physical block id from the block table being
 //    the outermost coordinate, into a ring of shared-memory stages guarded by
@@ -131,9 +131,13 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
     int* table = reinterpret_cast<int*>(empty_bar + S);
     volatile int* abort_flag = table + kMaxChunkPages;
 
-    const int split = blockIdx.x;
-    const int g = blockIdx.y;   // KV head
-    const int b = blockIdx.z;   // sequence
+    // Grid order (KV head fastest, then sequence, then partition): all first
+    // partitions run before any second one, so sequences that share physical
+    // blocks (a common prompt prefix) read them close together in time and the
+    // repeats hit in L2.
+    const int g = blockIdx.x;       // KV head
+    const int b = blockIdx.y;       // sequence
+    const int split = blockIdx.z;   // KV partition
     const int tid = threadIdx.x;
     const int warp = tid >> 5;
     const int lane = tid & 31;
@@ -763,7 +767,7 @@ extern "C" pkv_status pkv_decode_attention(void* out, const void* q, const void*
         p.partial_lse = p.partial_o + (size_t)num_seqs * num_q_heads * plan.num_splits * head_dim;
     }
     cudaStream_t s = (cudaStream_t)stream;
-    dim3 grid(plan.num_splits, num_kv_heads, num_seqs);
+    dim3 grid(num_kv_heads, num_seqs, plan.num_splits);
     cudaError_t e = dtype == PKV_FP16 ? launch_decode<__half>(mk, mv, p, head_dim, grid, s)
                                       : launch_decode<__nv_bfloat16>(mk, mv, p, head_dim, grid, s);
     if (e != cudaSuccess) {
