@@ -55,7 +55,7 @@ struct Tile {
     static constexpr int kStages = D == 128 ? 8 : 16;         // ring depth: 64 KB either way
     static constexpr int kRingBytes = kStages * kStageBytes;
     static constexpr int kSmemBytes = 1024 /*align*/ + kRingBytes + 2 * kStages * 8 +
-                                      kMaxChunkPages * 4 + 16;
+                                      (kMaxChunkPages + 1) * 4 + 16;
 };
 
 struct DecodeParams {
@@ -73,6 +73,8 @@ struct DecodeParams {
     int group;           // query heads per KV head
     int num_splits;
     int chunk_tokens;    // tokens per partition (a multiple of block_size and of 16)
+    int stagger_tokens;  // partition-boundary shift step (a multiple of 16), 0 = none
+    int num_kv_heads;
     int max_context_len;
     float scale_log2;    // scale * log2(e)
 };
@@ -80,6 +82,24 @@ struct DecodeParams {
 // Context length of sequence b as the kernels use it: negative or too long
 // values are clamped (and flagged by the decode kernel).
 __device__ __forceinline__ int clamped_len(int n, int cap) { return n < 0 ? 0 : (n > cap ? cap : n); }
+
+// Partition geometry of one (sequence b, KV head g) pair.  Partition j covers
+// tokens [j*C - shift, (j+1)*C - shift) of the context, clipped to [0, n), where
+// C = chunk_tokens and shift = ((b * H_kv + g) % 3) * stagger.  Staggering the
+// boundaries of neighbouring pairs gives CTAs of one wave different lengths,
+// so the waves drift apart and one CTA's set-up and wind-down overlap other
+// CTAs' streaming instead of lining up across the whole GPU.
+struct Partition {
+    int shift;
+    int nsplit;   // partitions with tokens (1 when n == 0)
+};
+__device__ __forceinline__ Partition partition_of(int n, int b, int g, int num_kv_heads,
+                                                  int chunk, int stagger) {
+    Partition pt;
+    pt.shift = ((b * num_kv_heads + g) % 3) * stagger;
+    pt.nsplit = n > 0 ? (n + pt.shift + chunk - 1) / chunk : 1;
+    return pt;
+}
 
 __device__ __forceinline__ uint32_t pack2(float lo, float hi, __nv_bfloat16) {
     __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
@@ -129,7 +149,7 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
     uint64_t* full_bar = reinterpret_cast<uint64_t*>(ring + Cfg::kRingBytes);
     uint64_t* empty_bar = full_bar + S;
     int* table = reinterpret_cast<int*>(empty_bar + S);
-    volatile int* abort_flag = table + kMaxChunkPages;
+    volatile int* abort_flag = table + kMaxChunkPages + 1;
 
     // Grid order (KV head fastest, then sequence, then partition): all first
     // partitions run before any second one, so sequences that share physical
@@ -151,15 +171,27 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
 
     const int cap = min(p.max_blocks_per_seq * bs, p.max_context_len);
     const int n_raw = __ldg(p.context_lens + b);
+    // Partition start does not depend on the context length, so the producer
+    // warp fetches the block-table slice at the same time as the length.
+    const int shift = ((b * p.num_kv_heads + g) % 3) * p.stagger_tokens;
+    const int t_begin = max(0, split * p.chunk_tokens - shift);
+    const int page0 = t_begin / bs;
+    const int max_pages = min(p.max_blocks_per_seq - page0, p.chunk_tokens / bs + 1);
+    const int32_t* row = p.block_tables + (int64_t)b * p.max_blocks_per_seq + page0;
+    int blk_r[3] = {-1, -1, -1};
+    if (warp == kConsumerWarps) {
+#pragma unroll
+        for (int r = 0; r < 3; ++r)
+            if (lane + 32 * r < max_pages) blk_r[r] = __ldg(row + lane + 32 * r);
+    }
     if ((n_raw < 0 || n_raw > cap) && split == 0 && g == 0 && tid == 0)
         flag_error(p.err_flag, PKV_EFLAG_CONTEXT_LEN);
     const int n = clamped_len(n_raw, cap);
-    const int nsplit = max(1, (n + p.chunk_tokens - 1) / p.chunk_tokens);
-    if (split >= nsplit) return;
-    const int t_begin = split * p.chunk_tokens;
-    const int t_end = min(n, t_begin + p.chunk_tokens);
+    const Partition pt = partition_of(n, b, g, p.num_kv_heads, p.chunk_tokens, p.stagger_tokens);
+    if (split >= pt.nsplit) return;
+    const int t_end = min(n, (split + 1) * p.chunk_tokens - shift);
     const int nstages = t_end > t_begin ? (t_end - t_begin + kStageTokens - 1) / kStageTokens : 0;
-    const int page0 = t_begin / bs;
+    const int nsplit = pt.nsplit;
 
     if (tid == 0) {
         for (int s = 0; s < S; ++s) {
@@ -170,16 +202,19 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
         ptx::fence_barrier_init();
     }
     if (warp == kConsumerWarps) {
-        // Stage this partition's slice of the block table, validating each id.
+        // Keep this partition's slice of the block table, validating each id.
         const int npages = t_end > t_begin ? (t_end + bs - 1) / bs - page0 : 0;
-        const int32_t* row = p.block_tables + (int64_t)b * p.max_blocks_per_seq + page0;
-        for (int i = lane; i < npages; i += 32) {
-            int blk = __ldg(row + i);
-            if (blk < 0 || blk >= p.num_blocks) {
-                flag_error(p.err_flag, PKV_EFLAG_BLOCK_ID);
-                blk = -1;
+#pragma unroll
+        for (int r = 0; r < 3; ++r) {
+            const int i = lane + 32 * r;
+            if (i < npages) {
+                int blk = blk_r[r];
+                if (blk < 0 || blk >= p.num_blocks) {
+                    flag_error(p.err_flag, PKV_EFLAG_BLOCK_ID);
+                    blk = -1;
+                }
+                table[i] = blk;
             }
-            table[i] = blk;
         }
         if (lane == 0) {
             ptx::prefetch_tensormap(&tm_k);
@@ -418,33 +453,56 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
         }
         ptx::named_barrier_sync(1, kConsumerWarps * 32);
 
+        // Per-head combine factors, once per head: c_w = e^(m_w - m*) / L with
+        // L = sum_w e^(m_w - m*) l_w, and the head's log-sum-exp.
         const int G = p.group;
-        for (int idx = tid; idx < G * D; idx += kConsumerWarps * 32) {
-            const int h = idx / D;
-            const int j = idx - h * D;
+        float* sm_f = sm_l + kConsumerWarps * HP;   // [HP][warps]
+        float* sm_lse = sm_f + HP * kConsumerWarps; // [HP]
+        if (tid < G) {
+            const int h = tid;
             float mx = -INFINITY;
 #pragma unroll
             for (int w = 0; w < kConsumerWarps; ++w) mx = fmaxf(mx, sm_m[w * HP + h]);
-            float acc = 0.f, den = 0.f;
-            if (mx != -INFINITY) {
+            float c[kConsumerWarps];
+            float den = 0.f;
 #pragma unroll
-                for (int w = 0; w < kConsumerWarps; ++w) {
-                    const float mw = sm_m[w * HP + h];
-                    if (mw == -INFINITY) continue;
-                    const float c = exp2f(mw - mx);
-                    den = fmaf(sm_l[w * HP + h], c, den);
-                    acc = fmaf(sm_o[(w * HP + h) * OSTRIDE + j], c, acc);
-                }
+            for (int w = 0; w < kConsumerWarps; ++w) {
+                const float mw = sm_m[w * HP + h];
+                c[w] = (mx == -INFINITY || mw == -INFINITY) ? 0.f : exp2f(mw - mx);
+                den = fmaf(sm_l[w * HP + h], c[w], den);
             }
-            const float val = den > 0.f ? acc / den : 0.f;
+            const float inv = den > 0.f ? 1.f / den : 0.f;
+#pragma unroll
+            for (int w = 0; w < kConsumerWarps; ++w) sm_f[h * kConsumerWarps + w] = c[w] * inv;
+            sm_lse[h] = den > 0.f ? (mx + log2f(den)) * kLn2 : -INFINITY;
+        }
+        ptx::named_barrier_sync(1, kConsumerWarps * 32);
+
+        // Four consecutive dims of one head per thread and iteration.
+        for (int idx = tid; idx < G * (D / 4); idx += kConsumerWarps * 32) {
+            const int h = idx / (D / 4);
+            const int j = (idx - h * (D / 4)) * 4;
+            float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+            for (int w = 0; w < kConsumerWarps; ++w) {
+                const float f = sm_f[h * kConsumerWarps + w];
+                const float4 v = *reinterpret_cast<const float4*>(sm_o + (w * HP + h) * OSTRIDE + j);
+                acc.x = fmaf(v.x, f, acc.x);
+                acc.y = fmaf(v.y, f, acc.y);
+                acc.z = fmaf(v.z, f, acc.z);
+                acc.w = fmaf(v.w, f, acc.w);
+            }
             const int hq = g * G + h;
             if (nsplit == 1) {
-                T* out = static_cast<T*>(p.out);
-                out[((int64_t)b * p.num_q_heads + hq) * D + j] = from_float(val, T());
+                T* out = static_cast<T*>(p.out) + ((int64_t)b * p.num_q_heads + hq) * D + j;
+                uint2 packed;
+                packed.x = pack2(acc.x, acc.y, T());
+                packed.y = pack2(acc.z, acc.w, T());
+                *reinterpret_cast<uint2*>(out) = packed;
             } else {
                 const int64_t prow = ((int64_t)b * p.num_q_heads + hq) * p.num_splits + split;
-                p.partial_o[prow * D + j] = val;
-                if (j == 0) p.partial_lse[prow] = den > 0.f ? (mx + log2f(den)) * kLn2 : -INFINITY;
+                *reinterpret_cast<float4*>(p.partial_o + prow * D + j) = acc;
+                if (j == 0) p.partial_lse[prow] = sm_lse[h];
             }
         }
     }
@@ -460,9 +518,12 @@ struct MergeParams {
     const float* partial_lse;
     const int32_t* context_lens;  // nullable
     int num_q_heads;
+    int num_kv_heads;
+    int group;
     int num_splits;
     int head_dim;
     int chunk_tokens;
+    int stagger_tokens;
     int cap;                      // context clamp, as in the decode kernel
 };
 
@@ -479,7 +540,8 @@ merge_kernel(const MergeParams p) {
     int ns = p.num_splits;
     if (p.context_lens != nullptr) {
         const int n = clamped_len(__ldg(p.context_lens + b), p.cap);
-        ns = max(1, (n + p.chunk_tokens - 1) / p.chunk_tokens);
+        ns = partition_of(n, b, h / p.group, p.num_kv_heads, p.chunk_tokens, p.stagger_tokens)
+                 .nsplit;
         if (ns <= 1) return;
     }
     const int64_t row = (int64_t)b * p.num_q_heads + h;
@@ -544,8 +606,9 @@ static int current_sm_count() {
 }
 
 struct Plan {
-    int num_splits;
+    int num_splits;      // partitions per sequence, at most
     int chunk_tokens;
+    int stagger_tokens;
     size_t workspace_bytes;
 };
 
@@ -586,10 +649,18 @@ static pkv_status make_plan(int num_seqs, int num_q_heads, int num_kv_heads, int
         chunk_pages = (max_pages + num_splits - 1) / num_splits;
     }
     chunk_pages = std::min(std::max(chunk_pages, 1), kMaxChunkPages);
-    int splits = (max_pages + chunk_pages - 1) / chunk_pages;
-    if (splits > PKV_MAX_SPLITS) return PKV_ERR_UNSUPPORTED;  // context too long for the plan
+    const int chunk = chunk_pages * block_size;
+    // Staggered boundaries (automatic plans with more than one partition only):
+    // shifts of 0, 1/3 and 2/3 of a partition, in whole 16-token stages.
+    int stagger = 0;
+    if (num_splits == 0 && max_context_len > chunk) stagger = (chunk / 3) / 16 * 16;
+    const int64_t splits64 =
+        std::max<int64_t>(1, ((int64_t)max_context_len + 2 * stagger + chunk - 1) / chunk);
+    if (splits64 > PKV_MAX_SPLITS) return PKV_ERR_UNSUPPORTED;  // context too long for the plan
+    const int splits = (int)splits64;
     plan->num_splits = splits;
-    plan->chunk_tokens = chunk_pages * block_size;
+    plan->chunk_tokens = chunk;
+    plan->stagger_tokens = stagger;
     plan->workspace_bytes =
         splits > 1 ? (size_t)num_seqs * num_q_heads * splits * (head_dim + 1) * sizeof(float) + 256
                    : 0;
@@ -758,6 +829,8 @@ extern "C" pkv_status pkv_decode_attention(void* out, const void* q, const void*
     p.group = num_q_heads / num_kv_heads;
     p.num_splits = plan.num_splits;
     p.chunk_tokens = plan.chunk_tokens;
+    p.stagger_tokens = plan.stagger_tokens;
+    p.num_kv_heads = num_kv_heads;
     p.max_context_len = max_context_len;
     p.scale_log2 = scale * kLog2e;
     p.partial_o = nullptr;
@@ -781,9 +854,12 @@ extern "C" pkv_status pkv_decode_attention(void* out, const void* q, const void*
         mp.partial_lse = p.partial_lse;
         mp.context_lens = context_lens;
         mp.num_q_heads = num_q_heads;
+        mp.num_kv_heads = num_kv_heads;
+        mp.group = num_q_heads / num_kv_heads;
         mp.num_splits = plan.num_splits;
         mp.head_dim = head_dim;
         mp.chunk_tokens = plan.chunk_tokens;
+        mp.stagger_tokens = plan.stagger_tokens;
         mp.cap = std::min(max_blocks_per_seq * block_size, max_context_len);
         e = dtype == PKV_FP16 ? launch_merge<__half>(mp, num_q_heads, num_seqs, s)
                               : launch_merge<__nv_bfloat16>(mp, num_q_heads, num_seqs, s);
@@ -813,9 +889,12 @@ extern "C" pkv_status pkv_merge(void* out, const float* partial_o, const float* 
     mp.partial_lse = partial_lse;
     mp.context_lens = nullptr;
     mp.num_q_heads = num_q_heads;
+    mp.num_kv_heads = 1;
+    mp.group = num_q_heads;
     mp.num_splits = num_splits;
     mp.head_dim = head_dim;
     mp.chunk_tokens = 1;
+    mp.stagger_tokens = 0;
     mp.cap = 0;
     cudaStream_t s = (cudaStream_t)stream;
     cudaError_t e = dtype == PKV_FP16 ? launch_merge<__half>(mp, num_q_heads, num_seqs, s)

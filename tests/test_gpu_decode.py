@@ -167,3 +167,10 @@ def test_full_size_sampled(name):
     # outputs of every sequence are finite and bounded by max |V| (a convex combination)
     assert torch.isfinite(out).all()
     assert float(out.abs().max()) <= float(w.v_cache.abs().max()) * (1 + 2**-7)
+
+
+def test_long_context_plan_uses_at_least_four_partitions():
+    w = make_workload("c4", with_values=False)
+    s = w.spec
+    assert pkv.decode_num_splits(s.num_seqs, s.num_q_heads, s.num_kv_heads, s.head_dim,
+                                 s.block_size, w.max_context_len, 0) >= 4
