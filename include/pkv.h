@@ -184,6 +184,7 @@ pkv_status pkv_decode_attention_noalloc(void* out, const void* q, const void* k_
  *   out          [num_seqs][num_q_heads][head_dim] (written), dtype
  *   partial_o    float32 [num_seqs][num_q_heads][num_splits][head_dim]
  *   partial_lse  float32 [num_seqs][num_q_heads][num_splits], natural log
+ *   head_dim must be a multiple of 4, at most 512 (PKV_ERR_UNSUPPORTED otherwise).
  */
 pkv_status pkv_merge(void* out, const float* partial_o, const float* partial_lse, int num_seqs,
                      int num_q_heads, int num_splits, int head_dim, pkv_dtype dtype,

@@ -17,6 +17,10 @@ append_kernel(const uint4* __restrict__ k_new, const uint4* __restrict__ v_new,
               uint4* __restrict__ k_cache, uint4* __restrict__ v_cache,
               const int64_t* __restrict__ slot_mapping, int64_t num_slots, int row_vecs,
               int32_t* err_flag) {
+    // Launched as a programmatic dependent: let the next kernel (the decode)
+    // get scheduled now, then wait for the previous one before touching memory.
+    asm volatile("griddepcontrol.launch_dependents;" :::);
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     const int i = blockIdx.x;
     const int64_t slot = __ldg(slot_mapping + i);
     if (slot < 0) return;  // padding
@@ -91,10 +95,23 @@ extern "C" pkv_status pkv_append(const void* k_new, const void* v_new, void* k_c
     const int64_t row_bytes = (int64_t)num_kv_heads * head_dim * 2;
     if (row_bytes % 16 != 0 || row_bytes / 16 > INT_MAX) return PKV_ERR_UNSUPPORTED;
     const int row_vecs = (int)(row_bytes / 16);
-    append_kernel<<<num_tokens, 128, 0, (cudaStream_t)stream>>>(
-        (const uint4*)k_new, (const uint4*)v_new, (uint4*)k_cache, (uint4*)v_cache, slot_mapping,
-        (int64_t)num_blocks * block_size, row_vecs, err_flag);
-    return cudaGetLastError() == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(num_tokens);
+    cfg.blockDim = dim3(128);
+    cfg.stream = (cudaStream_t)stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    const cudaError_t e = cudaLaunchKernelEx(
+        &cfg, append_kernel, (const uint4*)k_new, (const uint4*)v_new, (uint4*)k_cache,
+        (uint4*)v_cache, slot_mapping, (int64_t)num_blocks * block_size, row_vecs, err_flag);
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return PKV_ERR_CUDA;
+    }
+    return PKV_OK;
 }
 
 extern "C" pkv_status pkv_gather(void* k_out, void* v_out, const void* k_cache,

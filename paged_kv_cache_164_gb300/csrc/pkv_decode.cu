@@ -508,10 +508,13 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
     }
 }
 
-// Merge of split partials: one CTA per (query head, sequence).  With
-// context_lens given, a sequence whose context fits one partition was written
-// directly by the decode kernel and is skipped, and only its first
-// ceil(n / chunk_tokens) partials are read; without, all num_splits are merged.
+// Merge of split partials (log-sum-exp rule): one CTA per (query head,
+// sequence).  Its threads cover the head's dims four at a time and, across
+// thread groups, interleaved subsets of the partitions; the groups' sums meet
+// in shared memory.  With context_lens given (the decode path), a sequence
+// whose context fitted a single partition was written by the decode kernel and
+// is skipped, and only the partitions that hold tokens are read.  Without
+// (pkv_merge), every row merges all num_splits partials.
 struct MergeParams {
     void* out;
     const float* partial_o;
@@ -519,9 +522,9 @@ struct MergeParams {
     const int32_t* context_lens;  // nullable
     int num_q_heads;
     int num_kv_heads;
-    int group;
+    int group;                    // query heads per KV head
     int num_splits;
-    int head_dim;
+    int head_dim;                 // a multiple of 4, at most 4 * kMergeThreads
     int chunk_tokens;
     int stagger_tokens;
     int cap;                      // context clamp, as in the decode kernel
@@ -532,10 +535,12 @@ constexpr int kMergeThreads = 128;
 template <typename T>
 __global__ void __launch_bounds__(kMergeThreads)
 merge_kernel(const MergeParams p) {
-    __shared__ float w_s[PKV_MAX_SPLITS];
-    __shared__ float red[kMergeThreads / 32];
+    __shared__ float4 part[kMergeThreads];
+    __shared__ float s_mx, s_inv;
     const int h = blockIdx.x;
     const int b = blockIdx.y;
+    const int tid = threadIdx.x;
+    ptx::launch_dependents();
     ptx::grid_dependency_wait();
     int ns = p.num_splits;
     if (p.context_lens != nullptr) {
@@ -546,40 +551,60 @@ merge_kernel(const MergeParams p) {
     }
     const int64_t row = (int64_t)b * p.num_q_heads + h;
     const float* lse = p.partial_lse + row * p.num_splits;
-    float mx = -INFINITY;
-    for (int s = threadIdx.x; s < ns; s += kMergeThreads) mx = fmaxf(mx, lse[s]);
+    if (tid < 32) {  // m* = max_p lse_p and 1 / sum_p e^(lse_p - m*)
+        float mx = -INFINITY;
+        for (int sp = tid; sp < ns; sp += 32) mx = fmaxf(mx, lse[sp]);
 #pragma unroll
-    for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
-    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = mx;
-    __syncthreads();
-    mx = red[0];
+        for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+        float den = 0.f;
+        if (mx != -INFINITY)
+            for (int sp = tid; sp < ns; sp += 32) {
+                const float ls = lse[sp];
+                if (ls != -INFINITY) den += exp2f((ls - mx) * kLog2e);
+            }
 #pragma unroll
-    for (int w = 1; w < kMergeThreads / 32; ++w) mx = fmaxf(mx, red[w]);
-    __syncthreads();
-    float den = 0.f;
-    for (int s = threadIdx.x; s < ns; s += kMergeThreads) {
-        const float ls = lse[s];
-        const float w = (mx == -INFINITY || ls == -INFINITY) ? 0.f : expf(ls - mx);
-        w_s[s] = w;
-        den += w;
-    }
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) den += __shfl_xor_sync(0xffffffffu, den, off);
-    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = den;
-    __syncthreads();
-    den = 0.f;
-#pragma unroll
-    for (int w = 0; w < kMergeThreads / 32; ++w) den += red[w];
-    const float inv = den > 0.f ? 1.f / den : 0.f;
-    const float* po = p.partial_o + row * p.num_splits * p.head_dim;
-    T* out = static_cast<T*>(p.out) + row * p.head_dim;
-    for (int j = threadIdx.x; j < p.head_dim; j += kMergeThreads) {
-        float acc = 0.f;
-        for (int s = 0; s < ns; ++s) {
-            const float w = w_s[s];
-            if (w != 0.f) acc = fmaf(w, po[(int64_t)s * p.head_dim + j], acc);
+        for (int off = 16; off > 0; off >>= 1) den += __shfl_xor_sync(0xffffffffu, den, off);
+        if (tid == 0) {
+            s_mx = mx;
+            s_inv = den > 0.f ? 1.f / den : 0.f;
         }
-        out[j] = from_float(acc * inv, T());
+    }
+    __syncthreads();
+    const int cols = p.head_dim / 4;          // float4 columns
+    const int groups = kMergeThreads / cols;  // partition subsets
+    const int col = tid % cols;
+    const int grp = tid / cols;
+    const float mx = s_mx;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (grp < groups && mx != -INFINITY) {
+        const float* po = p.partial_o + row * p.num_splits * p.head_dim + col * 4;
+        for (int sp = grp; sp < ns; sp += groups) {
+            const float ls = lse[sp];
+            if (ls == -INFINITY) continue;  // an empty partition may hold anything
+            const float wgt = exp2f((ls - mx) * kLog2e);
+            const float4 v = *reinterpret_cast<const float4*>(po + (int64_t)sp * p.head_dim);
+            acc.x = fmaf(wgt, v.x, acc.x);
+            acc.y = fmaf(wgt, v.y, acc.y);
+            acc.z = fmaf(wgt, v.z, acc.z);
+            acc.w = fmaf(wgt, v.w, acc.w);
+        }
+    }
+    part[tid] = acc;
+    __syncthreads();
+    if (tid < cols) {
+        float4 sum = part[tid];
+        for (int gi = 1; gi < groups; ++gi) {
+            const float4 v = part[gi * cols + tid];
+            sum.x += v.x;
+            sum.y += v.y;
+            sum.z += v.z;
+            sum.w += v.w;
+        }
+        const float inv = s_inv;
+        uint2 packed;
+        packed.x = pack2(sum.x * inv, sum.y * inv, T());
+        packed.y = pack2(sum.z * inv, sum.w * inv, T());
+        *reinterpret_cast<uint2*>(static_cast<T*>(p.out) + row * p.head_dim + tid * 4) = packed;
     }
 }
 
@@ -640,7 +665,7 @@ static pkv_status make_plan(int num_seqs, int num_q_heads, int num_kv_heads, int
         const int sms = current_sm_count();
         if (sms <= 0) return PKV_ERR_CUDA;
         const int64_t units = (int64_t)std::max(1, num_seqs) * num_kv_heads;
-        const int64_t target = 4LL * 3 * sms;  // four waves of three resident CTAs per SM
+        const int64_t target = 3LL * 3 * sms;  // three waves of three resident CTAs per SM
         const int64_t want = std::max<int64_t>(1, (target + units - 1) / units);
         chunk_pages = (int)((max_pages + want - 1) / want);
         const int min_pages = std::max(1, 256 / block_size);
@@ -742,10 +767,9 @@ static cudaError_t launch_decode(const CUtensorMap& mk, const CUtensorMap& mv,
 }
 
 template <typename T>
-static cudaError_t launch_merge(const MergeParams& p, int rows_h, int rows_b,
-                                cudaStream_t stream) {
+static cudaError_t launch_merge(const MergeParams& p, int groups, int seqs, cudaStream_t stream) {
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(rows_h, rows_b);
+    cfg.gridDim = dim3(groups, seqs);
     cfg.blockDim = dim3(kMergeThreads);
     cfg.dynamicSmemBytes = 0;
     cfg.stream = stream;
@@ -879,9 +903,10 @@ extern "C" pkv_status pkv_merge(void* out, const float* partial_o, const float* 
         return PKV_ERR_INVALID_ARG;
     if (num_seqs == 0) return PKV_OK;
     if (!out || !partial_o || !partial_lse) return PKV_ERR_INVALID_ARG;
-    if ((reinterpret_cast<uintptr_t>(out) & 1u) || (reinterpret_cast<uintptr_t>(partial_o) & 3u) ||
+    if ((reinterpret_cast<uintptr_t>(out) & 7u) || (reinterpret_cast<uintptr_t>(partial_o) & 15u) ||
         (reinterpret_cast<uintptr_t>(partial_lse) & 3u))
         return PKV_ERR_INVALID_ARG;
+    if (head_dim % 4 != 0 || head_dim > 4 * kMergeThreads) return PKV_ERR_UNSUPPORTED;
     if (num_seqs > 65535) return PKV_ERR_UNSUPPORTED;
     MergeParams mp;
     mp.out = out;
@@ -889,8 +914,8 @@ extern "C" pkv_status pkv_merge(void* out, const float* partial_o, const float* 
     mp.partial_lse = partial_lse;
     mp.context_lens = nullptr;
     mp.num_q_heads = num_q_heads;
-    mp.num_kv_heads = 1;
-    mp.group = num_q_heads;
+    mp.num_kv_heads = num_q_heads;
+    mp.group = 1;  // partition geometry is not used without context_lens
     mp.num_splits = num_splits;
     mp.head_dim = head_dim;
     mp.chunk_tokens = 1;
