@@ -215,6 +215,17 @@ pkv_status pkv_gather(void* k_out, void* v_out, const void* k_cache, const void*
  */
 pkv_status pkv_check_error(const int32_t* err_flag, void* stream, int32_t* flags_out);
 
+/*
+ * Self-test of the kernels' failure path (the pages have no counterpart):
+ * launches one warp that waits, with the same bounded-wait routine the decode
+ * kernel uses, on an mbarrier phase that nothing completes.  After limit_ns
+ * nanoseconds (1 .. 1e9) the wait gives up and PKV_EFLAG_TIMEOUT is OR-ed into
+ * *err_flag, so pkv_check_error then returns PKV_ERR_DEVICE_TIMEOUT and the
+ * context stays usable.  Asynchronous on `stream`.
+ */
+pkv_status pkv_selftest_wait_timeout(int32_t* err_flag, unsigned long long limit_ns,
+                                     void* stream);
+
 /* A static, human-readable name for a status. */
 const char* pkv_status_string(pkv_status status);
 

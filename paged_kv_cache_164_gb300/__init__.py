@@ -72,8 +72,9 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.pkv_status_string.argtypes = [i]
     lib.pkv_status_string.restype = ctypes.c_char_p
     lib.pkv_max_group_size.argtypes = []
+    lib.pkv_selftest_wait_timeout.argtypes = [p, ctypes.c_ulonglong, p]
     for name in ("pkv_append", "pkv_decode_attention", "pkv_decode_attention_noalloc",
-                 "pkv_merge", "pkv_gather",
+                 "pkv_merge", "pkv_gather", "pkv_selftest_wait_timeout",
                  "pkv_check_error", "pkv_max_group_size"):
         getattr(lib, name).restype = i
     _lib = lib
@@ -279,6 +280,13 @@ def check_error(err_flag: torch.Tensor, stream=None) -> int:
     if st not in (0, 5, 6):
         raise PkvError(st, "pkv_check_error")
     return int(word.value)
+
+
+def selftest_wait_timeout(err_flag: torch.Tensor, limit_ns: int = 20_000_000, stream=None) -> None:
+    """Runs the bounded-wait self-test kernel (see pkv.h); the flag then reads EFLAG_TIMEOUT."""
+    st = load().pkv_selftest_wait_timeout(_dev(err_flag, "err_flag", torch.int32), int(limit_ns),
+                                          _stream(stream, err_flag.device))
+    _check(st, "pkv_selftest_wait_timeout")
 
 
 def status_string(status: int) -> str:

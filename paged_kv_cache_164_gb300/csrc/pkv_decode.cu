@@ -119,13 +119,14 @@ __device__ __forceinline__ float2 unpack2(uint32_t x, __half) {
 // Bounded wait on an mbarrier phase.  Returns false (after raising the CTA's
 // abort flag and the device error bit on expiry) if the phase did not complete.
 __device__ __forceinline__ bool wait_phase(uint32_t bar, uint32_t parity, volatile int* abort_flag,
-                                           int32_t* err_flag) {
+                                           int32_t* err_flag,
+                                           uint64_t limit_ns = kWaitLimitNs) {
     if (ptx::mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = ptx::globaltimer();
     while (true) {
         if (ptx::mbar_try_wait(bar, parity)) return true;
         if (*abort_flag) return false;
-        if (ptx::globaltimer() - t0 > kWaitLimitNs) {
+        if (ptx::globaltimer() - t0 > limit_ns) {
             *abort_flag = 1;
             flag_error(err_flag, PKV_EFLAG_TIMEOUT);
             return false;
@@ -608,6 +609,22 @@ merge_kernel(const MergeParams p) {
     }
 }
 
+// Self-test of the bounded wait: one warp waits on a barrier phase that
+// nothing completes, so the wait must give up after limit_ns, raise
+// PKV_EFLAG_TIMEOUT and return.
+__global__ void __launch_bounds__(32) wait_timeout_selftest_kernel(int32_t* err_flag,
+                                                                   uint64_t limit_ns) {
+    __shared__ uint64_t bar;
+    __shared__ int abort_word;
+    if (threadIdx.x == 0) {
+        ptx::mbar_init(ptx::smem_addr(&bar), 1);
+        abort_word = 0;
+        ptx::fence_barrier_init();
+    }
+    __syncwarp();
+    wait_phase(ptx::smem_addr(&bar), 0, &abort_word, err_flag, limit_ns);
+}
+
 // ---------------------------------------------------------------------------
 // Host side: split planning, tensor maps, launches
 // ---------------------------------------------------------------------------
@@ -929,4 +946,12 @@ extern "C" pkv_status pkv_merge(void* out, const float* partial_o, const float* 
         return PKV_ERR_CUDA;
     }
     return PKV_OK;
+}
+
+extern "C" pkv_status pkv_selftest_wait_timeout(int32_t* err_flag, unsigned long long limit_ns,
+                                                void* stream) {
+    if (err_flag == nullptr || limit_ns == 0 || limit_ns > 1000000000ull)
+        return PKV_ERR_INVALID_ARG;
+    wait_timeout_selftest_kernel<<<1, 32, 0, (cudaStream_t)stream>>>(err_flag, limit_ns);
+    return cudaGetLastError() == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
 }

@@ -70,3 +70,19 @@ def test_workspace_too_small_is_rejected():
         pkv.decode_attention(w.q, w.k_cache, w.v_cache, w.block_tables, w.context_lens,
                              w.max_context_len, num_splits=2, workspace=small)
     assert e.value.status == 3
+
+
+def test_bounded_wait_expires_with_a_status_not_a_hang():
+    import time
+    flag = pkv.new_error_flag("cuda")
+    t0 = time.perf_counter()
+    pkv.selftest_wait_timeout(flag, limit_ns=20_000_000)
+    assert pkv.check_error(flag) == pkv.EFLAG_TIMEOUT
+    assert time.perf_counter() - t0 < 5.0
+    # the context is still usable afterwards
+    w = make_workload("c1", device="cuda")
+    expect, _, _ = oracle_after_append(w)
+    pkv.append(w.k_new, w.v_new, w.k_cache, w.v_cache, w.slot_mapping)
+    out = pkv.decode_attention(w.q, w.k_cache, w.v_cache, w.block_tables, w.context_lens,
+                               w.max_context_len, scale=w.scale)
+    assert_attention_close(out, expect, "after timeout self-test")
