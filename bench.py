@@ -302,20 +302,38 @@ def run_gpu(args):
     s = w.spec
     nbytes = step_bytes(w)
     mcl = w.max_context_len
+    # Workloads whose sequences share prefix blocks use the shared-prefix decode
+    # (each group's prefix read once for all members) unless told otherwise.
+    shared = s.shared_prefix_groups > 0 and args.prefix_sharing
     splits = pkv.decode_num_splits(s.num_seqs, s.num_q_heads, s.num_kv_heads, s.head_dim,
                                    s.block_size, mcl, args.splits)
-    ws_bytes = pkv.workspace_size(s.num_seqs, s.num_q_heads, s.num_kv_heads, s.head_dim,
-                                  s.block_size, mcl, args.splits)
+    if shared:
+        ws_bytes = pkv.prefix_shared_workspace_size(
+            s.num_seqs, s.num_q_heads, s.num_kv_heads, s.head_dim, s.block_size, mcl,
+            w.group_prefix_len.numel(), w.max_group_size, w.max_prefix_len)
+    else:
+        ws_bytes = pkv.workspace_size(s.num_seqs, s.num_q_heads, s.num_kv_heads, s.head_dim,
+                                      s.block_size, mcl, args.splits)
     workspace = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device=device)
     out = torch.empty_like(w.q)
     flag = pkv.new_error_flag(device)
-    launches_per_step = 2 + (1 if splits > 1 else 0)  # append, decode, merge when split
+    # append, decode, merge when split; the shared-prefix path adds its prefix kernel
+    launches_per_step = 4 if shared else 2 + (1 if splits > 1 else 0)
+
+    def decode_call(q, block_tables, context_lens):
+        if shared:
+            pkv.decode_attention_prefix_shared(
+                q, w.k_cache, w.v_cache, block_tables, context_lens, mcl, w.group_start,
+                w.group_prefix_len, w.max_group_size, w.max_prefix_len, scale=w.scale, out=out,
+                workspace=workspace, err_flag=flag)
+        else:
+            pkv.decode_attention(q, w.k_cache, w.v_cache, block_tables, context_lens, mcl,
+                                 scale=w.scale, num_splits=args.splits, out=out,
+                                 workspace=workspace, err_flag=flag)
 
     def step():
         pkv.append(w.k_new, w.v_new, w.k_cache, w.v_cache, w.slot_mapping, err_flag=flag)
-        pkv.decode_attention(w.q, w.k_cache, w.v_cache, w.block_tables, w.context_lens, mcl,
-                             scale=w.scale, num_splits=args.splits, out=out,
-                             workspace=workspace, err_flag=flag)
+        decode_call(w.q, w.block_tables, w.context_lens)
 
     for _ in range(args.warmup):
         step()
@@ -325,9 +343,7 @@ def run_gpu(args):
     stream = torch.cuda.current_stream(device)
 
     def decode_only():
-        pkv.decode_attention(w.q, w.k_cache, w.v_cache, w.block_tables, w.context_lens, mcl,
-                             scale=w.scale, num_splits=args.splits, out=out,
-                             workspace=workspace, err_flag=flag)
+        decode_call(w.q, w.block_tables, w.context_lens)
 
     # Timed region: K whole steps back to back (the library chains its kernels
     # with programmatic dependent launch, so no event sits between them).
@@ -381,10 +397,7 @@ def run_gpu(args):
             dev_in[k].copy_(t, non_blocking=True)
         pkv.append(dev_in["k_new"], dev_in["v_new"], w.k_cache, w.v_cache,
                    dev_in["slot_mapping"], err_flag=flag)
-        pkv.decode_attention(dev_in["q"], w.k_cache, w.v_cache, dev_in["block_tables"],
-                             dev_in["context_lens"], mcl, scale=w.scale,
-                             num_splits=args.splits, out=out, workspace=workspace,
-                             err_flag=flag)
+        decode_call(dev_in["q"], dev_in["block_tables"], dev_in["context_lens"])
         out_h.copy_(out, non_blocking=True)
 
     for _ in range(max(3, args.warmup // 2)):
@@ -433,6 +446,7 @@ def run_gpu(args):
                    "num_kv_heads": s.num_kv_heads, "head_dim": s.head_dim,
                    "block_size": s.block_size, "context_tokens": int(w.context_lens.sum()),
                    "max_context_len": mcl, "num_splits": splits, "accumulate": "fp32",
+                   "shared_prefix_decode": shared,
                    "kv_bytes_unique": nbytes["kv_unique"],
                    "decode_bytes_per_step": nbytes["decode"],
                    "decode_bytes_logical": nbytes["decode_logical"],
@@ -444,7 +458,8 @@ def run_gpu(args):
         "decode_ms": round(decode_ms, 5),
         "roofline": {"bound": "hbm", "achieved": round(decode_gbs, 2), "peak": peak,
                      "unit": "GB/s", "frac": round(decode_gbs / peak, 4),
-                     "traffic": traffic, "kernel": "decode_kernel + merge_kernel (one decode call, back to back)",
+                     "traffic": traffic, "kernel": ("prefix_kernel + decode_kernel + merge_kernel" if shared else
+                                "decode_kernel + merge_kernel") + " (one decode call, back to back)",
                      "peak_source": f"{peak_src} hbm_gbs"},
         "cpu_baseline": cpu,
         "e2e": {"value": round(bytes_all / (e2e_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
@@ -468,6 +483,8 @@ def main(argv=None):
     ap.add_argument("--splits", type=int, default=0, help="KV partitions (0 = automatic)")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", dest="cpu_baseline", action="store_false")
+    ap.add_argument("--no-prefix-sharing", dest="prefix_sharing", action="store_false",
+                    help="decode shared-prefix workloads with the plain path")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("at least 3 warm-up steps")

@@ -55,6 +55,8 @@ typedef enum { PKV_FP16 = 0, PKV_BF16 = 1 } pkv_dtype;
 #define PKV_EFLAG_CONTEXT_LEN   0x4  /* context_len > max_blocks_per_seq * block_size,
                                         > max_context_len, or negative */
 #define PKV_EFLAG_TIMEOUT       0x8  /* a bounded wait inside a kernel expired */
+#define PKV_EFLAG_GROUP         0x10 /* a shared-prefix group was malformed (its members were
+                                        decoded without the shared prefix) */
 
 #define PKV_MAX_SPLITS 1024           /* upper bound on split-K partitions per sequence */
 
@@ -171,6 +173,46 @@ pkv_status pkv_decode_attention_noalloc(void* out, const void* q, const void* k_
                                         int block_size, int num_q_heads, int num_kv_heads,
                                         int head_dim, float scale, int num_splits,
                                         pkv_dtype dtype, int32_t* err_flag, void* stream);
+
+/*
+ * Decode attention with shared prompt prefixes.
+ *
+ * Same result as pkv_decode_attention, for batches whose sequences share
+ * physical prefix blocks (Copy-on-Write sharing of a common prefix,
+ * [inference] "PagedAttention", Copy-on-Write; prefix trees, [chapter12]
+ * RadixAttention): sequences group_start[p] .. group_start[p+1]-1 form group
+ * p, and the first group_prefix_len[p] tokens of each member are the same
+ * blocks, listed in the block table of the group's first member.  Each group's
+ * prefix K/V is read once for all members' queries (the members' query rows
+ * stand in for a GQA group's heads on the tensor cores); the suffixes are
+ * decoded per sequence; the partials are merged by log-sum-exp.
+ *
+ *   group_start       int32 [num_groups + 1], device: 0 = group_start[0] <= ...
+ *                     <= group_start[num_groups] = num_seqs (a sequence that
+ *                     shares nothing is a group of one with prefix 0)
+ *   group_prefix_len  int32 [num_groups], device: a multiple of block_size,
+ *                     at most max_prefix_len and each member's context
+ *                     (members with a shorter context are masked correctly)
+ *   max_group_size, max_prefix_len  host-side bounds used to plan
+ *   workspace         at least pkv_prefix_shared_workspace_size(...) bytes;
+ *                     contents on entry do not matter
+ *   err_flag          nullable; also PKV_EFLAG_GROUP for a malformed group, whose
+ *                     members are then decoded without the shared prefix
+ *                     (still the correct result)
+ * The precondition that members' tables hold the group's prefix blocks is not
+ * checked: the prefix is read from the first member's table.
+ */
+size_t pkv_prefix_shared_workspace_size(int num_seqs, int num_q_heads, int num_kv_heads,
+                                        int head_dim, int block_size, int max_context_len,
+                                        int num_groups, int max_group_size, int max_prefix_len);
+
+pkv_status pkv_decode_attention_prefix_shared(
+    void* out, const void* q, const void* k_cache, const void* v_cache,
+    const int32_t* block_tables, int max_blocks_per_seq, const int32_t* context_lens,
+    int max_context_len, int num_seqs, int num_blocks, int block_size, int num_q_heads,
+    int num_kv_heads, int head_dim, float scale, int num_groups, const int32_t* group_start,
+    const int32_t* group_prefix_len, int max_group_size, int max_prefix_len, void* workspace,
+    size_t workspace_bytes, pkv_dtype dtype, int32_t* err_flag, void* stream);
 
 /*
  * Log-sum-exp merge of split-K partials ([inference] combine_result and the

@@ -32,7 +32,7 @@ PKV_OK = 0
 STATUS_NAMES = {0: "PKV_OK", 1: "PKV_ERR_INVALID_ARG", 2: "PKV_ERR_UNSUPPORTED",
                 3: "PKV_ERR_WORKSPACE", 4: "PKV_ERR_CUDA", 5: "PKV_ERR_DEVICE_INDEX",
                 6: "PKV_ERR_DEVICE_TIMEOUT"}
-EFLAG_BLOCK_ID, EFLAG_SLOT, EFLAG_CONTEXT_LEN, EFLAG_TIMEOUT = 0x1, 0x2, 0x4, 0x8
+EFLAG_BLOCK_ID, EFLAG_SLOT, EFLAG_CONTEXT_LEN, EFLAG_TIMEOUT, EFLAG_GROUP = 0x1, 0x2, 0x4, 0x8, 0x10
 MAX_SPLITS = 1024
 _DTYPES = {torch.float16: 0, torch.bfloat16: 1}
 SIZE_MAX = ctypes.c_size_t(-1).value
@@ -66,6 +66,10 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
                                          i, p, p]
     lib.pkv_decode_attention_noalloc.argtypes = [p, p, p, p, p, i, p, i, i, i, i, i, i, i, f,
                                                  i, i, p, p]
+    lib.pkv_prefix_shared_workspace_size.argtypes = [i, i, i, i, i, i, i, i, i]
+    lib.pkv_prefix_shared_workspace_size.restype = sz
+    lib.pkv_decode_attention_prefix_shared.argtypes = [p, p, p, p, p, i, p, i, i, i, i, i, i, i, f,
+                                                       i, p, p, i, i, p, sz, i, p, p]
     lib.pkv_merge.argtypes = [p, p, p, i, i, i, i, i, p]
     lib.pkv_gather.argtypes = [p, p, p, p, p, i, p, i, i, i, i, i, i, i, p, p]
     lib.pkv_check_error.argtypes = [p, p, ctypes.POINTER(ctypes.c_int32)]
@@ -74,6 +78,7 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.pkv_max_group_size.argtypes = []
     lib.pkv_selftest_wait_timeout.argtypes = [p, ctypes.c_ulonglong, p]
     for name in ("pkv_append", "pkv_decode_attention", "pkv_decode_attention_noalloc",
+                 "pkv_decode_attention_prefix_shared",
                  "pkv_merge", "pkv_gather", "pkv_selftest_wait_timeout",
                  "pkv_check_error", "pkv_max_group_size"):
         getattr(lib, name).restype = i
@@ -191,6 +196,64 @@ def decode_attention(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tens
         int(max_context_len), b, nb, bs, h_q, h_kv, d, float(scale), int(num_splits), ws_ptr,
         ws_bytes, _kv_dtype(k_cache), _opt(err_flag, "err_flag"), _stream(stream, q.device))
     _check(st, "pkv_decode_attention")
+    return out
+
+
+def prefix_shared_workspace_size(num_seqs: int, num_q_heads: int, num_kv_heads: int,
+                                 head_dim: int, block_size: int, max_context_len: int,
+                                 num_groups: int, max_group_size: int, max_prefix_len: int) -> int:
+    """Bytes of workspace ``decode_attention_prefix_shared`` needs on the current device."""
+    n = load().pkv_prefix_shared_workspace_size(num_seqs, num_q_heads, num_kv_heads, head_dim,
+                                                block_size, max_context_len, num_groups,
+                                                max_group_size, max_prefix_len)
+    if n == SIZE_MAX:
+        raise PkvError(1, "pkv_prefix_shared_workspace_size")
+    return int(n)
+
+
+def decode_attention_prefix_shared(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
+                                   block_tables: torch.Tensor, context_lens: torch.Tensor,
+                                   max_context_len: int, group_start: torch.Tensor,
+                                   group_prefix_len: torch.Tensor, max_group_size: int,
+                                   max_prefix_len: int, scale: Optional[float] = None,
+                                   out: Optional[torch.Tensor] = None,
+                                   workspace: Optional[torch.Tensor] = None,
+                                   err_flag: Optional[torch.Tensor] = None,
+                                   stream=None) -> torch.Tensor:
+    """``decode_attention`` for batches whose sequences share prompt-prefix blocks.
+
+    group_start int32 [G+1] and group_prefix_len int32 [G] (device) describe
+    contiguous groups of sequences whose first group_prefix_len[p] tokens are
+    the same physical blocks; each group's prefix is read once for all members.
+    """
+    lib = load()
+    b, h_q, d = q.shape
+    nb, bs, h_kv, d2 = k_cache.shape
+    ng = group_prefix_len.shape[0]
+    if d2 != d or v_cache.shape != k_cache.shape or block_tables.dim() != 2 or \
+            block_tables.shape[0] != b or context_lens.shape != (b,) or \
+            group_start.shape != (ng + 1,):
+        raise ValueError("inconsistent shared-prefix decode shapes")
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    dt = k_cache.dtype
+    if out is None:
+        out = torch.empty_like(q)
+    need = prefix_shared_workspace_size(b, h_q, h_kv, d, bs, max_context_len, ng, max_group_size,
+                                        max_prefix_len)
+    if workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    st = lib.pkv_decode_attention_prefix_shared(
+        _dev(out, "out", dt), _dev(q, "q", dt), _dev(k_cache, "k_cache", dt),
+        _dev(v_cache, "v_cache", dt), _dev(block_tables, "block_tables", torch.int32),
+        block_tables.shape[1], _dev(context_lens, "context_lens", torch.int32),
+        int(max_context_len), b, nb, bs, h_q, h_kv, d, float(scale), ng,
+        _dev(group_start, "group_start", torch.int32),
+        _dev(group_prefix_len, "group_prefix_len", torch.int32), int(max_group_size),
+        int(max_prefix_len), _dev(workspace, "workspace"),
+        workspace.numel() * workspace.element_size(), _kv_dtype(k_cache),
+        _opt(err_flag, "err_flag"), _stream(stream, q.device))
+    _check(st, "pkv_decode_attention_prefix_shared")
     return out
 
 

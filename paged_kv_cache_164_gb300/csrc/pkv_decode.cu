@@ -65,6 +65,9 @@ struct DecodeParams {
     const int32_t* context_lens;
     float* partial_o;    // [B][H_q][num_splits][D] when num_splits > 1
     float* partial_lse;  // [B][H_q][num_splits]
+    const int2* seq_info;  // nullable: per sequence (shared-prefix tokens, prefix partials written)
+    const int2* items;     // nullable: compact list of (unit b*H_kv+g, partition); CTA x takes item x
+    const int* item_count;
     int32_t* err_flag;
     int max_blocks_per_seq;
     int num_blocks;
@@ -101,6 +104,15 @@ __device__ __forceinline__ Partition partition_of(int n, int b, int g, int num_k
     return pt;
 }
 
+// Partitions of a sequence's suffix of `suffix` tokens.  Without a shared
+// prefix (slot0 == 0) an empty context still gets one partition, whose CTA
+// writes the zero row; after a prefix, an empty suffix has none.
+__device__ __forceinline__ int suffix_partitions(int suffix, int slot0, int b, int g,
+                                                 int num_kv_heads, int chunk, int stagger) {
+    if (slot0 > 0 && suffix == 0) return 0;
+    return partition_of(suffix, b, g, num_kv_heads, chunk, stagger).nsplit;
+}
+
 __device__ __forceinline__ uint32_t pack2(float lo, float hi, __nv_bfloat16) {
     __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
     return *reinterpret_cast<uint32_t*>(&v);
@@ -134,6 +146,135 @@ __device__ __forceinline__ bool wait_phase(uint32_t bar, uint32_t parity, volati
     }
 }
 
+// One 16-token stage of K and V, staged in shared memory (128-byte swizzled
+// rows of 64 dims, K then V), against the query columns held in `qb`:
+// S^T = K Q^T on the tensor cores, the base-2 online-softmax update of
+// (m, l, O^T), and O^T = alpha * O^T + V^T P^T.  Columns are query rows (the
+// heads of a GQA group, or rows of several sequences); `qb`, `o`, `m*`, `l*`
+// hold, per 8-column group nt, columns nt*8 + 2*(lane%4) and +1.  Token i
+// (0..15) of the stage takes part only when i < nvalid, and, with ROW_LIMITS,
+// only for the columns c with tok0 + i < lim[nt][c]; V rows of tokens at
+// i >= nvalid are zeroed in registers so unused slots never reach the output.
+template <typename T, int D, int NT, bool ROW_LIMITS>
+__device__ __forceinline__ void stage_update(uint32_t kbase, uint32_t vbase, int nvalid, int tok0,
+                                             const int (&lim)[NT][2],
+                                             const uint32_t (&qb)[NT][D / 16][2],
+                                             float (&o)[NT][D / 16][4], float (&m0)[NT],
+                                             float (&m1)[NT], float (&l0)[NT], float (&l1)[NT],
+                                             float scale_log2, int lane) {
+    constexpr int KSTEPS = D / 16;
+    constexpr int kRegionBytes = kStageTokens * 128;
+    const int gq = lane >> 2;
+    const int tq = lane & 3;
+    // ldmatrix row offsets (the swizzle XORs the 16-byte chunk index with the
+    // row index mod 8; rows here are tokens).
+    const int mi = lane >> 3;
+    const int r8 = lane & 7;
+    const int k_tok = (mi & 1) * 8 + r8;   // K: matrices (t0-7,c), (t8-15,c), (t0-7,c+1), (t8-15,c+1)
+    const int k_csel = mi >> 1;
+    const int v_tok = (mi >> 1) * 8 + r8;  // V: matrices (t0-7,c), (t0-7,c+1), (t8-15,c), (t8-15,c+1)
+    const int v_csel = mi & 1;
+
+    // S^T = K Q^T
+    float s[NT][4];
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+        for (int c = 0; c < 4; ++c) s[nt][c] = 0.f;
+#pragma unroll
+    for (int ks = 0; ks < KSTEPS; ++ks) {
+        const int chunk = ks * 2 + k_csel;
+        const uint32_t addr =
+            kbase + (chunk >> 3) * kRegionBytes + k_tok * 128 + (((chunk & 7) ^ r8) << 4);
+        uint32_t a[4];
+        ptx::ldmatrix_x4(a, addr);
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) ptx::mma_16816<T>(s[nt], a, qb[nt][ks][0], qb[nt][ks][1]);
+    }
+
+    // Online softmax in base 2.  s[nt][0]: (token gq, column 2tq), [1]: (gq, 2tq+1),
+    // [2]: (gq+8, 2tq), [3]: (gq+8, 2tq+1).
+    const bool lo_ok = gq < nvalid;
+    const bool hi_ok = gq + 8 < nvalid;
+    uint32_t pb_hi[NT][2], pb_lo[NT][2];
+    float alpha0[NT], alpha1[NT];
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+#pragma unroll
+        for (int c = 0; c < 4; ++c) s[nt][c] *= scale_log2;
+        if (!lo_ok) s[nt][0] = s[nt][1] = -INFINITY;
+        if (!hi_ok) s[nt][2] = s[nt][3] = -INFINITY;
+        if constexpr (ROW_LIMITS) {
+            if (tok0 + gq >= lim[nt][0]) s[nt][0] = -INFINITY;
+            if (tok0 + gq >= lim[nt][1]) s[nt][1] = -INFINITY;
+            if (tok0 + gq + 8 >= lim[nt][0]) s[nt][2] = -INFINITY;
+            if (tok0 + gq + 8 >= lim[nt][1]) s[nt][3] = -INFINITY;
+        }
+        float mx0 = fmaxf(s[nt][0], s[nt][2]);
+        float mx1 = fmaxf(s[nt][1], s[nt][3]);
+#pragma unroll
+        for (int off = 4; off < 32; off <<= 1) {
+            mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
+            mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
+        }
+        const float mn0 = fmaxf(m0[nt], mx0);
+        const float mn1 = fmaxf(m1[nt], mx1);
+        const float ref0 = mn0 == -INFINITY ? 0.f : mn0;
+        const float ref1 = mn1 == -INFINITY ? 0.f : mn1;
+        alpha0[nt] = exp2f(m0[nt] - ref0);
+        alpha1[nt] = exp2f(m1[nt] - ref1);
+        m0[nt] = mn0;
+        m1[nt] = mn1;
+        const float p0 = exp2f(s[nt][0] - ref0);
+        const float p1 = exp2f(s[nt][1] - ref1);
+        const float p2 = exp2f(s[nt][2] - ref0);
+        const float p3 = exp2f(s[nt][3] - ref1);
+        l0[nt] = l0[nt] * alpha0[nt] + (p0 + p2);
+        l1[nt] = l1[nt] * alpha1[nt] + (p1 + p3);
+        // P as hi + lo 16-bit terms, transposed into P^T operand fragments.
+        const uint32_t h01 = pack2(p0, p1, T());
+        const uint32_t h23 = pack2(p2, p3, T());
+        const float2 r01 = unpack2(h01, T());
+        const float2 r23 = unpack2(h23, T());
+        const uint32_t l01 = pack2(p0 - r01.x, p1 - r01.y, T());
+        const uint32_t l23 = pack2(p2 - r23.x, p3 - r23.y, T());
+        pb_hi[nt][0] = ptx::movmatrix_trans(h01);
+        pb_hi[nt][1] = ptx::movmatrix_trans(h23);
+        pb_lo[nt][0] = ptx::movmatrix_trans(l01);
+        pb_lo[nt][1] = ptx::movmatrix_trans(l23);
+    }
+
+    // O^T = alpha * O^T + V^T P^T
+    uint32_t vmask_lo = 0xffffffffu, vmask_hi = 0xffffffffu;
+    if (nvalid < kStageTokens) {
+        // A fragments of V^T hold tokens 2tq, 2tq+1 (a0, a1) and 2tq+8, 2tq+9 (a2, a3)
+        vmask_lo = (2 * tq < nvalid ? 0x0000ffffu : 0u) | (2 * tq + 1 < nvalid ? 0xffff0000u : 0u);
+        vmask_hi =
+            (2 * tq + 8 < nvalid ? 0x0000ffffu : 0u) | (2 * tq + 9 < nvalid ? 0xffff0000u : 0u);
+    }
+#pragma unroll
+    for (int mt = 0; mt < KSTEPS; ++mt) {
+        const int chunk = mt * 2 + v_csel;
+        const uint32_t addr =
+            vbase + (chunk >> 3) * kRegionBytes + v_tok * 128 + (((chunk & 7) ^ r8) << 4);
+        uint32_t a[4];
+        ptx::ldmatrix_x4_trans(a, addr);
+        a[0] &= vmask_lo;
+        a[1] &= vmask_lo;
+        a[2] &= vmask_hi;
+        a[3] &= vmask_hi;
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+            o[nt][mt][0] *= alpha0[nt];
+            o[nt][mt][1] *= alpha1[nt];
+            o[nt][mt][2] *= alpha0[nt];
+            o[nt][mt][3] *= alpha1[nt];
+            ptx::mma_16816<T>(o[nt][mt], a, pb_hi[nt][0], pb_hi[nt][1]);
+            ptx::mma_16816<T>(o[nt][mt], a, pb_lo[nt][0], pb_lo[nt][1]);
+        }
+    }
+}
+
 // NT = number of 8-head groups (1: G <= 8, 2: G <= 16).
 template <typename T, int D, int NT>
 __global__ void __launch_bounds__(kThreads, 3)
@@ -152,13 +293,6 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
     int* table = reinterpret_cast<int*>(empty_bar + S);
     volatile int* abort_flag = table + kMaxChunkPages + 1;
 
-    // Grid order (KV head fastest, then sequence, then partition): all first
-    // partitions run before any second one, so sequences that share physical
-    // blocks (a common prompt prefix) read them close together in time and the
-    // repeats hit in L2.
-    const int g = blockIdx.x;       // KV head
-    const int b = blockIdx.y;       // sequence
-    const int split = blockIdx.z;   // KV partition
     const int tid = threadIdx.x;
     const int warp = tid >> 5;
     const int lane = tid & 31;
@@ -170,12 +304,40 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
     // Inputs may come from the previous kernel on the stream (the append).
     ptx::grid_dependency_wait();
 
+    int g, b, split;
+    if (p.items != nullptr) {
+        // A compact work list built on the device: only partitions with tokens
+        // get a CTA; grid positions past the end of the list exit at once.
+        if ((int)blockIdx.x >= *p.item_count) return;
+        const int2 it = p.items[blockIdx.x];
+        g = it.x % p.num_kv_heads;
+        b = it.x / p.num_kv_heads;
+        split = it.y;
+    } else {
+        // Grid order (KV head fastest, then sequence, then partition): all first
+        // partitions run before any second one, so sequences that share physical
+        // blocks (a common prompt prefix) read them close together in time and
+        // the repeats hit in L2.
+        g = blockIdx.x;
+        b = blockIdx.y;
+        split = blockIdx.z;
+    }
+
     const int cap = min(p.max_blocks_per_seq * bs, p.max_context_len);
     const int n_raw = __ldg(p.context_lens + b);
+    // With a shared prefix (seq_info), the first `start` tokens were attended by
+    // the prefix kernel, which wrote this sequence's partials 0 .. slot0-1; the
+    // partitions here cover the suffix and write from partial slot0 on.
+    int start = 0, slot0 = 0;
+    if (p.seq_info != nullptr) {
+        const int2 si = __ldcg(p.seq_info + b);
+        start = si.x;
+        slot0 = si.y;
+    }
     // Partition start does not depend on the context length, so the producer
     // warp fetches the block-table slice at the same time as the length.
     const int shift = ((b * p.num_kv_heads + g) % 3) * p.stagger_tokens;
-    const int t_begin = max(0, split * p.chunk_tokens - shift);
+    const int t_begin = start + max(0, split * p.chunk_tokens - shift);
     const int page0 = t_begin / bs;
     const int max_pages = min(p.max_blocks_per_seq - page0, p.chunk_tokens / bs + 1);
     const int32_t* row = p.block_tables + (int64_t)b * p.max_blocks_per_seq + page0;
@@ -188,11 +350,13 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
     if ((n_raw < 0 || n_raw > cap) && split == 0 && g == 0 && tid == 0)
         flag_error(p.err_flag, PKV_EFLAG_CONTEXT_LEN);
     const int n = clamped_len(n_raw, cap);
-    const Partition pt = partition_of(n, b, g, p.num_kv_heads, p.chunk_tokens, p.stagger_tokens);
-    if (split >= pt.nsplit) return;
-    const int t_end = min(n, (split + 1) * p.chunk_tokens - shift);
+    const int suffix = max(0, n - start);
+    const int nsplit = suffix_partitions(suffix, slot0, b, g, p.num_kv_heads, p.chunk_tokens,
+                                         p.stagger_tokens);
+    if (split >= nsplit) return;
+    const int t_end = min(n, start + (split + 1) * p.chunk_tokens - shift);
     const int nstages = t_end > t_begin ? (t_end - t_begin + kStageTokens - 1) / kStageTokens : 0;
-    const int nsplit = pt.nsplit;
+    const bool direct = slot0 == 0 && nsplit == 1;  // the whole answer is this CTA's
 
     if (tid == 0) {
         for (int s = 0; s < S; ++s) {
@@ -296,14 +460,9 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
                 for (int c = 0; c < 4; ++c) o[nt][mt][c] = 0.f;
         }
 
-        // Per-lane ldmatrix row offsets (the 128-byte swizzle XORs the 16-byte
-        // chunk index with the row index mod 8; rows here are tokens).
-        const int mi = lane >> 3;
-        const int r8 = lane & 7;
-        const int k_tok = (mi & 1) * 8 + r8;    // K: matrices (t0-7,c), (t8-15,c), (t0-7,c+1), (t8-15,c+1)
-        const int k_csel = mi >> 1;
-        const int v_tok = (mi >> 1) * 8 + r8;   // V: matrices (t0-7,c), (t0-7,c+1), (t8-15,c), (t8-15,c+1)
-        const int v_csel = mi & 1;
+        int no_limit[NT][2];
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) no_limit[nt][0] = no_limit[nt][1] = INT_MAX;
 
         for (int i = warp; i < nstages; i += kConsumerWarps) {
             const int slot = i % S;
@@ -314,102 +473,8 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
             const int nvalid = blk >= 0 ? min(kStageTokens, t_end - tok0) : 0;
             if (nvalid > 0) {
                 const uint32_t kbase = ring_addr + slot * Cfg::kStageBytes;
-                const uint32_t vbase = kbase + Cfg::kHalfBytes;
-
-                // S^T = K Q^T
-                float s[NT][4];
-#pragma unroll
-                for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-                    for (int c = 0; c < 4; ++c) s[nt][c] = 0.f;
-#pragma unroll
-                for (int ks = 0; ks < KSTEPS; ++ks) {
-                    const int chunk = ks * 2 + k_csel;
-                    const uint32_t addr = kbase + (chunk >> 3) * Cfg::kRegionBytes + k_tok * 128 +
-                                          (((chunk & 7) ^ r8) << 4);
-                    uint32_t a[4];
-                    ptx::ldmatrix_x4(a, addr);
-#pragma unroll
-                    for (int nt = 0; nt < NT; ++nt)
-                        ptx::mma_16816<T>(s[nt], a, qb[nt][ks][0], qb[nt][ks][1]);
-                }
-
-                // Online softmax in base 2.  s[nt][0]: (token gq, head 2tq), [1]: (gq, 2tq+1),
-                // [2]: (gq+8, 2tq), [3]: (gq+8, 2tq+1).
-                const bool lo_ok = gq < nvalid;
-                const bool hi_ok = gq + 8 < nvalid;
-                uint32_t pb_hi[NT][2], pb_lo[NT][2];
-                float alpha0[NT], alpha1[NT];
-#pragma unroll
-                for (int nt = 0; nt < NT; ++nt) {
-#pragma unroll
-                    for (int c = 0; c < 4; ++c) s[nt][c] *= p.scale_log2;
-                    if (!lo_ok) s[nt][0] = s[nt][1] = -INFINITY;
-                    if (!hi_ok) s[nt][2] = s[nt][3] = -INFINITY;
-                    float mx0 = fmaxf(s[nt][0], s[nt][2]);
-                    float mx1 = fmaxf(s[nt][1], s[nt][3]);
-#pragma unroll
-                    for (int off = 4; off < 32; off <<= 1) {
-                        mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
-                        mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
-                    }
-                    const float mn0 = fmaxf(m0[nt], mx0);
-                    const float mn1 = fmaxf(m1[nt], mx1);
-                    const float ref0 = mn0 == -INFINITY ? 0.f : mn0;
-                    const float ref1 = mn1 == -INFINITY ? 0.f : mn1;
-                    alpha0[nt] = exp2f(m0[nt] - ref0);
-                    alpha1[nt] = exp2f(m1[nt] - ref1);
-                    m0[nt] = mn0;
-                    m1[nt] = mn1;
-                    const float p0 = exp2f(s[nt][0] - ref0);
-                    const float p1 = exp2f(s[nt][1] - ref1);
-                    const float p2 = exp2f(s[nt][2] - ref0);
-                    const float p3 = exp2f(s[nt][3] - ref1);
-                    l0[nt] = l0[nt] * alpha0[nt] + (p0 + p2);
-                    l1[nt] = l1[nt] * alpha1[nt] + (p1 + p3);
-                    // P as hi + lo 16-bit terms, transposed into P^T operand fragments.
-                    const uint32_t h01 = pack2(p0, p1, T());
-                    const uint32_t h23 = pack2(p2, p3, T());
-                    const float2 r01 = unpack2(h01, T());
-                    const float2 r23 = unpack2(h23, T());
-                    const uint32_t l01 = pack2(p0 - r01.x, p1 - r01.y, T());
-                    const uint32_t l23 = pack2(p2 - r23.x, p3 - r23.y, T());
-                    pb_hi[nt][0] = ptx::movmatrix_trans(h01);
-                    pb_hi[nt][1] = ptx::movmatrix_trans(h23);
-                    pb_lo[nt][0] = ptx::movmatrix_trans(l01);
-                    pb_lo[nt][1] = ptx::movmatrix_trans(l23);
-                }
-
-                // O^T = alpha * O^T + V^T P^T
-                uint32_t vmask_lo = 0xffffffffu, vmask_hi = 0xffffffffu;
-                if (nvalid < kStageTokens) {
-                    // A fragments of V^T hold tokens 2tq, 2tq+1 (a0, a1) and 2tq+8, 2tq+9 (a2, a3)
-                    vmask_lo = (2 * tq < nvalid ? 0x0000ffffu : 0u) |
-                               (2 * tq + 1 < nvalid ? 0xffff0000u : 0u);
-                    vmask_hi = (2 * tq + 8 < nvalid ? 0x0000ffffu : 0u) |
-                               (2 * tq + 9 < nvalid ? 0xffff0000u : 0u);
-                }
-#pragma unroll
-                for (int mt = 0; mt < KSTEPS; ++mt) {
-                    const int chunk = mt * 2 + v_csel;
-                    const uint32_t addr = vbase + (chunk >> 3) * Cfg::kRegionBytes + v_tok * 128 +
-                                          (((chunk & 7) ^ r8) << 4);
-                    uint32_t a[4];
-                    ptx::ldmatrix_x4_trans(a, addr);
-                    a[0] &= vmask_lo;
-                    a[1] &= vmask_lo;
-                    a[2] &= vmask_hi;
-                    a[3] &= vmask_hi;
-#pragma unroll
-                    for (int nt = 0; nt < NT; ++nt) {
-                        o[nt][mt][0] *= alpha0[nt];
-                        o[nt][mt][1] *= alpha1[nt];
-                        o[nt][mt][2] *= alpha0[nt];
-                        o[nt][mt][3] *= alpha1[nt];
-                        ptx::mma_16816<T>(o[nt][mt], a, pb_hi[nt][0], pb_hi[nt][1]);
-                        ptx::mma_16816<T>(o[nt][mt], a, pb_lo[nt][0], pb_lo[nt][1]);
-                    }
-                }
+                stage_update<T, D, NT, false>(kbase, kbase + Cfg::kHalfBytes, nvalid, 0, no_limit, qb,
+                                              o, m0, m1, l0, l1, p.scale_log2, lane);
             }
             __syncwarp();
             if (lane == 0) ptx::mbar_arrive(ptx::smem_addr(&empty_bar[slot]));
@@ -494,19 +559,383 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
                 acc.w = fmaf(v.w, f, acc.w);
             }
             const int hq = g * G + h;
-            if (nsplit == 1) {
+            if (direct) {
                 T* out = static_cast<T*>(p.out) + ((int64_t)b * p.num_q_heads + hq) * D + j;
                 uint2 packed;
                 packed.x = pack2(acc.x, acc.y, T());
                 packed.y = pack2(acc.z, acc.w, T());
                 *reinterpret_cast<uint2*>(out) = packed;
             } else {
-                const int64_t prow = ((int64_t)b * p.num_q_heads + hq) * p.num_splits + split;
+                const int64_t prow =
+                    ((int64_t)b * p.num_q_heads + hq) * p.num_splits + slot0 + split;
                 *reinterpret_cast<float4*>(p.partial_o + prow * D + j) = acc;
                 if (j == 0) p.partial_lse[prow] = sm_lse[h];
             }
         }
     }
+}
+
+// ---------------------------------------------------------------------------
+// Shared-prefix decode: the prefix kernel
+// ---------------------------------------------------------------------------
+// Sequences come in contiguous groups (group_start); the first prefix_len
+// tokens of every member of group p are the same physical blocks (a shared
+// prompt, [inference] Copy-on-Write; RadixAttention in [chapter12]).  Each
+// group's prefix K/V tiles are streamed once per (KV head, 64 query rows,
+// prefix partition) and applied to all members' queries at once: the query
+// rows of the members take the place of a GQA group's heads.  The suffixes
+// go through the decode kernel; the merge kernel combines everything.
+
+struct PrefixParams {
+    const void* q;
+    const int32_t* block_tables;
+    const int32_t* context_lens;
+    const int32_t* group_start;       // [num_groups + 1]
+    const int32_t* group_prefix_len;  // [num_groups]
+    float* partial_o;                 // [B][H_q][num_splits][D]
+    float* partial_lse;               // [B][H_q][num_splits]
+    int32_t* err_flag;
+    int max_blocks_per_seq;
+    int num_blocks;
+    int block_size;
+    int num_seqs;
+    int num_q_heads;
+    int num_kv_heads;
+    int group;            // query heads per KV head
+    int num_splits;       // partial slots per (sequence, query head)
+    int num_groups;
+    int max_group_size;
+    int max_prefix_len;
+    int prefix_chunk;     // prefix tokens per partition (a multiple of block_size)
+    int cap;              // context clamp
+    float scale_log2;
+};
+
+constexpr int kPrefixRows = kConsumerWarps * 16;  // query rows per prefix CTA
+
+// A group is used only when its bounds and prefix length are sane; otherwise
+// its members are decoded in full by the decode kernel (and the error flagged).
+__device__ __forceinline__ bool group_valid(const int32_t* group_start,
+                                            const int32_t* group_prefix_len, int grp, int num_seqs,
+                                            int max_group_size, int max_prefix_len, int block_size,
+                                            int max_blocks_per_seq, int& first, int& last,
+                                            int& plen) {
+    first = group_start[grp];
+    last = group_start[grp + 1];
+    plen = group_prefix_len[grp];
+    return first >= 0 && first <= last && last <= num_seqs && last - first <= max_group_size &&
+           plen >= 0 && plen <= max_prefix_len && plen % block_size == 0 &&
+           plen <= max_blocks_per_seq * block_size;
+}
+
+__device__ __forceinline__ bool prefix_group_valid(const PrefixParams& p, int grp, int& first,
+                                                   int& last, int& plen) {
+    return group_valid(p.group_start, p.group_prefix_len, grp, p.num_seqs, p.max_group_size,
+                       p.max_prefix_len, p.block_size, p.max_blocks_per_seq, first, last, plen);
+}
+
+template <typename T, int D>
+__global__ void __launch_bounds__(kThreads, 2)
+prefix_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
+              const PrefixParams p) {
+    constexpr int NT = 2;  // 16 query rows per consumer warp
+    using Cfg = Tile<D>;
+    constexpr int S = Cfg::kStages;
+    constexpr int KSTEPS = D / 16;
+
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                               ~uintptr_t(1023));
+    uint8_t* ring = smem;
+    uint64_t* full_bar = reinterpret_cast<uint64_t*>(ring + Cfg::kRingBytes);
+    uint64_t* empty_bar = full_bar + S;
+    int* table = reinterpret_cast<int*>(empty_bar + S);
+    volatile int* abort_flag = table + kMaxChunkPages + 1;
+
+    const int rb = blockIdx.x;                       // block of kPrefixRows query rows
+    const int g = blockIdx.y % p.num_kv_heads;       // KV head
+    const int grp = blockIdx.y / p.num_kv_heads;     // group
+    const int part = blockIdx.z;                     // prefix partition
+    const int tid = threadIdx.x;
+    const int warp = tid >> 5;
+    const int lane = tid & 31;
+    const int bs = p.block_size;
+
+    ptx::launch_dependents();
+    ptx::grid_dependency_wait();
+
+    if (grp >= p.num_groups) return;
+    int first, last, plen;
+    if (!prefix_group_valid(p, grp, first, last, plen)) return;
+    const int rows = (last - first) * p.group;
+    const int row0 = rb * kPrefixRows;
+    const int t_begin = part * p.prefix_chunk;
+    const int t_end = min(plen, t_begin + p.prefix_chunk);
+    if (row0 >= rows || t_begin >= t_end) return;
+    const int nstages = (t_end - t_begin + kStageTokens - 1) / kStageTokens;
+    const int page0 = t_begin / bs;
+
+    if (tid == 0) {
+        for (int st = 0; st < S; ++st) {
+            ptx::mbar_init(ptx::smem_addr(&full_bar[st]), 1);
+            ptx::mbar_init(ptx::smem_addr(&empty_bar[st]), kConsumerWarps);  // every warp reads every stage
+        }
+        *abort_flag = 0;
+        ptx::fence_barrier_init();
+    }
+    if (warp == kConsumerWarps) {
+        // The prefix blocks, from the group's first member's table.
+        const int npages = (t_end + bs - 1) / bs - page0;
+        const int32_t* trow = p.block_tables + (int64_t)first * p.max_blocks_per_seq + page0;
+        for (int i = lane; i < npages; i += 32) {
+            int blk = __ldg(trow + i);
+            if (blk < 0 || blk >= p.num_blocks) {
+                flag_error(p.err_flag, PKV_EFLAG_BLOCK_ID);
+                blk = -1;
+            }
+            table[i] = blk;
+        }
+        if (lane == 0) {
+            ptx::prefetch_tensormap(&tm_k);
+            ptx::prefetch_tensormap(&tm_v);
+        }
+    }
+    __syncthreads();
+    const uint32_t ring_addr = ptx::smem_addr(ring);
+
+    if (warp == kConsumerWarps) {
+        // ------------------------------------------------------------ producer
+        if (lane == 0) {
+            const uint64_t policy = ptx::l2_policy_evict_first();
+            int issued = 0;
+            for (int i = 0; i < nstages; ++i) {
+                const int slot = i % S;
+                if (i >= S && !wait_phase(ptx::smem_addr(&empty_bar[slot]), ((i / S) - 1) & 1,
+                                          abort_flag, p.err_flag))
+                    break;
+                const int tok0 = t_begin + i * kStageTokens;
+                const int blk = table[tok0 / bs - page0];
+                const uint32_t fb = ptx::smem_addr(&full_bar[slot]);
+                if (blk >= 0) {
+                    const uint32_t kdst = ring_addr + slot * Cfg::kStageBytes;
+                    ptx::mbar_arrive_expect_tx(fb, Cfg::kStageBytes);
+#pragma unroll
+                    for (int r = 0; r < Cfg::kRegions; ++r) {
+                        ptx::tma_load_4d(kdst + r * Cfg::kRegionBytes, &tm_k, fb, r * 64, g,
+                                         tok0 % bs, blk, policy);
+                        ptx::tma_load_4d(kdst + Cfg::kHalfBytes + r * Cfg::kRegionBytes, &tm_v, fb,
+                                         r * 64, g, tok0 % bs, blk, policy);
+                    }
+                } else {
+                    ptx::mbar_arrive(fb);
+                }
+                issued = i + 1;
+            }
+            if (*abort_flag) {
+                for (int i = max(0, issued - S); i < issued; ++i) {
+                    const uint32_t fb = ptx::smem_addr(&full_bar[i % S]);
+                    const uint64_t t0 = ptx::globaltimer();
+                    while (!ptx::mbar_try_wait(fb, (i / S) & 1) &&
+                           ptx::globaltimer() - t0 < kWaitLimitNs) {
+                    }
+                }
+            }
+        }
+    } else {
+        // ------------------------------------------------------------ consumers
+        const int gq = lane >> 2;
+        const int tq = lane & 3;
+        const int wrow = row0 + warp * 16;  // this warp's first row; column c of tile nt is row wrow + nt*8 + c
+        // Q^T operand fragments of this warp's 16 rows, and each column's context limit.
+        uint32_t qb[NT][KSTEPS][2];
+        int lim[NT][2];
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+            const int r = wrow + nt * 8 + gq;
+            const bool ok = r < rows;
+            const int seq = first + (ok ? r / p.group : 0);
+            const int head = g * p.group + (ok ? r % p.group : 0);
+            const uint32_t* qrow = reinterpret_cast<const uint32_t*>(
+                static_cast<const T*>(p.q) + ((int64_t)seq * p.num_q_heads + head) * D);
+#pragma unroll
+            for (int ks = 0; ks < KSTEPS; ++ks) {
+                qb[nt][ks][0] = ok ? __ldg(qrow + (ks * 16 + 2 * tq) / 2) : 0u;
+                qb[nt][ks][1] = ok ? __ldg(qrow + (ks * 16 + 8 + 2 * tq) / 2) : 0u;
+            }
+#pragma unroll
+            for (int c = 0; c < 2; ++c) {
+                const int rc = wrow + nt * 8 + 2 * tq + c;
+                lim[nt][c] = rc < rows
+                                 ? clamped_len(__ldg(p.context_lens + first + rc / p.group), p.cap)
+                                 : 0;
+            }
+        }
+        float o[NT][KSTEPS][4];
+        float m0[NT], m1[NT], l0[NT], l1[NT];
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+            m0[nt] = m1[nt] = -INFINITY;
+            l0[nt] = l1[nt] = 0.f;
+#pragma unroll
+            for (int mt = 0; mt < KSTEPS; ++mt)
+#pragma unroll
+                for (int c = 0; c < 4; ++c) o[nt][mt][c] = 0.f;
+        }
+        bool aborted = false;
+        for (int i = 0; i < nstages; ++i) {
+            const int slot = i % S;
+            if (!wait_phase(ptx::smem_addr(&full_bar[slot]), (i / S) & 1, abort_flag, p.err_flag)) {
+                aborted = true;
+                break;
+            }
+            const int tok0 = t_begin + i * kStageTokens;
+            const int blk = table[tok0 / bs - page0];
+            const int nvalid = blk >= 0 ? min(kStageTokens, t_end - tok0) : 0;
+            if (nvalid > 0 && wrow < rows) {
+                const uint32_t kbase = ring_addr + slot * Cfg::kStageBytes;
+                stage_update<T, D, NT, true>(kbase, kbase + Cfg::kHalfBytes, nvalid, tok0, lim, qb, o,
+                                             m0, m1, l0, l1, p.scale_log2, lane);
+            }
+            __syncwarp();
+            if (lane == 0) ptx::mbar_arrive(ptx::smem_addr(&empty_bar[slot]));
+        }
+        if (!aborted && wrow < rows) {
+            // This warp's rows are complete for this partition: normalise and store.
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt) {
+                float la = l0[nt], lb = l1[nt];
+#pragma unroll
+                for (int off = 4; off < 32; off <<= 1) {
+                    la += __shfl_xor_sync(0xffffffffu, la, off);
+                    lb += __shfl_xor_sync(0xffffffffu, lb, off);
+                }
+#pragma unroll
+                for (int c = 0; c < 2; ++c) {
+                    const int rc = wrow + nt * 8 + 2 * tq + c;
+                    if (rc >= rows) continue;
+                    const float l = c == 0 ? la : lb;
+                    const float m = c == 0 ? m0[nt] : m1[nt];
+                    const float inv = l > 0.f ? 1.f / l : 0.f;
+                    const int seq = first + rc / p.group;
+                    const int head = g * p.group + rc % p.group;
+                    const int64_t prow = ((int64_t)seq * p.num_q_heads + head) * p.num_splits + part;
+                    float* dst = p.partial_o + prow * D;
+#pragma unroll
+                    for (int mt = 0; mt < KSTEPS; ++mt) {
+                        dst[mt * 16 + gq] = o[nt][mt][c] * inv;
+                        dst[mt * 16 + gq + 8] = o[nt][mt][c + 2] * inv;
+                    }
+                    if (gq == 0) p.partial_lse[prow] = l > 0.f ? (m + log2f(l)) * kLn2 : -INFINITY;
+                }
+            }
+        }
+    }
+    __syncthreads();
+}
+
+// ---------------------------------------------------------------------------
+// Shared-prefix decode: the plan kernel
+// ---------------------------------------------------------------------------
+// One CTA writes, for every sequence, its (shared-prefix tokens, prefix
+// partials) record and the compact list of the suffix partitions that hold
+// tokens, unit by unit ((sequence, KV head) pairs, KV head fastest).  The
+// decode grid is sized for the longest sequence; with the list, only real
+// partitions get a CTA and the rest of the grid exits at once.
+
+struct PlanParams {
+    const int32_t* context_lens;
+    const int32_t* group_start;
+    const int32_t* group_prefix_len;
+    int2* seq_info;   // [B] out
+    int2* items;      // out: (unit, partition)
+    int* item_count;  // out
+    int32_t* err_flag;
+    int num_seqs;
+    int num_kv_heads;
+    int num_groups;
+    int max_group_size;
+    int max_prefix_len;
+    int block_size;
+    int max_blocks_per_seq;
+    int prefix_chunk;
+    int chunk_tokens;
+    int stagger_tokens;
+    int cap;
+};
+
+constexpr int kPlanThreads = 1024;
+
+__global__ void __launch_bounds__(kPlanThreads) plan_kernel(const PlanParams p) {
+    __shared__ int warp_sum[kPlanThreads / 32];
+    __shared__ int base;
+    const int tid = threadIdx.x;
+    const int lane = tid & 31;
+    const int warp = tid >> 5;
+    ptx::launch_dependents();
+    ptx::grid_dependency_wait();
+
+    // 1. per-sequence prefix records (a search of group_start)
+    for (int b = tid; b < p.num_seqs; b += kPlanThreads) {
+        int2 info = make_int2(0, 0);
+        if (p.num_groups > 0) {
+            int lo = 0, hi = p.num_groups - 1;  // last group with group_start <= b
+            while (lo < hi) {
+                const int mid = (lo + hi + 1) >> 1;
+                if (p.group_start[mid] <= b) lo = mid; else hi = mid - 1;
+            }
+            int first, last, plen;
+            if (group_valid(p.group_start, p.group_prefix_len, lo, p.num_seqs, p.max_group_size,
+                            p.max_prefix_len, p.block_size, p.max_blocks_per_seq, first, last,
+                            plen) &&
+                first <= b && b < last)
+                info = make_int2(plen, (plen + p.prefix_chunk - 1) / p.prefix_chunk);
+            else
+                flag_error(p.err_flag, PKV_EFLAG_GROUP);
+        }
+        p.seq_info[b] = info;
+    }
+    if (tid == 0) base = 0;
+    __syncthreads();
+
+    // 2. the suffix partitions with tokens, unit by unit (block-wide scans)
+    const int units = p.num_seqs * p.num_kv_heads;
+    for (int u0 = 0; u0 < units; u0 += kPlanThreads) {
+        const int u = u0 + tid;
+        int cnt = 0;
+        if (u < units) {
+            const int b = u / p.num_kv_heads;
+            const int g = u - b * p.num_kv_heads;
+            const int2 info = p.seq_info[b];
+            const int n = clamped_len(p.context_lens[b], p.cap);
+            cnt = suffix_partitions(max(0, n - info.x), info.y, b, g, p.num_kv_heads,
+                                    p.chunk_tokens, p.stagger_tokens);
+        }
+        int incl = cnt;  // inclusive warp scan
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            const int v = __shfl_up_sync(0xffffffffu, incl, off);
+            if (lane >= off) incl += v;
+        }
+        if (lane == 31) warp_sum[warp] = incl;
+        __syncthreads();
+        if (warp == 0) {
+            const int w = warp_sum[lane];
+            int wi = w;
+#pragma unroll
+            for (int off = 1; off < 32; off <<= 1) {
+                const int v = __shfl_up_sync(0xffffffffu, wi, off);
+                if (lane >= off) wi += v;
+            }
+            warp_sum[lane] = wi - w;  // exclusive prefix of the warp totals
+        }
+        __syncthreads();
+        const int pos = base + warp_sum[warp] + incl - cnt;
+        for (int j = 0; j < cnt; ++j) p.items[pos + j] = make_int2(u, j);
+        __syncthreads();
+        if (tid == kPlanThreads - 1) base = pos + cnt;
+        __syncthreads();
+    }
+    if (tid == 0) *p.item_count = base;
 }
 
 // Merge of split partials (log-sum-exp rule): one CTA per (query head,
@@ -521,6 +950,7 @@ struct MergeParams {
     const float* partial_o;
     const float* partial_lse;
     const int32_t* context_lens;  // nullable
+    const int2* seq_info;         // nullable: shared-prefix tokens and prefix partials per sequence
     int num_q_heads;
     int num_kv_heads;
     int group;                    // query heads per KV head
@@ -545,10 +975,16 @@ merge_kernel(const MergeParams p) {
     ptx::grid_dependency_wait();
     int ns = p.num_splits;
     if (p.context_lens != nullptr) {
+        int start = 0, slot0 = 0;
+        if (p.seq_info != nullptr) {
+            const int2 si = __ldcg(p.seq_info + b);
+            start = si.x;
+            slot0 = si.y;
+        }
         const int n = clamped_len(__ldg(p.context_lens + b), p.cap);
-        ns = partition_of(n, b, h / p.group, p.num_kv_heads, p.chunk_tokens, p.stagger_tokens)
-                 .nsplit;
-        if (ns <= 1) return;
+        ns = slot0 + suffix_partitions(max(0, n - start), slot0, b, h / p.group, p.num_kv_heads,
+                                       p.chunk_tokens, p.stagger_tokens);
+        if (slot0 == 0 && ns <= 1) return;  // written directly by the decode kernel
     }
     const int64_t row = (int64_t)b * p.num_q_heads + h;
     const float* lse = p.partial_lse + row * p.num_splits;
@@ -798,6 +1234,75 @@ static cudaError_t launch_merge(const MergeParams& p, int groups, int seqs, cuda
     return cudaLaunchKernelEx(&cfg, merge_kernel<T>, p);
 }
 
+template <typename T, int D>
+static cudaError_t launch_prefix_t(const CUtensorMap& mk, const CUtensorMap& mv,
+                                   const PrefixParams& p, dim3 grid, cudaStream_t stream) {
+    auto kern = prefix_kernel<T, D>;
+    static std::once_flag once;
+    static cudaError_t attr_err = cudaSuccess;
+    std::call_once(once, [&] {
+        attr_err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                        Tile<D>::kSmemBytes);
+    });
+    if (attr_err != cudaSuccess) return attr_err;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = Tile<D>::kSmemBytes;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, mk, mv, p);
+}
+
+// Plan of a shared-prefix call: prefix partitions sized so the prefix kernel
+// fills about three waves of resident CTAs, the suffixes planned like a plain
+// decode, and per (sequence, query head) the prefix partials first, then the
+// suffix partials.
+struct PrefixPlan {
+    Plan suffix;
+    int prefix_chunk;
+    int prefix_parts;
+    int total_splits;
+    int row_blocks;
+    size_t workspace_bytes;
+};
+
+static pkv_status make_prefix_plan(int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
+                                   int block_size, int max_context_len, int num_groups,
+                                   int max_group_size, int max_prefix_len, PrefixPlan* pp) {
+    if (num_groups < 0 || max_group_size < 0 || max_prefix_len < 0) return PKV_ERR_INVALID_ARG;
+    pkv_status st = make_plan(num_seqs, num_q_heads, num_kv_heads, head_dim, block_size,
+                              max_context_len, 0, &pp->suffix);
+    if (st != PKV_OK) return st;
+    const int group = num_q_heads / num_kv_heads;
+    const int64_t rows = (int64_t)max_group_size * group;
+    pp->row_blocks = (int)std::max<int64_t>(1, (rows + kPrefixRows - 1) / kPrefixRows);
+    if ((int64_t)num_groups * num_kv_heads > 65535 || pp->row_blocks > 65535)
+        return PKV_ERR_UNSUPPORTED;
+    const int sms = current_sm_count();
+    if (sms <= 0) return PKV_ERR_CUDA;
+    const int64_t units = std::max<int64_t>(1, (int64_t)num_groups * num_kv_heads * pp->row_blocks);
+    const int64_t want = std::max<int64_t>(1, (3LL * 3 * sms + units - 1) / units);
+    const int prefix_pages = (max_prefix_len + block_size - 1) / block_size;
+    int cp = (int)((prefix_pages + want - 1) / want);
+    cp = std::min(std::max(cp, std::max(1, 256 / block_size)), kMaxChunkPages);
+    pp->prefix_chunk = cp * block_size;
+    pp->prefix_parts = max_prefix_len > 0 ? (max_prefix_len + pp->prefix_chunk - 1) / pp->prefix_chunk
+                                          : 0;
+    pp->total_splits = pp->prefix_parts + pp->suffix.num_splits;
+    if (pp->total_splits > PKV_MAX_SPLITS) return PKV_ERR_UNSUPPORTED;
+    const size_t partial_floats = (size_t)num_seqs * num_q_heads * pp->total_splits * (head_dim + 1);
+    const size_t items = (size_t)num_seqs * num_kv_heads * pp->suffix.num_splits;
+    // partials | per-sequence records | work list | its length
+    pp->workspace_bytes = ((partial_floats * sizeof(float) + 15) & ~size_t(15)) +
+                          (size_t)num_seqs * sizeof(int2) + items * sizeof(int2) + 16 + 256;
+    return PKV_OK;
+}
+
 }  // namespace pkv
 
 using namespace pkv;
@@ -876,6 +1381,9 @@ extern "C" pkv_status pkv_decode_attention(void* out, const void* q, const void*
     p.scale_log2 = scale * kLog2e;
     p.partial_o = nullptr;
     p.partial_lse = nullptr;
+    p.seq_info = nullptr;
+    p.items = nullptr;
+    p.item_count = nullptr;
     if (plan.num_splits > 1) {
         p.partial_o = static_cast<float*>(workspace);
         p.partial_lse = p.partial_o + (size_t)num_seqs * num_q_heads * plan.num_splits * head_dim;
@@ -894,6 +1402,7 @@ extern "C" pkv_status pkv_decode_attention(void* out, const void* q, const void*
         mp.partial_o = p.partial_o;
         mp.partial_lse = p.partial_lse;
         mp.context_lens = context_lens;
+        mp.seq_info = nullptr;
         mp.num_q_heads = num_q_heads;
         mp.num_kv_heads = num_kv_heads;
         mp.group = num_q_heads / num_kv_heads;
@@ -930,6 +1439,7 @@ extern "C" pkv_status pkv_merge(void* out, const float* partial_o, const float* 
     mp.partial_o = partial_o;
     mp.partial_lse = partial_lse;
     mp.context_lens = nullptr;
+    mp.seq_info = nullptr;
     mp.num_q_heads = num_q_heads;
     mp.num_kv_heads = num_q_heads;
     mp.group = 1;  // partition geometry is not used without context_lens
@@ -954,4 +1464,192 @@ extern "C" pkv_status pkv_selftest_wait_timeout(int32_t* err_flag, unsigned long
         return PKV_ERR_INVALID_ARG;
     wait_timeout_selftest_kernel<<<1, 32, 0, (cudaStream_t)stream>>>(err_flag, limit_ns);
     return cudaGetLastError() == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
+}
+
+extern "C" size_t pkv_prefix_shared_workspace_size(int num_seqs, int num_q_heads, int num_kv_heads,
+                                                   int head_dim, int block_size,
+                                                   int max_context_len, int num_groups,
+                                                   int max_group_size, int max_prefix_len) {
+    PrefixPlan pp;
+    if (make_prefix_plan(num_seqs, num_q_heads, num_kv_heads, head_dim, block_size,
+                         max_context_len, num_groups, max_group_size, max_prefix_len,
+                         &pp) != PKV_OK)
+        return SIZE_MAX;
+    return pp.workspace_bytes;
+}
+
+extern "C" pkv_status pkv_decode_attention_prefix_shared(
+    void* out, const void* q, const void* k_cache, const void* v_cache,
+    const int32_t* block_tables, int max_blocks_per_seq, const int32_t* context_lens,
+    int max_context_len, int num_seqs, int num_blocks, int block_size, int num_q_heads,
+    int num_kv_heads, int head_dim, float scale, int num_groups, const int32_t* group_start,
+    const int32_t* group_prefix_len, int max_group_size, int max_prefix_len, void* workspace,
+    size_t workspace_bytes, pkv_dtype dtype, int32_t* err_flag, void* stream) {
+    pkv_status st = check_shapes(num_seqs, num_q_heads, num_kv_heads, head_dim, block_size,
+                                 max_context_len, 0);
+    if (st != PKV_OK) return st;
+    if ((dtype != PKV_FP16 && dtype != PKV_BF16) || max_blocks_per_seq <= 0 || num_blocks <= 0 ||
+        !std::isfinite(scale) || num_groups < 0 || max_group_size < 0 || max_prefix_len < 0)
+        return PKV_ERR_INVALID_ARG;
+    if (num_seqs == 0) return PKV_OK;
+    if (!out || !q || !k_cache || !v_cache || !block_tables || !context_lens || !workspace ||
+        (num_groups > 0 && (!group_start || !group_prefix_len)))
+        return PKV_ERR_INVALID_ARG;
+    if (!aligned16(out) || !aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) ||
+        !aligned16(workspace) || (reinterpret_cast<uintptr_t>(block_tables) & 3u) ||
+        (reinterpret_cast<uintptr_t>(context_lens) & 3u) ||
+        (reinterpret_cast<uintptr_t>(group_start) & 3u) ||
+        (reinterpret_cast<uintptr_t>(group_prefix_len) & 3u))
+        return PKV_ERR_INVALID_ARG;
+    if ((int64_t)max_blocks_per_seq * block_size > INT_MAX) return PKV_ERR_UNSUPPORTED;
+    PrefixPlan pp;
+    st = make_prefix_plan(num_seqs, num_q_heads, num_kv_heads, head_dim, block_size,
+                          max_context_len, num_groups, max_group_size, max_prefix_len, &pp);
+    if (st != PKV_OK) return st;
+    if (workspace_bytes < pp.workspace_bytes) return PKV_ERR_WORKSPACE;
+
+    CUtensorMap mk, mv;
+    if (!make_cache_map(&mk, k_cache, dtype, num_blocks, block_size, num_kv_heads, head_dim) ||
+        !make_cache_map(&mv, v_cache, dtype, num_blocks, block_size, num_kv_heads, head_dim))
+        return PKV_ERR_CUDA;
+
+    float* partial_o = static_cast<float*>(workspace);
+    float* partial_lse = partial_o + (size_t)num_seqs * num_q_heads * pp.total_splits * head_dim;
+    const size_t partial_floats = (size_t)num_seqs * num_q_heads * pp.total_splits * (head_dim + 1);
+    int2* seq_info = reinterpret_cast<int2*>(static_cast<char*>(workspace) +
+                                             ((partial_floats * sizeof(float) + 15) & ~size_t(15)));
+    const int64_t num_items = (int64_t)num_seqs * num_kv_heads * pp.suffix.num_splits;
+    int2* items = seq_info + num_seqs;
+    int* item_count = reinterpret_cast<int*>(items + num_items);
+    const int cap = std::min(max_blocks_per_seq * block_size, max_context_len);
+    cudaStream_t s = (cudaStream_t)stream;
+
+    // 1. every sequence's prefix record and the list of suffix partitions with tokens
+    PlanParams pl;
+    pl.context_lens = context_lens;
+    pl.group_start = group_start;
+    pl.group_prefix_len = group_prefix_len;
+    pl.seq_info = seq_info;
+    pl.items = items;
+    pl.item_count = item_count;
+    pl.err_flag = err_flag;
+    pl.num_seqs = num_seqs;
+    pl.num_kv_heads = num_kv_heads;
+    pl.num_groups = num_groups;
+    pl.max_group_size = max_group_size;
+    pl.max_prefix_len = max_prefix_len;
+    pl.block_size = block_size;
+    pl.max_blocks_per_seq = max_blocks_per_seq;
+    pl.prefix_chunk = pp.prefix_chunk;
+    pl.chunk_tokens = pp.suffix.chunk_tokens;
+    pl.stagger_tokens = pp.suffix.stagger_tokens;
+    pl.cap = cap;
+    {
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(1);
+        cfg.blockDim = dim3(kPlanThreads);
+        cfg.stream = s;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        if (cudaLaunchKernelEx(&cfg, plan_kernel, pl) != cudaSuccess) {
+            cudaGetLastError();
+            return PKV_ERR_CUDA;
+        }
+    }
+
+    // 2. prefix partials of every group
+    PrefixParams pr;
+    pr.q = q;
+    pr.block_tables = block_tables;
+    pr.context_lens = context_lens;
+    pr.group_start = group_start;
+    pr.group_prefix_len = group_prefix_len;
+    pr.partial_o = partial_o;
+    pr.partial_lse = partial_lse;
+    pr.err_flag = err_flag;
+    pr.max_blocks_per_seq = max_blocks_per_seq;
+    pr.num_blocks = num_blocks;
+    pr.block_size = block_size;
+    pr.num_seqs = num_seqs;
+    pr.num_q_heads = num_q_heads;
+    pr.num_kv_heads = num_kv_heads;
+    pr.group = num_q_heads / num_kv_heads;
+    pr.num_splits = pp.total_splits;
+    pr.num_groups = num_groups;
+    pr.max_group_size = max_group_size;
+    pr.max_prefix_len = max_prefix_len;
+    pr.prefix_chunk = pp.prefix_chunk;
+    pr.cap = cap;
+    pr.scale_log2 = scale * kLog2e;
+    if (pr.group > 16) return PKV_ERR_UNSUPPORTED;
+    const dim3 pgrid(pp.row_blocks, std::max(1, num_groups * num_kv_heads),
+                     std::max(1, pp.prefix_parts));
+    cudaError_t e;
+    if (head_dim == 64)
+        e = dtype == PKV_FP16 ? launch_prefix_t<__half, 64>(mk, mv, pr, pgrid, s)
+                              : launch_prefix_t<__nv_bfloat16, 64>(mk, mv, pr, pgrid, s);
+    else
+        e = dtype == PKV_FP16 ? launch_prefix_t<__half, 128>(mk, mv, pr, pgrid, s)
+                              : launch_prefix_t<__nv_bfloat16, 128>(mk, mv, pr, pgrid, s);
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return PKV_ERR_CUDA;
+    }
+
+    // 3. suffix partials (or the whole answer for sequences without a prefix)
+    DecodeParams p;
+    p.out = out;
+    p.q = q;
+    p.block_tables = block_tables;
+    p.context_lens = context_lens;
+    p.partial_o = partial_o;
+    p.partial_lse = partial_lse;
+    p.seq_info = seq_info;
+    p.items = items;
+    p.item_count = item_count;
+    p.err_flag = err_flag;
+    p.max_blocks_per_seq = max_blocks_per_seq;
+    p.num_blocks = num_blocks;
+    p.block_size = block_size;
+    p.num_q_heads = num_q_heads;
+    p.group = num_q_heads / num_kv_heads;
+    p.num_splits = pp.total_splits;
+    p.chunk_tokens = pp.suffix.chunk_tokens;
+    p.stagger_tokens = pp.suffix.stagger_tokens;
+    p.num_kv_heads = num_kv_heads;
+    p.max_context_len = max_context_len;
+    p.scale_log2 = scale * kLog2e;
+    const dim3 grid((unsigned)num_items);
+    e = dtype == PKV_FP16 ? launch_decode<__half>(mk, mv, p, head_dim, grid, s)
+                          : launch_decode<__nv_bfloat16>(mk, mv, p, head_dim, grid, s);
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return PKV_ERR_CUDA;
+    }
+
+    // 4. merge
+    MergeParams mp;
+    mp.out = out;
+    mp.partial_o = partial_o;
+    mp.partial_lse = partial_lse;
+    mp.context_lens = context_lens;
+    mp.seq_info = seq_info;
+    mp.num_q_heads = num_q_heads;
+    mp.num_kv_heads = num_kv_heads;
+    mp.group = num_q_heads / num_kv_heads;
+    mp.num_splits = pp.total_splits;
+    mp.head_dim = head_dim;
+    mp.chunk_tokens = pp.suffix.chunk_tokens;
+    mp.stagger_tokens = pp.suffix.stagger_tokens;
+    mp.cap = cap;
+    e = dtype == PKV_FP16 ? launch_merge<__half>(mp, num_q_heads, num_seqs, s)
+                          : launch_merge<__nv_bfloat16>(mp, num_q_heads, num_seqs, s);
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return PKV_ERR_CUDA;
+    }
+    return PKV_OK;
 }

@@ -98,7 +98,19 @@ class Workload:
     k_cache: Optional[torch.Tensor]  # [num_blocks, bs, H_kv, d], state before the append
     v_cache: Optional[torch.Tensor]
     shared_blocks: int = 0          # physical blocks referenced by more than one sequence
+    # contiguous groups sharing prefix blocks: group_start int32 [G+1],
+    # group_prefix_len int32 [G] (a sequence sharing nothing is a group of one)
+    group_start: Optional[torch.Tensor] = None
+    group_prefix_len: Optional[torch.Tensor] = None
     extra: dict = field(default_factory=dict)
+
+    @property
+    def max_group_size(self) -> int:
+        return int((self.group_start[1:] - self.group_start[:-1]).max()) if self.group_start is not None else 1
+
+    @property
+    def max_prefix_len(self) -> int:
+        return int(self.group_prefix_len.max()) if self.group_prefix_len is not None else 0
 
     @property
     def torch_dtype(self) -> torch.dtype:
@@ -216,12 +228,20 @@ def make_workload(name_or_spec, device="cpu", poison: bool = False, with_values:
     dev = torch.device(device)
     scale = spec.scale if spec.scale is not None else 1.0 / math.sqrt(spec.head_dim)
     shared = groups * prefix_pages
+    if groups:
+        per = b // groups
+        gstart = torch.arange(0, b + 1, per, dtype=torch.int32)
+        gplen = torch.full((groups,), prefix_pages * bs, dtype=torch.int32)
+    else:
+        gstart = torch.arange(0, b + 1, dtype=torch.int32)
+        gplen = torch.zeros(b, dtype=torch.int32)
+    gstart, gplen = gstart.to(dev), gplen.to(dev)
     if not with_values:
         return Workload(spec=spec, scale=scale, num_blocks=num_blocks,
                         context_lens=lens.to(torch.int32).to(dev),
                         block_tables=tables.to(dev), slot_mapping=slot.to(dev), q=None,
                         k_new=None, v_new=None, k_cache=None, v_cache=None,
-                        shared_blocks=shared)
+                        shared_blocks=shared, group_start=gstart, group_prefix_len=gplen)
     vg = torch.Generator(device=dev).manual_seed(spec.seed * 7919 + 17)
     h_kv, h_q, d = spec.num_kv_heads, spec.num_q_heads, spec.head_dim
     q = _values((b, h_q, d), tdt, dev, vg)
@@ -244,7 +264,8 @@ def make_workload(name_or_spec, device="cpu", poison: bool = False, with_values:
     return Workload(spec=spec, scale=scale, num_blocks=num_blocks,
                     context_lens=lens.to(torch.int32).to(dev), block_tables=tables.to(dev),
                     slot_mapping=slot.to(dev), q=q, k_new=k_new, v_new=v_new,
-                    k_cache=k_cache, v_cache=v_cache, shared_blocks=shared)
+                    k_cache=k_cache, v_cache=v_cache, shared_blocks=shared,
+                    group_start=gstart, group_prefix_len=gplen)
 
 
 def make_append_case(num_tokens: int, num_blocks: int, block_size: int, num_kv_heads: int,
