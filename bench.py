@@ -305,12 +305,14 @@ def run_gpu(args):
     # Workloads whose sequences share prefix blocks use the shared-prefix decode
     # (each group's prefix read once for all members) unless told otherwise.
     shared = s.shared_prefix_groups > 0 and args.prefix_sharing
+    # Host-side bounds of the group metadata, read once (each read syncs the device).
+    max_group_size, max_prefix_len = w.max_group_size, w.max_prefix_len
     splits = pkv.decode_num_splits(s.num_seqs, s.num_q_heads, s.num_kv_heads, s.head_dim,
                                    s.block_size, mcl, args.splits)
     if shared:
         ws_bytes = pkv.prefix_shared_workspace_size(
             s.num_seqs, s.num_q_heads, s.num_kv_heads, s.head_dim, s.block_size, mcl,
-            w.group_prefix_len.numel(), w.max_group_size, w.max_prefix_len)
+            w.group_prefix_len.numel(), max_group_size, max_prefix_len)
     else:
         ws_bytes = pkv.workspace_size(s.num_seqs, s.num_q_heads, s.num_kv_heads, s.head_dim,
                                       s.block_size, mcl, args.splits)
@@ -324,7 +326,7 @@ def run_gpu(args):
         if shared:
             pkv.decode_attention_prefix_shared(
                 q, w.k_cache, w.v_cache, block_tables, context_lens, mcl, w.group_start,
-                w.group_prefix_len, w.max_group_size, w.max_prefix_len, scale=w.scale, out=out,
+                w.group_prefix_len, max_group_size, max_prefix_len, scale=w.scale, out=out,
                 workspace=workspace, err_flag=flag)
         else:
             pkv.decode_attention(q, w.k_cache, w.v_cache, block_tables, context_lens, mcl,
