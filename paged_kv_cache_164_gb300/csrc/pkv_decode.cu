@@ -576,15 +576,28 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
 }
 
 // ---------------------------------------------------------------------------
-// Shared-prefix decode: the prefix kernel
+// Shared-prefix decode: the prefix kernel (5th-generation tensor cores)
 // ---------------------------------------------------------------------------
 // Sequences come in contiguous groups (group_start); the first prefix_len
 // tokens of every member of group p are the same physical blocks (a shared
-// prompt, [inference] Copy-on-Write; RadixAttention in [chapter12]).  Each
-// group's prefix K/V tiles are streamed once per (KV head, 64 query rows,
-// prefix partition) and applied to all members' queries at once: the query
-// rows of the members take the place of a GQA group's heads.  The suffixes
-// go through the decode kernel; the merge kernel combines everything.
+// prompt, [inference] Copy-on-Write; RadixAttention in [chapter12]).  For one
+// (group, KV head) the members' query rows form a dense matrix Q [rows x D]
+// (row r is query head g*group + r % group of sequence first + r / group) that
+// meets every prefix token once: softmax(Q K^T * scale) V over the prefix is a
+// real contraction, so it runs on tcgen05.  One CTA takes 128 query rows and
+// one prefix partition, in tiles of 64 tokens:
+//   S = Q K^T        tcgen05.mma M=128, N=64, 16-dim steps; S in tensor memory
+//   softmax          one thread per query row, reading its row of S directly
+//   O += P V         M=128, N=D, 16-token steps; P enters as hi + lo 16-bit
+//                    terms (as in the decode kernel); O stays in tensor memory
+// Warp 4 streams K/V tiles by TMA into a 3-stage ring, warp 5 owns the tensor
+// memory and one of its lanes issues the MMAs, warps 0-3 run the softmax and
+// write the rows' normalised O and log-sum-exp as their prefix partials.  S is
+// double-buffered, so S of the next tile is computed during this tile's
+// softmax.  A row's reference max is raised (and its O rescaled in tensor
+// memory) only when the running max exceeds it by more than 2^8; P stays
+// below 256 and the final normalisation uses the same reference, so the
+// result is the same softmax.
 
 struct PrefixParams {
     const void* q;
@@ -606,12 +619,47 @@ struct PrefixParams {
     int num_groups;
     int max_group_size;
     int max_prefix_len;
-    int prefix_chunk;     // prefix tokens per partition (a multiple of block_size)
+    int prefix_chunk;     // prefix tokens per partition (a multiple of 64 and of block_size)
     int cap;              // context clamp
     float scale_log2;
 };
 
-constexpr int kPrefixRows = kConsumerWarps * 16;  // query rows per prefix CTA
+constexpr int kPrefixTileRows = 128;     // query rows per CTA (MMA M)
+constexpr int kPrefixTileTokens = 64;    // tokens per tile (N of S, K of O)
+constexpr int kPrefixStages = 3;
+constexpr int kPrefixSoftmaxWarps = 4;   // one thread per query row
+constexpr int kPrefixThreads = (kPrefixSoftmaxWarps + 2) * 32;
+constexpr int kPrefixTmaWarp = kPrefixSoftmaxWarps;
+constexpr int kPrefixMmaWarp = kPrefixSoftmaxWarps + 1;
+constexpr float kRescaleLog2 = 8.f;      // P values stay below 2^8 between rescales
+
+template <int D>
+struct PrefixTile {
+    static constexpr int kRegions = D / 64;                            // 128-byte column blocks
+    static constexpr int kQRegionBytes = kPrefixTileRows * 128;
+    static constexpr int kQBytes = kRegions * kQRegionBytes;
+    static constexpr int kKVRegionBytes = kPrefixTileTokens * 128;     // 64 tokens x 64 dims
+    static constexpr int kHalfBytes = kRegions * kKVRegionBytes;       // K (or V) of one tile
+    static constexpr int kStageBytes = 2 * kHalfBytes;
+    static constexpr int kPBytes = kPrefixTileRows * kPrefixTileTokens * 2;  // P hi (or lo)
+    // full[stages], empty[stages], s_full[2], p_ready, o_done, q_ready, drain
+    static constexpr int kBarriers = 2 * kPrefixStages + 6;
+    static constexpr int kSmemBytes = 1024 + kQBytes + kPrefixStages * kStageBytes + 2 * kPBytes +
+                                      kBarriers * 8 + (kMaxChunkPages + 1) * 4 + 64;
+    static constexpr uint32_t kTmemCols = 256;  // S0, S1 (64 columns each), O (D columns)
+    static constexpr uint32_t kColO = 2 * kPrefixTileTokens;
+    static_assert(kColO + D <= kTmemCols, "tensor memory layout");
+};
+
+// Instruction descriptor of tcgen05.mma kind::f16: fp32 accumulator, A and B
+// of one 16-bit type (0 = fp16, 1 = bf16), A K-major, B K-major or MN-major.
+__host__ __device__ constexpr uint32_t mma_idesc(uint32_t fmt, int m, int n, bool b_mn_major) {
+    return (1u << 4) | (fmt << 7) | (fmt << 10) | ((b_mn_major ? 1u : 0u) << 16) |
+           ((uint32_t)(n >> 3) << 17) | ((uint32_t)(m >> 4) << 24);
+}
+template <typename T> struct F16Format;
+template <> struct F16Format<__half> { static constexpr uint32_t value = 0; };
+template <> struct F16Format<__nv_bfloat16> { static constexpr uint32_t value = 1; };
 
 // A group is used only when its bounds and prefix length are sane; otherwise
 // its members are decoded in full by the decode kernel (and the error flagged).
@@ -634,28 +682,48 @@ __device__ __forceinline__ bool prefix_group_valid(const PrefixParams& p, int gr
                        p.max_prefix_len, p.block_size, p.max_blocks_per_seq, first, last, plen);
 }
 
+// A bounded wait whose outcome is the same for the whole warp (a lane that
+// gives up raises the CTA's abort flag; the warp then leaves together, so
+// warp-collective tensor-memory instructions never run on part of a warp).
+__device__ __forceinline__ bool warp_wait_phase(uint32_t bar, uint32_t parity,
+                                                volatile int* abort_flag, int32_t* err_flag) {
+    const bool ok = wait_phase(bar, parity, abort_flag, err_flag);
+    return __all_sync(0xffffffffu, ok);
+}
+
 template <typename T, int D>
-__global__ void __launch_bounds__(kThreads, 2)
+__global__ void __launch_bounds__(kPrefixThreads, 1)
 prefix_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
               const PrefixParams p) {
-    constexpr int NT = 2;  // 16 query rows per consumer warp
-    using Cfg = Tile<D>;
-    constexpr int S = Cfg::kStages;
+    using Cfg = PrefixTile<D>;
+    constexpr int NS = kPrefixStages;
+    constexpr int R = Cfg::kRegions;
     constexpr int KSTEPS = D / 16;
+    constexpr int TT = kPrefixTileTokens;
 
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                ~uintptr_t(1023));
-    uint8_t* ring = smem;
-    uint64_t* full_bar = reinterpret_cast<uint64_t*>(ring + Cfg::kRingBytes);
-    uint64_t* empty_bar = full_bar + S;
-    int* table = reinterpret_cast<int*>(empty_bar + S);
+    uint8_t* sq = smem;                          // Q: [region][128 rows][128 B], swizzled
+    uint8_t* ring = sq + Cfg::kQBytes;           // stages of K [region][64][128 B], then V
+    uint8_t* sp = ring + NS * Cfg::kStageBytes;  // P hi, then P lo: [128 rows][128 B], swizzled
+    uint64_t* bars = reinterpret_cast<uint64_t*>(sp + 2 * Cfg::kPBytes);
+    uint64_t* full_bar = bars;
+    uint64_t* empty_bar = bars + NS;
+    uint64_t* s_full = bars + 2 * NS;  // [2]
+    uint64_t* p_ready = s_full + 2;
+    uint64_t* o_done = p_ready + 1;
+    uint64_t* q_ready = o_done + 1;
+    uint64_t* drain = q_ready + 1;
+    int* table = reinterpret_cast<int*>(bars + Cfg::kBarriers);
     volatile int* abort_flag = table + kMaxChunkPages + 1;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(table + kMaxChunkPages + 2);
+    int* warp_lim = table + kMaxChunkPages + 3;  // [kPrefixSoftmaxWarps]
 
-    const int rb = blockIdx.x;                       // block of kPrefixRows query rows
-    const int g = blockIdx.y % p.num_kv_heads;       // KV head
-    const int grp = blockIdx.y / p.num_kv_heads;     // group
-    const int part = blockIdx.z;                     // prefix partition
+    const int rt = blockIdx.x;                     // tile of 128 query rows
+    const int g = blockIdx.y % p.num_kv_heads;     // KV head
+    const int grp = blockIdx.y / p.num_kv_heads;   // group
+    const int part = blockIdx.z;                   // prefix partition
     const int tid = threadIdx.x;
     const int warp = tid >> 5;
     const int lane = tid & 31;
@@ -668,24 +736,41 @@ prefix_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
     int first, last, plen;
     if (!prefix_group_valid(p, grp, first, last, plen)) return;
     const int rows = (last - first) * p.group;
-    const int row0 = rb * kPrefixRows;
+    const int row0 = rt * kPrefixTileRows;
     const int t_begin = part * p.prefix_chunk;
-    const int t_end = min(plen, t_begin + p.prefix_chunk);
-    if (row0 >= rows || t_begin >= t_end) return;
-    const int nstages = (t_end - t_begin + kStageTokens - 1) / kStageTokens;
+    const int t_chunk_end = min(plen, t_begin + p.prefix_chunk);
+    if (row0 >= rows || t_begin >= t_chunk_end) return;
     const int page0 = t_begin / bs;
 
+    // This thread's query row (softmax warps) and its context limit.
+    const int r = row0 + tid;
+    const bool row_ok = warp < kPrefixSoftmaxWarps && r < rows;
+    const int seq = first + (row_ok ? r / p.group : 0);
+    const int head = g * p.group + (row_ok ? r % p.group : 0);
+    const int lim = row_ok ? clamped_len(__ldg(p.context_lens + seq), p.cap) : 0;
+
     if (tid == 0) {
-        for (int st = 0; st < S; ++st) {
+        for (int st = 0; st < NS; ++st) {
             ptx::mbar_init(ptx::smem_addr(&full_bar[st]), 1);
-            ptx::mbar_init(ptx::smem_addr(&empty_bar[st]), kConsumerWarps);  // every warp reads every stage
+            ptx::mbar_init(ptx::smem_addr(&empty_bar[st]), 1);
         }
+        ptx::mbar_init(ptx::smem_addr(&s_full[0]), 1);
+        ptx::mbar_init(ptx::smem_addr(&s_full[1]), 1);
+        ptx::mbar_init(ptx::smem_addr(p_ready), kPrefixSoftmaxWarps * 32);
+        ptx::mbar_init(ptx::smem_addr(o_done), 1);
+        ptx::mbar_init(ptx::smem_addr(q_ready), kPrefixSoftmaxWarps * 32);
+        ptx::mbar_init(ptx::smem_addr(drain), 1);
         *abort_flag = 0;
         ptx::fence_barrier_init();
     }
-    if (warp == kConsumerWarps) {
-        // The prefix blocks, from the group's first member's table.
-        const int npages = (t_end + bs - 1) / bs - page0;
+    if (warp < kPrefixSoftmaxWarps) {
+        int m = lim;
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) m = max(m, __shfl_xor_sync(0xffffffffu, m, off));
+        if (lane == 0) warp_lim[warp] = m;
+    } else if (warp == kPrefixTmaWarp) {
+        // The partition's slice of the block table (from the first member's row).
+        const int npages = (t_chunk_end + bs - 1) / bs - page0;
         const int32_t* trow = p.block_tables + (int64_t)first * p.max_blocks_per_seq + page0;
         for (int i = lane; i < npages; i += 32) {
             int blk = __ldg(trow + i);
@@ -699,138 +784,290 @@ prefix_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
             ptx::prefetch_tensormap(&tm_k);
             ptx::prefetch_tensormap(&tm_v);
         }
+    } else {
+        ptx::tmem_alloc(ptx::smem_addr(tmem_slot), Cfg::kTmemCols);
+        ptx::tmem_relinquish_alloc_permit();
     }
+    ptx::tc_fence_before_sync();
     __syncthreads();
+    ptx::tc_fence_after_sync();
+    const uint32_t tmem = *tmem_slot;
+    // Tokens past every row's context take no part for any row of this CTA: not read.
+    int max_lim = 0;
+#pragma unroll
+    for (int w = 0; w < kPrefixSoftmaxWarps; ++w) max_lim = max(max_lim, warp_lim[w]);
+    const int t_end = min(t_chunk_end, max(t_begin, max_lim));
+    const int ntiles = (t_end - t_begin + TT - 1) / TT;
     const uint32_t ring_addr = ptx::smem_addr(ring);
+    const uint32_t q_addr = ptx::smem_addr(sq);
+    const uint32_t p_addr = ptx::smem_addr(sp);
 
-    if (warp == kConsumerWarps) {
+    if (warp == kPrefixTmaWarp) {
         // ------------------------------------------------------------ producer
         if (lane == 0) {
-            const uint64_t policy = ptx::l2_policy_evict_first();
+            const uint64_t policy = ptx::l2_policy_evict_last();  // other row tiles read it too
             int issued = 0;
-            for (int i = 0; i < nstages; ++i) {
-                const int slot = i % S;
-                if (i >= S && !wait_phase(ptx::smem_addr(&empty_bar[slot]), ((i / S) - 1) & 1,
-                                          abort_flag, p.err_flag))
+            for (int j = 0; j < ntiles; ++j) {
+                const int slot = j % NS;
+                if (j >= NS && !wait_phase(ptx::smem_addr(&empty_bar[slot]), ((j / NS) - 1) & 1,
+                                           abort_flag, p.err_flag))
                     break;
-                const int tok0 = t_begin + i * kStageTokens;
-                const int blk = table[tok0 / bs - page0];
+                const uint32_t kdst = ring_addr + slot * Cfg::kStageBytes;
                 const uint32_t fb = ptx::smem_addr(&full_bar[slot]);
-                if (blk >= 0) {
-                    const uint32_t kdst = ring_addr + slot * Cfg::kStageBytes;
-                    ptx::mbar_arrive_expect_tx(fb, Cfg::kStageBytes);
+                uint32_t bytes = 0;
 #pragma unroll
-                    for (int r = 0; r < Cfg::kRegions; ++r) {
-                        ptx::tma_load_4d(kdst + r * Cfg::kRegionBytes, &tm_k, fb, r * 64, g,
-                                         tok0 % bs, blk, policy);
-                        ptx::tma_load_4d(kdst + Cfg::kHalfBytes + r * Cfg::kRegionBytes, &tm_v, fb,
-                                         r * 64, g, tok0 % bs, blk, policy);
-                    }
-                } else {
-                    ptx::mbar_arrive(fb);
+                for (int bx = 0; bx < TT / kStageTokens; ++bx) {
+                    const int tok0 = t_begin + j * TT + bx * kStageTokens;
+                    if (tok0 < t_end && table[tok0 / bs - page0] >= 0)
+                        bytes += 2 * R * kStageTokens * 128;
                 }
-                issued = i + 1;
+                if (bytes == 0) {
+                    ptx::mbar_arrive(fb);  // nothing to load: every token of the tile is masked
+                } else {
+                    ptx::mbar_arrive_expect_tx(fb, bytes);
+#pragma unroll
+                    for (int bx = 0; bx < TT / kStageTokens; ++bx) {
+                        const int tok0 = t_begin + j * TT + bx * kStageTokens;
+                        if (tok0 >= t_end) continue;
+                        const int blk = table[tok0 / bs - page0];
+                        if (blk < 0) continue;
+#pragma unroll
+                        for (int rr = 0; rr < R; ++rr) {
+                            const uint32_t off = rr * Cfg::kKVRegionBytes + bx * kStageTokens * 128;
+                            ptx::tma_load_4d(kdst + off, &tm_k, fb, rr * 64, g, tok0 % bs, blk,
+                                             policy);
+                            ptx::tma_load_4d(kdst + Cfg::kHalfBytes + off, &tm_v, fb, rr * 64, g,
+                                             tok0 % bs, blk, policy);
+                        }
+                    }
+                }
+                issued = j + 1;
             }
             if (*abort_flag) {
-                for (int i = max(0, issued - S); i < issued; ++i) {
-                    const uint32_t fb = ptx::smem_addr(&full_bar[i % S]);
+                for (int j = max(0, issued - NS); j < issued; ++j) {
+                    const uint32_t fb = ptx::smem_addr(&full_bar[j % NS]);
                     const uint64_t t0 = ptx::globaltimer();
-                    while (!ptx::mbar_try_wait(fb, (i / S) & 1) &&
+                    while (!ptx::mbar_try_wait(fb, (j / NS) & 1) &&
                            ptx::globaltimer() - t0 < kWaitLimitNs) {
                     }
                 }
             }
         }
-    } else {
-        // ------------------------------------------------------------ consumers
-        const int gq = lane >> 2;
-        const int tq = lane & 3;
-        const int wrow = row0 + warp * 16;  // this warp's first row; column c of tile nt is row wrow + nt*8 + c
-        // Q^T operand fragments of this warp's 16 rows, and each column's context limit.
-        uint32_t qb[NT][KSTEPS][2];
-        int lim[NT][2];
+    } else if (warp == kPrefixMmaWarp) {
+        // ------------------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            constexpr uint32_t fmt = F16Format<T>::value;
+            constexpr uint32_t idesc_s = mma_idesc(fmt, kPrefixTileRows, TT, false);
+            constexpr uint32_t idesc_o = mma_idesc(fmt, kPrefixTileRows, D, true);
+            bool ok = wait_phase(ptx::smem_addr(q_ready), 0, abort_flag, p.err_flag);
+            if (ok) ptx::tc_fence_after_sync();
+            // S(j) = Q K(j)^T into S buffer j % 2
+            auto issue_s = [&](int j) -> bool {
+                const int slot = j % NS;
+                if (!wait_phase(ptx::smem_addr(&full_bar[slot]), (j / NS) & 1, abort_flag,
+                                p.err_flag))
+                    return false;
+                ptx::tc_fence_after_sync();
+                const uint32_t kb = ring_addr + slot * Cfg::kStageBytes;
 #pragma unroll
-        for (int nt = 0; nt < NT; ++nt) {
-            const int r = wrow + nt * 8 + gq;
-            const bool ok = r < rows;
-            const int seq = first + (ok ? r / p.group : 0);
-            const int head = g * p.group + (ok ? r % p.group : 0);
-            const uint32_t* qrow = reinterpret_cast<const uint32_t*>(
+                for (int ks = 0; ks < KSTEPS; ++ks) {
+                    const uint32_t koff = (ks / 4) * Cfg::kQRegionBytes + (ks % 4) * 32;
+                    const uint64_t a = ptx::smem_desc_sw128(q_addr + koff, 16, 1024);
+                    const uint64_t b = ptx::smem_desc_sw128(
+                        kb + (ks / 4) * Cfg::kKVRegionBytes + (ks % 4) * 32, 16, 1024);
+                    ptx::tc_mma_f16(tmem + (j % 2) * TT, a, b, idesc_s, ks > 0 ? 1u : 0u);
+                }
+                ptx::tc_commit(ptx::smem_addr(&s_full[j % 2]));
+                return true;
+            };
+            for (int j = 0; j < 2 && j < ntiles && ok; ++j) ok = issue_s(j);
+            for (int j = 0; j < ntiles && ok; ++j) {
+                // O += P(j) V(j) once the softmax has written P(j)
+                if (!wait_phase(ptx::smem_addr(p_ready), j & 1, abort_flag, p.err_flag)) {
+                    ok = false;
+                    break;
+                }
+                ptx::tc_fence_after_sync();
+                const uint32_t vb = ring_addr + (j % NS) * Cfg::kStageBytes + Cfg::kHalfBytes;
+#pragma unroll
+                for (int kt = 0; kt < TT / 16; ++kt) {
+                    const uint64_t b = ptx::smem_desc_sw128(vb + kt * 16 * 128, Cfg::kKVRegionBytes, 1024);
+                    const uint64_t a_hi = ptx::smem_desc_sw128(p_addr + kt * 32, 16, 1024);
+                    const uint64_t a_lo = ptx::smem_desc_sw128(p_addr + Cfg::kPBytes + kt * 32, 16, 1024);
+                    ptx::tc_mma_f16(tmem + Cfg::kColO, a_hi, b, idesc_o, (j > 0 || kt > 0) ? 1u : 0u);
+                    ptx::tc_mma_f16(tmem + Cfg::kColO, a_lo, b, idesc_o, 1u);
+                }
+                ptx::tc_commit(ptx::smem_addr(o_done));
+                ptx::tc_commit(ptx::smem_addr(&empty_bar[j % NS]));
+                if (j + 2 < ntiles) ok = issue_s(j + 2);
+            }
+            // every MMA has completed before the tensor memory is released
+            ptx::tc_commit(ptx::smem_addr(drain));
+            const uint64_t t0 = ptx::globaltimer();
+            while (!ptx::mbar_try_wait(ptx::smem_addr(drain), 0) &&
+                   ptx::globaltimer() - t0 < kWaitLimitNs) {
+            }
+        }
+    } else {
+        // ------------------------------------------------------------ softmax rows
+        // This row of Q into shared memory (16-byte chunk c of a 128-byte row
+        // lands at chunk c ^ (row % 8): the 128-byte swizzle of the MMA operand).
+        {
+            const uint4* src = reinterpret_cast<const uint4*>(
                 static_cast<const T*>(p.q) + ((int64_t)seq * p.num_q_heads + head) * D);
 #pragma unroll
-            for (int ks = 0; ks < KSTEPS; ++ks) {
-                qb[nt][ks][0] = ok ? __ldg(qrow + (ks * 16 + 2 * tq) / 2) : 0u;
-                qb[nt][ks][1] = ok ? __ldg(qrow + (ks * 16 + 8 + 2 * tq) / 2) : 0u;
+            for (int c = 0; c < D / 8; ++c) {
+                const uint4 v = row_ok ? __ldg(src + c) : make_uint4(0u, 0u, 0u, 0u);
+                *reinterpret_cast<uint4*>(sq + (c / 8) * Cfg::kQRegionBytes + tid * 128 +
+                                          (((c % 8) ^ (tid & 7)) << 4)) = v;
             }
-#pragma unroll
-            for (int c = 0; c < 2; ++c) {
-                const int rc = wrow + nt * 8 + 2 * tq + c;
-                lim[nt][c] = rc < rows
-                                 ? clamped_len(__ldg(p.context_lens + first + rc / p.group), p.cap)
-                                 : 0;
-            }
+            ptx::fence_proxy_async_smem();
+            ptx::mbar_arrive(ptx::smem_addr(q_ready));
         }
-        float o[NT][KSTEPS][4];
-        float m0[NT], m1[NT], l0[NT], l1[NT];
-#pragma unroll
-        for (int nt = 0; nt < NT; ++nt) {
-            m0[nt] = m1[nt] = -INFINITY;
-            l0[nt] = l1[nt] = 0.f;
-#pragma unroll
-            for (int mt = 0; mt < KSTEPS; ++mt)
-#pragma unroll
-                for (int c = 0; c < 4; ++c) o[nt][mt][c] = 0.f;
-        }
-        bool aborted = false;
-        for (int i = 0; i < nstages; ++i) {
-            const int slot = i % S;
-            if (!wait_phase(ptx::smem_addr(&full_bar[slot]), (i / S) & 1, abort_flag, p.err_flag)) {
-                aborted = true;
+        const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
+        float m_ref = -INFINITY;  // reference max of this row's P (log2 domain)
+        float l = 0.f;
+        bool ok = true;
+        for (int j = 0; j < ntiles; ++j) {
+            if (!warp_wait_phase(ptx::smem_addr(&s_full[j % 2]), (j / 2) & 1, abort_flag,
+                                 p.err_flag)) {
+                ok = false;
                 break;
             }
-            const int tok0 = t_begin + i * kStageTokens;
-            const int blk = table[tok0 / bs - page0];
-            const int nvalid = blk >= 0 ? min(kStageTokens, t_end - tok0) : 0;
-            if (nvalid > 0 && wrow < rows) {
-                const uint32_t kbase = ring_addr + slot * Cfg::kStageBytes;
-                stage_update<T, D, NT, true>(kbase, kbase + Cfg::kHalfBytes, nvalid, tok0, lim, qb, o,
-                                             m0, m1, l0, l1, p.scale_log2, lane);
+            ptx::tc_fence_after_sync();
+            uint32_t sv[TT];
+            ptx::tmem_ld32(tmem + lane_base + (j % 2) * TT, *reinterpret_cast<uint32_t(*)[32]>(sv));
+            ptx::tmem_ld32(tmem + lane_base + (j % 2) * TT + 32,
+                           *reinterpret_cast<uint32_t(*)[32]>(sv + 32));
+            const int tile0 = t_begin + j * TT;
+            // Tokens of this row: present (a valid block, before t_end) and within its context.
+            int nvalid[TT / kStageTokens];
+#pragma unroll
+            for (int bx = 0; bx < TT / kStageTokens; ++bx) {
+                const int tok0 = tile0 + bx * kStageTokens;
+                nvalid[bx] = (tok0 < t_end && table[tok0 / bs - page0] >= 0)
+                                 ? min(kStageTokens, t_end - tok0)
+                                 : 0;
             }
-            __syncwarp();
-            if (lane == 0) ptx::mbar_arrive(ptx::smem_addr(&empty_bar[slot]));
+            float mx = -INFINITY;
+#pragma unroll
+            for (int i = 0; i < TT; ++i) {
+                const bool valid = (i % kStageTokens) < nvalid[i / kStageTokens] && tile0 + i < lim;
+                const float sc = valid ? __uint_as_float(sv[i]) * p.scale_log2 : -INFINITY;
+                sv[i] = __float_as_uint(sc);
+                mx = fmaxf(mx, sc);
+            }
+            float alpha = 1.f;
+            bool rescale = false;
+            if (m_ref == -INFINITY) {
+                m_ref = mx;  // O and l are still zero for this row
+            } else if (mx > m_ref + kRescaleLog2) {
+                alpha = exp2f(m_ref - mx);
+                m_ref = mx;
+                rescale = true;
+            }
+            const float ref = m_ref == -INFINITY ? 0.f : m_ref;
+            float rowsum = 0.f;
+#pragma unroll
+            for (int i = 0; i < TT; ++i) {
+                const float pv = exp2f(__uint_as_float(sv[i]) - ref);
+                rowsum += pv;
+                sv[i] = __float_as_uint(pv);
+            }
+            l = l * alpha + rowsum;
+            // P and O are free once the previous tile's O += P V has completed.
+            if (j > 0 && !warp_wait_phase(ptx::smem_addr(o_done), (j - 1) & 1, abort_flag,
+                                          p.err_flag)) {
+                ok = false;
+                break;
+            }
+            ptx::tc_fence_after_sync();
+            if (__any_sync(0xffffffffu, rescale)) {
+#pragma unroll
+                for (int c = 0; c < D / 32; ++c) {
+                    uint32_t ov[32];
+                    const uint32_t ta = tmem + lane_base + Cfg::kColO + c * 32;
+                    ptx::tmem_ld32(ta, ov);
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) ov[i] = __float_as_uint(__uint_as_float(ov[i]) * alpha);
+                    ptx::tmem_st32(ta, ov);
+                }
+            }
+            // P as hi + lo 16-bit terms, this row's 128 bytes of each (swizzled).
+#pragma unroll
+            for (int c = 0; c < TT / 8; ++c) {
+                uint32_t hi[4], lo[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const float p0 = __uint_as_float(sv[c * 8 + 2 * e]);
+                    const float p1 = __uint_as_float(sv[c * 8 + 2 * e + 1]);
+                    hi[e] = pack2(p0, p1, T());
+                    const float2 back = unpack2(hi[e], T());
+                    lo[e] = pack2(p0 - back.x, p1 - back.y, T());
+                }
+                const int off = tid * 128 + ((c ^ (tid & 7)) << 4);
+                *reinterpret_cast<uint4*>(sp + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+                *reinterpret_cast<uint4*>(sp + Cfg::kPBytes + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+            }
+            // V rows of tokens that were not loaded hold stale or uninitialised
+            // bytes: zero them so 0 * V stays 0.
+            bool partial = false;
+#pragma unroll
+            for (int bx = 0; bx < TT / kStageTokens; ++bx) partial |= nvalid[bx] < kStageTokens;
+            if (partial) {
+                uint8_t* vst = ring + (j % NS) * Cfg::kStageBytes + Cfg::kHalfBytes;
+                for (int idx = tid; idx < TT * R * 8; idx += kPrefixSoftmaxWarps * 32) {
+                    const int row = idx / (R * 8);
+                    const int rem = idx - row * (R * 8);
+                    if (row % kStageTokens >= nvalid[row / kStageTokens])
+                        *reinterpret_cast<uint4*>(vst + (rem / 8) * Cfg::kKVRegionBytes + row * 128 +
+                                                  (rem % 8) * 16) = make_uint4(0u, 0u, 0u, 0u);
+                }
+            }
+            ptx::fence_proxy_async_smem();
+            ptx::tc_fence_before_sync();
+            ptx::mbar_arrive(ptx::smem_addr(p_ready));
         }
-        if (!aborted && wrow < rows) {
-            // This warp's rows are complete for this partition: normalise and store.
+        if (ok && ntiles > 0)
+            ok = warp_wait_phase(ptx::smem_addr(o_done), (ntiles - 1) & 1, abort_flag, p.err_flag);
+        if (ok) {
+            // Epilogue: this row's normalised O and log-sum-exp as prefix partial `part`.
+            ptx::tc_fence_after_sync();
+            const float inv = l > 0.f ? 1.f / l : 0.f;
+            const int64_t prow = ((int64_t)seq * p.num_q_heads + head) * p.num_splits + part;
+            float* dst = p.partial_o + prow * D;
 #pragma unroll
-            for (int nt = 0; nt < NT; ++nt) {
-                float la = l0[nt], lb = l1[nt];
+            for (int c = 0; c < D / 32; ++c) {
+                uint32_t ov[32];
+                if (ntiles > 0) {
+                    ptx::tmem_ld32(tmem + lane_base + Cfg::kColO + c * 32, ov);
+                } else {
 #pragma unroll
-                for (int off = 4; off < 32; off <<= 1) {
-                    la += __shfl_xor_sync(0xffffffffu, la, off);
-                    lb += __shfl_xor_sync(0xffffffffu, lb, off);
+                    for (int i = 0; i < 32; ++i) ov[i] = 0u;
                 }
+                if (row_ok) {
 #pragma unroll
-                for (int c = 0; c < 2; ++c) {
-                    const int rc = wrow + nt * 8 + 2 * tq + c;
-                    if (rc >= rows) continue;
-                    const float l = c == 0 ? la : lb;
-                    const float m = c == 0 ? m0[nt] : m1[nt];
-                    const float inv = l > 0.f ? 1.f / l : 0.f;
-                    const int seq = first + rc / p.group;
-                    const int head = g * p.group + rc % p.group;
-                    const int64_t prow = ((int64_t)seq * p.num_q_heads + head) * p.num_splits + part;
-                    float* dst = p.partial_o + prow * D;
-#pragma unroll
-                    for (int mt = 0; mt < KSTEPS; ++mt) {
-                        dst[mt * 16 + gq] = o[nt][mt][c] * inv;
-                        dst[mt * 16 + gq + 8] = o[nt][mt][c + 2] * inv;
+                    for (int i = 0; i < 32; i += 4) {
+                        float4 v;
+                        v.x = l > 0.f ? __uint_as_float(ov[i]) * inv : 0.f;
+                        v.y = l > 0.f ? __uint_as_float(ov[i + 1]) * inv : 0.f;
+                        v.z = l > 0.f ? __uint_as_float(ov[i + 2]) * inv : 0.f;
+                        v.w = l > 0.f ? __uint_as_float(ov[i + 3]) * inv : 0.f;
+                        *reinterpret_cast<float4*>(dst + c * 32 + i) = v;
                     }
-                    if (gq == 0) p.partial_lse[prow] = l > 0.f ? (m + log2f(l)) * kLn2 : -INFINITY;
                 }
             }
+            if (row_ok) p.partial_lse[prow] = l > 0.f ? (m_ref + log2f(l)) * kLn2 : -INFINITY;
         }
     }
+
+    ptx::tc_fence_before_sync();
     __syncthreads();
+    if (warp == kPrefixMmaWarp) {
+        __syncwarp();
+        ptx::tc_fence_after_sync();
+        ptx::tmem_dealloc(tmem, Cfg::kTmemCols);
+    }
 }
 
 // ---------------------------------------------------------------------------
@@ -1242,13 +1479,13 @@ static cudaError_t launch_prefix_t(const CUtensorMap& mk, const CUtensorMap& mv,
     static cudaError_t attr_err = cudaSuccess;
     std::call_once(once, [&] {
         attr_err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                        Tile<D>::kSmemBytes);
+                                        PrefixTile<D>::kSmemBytes);
     });
     if (attr_err != cudaSuccess) return attr_err;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = grid;
-    cfg.blockDim = dim3(kThreads);
-    cfg.dynamicSmemBytes = Tile<D>::kSmemBytes;
+    cfg.blockDim = dim3(kPrefixThreads);
+    cfg.dynamicSmemBytes = PrefixTile<D>::kSmemBytes;
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -1258,16 +1495,16 @@ static cudaError_t launch_prefix_t(const CUtensorMap& mk, const CUtensorMap& mv,
     return cudaLaunchKernelEx(&cfg, kern, mk, mv, p);
 }
 
-// Plan of a shared-prefix call: prefix partitions sized so the prefix kernel
-// fills about three waves of resident CTAs, the suffixes planned like a plain
-// decode, and per (sequence, query head) the prefix partials first, then the
-// suffix partials.
+// Plan of a shared-prefix call: the suffixes planned like a plain decode; the
+// prefix in partitions of whole 64-token tiles, as many as give about one
+// prefix CTA (128 query rows) per SM, at most kMaxChunkPages pages each; per
+// (sequence, query head) the prefix partials first, then the suffix partials.
 struct PrefixPlan {
     Plan suffix;
     int prefix_chunk;
     int prefix_parts;
     int total_splits;
-    int row_blocks;
+    int row_tiles;
     size_t workspace_bytes;
 };
 
@@ -1280,17 +1517,18 @@ static pkv_status make_prefix_plan(int num_seqs, int num_q_heads, int num_kv_hea
     if (st != PKV_OK) return st;
     const int group = num_q_heads / num_kv_heads;
     const int64_t rows = (int64_t)max_group_size * group;
-    pp->row_blocks = (int)std::max<int64_t>(1, (rows + kPrefixRows - 1) / kPrefixRows);
-    if ((int64_t)num_groups * num_kv_heads > 65535 || pp->row_blocks > 65535)
+    pp->row_tiles = (int)std::max<int64_t>(1, (rows + kPrefixTileRows - 1) / kPrefixTileRows);
+    if ((int64_t)num_groups * num_kv_heads > 65535 || pp->row_tiles > 65535)
         return PKV_ERR_UNSUPPORTED;
     const int sms = current_sm_count();
     if (sms <= 0) return PKV_ERR_CUDA;
-    const int64_t units = std::max<int64_t>(1, (int64_t)num_groups * num_kv_heads * pp->row_blocks);
-    const int64_t want = std::max<int64_t>(1, (3LL * 3 * sms + units - 1) / units);
-    const int prefix_pages = (max_prefix_len + block_size - 1) / block_size;
-    int cp = (int)((prefix_pages + want - 1) / want);
-    cp = std::min(std::max(cp, std::max(1, 256 / block_size)), kMaxChunkPages);
-    pp->prefix_chunk = cp * block_size;
+    const int64_t units = std::max<int64_t>(1, (int64_t)num_groups * num_kv_heads * pp->row_tiles);
+    const int64_t want = std::max<int64_t>(1, sms / units);
+    const int tiles = (max_prefix_len + kPrefixTileTokens - 1) / kPrefixTileTokens;
+    const int max_tiles = kMaxChunkPages * block_size / kPrefixTileTokens;
+    const int chunk_tiles =
+        std::min<int64_t>(max_tiles, std::max<int64_t>(1, (tiles + want - 1) / want));
+    pp->prefix_chunk = chunk_tiles * kPrefixTileTokens;
     pp->prefix_parts = max_prefix_len > 0 ? (max_prefix_len + pp->prefix_chunk - 1) / pp->prefix_chunk
                                           : 0;
     pp->total_splits = pp->prefix_parts + pp->suffix.num_splits;
@@ -1560,8 +1798,8 @@ extern "C" pkv_status pkv_decode_attention_prefix_shared(
         }
     }
 
-    // 2. prefix partials of every group
-    PrefixParams pr;
+    // 2. prefix partials of every group (tcgen05)
+    PrefixParams pr = {};
     pr.q = q;
     pr.block_tables = block_tables;
     pr.context_lens = context_lens;
@@ -1584,8 +1822,7 @@ extern "C" pkv_status pkv_decode_attention_prefix_shared(
     pr.prefix_chunk = pp.prefix_chunk;
     pr.cap = cap;
     pr.scale_log2 = scale * kLog2e;
-    if (pr.group > 16) return PKV_ERR_UNSUPPORTED;
-    const dim3 pgrid(pp.row_blocks, std::max(1, num_groups * num_kv_heads),
+    const dim3 pgrid(pp.row_tiles, std::max(1, num_groups * num_kv_heads),
                      std::max(1, pp.prefix_parts));
     cudaError_t e;
     if (head_dim == 64)

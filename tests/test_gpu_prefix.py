@@ -42,6 +42,10 @@ CASES = {
     "gqa16_big_group": dict(name="c3", num_seqs=40, num_q_heads=32, num_kv_heads=2, head_dim=128,
                             lengths=("prefix_lognormal", 160, 40, 1.0, 300), max_len_cap=320,
                             shared_prefix_groups=1, pool="free_list", seed=47),
+    # more than one plan-kernel chunk of groups and of (sequence, KV head) units
+    "1100_groups_of_one": dict(name="c3", num_seqs=1100, num_q_heads=4, num_kv_heads=2, head_dim=64,
+                               lengths=("prefix_lognormal", 16, 20, 0.5, 80), max_len_cap=96,
+                               shared_prefix_groups=1100, pool="free_list", seed=53),
 }
 
 
