@@ -590,7 +590,7 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
 //   softmax          one thread per query row, reading its row of S directly
 //   O += P V         M=128, N=D, 16-token steps; P enters as hi + lo 16-bit
 //                    terms (as in the decode kernel); O stays in tensor memory
-// Warp 4 streams K/V tiles by TMA into a 3-stage ring, warp 5 owns the tensor
+// Warp 4 streams K/V tiles by TMA into a 4-stage ring, warp 5 owns the tensor
 // memory and one of its lanes issues the MMAs, warps 0-3 run the softmax and
 // write the rows' normalised O and log-sum-exp as their prefix partials.  S is
 // double-buffered, so S of the next tile is computed during this tile's
@@ -626,7 +626,7 @@ struct PrefixParams {
 
 constexpr int kPrefixTileRows = 128;     // query rows per CTA (MMA M)
 constexpr int kPrefixTileTokens = 64;    // tokens per tile (N of S, K of O)
-constexpr int kPrefixStages = 3;
+constexpr int kPrefixStages = 4;
 constexpr int kPrefixSoftmaxWarps = 4;   // one thread per query row
 constexpr int kPrefixThreads = (kPrefixSoftmaxWarps + 2) * 32;
 constexpr int kPrefixTmaWarp = kPrefixSoftmaxWarps;
@@ -689,6 +689,23 @@ __device__ __forceinline__ bool warp_wait_phase(uint32_t bar, uint32_t parity,
                                                 volatile int* abort_flag, int32_t* err_flag) {
     const bool ok = wait_phase(bar, parity, abort_flag, err_flag);
     return __all_sync(0xffffffffu, ok);
+}
+
+// Two fp32 weights as hi + lo 16-bit terms packed in pairs (element 0 in the
+// low half).  bf16: both terms by truncation (a bit mask; hi + lo keeps p to
+// 2^-14 relative); fp16: both terms rounded to nearest.
+__device__ __forceinline__ void split_hi_lo(float p0, float p1, uint32_t& hi, uint32_t& lo,
+                                            __nv_bfloat16) {
+    const uint32_t b0 = __float_as_uint(p0), b1 = __float_as_uint(p1);
+    hi = __byte_perm(b0, b1, 0x7632);
+    const float r0 = p0 - __uint_as_float(b0 & 0xffff0000u);
+    const float r1 = p1 - __uint_as_float(b1 & 0xffff0000u);
+    lo = __byte_perm(__float_as_uint(r0), __float_as_uint(r1), 0x7632);
+}
+__device__ __forceinline__ void split_hi_lo(float p0, float p1, uint32_t& hi, uint32_t& lo, __half) {
+    hi = pack2(p0, p1, __half());
+    const float2 back = unpack2(hi, __half());
+    lo = pack2(p0 - back.x, p1 - back.y, __half());
 }
 
 template <typename T, int D>
@@ -804,52 +821,48 @@ prefix_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
 
     if (warp == kPrefixTmaWarp) {
         // ------------------------------------------------------------ producer
-        if (lane == 0) {
-            const uint64_t policy = ptx::l2_policy_evict_last();  // other row tiles read it too
-            int issued = 0;
-            for (int j = 0; j < ntiles; ++j) {
-                const int slot = j % NS;
-                if (j >= NS && !wait_phase(ptx::smem_addr(&empty_bar[slot]), ((j / NS) - 1) & 1,
-                                           abort_flag, p.err_flag))
-                    break;
-                const uint32_t kdst = ring_addr + slot * Cfg::kStageBytes;
-                const uint32_t fb = ptx::smem_addr(&full_bar[slot]);
-                uint32_t bytes = 0;
-#pragma unroll
-                for (int bx = 0; bx < TT / kStageTokens; ++bx) {
-                    const int tok0 = t_begin + j * TT + bx * kStageTokens;
-                    if (tok0 < t_end && table[tok0 / bs - page0] >= 0)
-                        bytes += 2 * R * kStageTokens * 128;
-                }
-                if (bytes == 0) {
+        // The tile's box loads (16-token page box x 64-dim region x K/V) are
+        // spread over the warp's lanes: one thread issuing them in turn is the
+        // bottleneck of this kernel, several lanes issue them at once.
+        constexpr int kBoxes = TT / kStageTokens;
+        constexpr int kLoads = kBoxes * R * 2;
+        static_assert(kLoads <= 32, "one load per lane");
+        const uint64_t policy = ptx::l2_policy_evict_last();  // other row tiles read it too
+        const int bx = lane / (R * 2);
+        const int rr = (lane / 2) % R;
+        const bool is_v = lane & 1;
+        int issued = 0;
+        for (int j = 0; j < ntiles; ++j) {
+            const int slot = j % NS;
+            if (j >= NS && !warp_wait_phase(ptx::smem_addr(&empty_bar[slot]), ((j / NS) - 1) & 1,
+                                            abort_flag, p.err_flag))
+                break;
+            const uint32_t kdst = ring_addr + slot * Cfg::kStageBytes;
+            const uint32_t fb = ptx::smem_addr(&full_bar[slot]);
+            const int tok0 = t_begin + j * TT + bx * kStageTokens;
+            const int blk = lane < kLoads && tok0 < t_end ? table[tok0 / bs - page0] : -1;
+            const uint32_t loads = __ballot_sync(0xffffffffu, blk >= 0);
+            if (lane == 0) {
+                if (loads == 0)
                     ptx::mbar_arrive(fb);  // nothing to load: every token of the tile is masked
-                } else {
-                    ptx::mbar_arrive_expect_tx(fb, bytes);
-#pragma unroll
-                    for (int bx = 0; bx < TT / kStageTokens; ++bx) {
-                        const int tok0 = t_begin + j * TT + bx * kStageTokens;
-                        if (tok0 >= t_end) continue;
-                        const int blk = table[tok0 / bs - page0];
-                        if (blk < 0) continue;
-#pragma unroll
-                        for (int rr = 0; rr < R; ++rr) {
-                            const uint32_t off = rr * Cfg::kKVRegionBytes + bx * kStageTokens * 128;
-                            ptx::tma_load_4d(kdst + off, &tm_k, fb, rr * 64, g, tok0 % bs, blk,
-                                             policy);
-                            ptx::tma_load_4d(kdst + Cfg::kHalfBytes + off, &tm_v, fb, rr * 64, g,
-                                             tok0 % bs, blk, policy);
-                        }
-                    }
-                }
-                issued = j + 1;
+                else
+                    ptx::mbar_arrive_expect_tx(fb, __popc(loads) * kStageTokens * 128);
             }
-            if (*abort_flag) {
-                for (int j = max(0, issued - NS); j < issued; ++j) {
-                    const uint32_t fb = ptx::smem_addr(&full_bar[j % NS]);
-                    const uint64_t t0 = ptx::globaltimer();
-                    while (!ptx::mbar_try_wait(fb, (j / NS) & 1) &&
-                           ptx::globaltimer() - t0 < kWaitLimitNs) {
-                    }
+            __syncwarp();
+            if (blk >= 0) {
+                const uint32_t off = (is_v ? Cfg::kHalfBytes : 0) + rr * Cfg::kKVRegionBytes +
+                                     bx * kStageTokens * 128;
+                ptx::tma_load_4d(kdst + off, is_v ? &tm_v : &tm_k, fb, rr * 64, g, tok0 % bs, blk,
+                                 policy);
+            }
+            issued = j + 1;
+        }
+        if (lane == 0 && *abort_flag) {
+            for (int j = max(0, issued - NS); j < issued; ++j) {
+                const uint32_t fb = ptx::smem_addr(&full_bar[j % NS]);
+                const uint64_t t0 = ptx::globaltimer();
+                while (!ptx::mbar_try_wait(fb, (j / NS) & 1) &&
+                       ptx::globaltimer() - t0 < kWaitLimitNs) {
                 }
             }
         }
@@ -942,39 +955,53 @@ prefix_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
             const int tile0 = t_begin + j * TT;
             // Tokens of this row: present (a valid block, before t_end) and within its context.
             int nvalid[TT / kStageTokens];
+            bool complete = tile0 + TT <= lim;
 #pragma unroll
             for (int bx = 0; bx < TT / kStageTokens; ++bx) {
                 const int tok0 = tile0 + bx * kStageTokens;
                 nvalid[bx] = (tok0 < t_end && table[tok0 / bs - page0] >= 0)
                                  ? min(kStageTokens, t_end - tok0)
                                  : 0;
+                complete &= nvalid[bx] == kStageTokens;
             }
-            float mx = -INFINITY;
+            float sc[TT];
 #pragma unroll
-            for (int i = 0; i < TT; ++i) {
-                const bool valid = (i % kStageTokens) < nvalid[i / kStageTokens] && tile0 + i < lim;
-                const float sc = valid ? __uint_as_float(sv[i]) * p.scale_log2 : -INFINITY;
-                sv[i] = __float_as_uint(sc);
-                mx = fmaxf(mx, sc);
+            for (int i = 0; i < TT; ++i) sc[i] = __uint_as_float(sv[i]) * p.scale_log2;
+            if (!complete) {
+#pragma unroll
+                for (int i = 0; i < TT; ++i)
+                    if (!((i % kStageTokens) < nvalid[i / kStageTokens] && tile0 + i < lim))
+                        sc[i] = -INFINITY;
             }
+            // row max, as a tree
+            float red[TT / 2];
+#pragma unroll
+            for (int i = 0; i < TT / 2; ++i) red[i] = fmaxf(sc[i], sc[i + TT / 2]);
+#pragma unroll
+            for (int w = TT / 4; w > 0; w >>= 1)
+#pragma unroll
+                for (int i = 0; i < w; ++i) red[i] = fmaxf(red[i], red[i + w]);
+            const float mx = red[0];
             float alpha = 1.f;
             bool rescale = false;
             if (m_ref == -INFINITY) {
                 m_ref = mx;  // O and l are still zero for this row
             } else if (mx > m_ref + kRescaleLog2) {
-                alpha = exp2f(m_ref - mx);
+                alpha = ptx::ex2_approx(m_ref - mx);
                 m_ref = mx;
                 rescale = true;
             }
             const float ref = m_ref == -INFINITY ? 0.f : m_ref;
-            float rowsum = 0.f;
 #pragma unroll
-            for (int i = 0; i < TT; ++i) {
-                const float pv = exp2f(__uint_as_float(sv[i]) - ref);
-                rowsum += pv;
-                sv[i] = __float_as_uint(pv);
-            }
-            l = l * alpha + rowsum;
+            for (int i = 0; i < TT; ++i) sc[i] = ptx::ex2_approx(sc[i] - ref);
+            // row sum, as a tree
+#pragma unroll
+            for (int i = 0; i < TT / 2; ++i) red[i] = sc[i] + sc[i + TT / 2];
+#pragma unroll
+            for (int w = TT / 4; w > 0; w >>= 1)
+#pragma unroll
+                for (int i = 0; i < w; ++i) red[i] += red[i + w];
+            l = l * alpha + red[0];
             // P and O are free once the previous tile's O += P V has completed.
             if (j > 0 && !warp_wait_phase(ptx::smem_addr(o_done), (j - 1) & 1, abort_flag,
                                           p.err_flag)) {
@@ -999,11 +1026,9 @@ prefix_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
                 uint32_t hi[4], lo[4];
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
-                    const float p0 = __uint_as_float(sv[c * 8 + 2 * e]);
-                    const float p1 = __uint_as_float(sv[c * 8 + 2 * e + 1]);
-                    hi[e] = pack2(p0, p1, T());
-                    const float2 back = unpack2(hi[e], T());
-                    lo[e] = pack2(p0 - back.x, p1 - back.y, T());
+                    const float p0 = sc[c * 8 + 2 * e];
+                    const float p1 = sc[c * 8 + 2 * e + 1];
+                    split_hi_lo(p0, p1, hi[e], lo[e], T());
                 }
                 const int off = tid * 128 + ((c ^ (tid & 7)) << 4);
                 *reinterpret_cast<uint4*>(sp + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);

@@ -212,6 +212,14 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32
         : "memory");
 }
 
+// 2^x by the hardware approximation (relative error about 2^-22; subnormal
+// results flush to zero).
+__device__ __forceinline__ float ex2_approx(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
 // ---- programmatic dependent launch ------------------------------------------------
 
 __device__ __forceinline__ void grid_dependency_wait() {
