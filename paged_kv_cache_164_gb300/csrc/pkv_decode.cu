@@ -76,7 +76,6 @@ struct DecodeParams {
     int group;           // query heads per KV head
     int num_splits;
     int chunk_tokens;    // tokens per partition (a multiple of block_size and of 16)
-    int stagger_tokens;  // partition-boundary shift step (a multiple of 16), 0 = none
     int num_kv_heads;
     int max_context_len;
     float scale_log2;    // scale * log2(e)
@@ -86,31 +85,14 @@ struct DecodeParams {
 // values are clamped (and flagged by the decode kernel).
 __device__ __forceinline__ int clamped_len(int n, int cap) { return n < 0 ? 0 : (n > cap ? cap : n); }
 
-// Partition geometry of one (sequence b, KV head g) pair.  Partition j covers
-// tokens [j*C - shift, (j+1)*C - shift) of the context, clipped to [0, n), where
-// C = chunk_tokens and shift = ((b * H_kv + g) % 3) * stagger.  Staggering the
-// boundaries of neighbouring pairs gives CTAs of one wave different lengths,
-// so the waves drift apart and one CTA's set-up and wind-down overlap other
-// CTAs' streaming instead of lining up across the whole GPU.
-struct Partition {
-    int shift;
-    int nsplit;   // partitions with tokens (1 when n == 0)
-};
-__device__ __forceinline__ Partition partition_of(int n, int b, int g, int num_kv_heads,
-                                                  int chunk, int stagger) {
-    Partition pt;
-    pt.shift = ((b * num_kv_heads + g) % 3) * stagger;
-    pt.nsplit = n > 0 ? (n + pt.shift + chunk - 1) / chunk : 1;
-    return pt;
-}
-
-// Partitions of a sequence's suffix of `suffix` tokens.  Without a shared
-// prefix (slot0 == 0) an empty context still gets one partition, whose CTA
-// writes the zero row; after a prefix, an empty suffix has none.
-__device__ __forceinline__ int suffix_partitions(int suffix, int slot0, int b, int g,
-                                                 int num_kv_heads, int chunk, int stagger) {
-    if (slot0 > 0 && suffix == 0) return 0;
-    return partition_of(suffix, b, g, num_kv_heads, chunk, stagger).nsplit;
+// Partitions of a sequence's suffix of `suffix` tokens (the whole context
+// without a shared prefix): partition j covers tokens [j*C, (j+1)*C) of it, C
+// = chunk_tokens.  Without a shared prefix (slot0 == 0) an empty context still
+// gets one partition, whose CTA writes the zero row; after a prefix, an empty
+// suffix has none.
+__device__ __forceinline__ int suffix_partitions(int suffix, int slot0, int chunk) {
+    if (suffix == 0) return slot0 > 0 ? 0 : 1;
+    return (suffix + chunk - 1) / chunk;
 }
 
 __device__ __forceinline__ uint32_t pack2(float lo, float hi, __nv_bfloat16) {
@@ -336,8 +318,7 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
     }
     // Partition start does not depend on the context length, so the producer
     // warp fetches the block-table slice at the same time as the length.
-    const int shift = ((b * p.num_kv_heads + g) % 3) * p.stagger_tokens;
-    const int t_begin = start + max(0, split * p.chunk_tokens - shift);
+    const int t_begin = start + split * p.chunk_tokens;
     const int page0 = t_begin / bs;
     const int max_pages = min(p.max_blocks_per_seq - page0, p.chunk_tokens / bs + 1);
     const int32_t* row = p.block_tables + (int64_t)b * p.max_blocks_per_seq + page0;
@@ -351,10 +332,9 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
         flag_error(p.err_flag, PKV_EFLAG_CONTEXT_LEN);
     const int n = clamped_len(n_raw, cap);
     const int suffix = max(0, n - start);
-    const int nsplit = suffix_partitions(suffix, slot0, b, g, p.num_kv_heads, p.chunk_tokens,
-                                         p.stagger_tokens);
+    const int nsplit = suffix_partitions(suffix, slot0, p.chunk_tokens);
     if (split >= nsplit) return;
-    const int t_end = min(n, start + (split + 1) * p.chunk_tokens - shift);
+    const int t_end = min(n, start + (split + 1) * p.chunk_tokens);
     const int nstages = t_end > t_begin ? (t_end - t_begin + kStageTokens - 1) / kStageTokens : 0;
     const bool direct = slot0 == 0 && nsplit == 1;  // the whole answer is this CTA's
 
@@ -1121,7 +1101,6 @@ struct PlanParams {
     int max_blocks_per_seq;
     int prefix_chunk;
     int chunk_tokens;
-    int stagger_tokens;
     int cap;
 };
 
@@ -1169,8 +1148,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const PlanParams p) 
             const int g = u - b * p.num_kv_heads;
             const int2 info = p.seq_info[b];
             const int n = clamped_len(p.context_lens[b], p.cap);
-            cnt = suffix_partitions(max(0, n - info.x), info.y, b, g, p.num_kv_heads,
-                                    p.chunk_tokens, p.stagger_tokens);
+            cnt = suffix_partitions(max(0, n - info.x), info.y, p.chunk_tokens);
         }
         int incl = cnt;  // inclusive warp scan
 #pragma unroll
@@ -1219,7 +1197,6 @@ struct MergeParams {
     int num_splits;
     int head_dim;                 // a multiple of 4, at most 4 * kMergeThreads
     int chunk_tokens;
-    int stagger_tokens;
     int cap;                      // context clamp, as in the decode kernel
 };
 
@@ -1244,8 +1221,7 @@ merge_kernel(const MergeParams p) {
             slot0 = si.y;
         }
         const int n = clamped_len(__ldg(p.context_lens + b), p.cap);
-        ns = slot0 + suffix_partitions(max(0, n - start), slot0, b, h / p.group, p.num_kv_heads,
-                                       p.chunk_tokens, p.stagger_tokens);
+        ns = slot0 + suffix_partitions(max(0, n - start), slot0, p.chunk_tokens);
         if (slot0 == 0 && ns <= 1) return;  // written directly by the decode kernel
     }
     const int64_t row = (int64_t)b * p.num_q_heads + h;
@@ -1348,7 +1324,6 @@ static int current_sm_count() {
 struct Plan {
     int num_splits;      // partitions per sequence, at most
     int chunk_tokens;
-    int stagger_tokens;
     size_t workspace_bytes;
 };
 
@@ -1367,8 +1342,9 @@ static pkv_status check_shapes(int num_seqs, int num_q_heads, int num_kv_heads, 
 }
 
 // Partitions: each is a whole number of pages, at most kMaxChunkPages; the
-// automatic plan aims at several waves of CTAs over the SMs so ragged lengths
-// balance, without cutting partitions below 256 tokens.
+// automatic plan sizes them so that, at the longest context, the CTAs fill
+// whole waves of resident CTAs (see the loop), without cutting partitions
+// below 256 tokens.
 static pkv_status make_plan(int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
                             int block_size, int max_context_len, int num_splits, Plan* plan) {
     pkv_status st = check_shapes(num_seqs, num_q_heads, num_kv_heads, head_dim, block_size,
@@ -1379,28 +1355,43 @@ static pkv_status make_plan(int num_seqs, int num_q_heads, int num_kv_heads, int
     if (num_splits == 0) {
         const int sms = current_sm_count();
         if (sms <= 0) return PKV_ERR_CUDA;
+        // Whole pages from 256 tokens up to kMaxChunkPages pages.  Among those
+        // partition counts, the fewest whose CTAs (at the longest context) fill
+        // their last wave of resident CTAs to 95%, else the best filled one:
+        // equal-length CTAs run in lock-step waves, so a partly empty last wave
+        // leaves SMs idle.
         const int64_t units = (int64_t)std::max(1, num_seqs) * num_kv_heads;
-        const int64_t target = 3LL * 3 * sms;  // three waves of three resident CTAs per SM
-        const int64_t want = std::max<int64_t>(1, (target + units - 1) / units);
-        chunk_pages = (int)((max_pages + want - 1) / want);
+        const double slots = 3.0 * sms;
         const int min_pages = std::max(1, 256 / block_size);
-        chunk_pages = std::max(chunk_pages, min_pages);
+        const int lo = std::max(1, (max_pages + kMaxChunkPages - 1) / kMaxChunkPages);
+        const int hi = std::max(lo, std::min(PKV_MAX_SPLITS, (max_pages + min_pages - 1) / min_pages));
+        double best_eff = -1.0;
+        chunk_pages = (max_pages + lo - 1) / lo;
+        for (int s = lo; s <= hi; ++s) {
+            const int cp = (max_pages + s - 1) / s;
+            const int splits = (max_pages + cp - 1) / cp;
+            if (splits != s) continue;  // the same partition as a smaller count
+            const double waves = (double)units * splits / slots;
+            const double eff = waves / std::ceil(waves);
+            if (eff > best_eff + 1e-9) {
+                best_eff = eff;
+                chunk_pages = cp;
+            }
+            if (eff >= 0.95) {
+                chunk_pages = cp;
+                break;
+            }
+        }
     } else {
         chunk_pages = (max_pages + num_splits - 1) / num_splits;
     }
     chunk_pages = std::min(std::max(chunk_pages, 1), kMaxChunkPages);
     const int chunk = chunk_pages * block_size;
-    // Staggered boundaries (automatic plans with more than one partition only):
-    // shifts of 0, 1/3 and 2/3 of a partition, in whole 16-token stages.
-    int stagger = 0;
-    if (num_splits == 0 && max_context_len > chunk) stagger = (chunk / 3) / 16 * 16;
-    const int64_t splits64 =
-        std::max<int64_t>(1, ((int64_t)max_context_len + 2 * stagger + chunk - 1) / chunk);
+    const int64_t splits64 = std::max<int64_t>(1, ((int64_t)max_context_len + chunk - 1) / chunk);
     if (splits64 > PKV_MAX_SPLITS) return PKV_ERR_UNSUPPORTED;  // context too long for the plan
     const int splits = (int)splits64;
     plan->num_splits = splits;
     plan->chunk_tokens = chunk;
-    plan->stagger_tokens = stagger;
     plan->workspace_bytes =
         splits > 1 ? (size_t)num_seqs * num_q_heads * splits * (head_dim + 1) * sizeof(float) + 256
                    : 0;
@@ -1638,7 +1629,6 @@ extern "C" pkv_status pkv_decode_attention(void* out, const void* q, const void*
     p.group = num_q_heads / num_kv_heads;
     p.num_splits = plan.num_splits;
     p.chunk_tokens = plan.chunk_tokens;
-    p.stagger_tokens = plan.stagger_tokens;
     p.num_kv_heads = num_kv_heads;
     p.max_context_len = max_context_len;
     p.scale_log2 = scale * kLog2e;
@@ -1672,7 +1662,6 @@ extern "C" pkv_status pkv_decode_attention(void* out, const void* q, const void*
         mp.num_splits = plan.num_splits;
         mp.head_dim = head_dim;
         mp.chunk_tokens = plan.chunk_tokens;
-        mp.stagger_tokens = plan.stagger_tokens;
         mp.cap = std::min(max_blocks_per_seq * block_size, max_context_len);
         e = dtype == PKV_FP16 ? launch_merge<__half>(mp, num_q_heads, num_seqs, s)
                               : launch_merge<__nv_bfloat16>(mp, num_q_heads, num_seqs, s);
@@ -1709,7 +1698,6 @@ extern "C" pkv_status pkv_merge(void* out, const float* partial_o, const float* 
     mp.num_splits = num_splits;
     mp.head_dim = head_dim;
     mp.chunk_tokens = 1;
-    mp.stagger_tokens = 0;
     mp.cap = 0;
     cudaStream_t s = (cudaStream_t)stream;
     cudaError_t e = dtype == PKV_FP16 ? launch_merge<__half>(mp, num_q_heads, num_seqs, s)
@@ -1805,7 +1793,6 @@ extern "C" pkv_status pkv_decode_attention_prefix_shared(
     pl.max_blocks_per_seq = max_blocks_per_seq;
     pl.prefix_chunk = pp.prefix_chunk;
     pl.chunk_tokens = pp.suffix.chunk_tokens;
-    pl.stagger_tokens = pp.suffix.stagger_tokens;
     pl.cap = cap;
     {
         cudaLaunchConfig_t cfg = {};
@@ -1880,7 +1867,6 @@ extern "C" pkv_status pkv_decode_attention_prefix_shared(
     p.group = num_q_heads / num_kv_heads;
     p.num_splits = pp.total_splits;
     p.chunk_tokens = pp.suffix.chunk_tokens;
-    p.stagger_tokens = pp.suffix.stagger_tokens;
     p.num_kv_heads = num_kv_heads;
     p.max_context_len = max_context_len;
     p.scale_log2 = scale * kLog2e;
@@ -1905,7 +1891,6 @@ extern "C" pkv_status pkv_decode_attention_prefix_shared(
     mp.num_splits = pp.total_splits;
     mp.head_dim = head_dim;
     mp.chunk_tokens = pp.suffix.chunk_tokens;
-    mp.stagger_tokens = pp.suffix.stagger_tokens;
     mp.cap = cap;
     e = dtype == PKV_FP16 ? launch_merge<__half>(mp, num_q_heads, num_seqs, s)
                           : launch_merge<__nv_bfloat16>(mp, num_q_heads, num_seqs, s);
