@@ -55,8 +55,14 @@ WORKLOAD_TEXT = {
 # measured on (digest of csrc/), else reported as null.
 NCU_TRAFFIC = {
     # ncu --metrics dram__bytes_read.sum,dram__bytes_write.sum -k regex:decode_kernel -s 4 -c 1
-    "c2": {"digest": "42afcdb1becbd985", "splits": 5, "bytes": 2312661504 + 4542976},
-    "c3": {"digest": "42afcdb1becbd985", "splits": 7, "bytes": 537523200 + 5306624},
+    "c2": {"digest": "2309677242f223bb", "splits": 4, "shared": False,
+           "bytes": 2312563200 + 4213504},
+    "c3": {"digest": "2309677242f223bb", "splits": 7, "shared": False,
+           "bytes": 537521920 + 5476352},
+    # shared-prefix path: decode_kernel (suffixes) + prefix_kernel (one --set full
+    # capture); the plan and merge kernels' few MB are not included
+    "c5": {"digest": "2309677242f223bb", "splits": 16, "shared": True,
+           "bytes": (1531743744 + 5607936) + (35738368 + 58112)},
 }
 
 
@@ -319,8 +325,9 @@ def run_gpu(args):
     workspace = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device=device)
     out = torch.empty_like(w.q)
     flag = pkv.new_error_flag(device)
-    # append, decode, merge when split; the shared-prefix path adds its prefix kernel
-    launches_per_step = 4 if shared else 2 + (1 if splits > 1 else 0)
+    # append, decode, merge when split; the shared-prefix path: append, plan,
+    # prefix, decode, merge
+    launches_per_step = 5 if shared else 2 + (1 if splits > 1 else 0)
 
     def decode_call(q, block_tables, context_lens):
         if shared:
@@ -428,7 +435,8 @@ def run_gpu(args):
     clocks = sampler.summary(t_begin, t_end) if sampler else None
     traffic = None
     rec = NCU_TRAFFIC.get(args.config)
-    if rec and rec.get("digest") == _kernel_digest() and rec.get("splits") == splits:
+    if rec and rec.get("digest") == _kernel_digest() and rec.get("splits") == splits and \
+            rec.get("shared") == shared:
         traffic = rec["bytes"]
 
     cpu = None
@@ -460,7 +468,7 @@ def run_gpu(args):
         "decode_ms": round(decode_ms, 5),
         "roofline": {"bound": "hbm", "achieved": round(decode_gbs, 2), "peak": peak,
                      "unit": "GB/s", "frac": round(decode_gbs / peak, 4),
-                     "traffic": traffic, "kernel": ("prefix_kernel + decode_kernel + merge_kernel" if shared else
+                     "traffic": traffic, "kernel": ("plan_kernel + prefix_kernel + decode_kernel + merge_kernel" if shared else
                                 "decode_kernel + merge_kernel") + " (one decode call, back to back)",
                      "peak_source": f"{peak_src} hbm_gbs"},
         "cpu_baseline": cpu,
