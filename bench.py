@@ -86,8 +86,9 @@ def _peaks():
         return FALLBACK_HBM_GBS, "fallback"
 
 
-def step_bytes(w) -> dict:
-    """Algorithmic bytes of one step of workload ``w`` (all 16-bit values: 2 bytes)."""
+def step_bytes(w, q_len: int = 1) -> dict:
+    """Algorithmic bytes of one step of workload ``w`` (all 16-bit values: 2 bytes),
+    with ``q_len`` query tokens per sequence (1: decode)."""
     import torch
     e = 2
     s = w.spec
@@ -104,15 +105,15 @@ def step_bytes(w) -> dict:
         slots.append(bt[b, t // bs] * bs + t % bs)
     unique_tokens = int(torch.unique(torch.cat(slots)).numel()) if slots else 0
     pages = int(((lens + bs - 1) // bs).sum())
-    qo = 2 * s.num_seqs * s.num_q_heads * s.head_dim * e
+    qo = 2 * s.num_seqs * q_len * s.num_q_heads * s.head_dim * e
     meta = pages * 4 + s.num_seqs * 4
     decode = 2 * unique_tokens * row + qo + meta
     decode_logical = 2 * logical_tokens * row + qo + meta
     append = 4 * s.num_seqs * row + 8 * s.num_seqs   # read k_new, v_new; write both; slots
-    flops = 4 * logical_tokens * s.num_q_heads * s.head_dim
+    flops = 4 * logical_tokens * q_len * s.num_q_heads * s.head_dim
     return dict(decode=decode, decode_logical=decode_logical, append=append,
                 step=decode + append, kv_unique=2 * unique_tokens * row, flops=flops,
-                tokens=s.num_seqs)
+                tokens=s.num_seqs * q_len)
 
 
 class ClockSampler:
@@ -229,9 +230,14 @@ def oracle_sample_rate(w, budget_s: float, seqs=None):
     s = w.spec
     row = s.num_kv_heads * s.head_dim * 2
 
+    q_len = q.shape[1] if q.ndim == 4 else 1  # several query tokens: causal multi-query
+
     def run(idx):
         t0 = time.perf_counter()
-        oracle.decode_attention(q[idx], kc, vc, bt[idx], cl[idx], w.scale, s.dtype)
+        if q.ndim == 4:
+            oracle.multi_query_attention(q[idx], kc, vc, bt[idx], cl[idx], w.scale, s.dtype)
+        else:
+            oracle.decode_attention(q[idx], kc, vc, bt[idx], cl[idx], w.scale, s.dtype)
         return time.perf_counter() - t0
 
     if seqs is None:
@@ -246,8 +252,9 @@ def oracle_sample_rate(w, budget_s: float, seqs=None):
         reps += 1
     secs /= reps
     toks = int(cl[seqs].sum())
-    nbytes = 2 * toks * row + 2 * len(seqs) * s.num_q_heads * s.head_dim * 2
-    desc = (f"oracle decode attention on the first {len(seqs)} of {s.num_seqs} sequences "
+    nbytes = 2 * toks * row + 2 * len(seqs) * q_len * s.num_q_heads * s.head_dim * 2
+    what = f"multi-query attention ({q_len} query tokens)" if q.ndim == 4 else "decode attention"
+    desc = (f"oracle {what} on the first {len(seqs)} of {s.num_seqs} sequences "
             f"({toks} context tokens) of the same workload, timed over {reps} runs")
     return nbytes / secs / 1e9, secs, desc, oracle.num_threads(), seqs
 
@@ -258,9 +265,12 @@ def run_reference(args):
     if rank != 0:
         return
     import torch
-    from workloads import make_workload
+    from workloads import make_queries, make_workload
     dev = "cuda" if torch.cuda.is_available() else "cpu"
-    w = make_workload(args.config, device=dev).to("cpu")
+    w = make_workload(args.config, device=dev)
+    if args.q_len > 0:
+        w.q = make_queries(w, args.q_len, seed=w.spec.seed + 101)
+    w = w.to("cpu")
     per_step = max(0.5, min(10.0, 150.0 / max(1, args.steps + args.warmup)))
     seqs = None
     for _ in range(args.warmup):
@@ -277,7 +287,8 @@ def run_reference(args):
             "ms_per_step": round(1e3 * statistics.median(secs_all), 3) if secs_all else None,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": "f64", "data": "synthetic",
-            "config": {"workload": args.config, "description": WORKLOAD_TEXT[args.config]},
+            "config": {"workload": args.config, "description": WORKLOAD_TEXT[args.config],
+                       "q_len": max(1, args.q_len)},
             "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": threads,
                              "kind": "oracle", "sample": desc},
             "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
@@ -290,7 +301,7 @@ def run_gpu(args):
     import torch.distributed as dist
 
     import paged_kv_cache_164_gb300 as pkv
-    from workloads import make_workload
+    from workloads import make_queries, make_workload
 
     ws, rank, local = _dist_env()
     if ws > 1:
@@ -306,16 +317,24 @@ def run_gpu(args):
     else:
         w = make_workload(args.config, device=device)
     s = w.spec
-    nbytes = step_bytes(w)
+    # --q-len N: causal multi-query attention of N query tokens per sequence
+    # (a prefill chunk or speculative verification) in place of the decode
+    mq = args.q_len > 0
+    if mq:
+        w.q = make_queries(w, args.q_len, seed=s.seed + 101)
+    nbytes = step_bytes(w, args.q_len if mq else 1)
     mcl = w.max_context_len
     # Workloads whose sequences share prefix blocks use the shared-prefix decode
     # (each group's prefix read once for all members) unless told otherwise.
-    shared = s.shared_prefix_groups > 0 and args.prefix_sharing
+    shared = s.shared_prefix_groups > 0 and args.prefix_sharing and not mq
     # Host-side bounds of the group metadata, read once (each read syncs the device).
     max_group_size, max_prefix_len = w.max_group_size, w.max_prefix_len
     splits = pkv.decode_num_splits(s.num_seqs, s.num_q_heads, s.num_kv_heads, s.head_dim,
                                    s.block_size, mcl, args.splits)
-    if shared:
+    if mq:
+        ws_bytes = pkv.multi_query_workspace_size(s.num_seqs, args.q_len, s.num_q_heads,
+                                                  s.num_kv_heads, s.head_dim, s.block_size, mcl)
+    elif shared:
         ws_bytes = pkv.prefix_shared_workspace_size(
             s.num_seqs, s.num_q_heads, s.num_kv_heads, s.head_dim, s.block_size, mcl,
             w.group_prefix_len.numel(), max_group_size, max_prefix_len)
@@ -327,10 +346,13 @@ def run_gpu(args):
     flag = pkv.new_error_flag(device)
     # append, decode, merge when split; the shared-prefix path: append, plan,
     # prefix, decode, merge
-    launches_per_step = 5 if shared else 2 + (1 if splits > 1 else 0)
+    launches_per_step = 3 if mq else 5 if shared else 2 + (1 if splits > 1 else 0)
 
     def decode_call(q, block_tables, context_lens):
-        if shared:
+        if mq:
+            pkv.multi_query_attention(q, w.k_cache, w.v_cache, block_tables, context_lens, mcl,
+                                      scale=w.scale, out=out, workspace=workspace, err_flag=flag)
+        elif shared:
             pkv.decode_attention_prefix_shared(
                 q, w.k_cache, w.v_cache, block_tables, context_lens, mcl, w.group_start,
                 w.group_prefix_len, max_group_size, max_prefix_len, scale=w.scale, out=out,
@@ -436,7 +458,7 @@ def run_gpu(args):
     traffic = None
     rec = NCU_TRAFFIC.get(args.config)
     if rec and rec.get("digest") == _kernel_digest() and rec.get("splits") == splits and \
-            rec.get("shared") == shared:
+            rec.get("shared") == shared and not mq:
         traffic = rec["bytes"]
 
     cpu = None
@@ -457,6 +479,7 @@ def run_gpu(args):
                    "block_size": s.block_size, "context_tokens": int(w.context_lens.sum()),
                    "max_context_len": mcl, "num_splits": splits, "accumulate": "fp32",
                    "shared_prefix_decode": shared,
+                   "q_len": args.q_len if mq else 1,
                    "kv_bytes_unique": nbytes["kv_unique"],
                    "decode_bytes_per_step": nbytes["decode"],
                    "decode_bytes_logical": nbytes["decode_logical"],
@@ -468,8 +491,11 @@ def run_gpu(args):
         "decode_ms": round(decode_ms, 5),
         "roofline": {"bound": "hbm", "achieved": round(decode_gbs, 2), "peak": peak,
                      "unit": "GB/s", "frac": round(decode_gbs / peak, 4),
-                     "traffic": traffic, "kernel": ("plan_kernel + prefix_kernel + decode_kernel + merge_kernel" if shared else
-                                "decode_kernel + merge_kernel") + " (one decode call, back to back)",
+                     "traffic": traffic,
+                     "kernel": ("prefix_kernel in multi-query mode (tcgen05) + merge_kernel" if mq
+                                else "plan_kernel + prefix_kernel + decode_kernel + merge_kernel"
+                                if shared else "decode_kernel + merge_kernel")
+                     + " (one attention call, back to back)",
                      "peak_source": f"{peak_src} hbm_gbs"},
         "cpu_baseline": cpu,
         "e2e": {"value": round(bytes_all / (e2e_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
@@ -491,6 +517,9 @@ def main(argv=None):
     ap.add_argument("--impl", choices=["mine", "reference"], default="mine")
     ap.add_argument("--config", default="c2", choices=sorted(WORKLOAD_TEXT))
     ap.add_argument("--splits", type=int, default=0, help="KV partitions (0 = automatic)")
+    ap.add_argument("--q-len", type=int, default=0,
+                    help="query tokens per sequence for causal multi-query attention "
+                         "(0 = single-token decode)")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", dest="cpu_baseline", action="store_false")
     ap.add_argument("--no-prefix-sharing", dest="prefix_sharing", action="store_false",

@@ -215,6 +215,40 @@ pkv_status pkv_decode_attention_prefix_shared(
     size_t workspace_bytes, pkv_dtype dtype, int32_t* err_flag, void* stream);
 
 /*
+ * Multi-query attention over the paged cache: q_len new query tokens per
+ * sequence, causal within the chunk.  This is the attention of a chunked-prefill
+ * chunk ([inference] "Chunked Prefill": the chunk's queries against the cached
+ * KV and the chunk's own KV) and of speculative verification, where the large
+ * model scores K drafted tokens plus one in a single pass ([inference]
+ * "投机采样 (Speculative Decoding)").  The chunk's K/V are appended first
+ * (pkv_append with q_len slots per sequence), so context_lens[b] counts them,
+ * and query token i of sequence b attends to positions 0 .. n_b - q_len + i
+ * (each query sees the keys up to its own position: [chapter12]
+ * Attention(Q_t, K_1:t, V_1:t)).
+ *
+ *   q, out        [num_seqs][q_len][num_q_heads][head_dim], dtype
+ *   context_lens  int32 [num_seqs], device: tokens in the cache per sequence,
+ *                 at least q_len (a shorter one is flagged PKV_EFLAG_CONTEXT_LEN;
+ *                 rows whose limit is not positive get a zero output)
+ *   other arguments as for pkv_decode_attention; workspace of at least
+ *   pkv_multi_query_workspace_size(...) bytes (contents on entry do not matter)
+ * Limits: num_seqs * num_kv_heads and num_seqs * q_len at most 65535.
+ * The (query token, query head) rows of one KV head form a dense matrix that
+ * meets every context token, so the products run on the tensor cores
+ * (tcgen05, 128 rows per CTA, accumulators in tensor memory), split over
+ * context partitions and merged by log-sum-exp as in pkv_merge.
+ */
+size_t pkv_multi_query_workspace_size(int num_seqs, int q_len, int num_q_heads, int num_kv_heads,
+                                      int head_dim, int block_size, int max_context_len);
+
+pkv_status pkv_multi_query_attention(
+    void* out, const void* q, const void* k_cache, const void* v_cache,
+    const int32_t* block_tables, int max_blocks_per_seq, const int32_t* context_lens,
+    int max_context_len, int num_seqs, int q_len, int num_blocks, int block_size,
+    int num_q_heads, int num_kv_heads, int head_dim, float scale, void* workspace,
+    size_t workspace_bytes, pkv_dtype dtype, int32_t* err_flag, void* stream);
+
+/*
  * Log-sum-exp merge of split-K partials ([inference] combine_result and the
  * exactness remark after it; [vllm-06] Flash-Decoding merges with the same
  * m / l rescale rule).  Each partial is stored normalised with its

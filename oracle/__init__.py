@@ -3,7 +3,8 @@
 A plain, slow, obviously correct CPU implementation (fp64) of what the CUDA
 library computes: the append (scatter through ``slot_mapping``), the gather
 through the block table, decode attention ``softmax(q K^T * scale) V`` with
-GQA, the pages' per-page partials and their online-softmax combine, and the
+GQA, causal multi-query attention (several new query tokens per sequence),
+the pages' per-page partials and their online-softmax combine, and the
 log-sum-exp merge of split partials.
 
 Only ``tests/``, ``__graft_entry__.smoke()`` and the benchmark's CPU-baseline
@@ -27,6 +28,7 @@ from .reference import (  # noqa: F401
     gather_kv,
     kv_cache_bytes,
     merge_lse,
+    multi_query_attention,
     num_threads,
     segment_partials,
 )

@@ -171,6 +171,33 @@ def decode_attention(q: np.ndarray, k_cache: np.ndarray, v_cache: np.ndarray,
     return out
 
 
+def multi_query_attention(q: np.ndarray, k_cache: np.ndarray, v_cache: np.ndarray,
+                          block_tables: np.ndarray, context_lens: np.ndarray, scale: float,
+                          dtype: str, lib: ctypes.CDLL = None) -> np.ndarray:
+    """Causal attention of q_len new query tokens per sequence, fp64.
+
+    q: uint16 [B, q_len, H_q, d]; the chunk's K/V are already in the cache and
+    counted by context_lens.  Query token i of sequence b attends to positions
+    0 .. n_b - q_len + i: a chunked-prefill chunk's queries see the cached KV
+    and the chunk's own KV up to their own position (LLM-101-CN "推理优化",
+    Chunked Prefill; each query attends to keys up to its own position, tutorial
+    chapter 12, Attention(Q_t, K_1:t, V_1:t)).  That is the decode-attention
+    definition applied to every query token with its own causal context length
+    (at least 0).  Returns float64 [B, q_len, H_q, d].
+    """
+    q = _bits(q)
+    num_seqs, q_len, h_q, d = q.shape
+    cl = np.asarray(context_lens, dtype=np.int64)
+    if cl.shape != (num_seqs,):
+        raise ValueError("inconsistent shapes")
+    limits = cl[:, None] - q_len + 1 + np.arange(q_len)[None, :]
+    rows = decode_attention(q.reshape(num_seqs * q_len, h_q, d), k_cache, v_cache,
+                            np.repeat(np.asarray(block_tables), q_len, axis=0),
+                            np.maximum(limits, 0).reshape(-1).astype(np.int32), scale, dtype,
+                            lib=lib)
+    return rows.reshape(num_seqs, q_len, h_q, d)
+
+
 def decode_attention_np(q: np.ndarray, k_cache: np.ndarray, v_cache: np.ndarray,
                         block_tables: np.ndarray, context_lens: np.ndarray,
                         scale: float) -> np.ndarray:

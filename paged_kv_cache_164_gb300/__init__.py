@@ -70,6 +70,10 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.pkv_prefix_shared_workspace_size.restype = sz
     lib.pkv_decode_attention_prefix_shared.argtypes = [p, p, p, p, p, i, p, i, i, i, i, i, i, i, f,
                                                        i, p, p, i, i, p, sz, i, p, p]
+    lib.pkv_multi_query_workspace_size.argtypes = [i, i, i, i, i, i, i]
+    lib.pkv_multi_query_workspace_size.restype = sz
+    lib.pkv_multi_query_attention.argtypes = [p, p, p, p, p, i, p, i, i, i, i, i, i, i, i, f, p,
+                                              sz, i, p, p]
     lib.pkv_merge.argtypes = [p, p, p, i, i, i, i, i, p]
     lib.pkv_gather.argtypes = [p, p, p, p, p, i, p, i, i, i, i, i, i, i, p, p]
     lib.pkv_check_error.argtypes = [p, p, ctypes.POINTER(ctypes.c_int32)]
@@ -78,7 +82,7 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.pkv_max_group_size.argtypes = []
     lib.pkv_selftest_wait_timeout.argtypes = [p, ctypes.c_ulonglong, p]
     for name in ("pkv_append", "pkv_decode_attention", "pkv_decode_attention_noalloc",
-                 "pkv_decode_attention_prefix_shared",
+                 "pkv_decode_attention_prefix_shared", "pkv_multi_query_attention",
                  "pkv_merge", "pkv_gather", "pkv_selftest_wait_timeout",
                  "pkv_check_error", "pkv_max_group_size"):
         getattr(lib, name).restype = i
@@ -254,6 +258,53 @@ def decode_attention_prefix_shared(q: torch.Tensor, k_cache: torch.Tensor, v_cac
         workspace.numel() * workspace.element_size(), _kv_dtype(k_cache),
         _opt(err_flag, "err_flag"), _stream(stream, q.device))
     _check(st, "pkv_decode_attention_prefix_shared")
+    return out
+
+
+def multi_query_workspace_size(num_seqs: int, q_len: int, num_q_heads: int, num_kv_heads: int,
+                               head_dim: int, block_size: int, max_context_len: int) -> int:
+    """Bytes of workspace ``multi_query_attention`` needs on the current device."""
+    n = load().pkv_multi_query_workspace_size(num_seqs, q_len, num_q_heads, num_kv_heads,
+                                              head_dim, block_size, max_context_len)
+    if n == SIZE_MAX:
+        raise PkvError(1, "pkv_multi_query_workspace_size")
+    return int(n)
+
+
+def multi_query_attention(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
+                          block_tables: torch.Tensor, context_lens: torch.Tensor,
+                          max_context_len: int, scale: Optional[float] = None,
+                          out: Optional[torch.Tensor] = None,
+                          workspace: Optional[torch.Tensor] = None,
+                          err_flag: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """Causal attention of q_len new query tokens per sequence over the paged cache.
+
+    q [B, q_len, H_q, d]; context_lens counts the cached tokens including the
+    q_len new ones (appended first); query token i of sequence b attends to
+    positions 0 .. context_lens[b] - q_len + i.
+    """
+    lib = load()
+    b, q_len, h_q, d = q.shape
+    nb, bs, h_kv, d2 = k_cache.shape
+    if d2 != d or v_cache.shape != k_cache.shape or block_tables.dim() != 2 or \
+            block_tables.shape[0] != b or context_lens.shape != (b,):
+        raise ValueError("inconsistent multi-query shapes")
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    dt = k_cache.dtype
+    if out is None:
+        out = torch.empty_like(q)
+    need = multi_query_workspace_size(b, q_len, h_q, h_kv, d, bs, max_context_len)
+    if workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    st = lib.pkv_multi_query_attention(
+        _dev(out, "out", dt), _dev(q, "q", dt), _dev(k_cache, "k_cache", dt),
+        _dev(v_cache, "v_cache", dt), _dev(block_tables, "block_tables", torch.int32),
+        block_tables.shape[1], _dev(context_lens, "context_lens", torch.int32),
+        int(max_context_len), b, q_len, nb, bs, h_q, h_kv, d, float(scale),
+        _dev(workspace, "workspace"), workspace.numel() * workspace.element_size(),
+        _kv_dtype(k_cache), _opt(err_flag, "err_flag"), _stream(stream, q.device))
+    _check(st, "pkv_multi_query_attention")
     return out
 
 

@@ -601,6 +601,7 @@ struct PrefixParams {
     int max_prefix_len;
     int prefix_chunk;     // prefix tokens per partition (a multiple of 64 and of block_size)
     int cap;              // context clamp
+    int q_len;            // 0: shared prefixes; > 0: multi-query (q_len query tokens per sequence)
     float scale_log2;
 };
 
@@ -719,8 +720,8 @@ prefix_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
 
     const int rt = blockIdx.x;                     // tile of 128 query rows
     const int g = blockIdx.y % p.num_kv_heads;     // KV head
-    const int grp = blockIdx.y / p.num_kv_heads;   // group
-    const int part = blockIdx.z;                   // prefix partition
+    const int grp = blockIdx.y / p.num_kv_heads;   // group (shared prefix) or sequence (multi-query)
+    const int part = blockIdx.z;                   // partition of the tokens
     const int tid = threadIdx.x;
     const int warp = tid >> 5;
     const int lane = tid & 31;
@@ -729,22 +730,51 @@ prefix_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
     ptx::launch_dependents();
     ptx::grid_dependency_wait();
 
-    if (grp >= p.num_groups) return;
-    int first, last, plen;
-    if (!prefix_group_valid(p, grp, first, last, plen)) return;
-    const int rows = (last - first) * p.group;
+    // The CTA's query rows and tokens.  Shared prefix (q_len == 0): row r is
+    // query head g*group + r % group of member first + r / group of group grp,
+    // against the group's prefix tokens.  Multi-query (q_len > 0): row r is
+    // query head g*group + r % group of query token i = r / group of sequence
+    // grp, against the sequence's context, causal within the chunk of q_len
+    // new tokens (token i sees positions < n - q_len + 1 + i).
+    int first, rows, t_limit, n_seq = 0;
+    if (p.q_len == 0) {
+        if (grp >= p.num_groups) return;
+        int last, plen;
+        if (!prefix_group_valid(p, grp, first, last, plen)) return;
+        rows = (last - first) * p.group;
+        t_limit = plen;
+    } else {
+        first = grp;
+        const int n_raw = __ldg(p.context_lens + first);
+        if ((n_raw < 0 || n_raw > p.cap || n_raw < p.q_len) && rt == 0 && g == 0 && part == 0 &&
+            threadIdx.x == 0)
+            flag_error(p.err_flag, PKV_EFLAG_CONTEXT_LEN);
+        n_seq = clamped_len(n_raw, p.cap);
+        rows = p.q_len * p.group;
+        t_limit = n_seq;
+    }
     const int row0 = rt * kPrefixTileRows;
     const int t_begin = part * p.prefix_chunk;
-    const int t_chunk_end = min(plen, t_begin + p.prefix_chunk);
+    const int t_chunk_end = min(t_limit, t_begin + p.prefix_chunk);
     if (row0 >= rows || t_begin >= t_chunk_end) return;
     const int page0 = t_begin / bs;
 
-    // This thread's query row (softmax warps) and its context limit.
+    // This thread's query row (softmax warps): its row of q and of the
+    // partials ([rows of q][H_q]), and its context limit.
     const int r = row0 + tid;
     const bool row_ok = warp < kPrefixSoftmaxWarps && r < rows;
-    const int seq = first + (row_ok ? r / p.group : 0);
     const int head = g * p.group + (row_ok ? r % p.group : 0);
-    const int lim = row_ok ? clamped_len(__ldg(p.context_lens + seq), p.cap) : 0;
+    int64_t qrow;
+    int lim = 0;
+    if (p.q_len == 0) {
+        const int seq = first + (row_ok ? r / p.group : 0);
+        qrow = (int64_t)seq * p.num_q_heads + head;
+        if (row_ok) lim = clamped_len(__ldg(p.context_lens + seq), p.cap);
+    } else {
+        const int i = row_ok ? r / p.group : 0;
+        qrow = ((int64_t)first * p.q_len + i) * p.num_q_heads + head;
+        if (row_ok) lim = max(0, n_seq - p.q_len + 1 + i);
+    }
 
     if (tid == 0) {
         for (int st = 0; st < NS; ++st) {
@@ -906,8 +936,7 @@ prefix_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
         // This row of Q into shared memory (16-byte chunk c of a 128-byte row
         // lands at chunk c ^ (row % 8): the 128-byte swizzle of the MMA operand).
         {
-            const uint4* src = reinterpret_cast<const uint4*>(
-                static_cast<const T*>(p.q) + ((int64_t)seq * p.num_q_heads + head) * D);
+            const uint4* src = reinterpret_cast<const uint4*>(static_cast<const T*>(p.q) + qrow * D);
 #pragma unroll
             for (int c = 0; c < D / 8; ++c) {
                 const uint4 v = row_ok ? __ldg(src + c) : make_uint4(0u, 0u, 0u, 0u);
@@ -1039,7 +1068,7 @@ prefix_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
             // Epilogue: this row's normalised O and log-sum-exp as prefix partial `part`.
             ptx::tc_fence_after_sync();
             const float inv = l > 0.f ? 1.f / l : 0.f;
-            const int64_t prow = ((int64_t)seq * p.num_q_heads + head) * p.num_splits + part;
+            const int64_t prow = qrow * p.num_splits + part;
             float* dst = p.partial_o + prow * D;
 #pragma unroll
             for (int c = 0; c < D / 32; ++c) {
@@ -1145,7 +1174,6 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const PlanParams p) 
         int cnt = 0;
         if (u < units) {
             const int b = u / p.num_kv_heads;
-            const int g = u - b * p.num_kv_heads;
             const int2 info = p.seq_info[b];
             const int n = clamped_len(p.context_lens[b], p.cap);
             cnt = suffix_partitions(max(0, n - info.x), info.y, p.chunk_tokens);
@@ -1183,8 +1211,10 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const PlanParams p) 
 // thread groups, interleaved subsets of the partitions; the groups' sums meet
 // in shared memory.  With context_lens given (the decode path), a sequence
 // whose context fitted a single partition was written by the decode kernel and
-// is skipped, and only the partitions that hold tokens are read.  Without
-// (pkv_merge), every row merges all num_splits partials.
+// is skipped, and only the partitions that hold tokens are read.  Multi-query
+// rows (q_len > 0) are always merged, from the partitions of their sequence's
+// context.  Without context_lens (pkv_merge), every row merges all num_splits
+// partials.
 struct MergeParams {
     void* out;
     const float* partial_o;
@@ -1198,6 +1228,7 @@ struct MergeParams {
     int head_dim;                 // a multiple of 4, at most 4 * kMergeThreads
     int chunk_tokens;
     int cap;                      // context clamp, as in the decode kernel
+    int q_len;                    // > 0: multi-query rows (sequence, query token); every row merged
 };
 
 constexpr int kMergeThreads = 128;
@@ -1208,12 +1239,16 @@ merge_kernel(const MergeParams p) {
     __shared__ float4 part[kMergeThreads];
     __shared__ float s_mx, s_inv;
     const int h = blockIdx.x;
-    const int b = blockIdx.y;
+    const int b = blockIdx.y;  // row of q: a sequence, or (sequence, query token) for multi-query
     const int tid = threadIdx.x;
     ptx::launch_dependents();
     ptx::grid_dependency_wait();
     int ns = p.num_splits;
-    if (p.context_lens != nullptr) {
+    if (p.q_len > 0) {
+        // multi-query partials: the partitions of the sequence's context
+        const int n = clamped_len(__ldg(p.context_lens + b / p.q_len), p.cap);
+        ns = (n + p.chunk_tokens - 1) / p.chunk_tokens;
+    } else if (p.context_lens != nullptr) {
         int start = 0, slot0 = 0;
         if (p.seq_info != nullptr) {
             const int2 si = __ldcg(p.seq_info + b);
@@ -1557,6 +1592,45 @@ static pkv_status make_prefix_plan(int num_seqs, int num_q_heads, int num_kv_hea
     return PKV_OK;
 }
 
+// Plan of a multi-query call: 128-row tiles of (query token, query head) rows
+// per (sequence, KV head); the context in partitions of whole 64-token tiles,
+// as many as give about one CTA per SM, at most kMaxChunkPages pages each.
+struct MultiQueryPlan {
+    int chunk;
+    int parts;
+    int row_tiles;
+    size_t workspace_bytes;
+};
+
+static pkv_status make_mq_plan(int num_seqs, int q_len, int num_q_heads, int num_kv_heads,
+                               int head_dim, int block_size, int max_context_len,
+                               MultiQueryPlan* mp) {
+    pkv_status st = check_shapes(num_seqs, num_q_heads, num_kv_heads, head_dim, block_size,
+                                 max_context_len, 0);
+    if (st != PKV_OK) return st;
+    if (q_len <= 0) return PKV_ERR_INVALID_ARG;
+    const int group = num_q_heads / num_kv_heads;
+    const int64_t rows = (int64_t)q_len * group;
+    mp->row_tiles = (int)((rows + kPrefixTileRows - 1) / kPrefixTileRows);
+    if ((int64_t)num_seqs * num_kv_heads > 65535 || mp->row_tiles > 65535 ||
+        (int64_t)num_seqs * q_len > 65535)
+        return PKV_ERR_UNSUPPORTED;
+    const int sms = current_sm_count();
+    if (sms <= 0) return PKV_ERR_CUDA;
+    const int64_t units = std::max<int64_t>(1, (int64_t)num_seqs * num_kv_heads * mp->row_tiles);
+    const int64_t want = std::max<int64_t>(1, sms / units);
+    const int tiles = std::max(1, (max_context_len + kPrefixTileTokens - 1) / kPrefixTileTokens);
+    const int max_tiles = kMaxChunkPages * block_size / kPrefixTileTokens;
+    const int chunk_tiles =
+        (int)std::min<int64_t>(max_tiles, std::max<int64_t>(1, (tiles + want - 1) / want));
+    mp->chunk = chunk_tiles * kPrefixTileTokens;
+    mp->parts = std::max(1, (max_context_len + mp->chunk - 1) / mp->chunk);
+    if (mp->parts > PKV_MAX_SPLITS || mp->parts > 65535) return PKV_ERR_UNSUPPORTED;
+    mp->workspace_bytes =
+        (size_t)num_seqs * q_len * num_q_heads * mp->parts * (head_dim + 1) * sizeof(float) + 256;
+    return PKV_OK;
+}
+
 }  // namespace pkv
 
 using namespace pkv;
@@ -1616,7 +1690,7 @@ extern "C" pkv_status pkv_decode_attention(void* out, const void* q, const void*
         !make_cache_map(&mv, v_cache, dtype, num_blocks, block_size, num_kv_heads, head_dim))
         return PKV_ERR_CUDA;
 
-    DecodeParams p;
+    DecodeParams p = {};
     p.out = out;
     p.q = q;
     p.block_tables = block_tables;
@@ -1650,7 +1724,7 @@ extern "C" pkv_status pkv_decode_attention(void* out, const void* q, const void*
         return PKV_ERR_CUDA;
     }
     if (plan.num_splits > 1) {
-        MergeParams mp;
+        MergeParams mp = {};
         mp.out = out;
         mp.partial_o = p.partial_o;
         mp.partial_lse = p.partial_lse;
@@ -1686,7 +1760,7 @@ extern "C" pkv_status pkv_merge(void* out, const float* partial_o, const float* 
         return PKV_ERR_INVALID_ARG;
     if (head_dim % 4 != 0 || head_dim > 4 * kMergeThreads) return PKV_ERR_UNSUPPORTED;
     if (num_seqs > 65535) return PKV_ERR_UNSUPPORTED;
-    MergeParams mp;
+    MergeParams mp = {};
     mp.out = out;
     mp.partial_o = partial_o;
     mp.partial_lse = partial_lse;
@@ -1776,7 +1850,7 @@ extern "C" pkv_status pkv_decode_attention_prefix_shared(
     cudaStream_t s = (cudaStream_t)stream;
 
     // 1. every sequence's prefix record and the list of suffix partitions with tokens
-    PlanParams pl;
+    PlanParams pl = {};
     pl.context_lens = context_lens;
     pl.group_start = group_start;
     pl.group_prefix_len = group_prefix_len;
@@ -1849,7 +1923,7 @@ extern "C" pkv_status pkv_decode_attention_prefix_shared(
     }
 
     // 3. suffix partials (or the whole answer for sequences without a prefix)
-    DecodeParams p;
+    DecodeParams p = {};
     p.out = out;
     p.q = q;
     p.block_tables = block_tables;
@@ -1879,7 +1953,7 @@ extern "C" pkv_status pkv_decode_attention_prefix_shared(
     }
 
     // 4. merge
-    MergeParams mp;
+    MergeParams mp = {};
     mp.out = out;
     mp.partial_o = partial_o;
     mp.partial_lse = partial_lse;
@@ -1894,6 +1968,108 @@ extern "C" pkv_status pkv_decode_attention_prefix_shared(
     mp.cap = cap;
     e = dtype == PKV_FP16 ? launch_merge<__half>(mp, num_q_heads, num_seqs, s)
                           : launch_merge<__nv_bfloat16>(mp, num_q_heads, num_seqs, s);
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return PKV_ERR_CUDA;
+    }
+    return PKV_OK;
+}
+
+extern "C" size_t pkv_multi_query_workspace_size(int num_seqs, int q_len, int num_q_heads,
+                                                 int num_kv_heads, int head_dim, int block_size,
+                                                 int max_context_len) {
+    MultiQueryPlan mp;
+    if (make_mq_plan(num_seqs, q_len, num_q_heads, num_kv_heads, head_dim, block_size,
+                     max_context_len, &mp) != PKV_OK)
+        return SIZE_MAX;
+    return mp.workspace_bytes;
+}
+
+extern "C" pkv_status pkv_multi_query_attention(
+    void* out, const void* q, const void* k_cache, const void* v_cache,
+    const int32_t* block_tables, int max_blocks_per_seq, const int32_t* context_lens,
+    int max_context_len, int num_seqs, int q_len, int num_blocks, int block_size,
+    int num_q_heads, int num_kv_heads, int head_dim, float scale, void* workspace,
+    size_t workspace_bytes, pkv_dtype dtype, int32_t* err_flag, void* stream) {
+    if ((dtype != PKV_FP16 && dtype != PKV_BF16) || max_blocks_per_seq <= 0 || num_blocks <= 0 ||
+        !std::isfinite(scale) || q_len <= 0)
+        return PKV_ERR_INVALID_ARG;
+    pkv_status st = check_shapes(num_seqs, num_q_heads, num_kv_heads, head_dim, block_size,
+                                 max_context_len, 0);
+    if (st != PKV_OK) return st;
+    if (num_seqs == 0) return PKV_OK;
+    if (!out || !q || !k_cache || !v_cache || !block_tables || !context_lens || !workspace)
+        return PKV_ERR_INVALID_ARG;
+    if (!aligned16(out) || !aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) ||
+        !aligned16(workspace) || (reinterpret_cast<uintptr_t>(block_tables) & 3u) ||
+        (reinterpret_cast<uintptr_t>(context_lens) & 3u))
+        return PKV_ERR_INVALID_ARG;
+    if ((int64_t)max_blocks_per_seq * block_size > INT_MAX) return PKV_ERR_UNSUPPORTED;
+    MultiQueryPlan mq;
+    st = make_mq_plan(num_seqs, q_len, num_q_heads, num_kv_heads, head_dim, block_size,
+                      max_context_len, &mq);
+    if (st != PKV_OK) return st;
+    if (workspace_bytes < mq.workspace_bytes) return PKV_ERR_WORKSPACE;
+
+    CUtensorMap mk, mv;
+    if (!make_cache_map(&mk, k_cache, dtype, num_blocks, block_size, num_kv_heads, head_dim) ||
+        !make_cache_map(&mv, v_cache, dtype, num_blocks, block_size, num_kv_heads, head_dim))
+        return PKV_ERR_CUDA;
+    float* partial_o = static_cast<float*>(workspace);
+    float* partial_lse = partial_o + (size_t)num_seqs * q_len * num_q_heads * mq.parts * head_dim;
+    const int cap = std::min(max_blocks_per_seq * block_size, max_context_len);
+    const int group = num_q_heads / num_kv_heads;
+    cudaStream_t s = (cudaStream_t)stream;
+
+    // 1. partials of every (query token, query head) row per context partition (tcgen05)
+    PrefixParams pr = {};
+    pr.q = q;
+    pr.block_tables = block_tables;
+    pr.context_lens = context_lens;
+    pr.partial_o = partial_o;
+    pr.partial_lse = partial_lse;
+    pr.err_flag = err_flag;
+    pr.max_blocks_per_seq = max_blocks_per_seq;
+    pr.num_blocks = num_blocks;
+    pr.block_size = block_size;
+    pr.num_seqs = num_seqs;
+    pr.num_q_heads = num_q_heads;
+    pr.num_kv_heads = num_kv_heads;
+    pr.group = group;
+    pr.num_splits = mq.parts;
+    pr.prefix_chunk = mq.chunk;
+    pr.cap = cap;
+    pr.q_len = q_len;
+    pr.scale_log2 = scale * kLog2e;
+    const dim3 pgrid(mq.row_tiles, num_seqs * num_kv_heads, mq.parts);
+    cudaError_t e;
+    if (head_dim == 64)
+        e = dtype == PKV_FP16 ? launch_prefix_t<__half, 64>(mk, mv, pr, pgrid, s)
+                              : launch_prefix_t<__nv_bfloat16, 64>(mk, mv, pr, pgrid, s);
+    else
+        e = dtype == PKV_FP16 ? launch_prefix_t<__half, 128>(mk, mv, pr, pgrid, s)
+                              : launch_prefix_t<__nv_bfloat16, 128>(mk, mv, pr, pgrid, s);
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return PKV_ERR_CUDA;
+    }
+
+    // 2. merge every row
+    MergeParams mp = {};
+    mp.out = out;
+    mp.partial_o = partial_o;
+    mp.partial_lse = partial_lse;
+    mp.context_lens = context_lens;
+    mp.num_q_heads = num_q_heads;
+    mp.num_kv_heads = num_kv_heads;
+    mp.group = group;
+    mp.num_splits = mq.parts;
+    mp.head_dim = head_dim;
+    mp.chunk_tokens = mq.chunk;
+    mp.cap = cap;
+    mp.q_len = q_len;
+    e = dtype == PKV_FP16 ? launch_merge<__half>(mp, num_q_heads, num_seqs * q_len, s)
+                          : launch_merge<__nv_bfloat16>(mp, num_q_heads, num_seqs * q_len, s);
     if (e != cudaSuccess) {
         cudaGetLastError();
         return PKV_ERR_CUDA;

@@ -87,6 +87,29 @@ def test_workspace_size_rejects_bad_arguments(lib):
     assert lib.pkv_decode_num_splits(2, 4, 2, 64, 16, 64, 8) == 4     # no more than the pages
 
 
+def _multi_query(lib, **kw):
+    a = dict(out=NULL, q=NULL, k=NULL, v=NULL, bt=NULL, mb=4, cl=NULL, mcl=64, B=2, ql=3, nb=8,
+             bs=16, hq=4, hkv=2, d=64, scale=0.125, ws=NULL, wsb=0, dt=0, err=NULL, stream=NULL)
+    a.update(kw)
+    return lib.pkv_multi_query_attention(a["out"], a["q"], a["k"], a["v"], a["bt"], a["mb"],
+                                         a["cl"], a["mcl"], a["B"], a["ql"], a["nb"], a["bs"],
+                                         a["hq"], a["hkv"], a["d"], a["scale"], a["ws"], a["wsb"],
+                                         a["dt"], a["err"], a["stream"])
+
+
+def test_multi_query_rejects_bad_arguments_without_launching(lib):
+    assert _multi_query(lib) == 1                 # null pointers
+    assert _multi_query(lib, ql=0) == 1           # no query tokens
+    assert _multi_query(lib, hq=5, hkv=2) == 1    # heads not a multiple
+    assert _multi_query(lib, d=96) == 2           # unsupported head_dim
+    assert _multi_query(lib, bs=8) == 2           # unsupported block_size
+    assert _multi_query(lib, dt=3) == 1
+    assert _multi_query(lib, scale=float("inf")) == 1
+    assert _multi_query(lib, B=0) == 0            # empty batch is a no-op
+    assert lib.pkv_multi_query_workspace_size(2, 0, 4, 2, 64, 16, 64) == pkv.SIZE_MAX
+    assert lib.pkv_multi_query_workspace_size(2, 3, 4, 2, 96, 16, 64) == pkv.SIZE_MAX
+
+
 def test_merge_and_gather_reject_bad_arguments(lib):
     assert lib.pkv_merge(NULL, NULL, NULL, 2, 4, 3, 64, 0, NULL) == 1
     assert lib.pkv_merge(NULL, NULL, NULL, 2, 4, 0, 64, 0, NULL) == 1

@@ -174,3 +174,20 @@ def test_long_context_plan_uses_at_least_four_partitions():
     s = w.spec
     assert pkv.decode_num_splits(s.num_seqs, s.num_q_heads, s.num_kv_heads, s.head_dim,
                                  s.block_size, w.max_context_len, 0) >= 4
+
+
+def test_direct_and_split_sequences_in_one_batch():
+    # Short sequences fit one partition and are written by the decode kernel
+    # directly; longer ones are split and merged.  Every explicit split count
+    # and the automatic plan must leave both kinds correct.
+    w = make_workload("c3", device="cuda", poison=True, num_seqs=4,
+                      lengths=("uniform", 200, 700), max_len_cap=768, seed=61)
+    expect, _, _ = oracle_after_append(w)
+    pkv.append(w.k_new, w.v_new, w.k_cache, w.v_cache, w.slot_mapping)
+    flag = pkv.new_error_flag("cuda")
+    for splits in (0, 1, 2, 3, 4, 5, 8):
+        out = pkv.decode_attention(w.q, w.k_cache, w.v_cache, w.block_tables, w.context_lens,
+                                   w.max_context_len, scale=w.scale, num_splits=splits,
+                                   err_flag=flag)
+        assert pkv.check_error(flag) == 0
+        assert_attention_close(out, expect, f"splits={splits}")

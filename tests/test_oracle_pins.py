@@ -15,7 +15,7 @@ import pytest
 import torch
 
 import oracle
-from workloads import bits, make_workload, make_append_case
+from workloads import bits, make_append_case, make_queries, make_workload
 
 GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
 
@@ -386,3 +386,65 @@ def test_append_reports_slot_beyond_pool():
     slots[3] = 4 * 16
     kc, vc = bits(c["k_cache"]).copy(), bits(c["v_cache"]).copy()
     assert oracle.append(kc, vc, bits(c["k_new"]), bits(c["v_new"]), slots) == -2
+
+
+# ---------------------------------------------------------------- multi-query (causal)
+
+def _causal_brute_force(q, k, v, n, scale):
+    """Contiguous causal attention for one sequence and one head, pure Python loops:
+    query token i of a chunk of L new tokens sees positions 0 .. n - L + i."""
+    L = q.shape[0]
+    out = np.zeros_like(q)
+    for i in range(L):
+        last = n - L + i
+        scores = [scale * float(np.dot(q[i], k[t])) for t in range(last + 1)]
+        m = max(scores)
+        w = [math.exp(x - m) for x in scores]
+        z = sum(w)
+        for t in range(last + 1):
+            out[i] += w[t] / z * v[t]
+    return out
+
+
+def test_multi_query_equals_causal_brute_force():
+    w = make_workload("c1")
+    s = w.spec
+    q_len = 4
+    q = make_queries(w, q_len, seed=3)
+    kc, vc = bits(w.k_cache), bits(w.v_cache)
+    bt = w.block_tables.numpy()
+    cl = w.context_lens.numpy()
+    got = oracle.multi_query_attention(bits(q), kc, vc, bt, cl, w.scale, s.dtype)
+    qv = oracle.decode_values(bits(q), s.dtype)
+    group = s.num_q_heads // s.num_kv_heads
+    for b in range(s.num_seqs):
+        n = int(cl[b])
+        for h in range(s.num_q_heads):
+            k, v = oracle.gather_kv(kc, vc, bt, n, b, h // group)
+            kd = oracle.decode_values(k, s.dtype)
+            vd = oracle.decode_values(v, s.dtype)
+            ref = _causal_brute_force(qv[b, :, h], kd, vd, n, w.scale)
+            assert np.allclose(got[b, :, h], ref, rtol=1e-12, atol=1e-13)
+
+
+def test_multi_query_of_one_token_is_decode_attention():
+    w = make_workload("c1")
+    q = make_queries(w, 1, seed=5)
+    args = (bits(w.k_cache), bits(w.v_cache), w.block_tables.numpy(), w.context_lens.numpy(),
+            w.scale, w.spec.dtype)
+    mq = oracle.multi_query_attention(bits(q), *args)
+    dec = oracle.decode_attention(bits(q)[:, 0], *args)
+    assert np.array_equal(mq[:, 0], dec)
+
+
+def test_multi_query_last_token_sees_whole_context_first_sees_less():
+    w = make_workload("c1")
+    q_len = 3
+    q = make_queries(w, q_len, seed=7)
+    kc, vc, bt, cl = bits(w.k_cache), bits(w.v_cache), w.block_tables.numpy(), w.context_lens.numpy()
+    mq = oracle.multi_query_attention(bits(q), kc, vc, bt, cl, w.scale, w.spec.dtype)
+    full = oracle.decode_attention(bits(q)[:, -1], kc, vc, bt, cl, w.scale, w.spec.dtype)
+    first = oracle.decode_attention(bits(q)[:, 0], kc, vc, bt, cl - (q_len - 1), w.scale,
+                                    w.spec.dtype)
+    assert np.array_equal(mq[:, -1], full)
+    assert np.array_equal(mq[:, 0], first)

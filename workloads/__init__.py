@@ -268,6 +268,15 @@ def make_workload(name_or_spec, device="cpu", poison: bool = False, with_values:
                     group_start=gstart, group_prefix_len=gplen)
 
 
+def make_queries(w: Workload, q_len: int, seed: int) -> torch.Tensor:
+    """Seeded N(0,1) queries [B, q_len, H_q, d] in the workload's dtype and device
+    (several new query tokens per sequence: a prefill chunk or drafted tokens)."""
+    s = w.spec
+    dev = w.context_lens.device
+    g = torch.Generator(device=dev).manual_seed(seed * 7919 + 29)
+    return _values((s.num_seqs, q_len, s.num_q_heads, s.head_dim), TORCH_DTYPES[s.dtype], dev, g)
+
+
 def make_append_case(num_tokens: int, num_blocks: int, block_size: int, num_kv_heads: int,
                      head_dim: int, dtype: str, seed: int, pad_fraction: float = 0.25,
                      device="cpu") -> dict:
