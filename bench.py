@@ -346,7 +346,10 @@ def run_gpu(args):
     flag = pkv.new_error_flag(device)
     # append, decode, merge when split; the shared-prefix path: append, plan,
     # prefix, decode, merge
-    launches_per_step = 3 if mq else 5 if shared else 2 + (1 if splits > 1 else 0)
+    # --fused: the append is done by the decode kernel (plain path only)
+    fused = args.fused and not mq and not shared
+    launches_per_step = (3 if mq else 5 if shared else
+                         (1 if fused else 2) + (1 if splits > 1 else 0))
 
     def decode_call(q, block_tables, context_lens):
         if mq:
@@ -363,6 +366,12 @@ def run_gpu(args):
                                  workspace=workspace, err_flag=flag)
 
     def step():
+        if fused:
+            pkv.append_decode_attention(w.q, w.k_new, w.v_new, w.k_cache, w.v_cache,
+                                        w.block_tables, w.context_lens, mcl, scale=w.scale,
+                                        num_splits=args.splits, out=out, workspace=workspace,
+                                        err_flag=flag)
+            return
         pkv.append(w.k_new, w.v_new, w.k_cache, w.v_cache, w.slot_mapping, err_flag=flag)
         decode_call(w.q, w.block_tables, w.context_lens)
 
@@ -383,12 +392,27 @@ def run_gpu(args):
         sampler.wait_first()
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
+    run_steps = None
+    if args.graph:
+        # one step captured in a CUDA graph (the library's set-up ran in the
+        # warm-up above), replayed K times: one graph launch per step
+        side = torch.cuda.Stream(device)
+        side.wait_stream(stream)
+        with torch.cuda.stream(side):
+            step()
+        stream.wait_stream(side)
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            step()
+        graph.replay()
+        torch.cuda.synchronize(device)
+        run_steps = graph.replay
     barrier(device)
     torch.cuda.synchronize(device)
     t_begin = time.time()
     e0.record(stream)
     for _ in range(args.steps):
-        step()
+        (run_steps or step)()
     e1.record(stream)
     torch.cuda.synchronize(device)
     t_end = time.time()
@@ -480,6 +504,7 @@ def run_gpu(args):
                    "max_context_len": mcl, "num_splits": splits, "accumulate": "fp32",
                    "shared_prefix_decode": shared,
                    "q_len": args.q_len if mq else 1,
+                   "fused_append": fused, "cuda_graph": bool(args.graph),
                    "kv_bytes_unique": nbytes["kv_unique"],
                    "decode_bytes_per_step": nbytes["decode"],
                    "decode_bytes_logical": nbytes["decode_logical"],
@@ -517,6 +542,10 @@ def main(argv=None):
     ap.add_argument("--impl", choices=["mine", "reference"], default="mine")
     ap.add_argument("--config", default="c2", choices=sorted(WORKLOAD_TEXT))
     ap.add_argument("--splits", type=int, default=0, help="KV partitions (0 = automatic)")
+    ap.add_argument("--fused", action="store_true",
+                    help="append inside the decode launch (pkv_append_decode_attention)")
+    ap.add_argument("--graph", action="store_true",
+                    help="time replays of one step captured in a CUDA graph")
     ap.add_argument("--q-len", type=int, default=0,
                     help="query tokens per sequence for causal multi-query attention "
                          "(0 = single-token decode)")

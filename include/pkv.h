@@ -139,6 +139,34 @@ pkv_status pkv_decode_attention(void* out, const void* q, const void* k_cache,
                                 void* stream);
 
 /*
+ * One decode step in one launch: the append of one new token per sequence
+ * followed by decode attention, with the append done by the decode kernel
+ * itself (the pages list KV-cache writes among the ops worth fusing into
+ * their neighbours: [vllm-06] kernel fusion).  The result, and the cache after
+ * the call, are those of pkv_append with slot_mapping[b] = the slot of
+ * position context_lens[b] - 1 of sequence b (block
+ * block_tables[b][(n-1) / block_size], offset (n-1) % block_size), followed by
+ * pkv_decode_attention.
+ *
+ *   k_new, v_new  [num_seqs][num_kv_heads][head_dim], dtype: sequence b's new
+ *                 token, written at position context_lens[b] - 1
+ *   k_cache, v_cache  written at those slots; the slots must not be shared
+ *                 with another sequence (a page being appended to is private)
+ *   other arguments as for pkv_decode_attention
+ * A sequence with a bad last block id, or a context_len that is negative or
+ * too long, is flagged and its new token is not written.
+ */
+pkv_status pkv_append_decode_attention(void* out, const void* q, const void* k_new,
+                                       const void* v_new, void* k_cache, void* v_cache,
+                                       const int32_t* block_tables, int max_blocks_per_seq,
+                                       const int32_t* context_lens, int max_context_len,
+                                       int num_seqs, int num_blocks, int block_size,
+                                       int num_q_heads, int num_kv_heads, int head_dim,
+                                       float scale, int num_splits, void* workspace,
+                                       size_t workspace_bytes, pkv_dtype dtype,
+                                       int32_t* err_flag, void* stream);
+
+/*
  * Decode attention for callers that cannot allocate device memory.
  *
  * The paper has no counterpart to this call; it exists for integration.  Some

@@ -64,6 +64,8 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.pkv_decode_num_splits.restype = i
     lib.pkv_decode_attention.argtypes = [p, p, p, p, p, i, p, i, i, i, i, i, i, i, f, i, p, sz,
                                          i, p, p]
+    lib.pkv_append_decode_attention.argtypes = [p, p, p, p, p, p, p, i, p, i, i, i, i, i, i, i,
+                                                f, i, p, sz, i, p, p]
     lib.pkv_decode_attention_noalloc.argtypes = [p, p, p, p, p, i, p, i, i, i, i, i, i, i, f,
                                                  i, i, p, p]
     lib.pkv_prefix_shared_workspace_size.argtypes = [i, i, i, i, i, i, i, i, i]
@@ -82,6 +84,7 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.pkv_max_group_size.argtypes = []
     lib.pkv_selftest_wait_timeout.argtypes = [p, ctypes.c_ulonglong, p]
     for name in ("pkv_append", "pkv_decode_attention", "pkv_decode_attention_noalloc",
+                 "pkv_append_decode_attention",
                  "pkv_decode_attention_prefix_shared", "pkv_multi_query_attention",
                  "pkv_merge", "pkv_gather", "pkv_selftest_wait_timeout",
                  "pkv_check_error", "pkv_max_group_size"):
@@ -200,6 +203,44 @@ def decode_attention(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tens
         int(max_context_len), b, nb, bs, h_q, h_kv, d, float(scale), int(num_splits), ws_ptr,
         ws_bytes, _kv_dtype(k_cache), _opt(err_flag, "err_flag"), _stream(stream, q.device))
     _check(st, "pkv_decode_attention")
+    return out
+
+
+def append_decode_attention(q: torch.Tensor, k_new: torch.Tensor, v_new: torch.Tensor,
+                            k_cache: torch.Tensor, v_cache: torch.Tensor,
+                            block_tables: torch.Tensor, context_lens: torch.Tensor,
+                            max_context_len: int, scale: Optional[float] = None,
+                            num_splits: int = 0, out: Optional[torch.Tensor] = None,
+                            workspace: Optional[torch.Tensor] = None,
+                            err_flag: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """One decode step in one launch: sequence b's new token (k_new[b], v_new[b],
+    [B, H_kv, d]) is written at position context_lens[b] - 1 of its block table,
+    then ``decode_attention`` runs over the updated cache."""
+    lib = load()
+    b, h_q, d = q.shape
+    nb, bs, h_kv, d2 = k_cache.shape
+    if d2 != d or v_cache.shape != k_cache.shape or block_tables.dim() != 2 or \
+            block_tables.shape[0] != b or context_lens.shape != (b,) or \
+            k_new.shape != (b, h_kv, d) or v_new.shape != (b, h_kv, d):
+        raise ValueError("inconsistent append-decode shapes")
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    dt = k_cache.dtype
+    if out is None:
+        out = torch.empty_like(q)
+    need = workspace_size(b, h_q, h_kv, d, bs, max_context_len, num_splits)
+    if workspace is None and need > 0:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    ws_ptr = ctypes.c_void_p(0) if workspace is None else _dev(workspace, "workspace")
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    st = lib.pkv_append_decode_attention(
+        _dev(out, "out", dt), _dev(q, "q", dt), _dev(k_new, "k_new", dt), _dev(v_new, "v_new", dt),
+        _dev(k_cache, "k_cache", dt), _dev(v_cache, "v_cache", dt),
+        _dev(block_tables, "block_tables", torch.int32), block_tables.shape[1],
+        _dev(context_lens, "context_lens", torch.int32), int(max_context_len), b, nb, bs, h_q,
+        h_kv, d, float(scale), int(num_splits), ws_ptr, ws_bytes, _kv_dtype(k_cache),
+        _opt(err_flag, "err_flag"), _stream(stream, q.device))
+    _check(st, "pkv_append_decode_attention")
     return out
 
 

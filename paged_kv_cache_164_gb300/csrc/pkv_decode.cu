@@ -65,6 +65,10 @@ struct DecodeParams {
     const int32_t* context_lens;
     float* partial_o;    // [B][H_q][num_splits][D] when num_splits > 1
     float* partial_lse;  // [B][H_q][num_splits]
+    const void* k_new;     // nullable: fused append of one new token per sequence ([B][H_kv][D])
+    const void* v_new;
+    void* k_cache;         // the caches, for the fused append's stores
+    void* v_cache;
     const int2* seq_info;  // nullable: per sequence (shared-prefix tokens, prefix partials written)
     const int2* items;     // nullable: compact list of (unit b*H_kv+g, partition); CTA x takes item x
     const int* item_count;
@@ -337,6 +341,26 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
     const int t_end = min(n, start + (split + 1) * p.chunk_tokens);
     const int nstages = t_end > t_begin ? (t_end - t_begin + kStageTokens - 1) / kStageTokens : 0;
     const bool direct = slot0 == 0 && nsplit == 1;  // the whole answer is this CTA's
+
+    // Fused append: the one CTA of (sequence, KV head) whose partition holds the
+    // last position n-1 first stores the new token's K and V rows of this KV
+    // head into that position's slot, then orders the stores before its own
+    // TMA reads (no other CTA reads that position).
+    if (p.k_new != nullptr && n_raw == n && n > 0 && t_begin <= n - 1 && n - 1 < t_end &&
+        warp < kConsumerWarps && tid < 2 * (D / 8)) {
+        const int pos = n - 1;
+        const int blk = __ldg(p.block_tables + (int64_t)b * p.max_blocks_per_seq + pos / bs);
+        if (blk >= 0 && blk < p.num_blocks) {
+            const bool is_v = tid >= D / 8;
+            const int c = tid % (D / 8);  // 16-byte chunk of the row
+            const int64_t src = ((int64_t)b * p.num_kv_heads + g) * (D / 8) + c;
+            const int64_t dst =
+                (((int64_t)blk * bs + pos % bs) * p.num_kv_heads + g) * (D / 8) + c;
+            const uint4 v = __ldg(static_cast<const uint4*>(is_v ? p.v_new : p.k_new) + src);
+            static_cast<uint4*>(is_v ? p.v_cache : p.k_cache)[dst] = v;
+            ptx::fence_proxy_async_global();
+        }
+    }
 
     if (tid == 0) {
         for (int s = 0; s < S; ++s) {
@@ -1655,14 +1679,15 @@ extern "C" int pkv_decode_num_splits(int num_seqs, int num_q_heads, int num_kv_h
     return plan.num_splits;
 }
 
-extern "C" pkv_status pkv_decode_attention(void* out, const void* q, const void* k_cache,
-                                           const void* v_cache, const int32_t* block_tables,
-                                           int max_blocks_per_seq, const int32_t* context_lens,
-                                           int max_context_len, int num_seqs, int num_blocks,
-                                           int block_size, int num_q_heads, int num_kv_heads,
-                                           int head_dim, float scale, int num_splits,
-                                           void* workspace, size_t workspace_bytes,
-                                           pkv_dtype dtype, int32_t* err_flag, void* stream) {
+// The plain decode, with the new tokens' K/V appended by the decode kernel
+// itself when k_new / v_new are given.
+static pkv_status decode_impl(void* out, const void* q, const void* k_new, const void* v_new,
+                              void* k_cache, void* v_cache, const int32_t* block_tables,
+                              int max_blocks_per_seq, const int32_t* context_lens,
+                              int max_context_len, int num_seqs, int num_blocks, int block_size,
+                              int num_q_heads, int num_kv_heads, int head_dim, float scale,
+                              int num_splits, void* workspace, size_t workspace_bytes,
+                              pkv_dtype dtype, int32_t* err_flag, void* stream) {
     pkv_status st = check_shapes(num_seqs, num_q_heads, num_kv_heads, head_dim, block_size,
                                  max_context_len, num_splits);
     if (st != PKV_OK) return st;
@@ -1675,6 +1700,9 @@ extern "C" pkv_status pkv_decode_attention(void* out, const void* q, const void*
     if (!aligned16(out) || !aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) ||
         (reinterpret_cast<uintptr_t>(block_tables) & 3u) ||
         (reinterpret_cast<uintptr_t>(context_lens) & 3u))
+        return PKV_ERR_INVALID_ARG;
+    if ((k_new == nullptr) != (v_new == nullptr) ||
+        (k_new != nullptr && (!aligned16(k_new) || !aligned16(v_new))))
         return PKV_ERR_INVALID_ARG;
     if ((int64_t)max_blocks_per_seq * block_size > INT_MAX) return PKV_ERR_UNSUPPORTED;
     Plan plan;
@@ -1711,6 +1739,10 @@ extern "C" pkv_status pkv_decode_attention(void* out, const void* q, const void*
     p.seq_info = nullptr;
     p.items = nullptr;
     p.item_count = nullptr;
+    p.k_new = k_new;
+    p.v_new = v_new;
+    p.k_cache = k_cache;
+    p.v_cache = v_cache;
     if (plan.num_splits > 1) {
         p.partial_o = static_cast<float*>(workspace);
         p.partial_lse = p.partial_o + (size_t)num_seqs * num_q_heads * plan.num_splits * head_dim;
@@ -1745,6 +1777,37 @@ extern "C" pkv_status pkv_decode_attention(void* out, const void* q, const void*
         }
     }
     return PKV_OK;
+}
+
+extern "C" pkv_status pkv_decode_attention(void* out, const void* q, const void* k_cache,
+                                           const void* v_cache, const int32_t* block_tables,
+                                           int max_blocks_per_seq, const int32_t* context_lens,
+                                           int max_context_len, int num_seqs, int num_blocks,
+                                           int block_size, int num_q_heads, int num_kv_heads,
+                                           int head_dim, float scale, int num_splits,
+                                           void* workspace, size_t workspace_bytes,
+                                           pkv_dtype dtype, int32_t* err_flag, void* stream) {
+    return decode_impl(out, q, nullptr, nullptr, const_cast<void*>(k_cache),
+                       const_cast<void*>(v_cache), block_tables, max_blocks_per_seq, context_lens,
+                       max_context_len, num_seqs, num_blocks, block_size, num_q_heads,
+                       num_kv_heads, head_dim, scale, num_splits, workspace, workspace_bytes,
+                       dtype, err_flag, stream);
+}
+
+extern "C" pkv_status pkv_append_decode_attention(
+    void* out, const void* q, const void* k_new, const void* v_new, void* k_cache, void* v_cache,
+    const int32_t* block_tables, int max_blocks_per_seq, const int32_t* context_lens,
+    int max_context_len, int num_seqs, int num_blocks, int block_size, int num_q_heads,
+    int num_kv_heads, int head_dim, float scale, int num_splits, void* workspace,
+    size_t workspace_bytes, pkv_dtype dtype, int32_t* err_flag, void* stream) {
+    const pkv_status st = check_shapes(num_seqs, num_q_heads, num_kv_heads, head_dim, block_size,
+                                       max_context_len, num_splits);
+    if (st != PKV_OK) return st;
+    if (num_seqs > 0 && (k_new == nullptr || v_new == nullptr)) return PKV_ERR_INVALID_ARG;
+    return decode_impl(out, q, k_new, v_new, k_cache, v_cache, block_tables, max_blocks_per_seq,
+                       context_lens, max_context_len, num_seqs, num_blocks, block_size,
+                       num_q_heads, num_kv_heads, head_dim, scale, num_splits, workspace,
+                       workspace_bytes, dtype, err_flag, stream);
 }
 
 extern "C" pkv_status pkv_merge(void* out, const float* partial_o, const float* partial_lse,

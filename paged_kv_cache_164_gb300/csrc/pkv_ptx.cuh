@@ -164,6 +164,12 @@ __device__ __forceinline__ void fence_proxy_async_smem() {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
+// Makes this thread's generic-proxy writes to global memory visible to later
+// async-proxy (TMA) reads.
+__device__ __forceinline__ void fence_proxy_async_global() {
+    asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+
 // Shared-memory matrix descriptor of a 128-byte-swizzled operand (rows of 128
 // bytes, 8-row atoms of 1024 bytes; the atom base must be 1024-byte aligned).
 // lbo / sbo are the leading / stride byte offsets of the canonical layout.

@@ -97,6 +97,17 @@ def _multi_query(lib, **kw):
                                          a["dt"], a["err"], a["stream"])
 
 
+def test_append_decode_rejects_bad_arguments_without_launching(lib):
+    f = lib.pkv_append_decode_attention
+    # null pointers (including the new tokens), bad head_dim, empty batch
+    assert f(NULL, NULL, NULL, NULL, NULL, NULL, NULL, 4, NULL, 64, 2, 8, 16, 4, 2, 64, 0.125, 1,
+             NULL, 0, 0, NULL, NULL) == 1
+    assert f(NULL, NULL, NULL, NULL, NULL, NULL, NULL, 4, NULL, 64, 2, 8, 16, 4, 2, 96, 0.125, 1,
+             NULL, 0, 0, NULL, NULL) == 2
+    assert f(NULL, NULL, NULL, NULL, NULL, NULL, NULL, 4, NULL, 64, 0, 8, 16, 4, 2, 64, 0.125, 1,
+             NULL, 0, 0, NULL, NULL) == 0
+
+
 def test_multi_query_rejects_bad_arguments_without_launching(lib):
     assert _multi_query(lib) == 1                 # null pointers
     assert _multi_query(lib, ql=0) == 1           # no query tokens
