@@ -301,7 +301,7 @@ def run_gpu(args):
     import torch.distributed as dist
 
     import paged_kv_cache_164_gb300 as pkv
-    from workloads import make_queries, make_workload
+    from workloads import make_queries, make_workload, to_head_major
 
     ws, rank, local = _dist_env()
     if ws > 1:
@@ -311,11 +311,18 @@ def run_gpu(args):
     torch.cuda.set_device(device)
     pkv.load()
 
+    # --block-size: the workload with another page size
+    overrides = {"block_size": args.block_size} if args.block_size else {}
     if ws > 1:  # an independent replica per rank
         from workloads import SPECS
-        w = make_workload(args.config, device=device, seed=SPECS[args.config].seed + 1000 * rank)
+        w = make_workload(args.config, device=device, seed=SPECS[args.config].seed + 1000 * rank,
+                          **overrides)
     else:
-        w = make_workload(args.config, device=device)
+        w = make_workload(args.config, device=device, **overrides)
+    layout = args.layout
+    if layout == "hnd":  # the same values in the head-major page layout
+        w.k_cache = to_head_major(w.k_cache)
+        w.v_cache = to_head_major(w.v_cache)
     s = w.spec
     # --q-len N: causal multi-query attention of N query tokens per sequence
     # (a prefill chunk or speculative verification) in place of the decode
@@ -354,25 +361,27 @@ def run_gpu(args):
     def decode_call(q, block_tables, context_lens):
         if mq:
             pkv.multi_query_attention(q, w.k_cache, w.v_cache, block_tables, context_lens, mcl,
-                                      scale=w.scale, out=out, workspace=workspace, err_flag=flag)
+                                      scale=w.scale, out=out, workspace=workspace, err_flag=flag,
+                                      layout=layout)
         elif shared:
             pkv.decode_attention_prefix_shared(
                 q, w.k_cache, w.v_cache, block_tables, context_lens, mcl, w.group_start,
                 w.group_prefix_len, max_group_size, max_prefix_len, scale=w.scale, out=out,
-                workspace=workspace, err_flag=flag)
+                workspace=workspace, err_flag=flag, layout=layout)
         else:
             pkv.decode_attention(q, w.k_cache, w.v_cache, block_tables, context_lens, mcl,
                                  scale=w.scale, num_splits=args.splits, out=out,
-                                 workspace=workspace, err_flag=flag)
+                                 workspace=workspace, err_flag=flag, layout=layout)
 
     def step():
         if fused:
             pkv.append_decode_attention(w.q, w.k_new, w.v_new, w.k_cache, w.v_cache,
                                         w.block_tables, w.context_lens, mcl, scale=w.scale,
                                         num_splits=args.splits, out=out, workspace=workspace,
-                                        err_flag=flag)
+                                        err_flag=flag, layout=layout)
             return
-        pkv.append(w.k_new, w.v_new, w.k_cache, w.v_cache, w.slot_mapping, err_flag=flag)
+        pkv.append(w.k_new, w.v_new, w.k_cache, w.v_cache, w.slot_mapping, err_flag=flag,
+                   layout=layout)
         decode_call(w.q, w.block_tables, w.context_lens)
 
     for _ in range(args.warmup):
@@ -451,7 +460,7 @@ def run_gpu(args):
         for k, t in host.items():
             dev_in[k].copy_(t, non_blocking=True)
         pkv.append(dev_in["k_new"], dev_in["v_new"], w.k_cache, w.v_cache,
-                   dev_in["slot_mapping"], err_flag=flag)
+                   dev_in["slot_mapping"], err_flag=flag, layout=layout)
         decode_call(dev_in["q"], dev_in["block_tables"], dev_in["context_lens"])
         out_h.copy_(out, non_blocking=True)
 
@@ -482,7 +491,7 @@ def run_gpu(args):
     traffic = None
     rec = NCU_TRAFFIC.get(args.config)
     if rec and rec.get("digest") == _kernel_digest() and rec.get("splits") == splits and \
-            rec.get("shared") == shared and not mq:
+            rec.get("shared") == shared and not mq and layout == "nhd" and not args.block_size:
         traffic = rec["bytes"]
 
     cpu = None
@@ -505,6 +514,7 @@ def run_gpu(args):
                    "shared_prefix_decode": shared,
                    "q_len": args.q_len if mq else 1,
                    "fused_append": fused, "cuda_graph": bool(args.graph),
+                   "layout": layout,
                    "kv_bytes_unique": nbytes["kv_unique"],
                    "decode_bytes_per_step": nbytes["decode"],
                    "decode_bytes_logical": nbytes["decode_logical"],
@@ -542,6 +552,11 @@ def main(argv=None):
     ap.add_argument("--impl", choices=["mine", "reference"], default="mine")
     ap.add_argument("--config", default="c2", choices=sorted(WORKLOAD_TEXT))
     ap.add_argument("--splits", type=int, default=0, help="KV partitions (0 = automatic)")
+    ap.add_argument("--layout", choices=["nhd", "hnd"], default="nhd",
+                    help="page layout: token major [blocks][bs][H_kv][d] or head major "
+                         "[blocks][H_kv][bs][d]")
+    ap.add_argument("--block-size", type=int, default=0,
+                    help="tokens per page (0 = the workload's own)")
     ap.add_argument("--fused", action="store_true",
                     help="append inside the decode launch (pkv_append_decode_attention)")
     ap.add_argument("--graph", action="store_true",

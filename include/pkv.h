@@ -16,6 +16,11 @@
  *   - 16-bit element types: PKV_FP16 (IEEE binary16) or PKV_BF16 (bfloat16).
  *   - Cache layout, "organised by page" ([inference] "PagedAttention 内核实现"):
  *       k_cache, v_cache: [num_blocks][block_size][num_kv_heads][head_dim]
+ *     or, with PKV_LAYOUT_HND OR-ed into the dtype argument of a call, head
+ *     major ([chapter12] PagedKVCache, one [heads][page_size][head_dim] slab
+ *     per page):
+ *       k_cache, v_cache: [num_blocks][num_kv_heads][block_size][head_dim]
+ *     where each (page, head) is one contiguous block_size x head_dim tile.
  *   - Argument errors are found on the host before any launch: the call
  *     returns a status and launches nothing.
  *   - Bad indices found on the device (a block id outside [0, num_blocks), a
@@ -23,7 +28,7 @@
  *     max_context_len) never fault: the offending token is skipped and a bit
  *     is OR-ed into the optional device word *err_flag (PKV_EFLAG_*), which
  *     the caller zero-initialises and reads back with pkv_check_error.
- *   - Supported sizes: head_dim in {64, 128}; block_size in {16, 32};
+ *   - Supported sizes: head_dim in {64, 128}; block_size in {16, 32, 64, 128};
  *     num_q_heads a multiple of num_kv_heads with at most 16 query heads per
  *     KV head.
  */
@@ -48,6 +53,10 @@ typedef enum {
 } pkv_status;
 
 typedef enum { PKV_FP16 = 0, PKV_BF16 = 1 } pkv_dtype;
+
+/* OR-ed into the dtype argument of a call that reads or writes the cache:
+   the caches are head major, [num_blocks][num_kv_heads][block_size][head_dim]. */
+#define PKV_LAYOUT_HND 0x100
 
 /* Bits OR-ed into *err_flag by the kernels. */
 #define PKV_EFLAG_BLOCK_ID      0x1  /* block id outside [0, num_blocks) */

@@ -125,6 +125,26 @@ def _kv_dtype(t: torch.Tensor) -> int:
     return _DTYPES[t.dtype]
 
 
+LAYOUT_HND = 0x100
+_LAYOUTS = ("nhd", "hnd")
+
+
+def _cache_dims(k_cache: torch.Tensor, layout: str):
+    """(num_blocks, block_size, num_kv_heads, head_dim) of a token-major ("nhd",
+    [blocks][bs][H_kv][d]) or head-major ("hnd", [blocks][H_kv][bs][d]) cache."""
+    if layout not in _LAYOUTS:
+        raise ValueError(f"layout must be one of {_LAYOUTS}, got {layout!r}")
+    if k_cache.dim() != 4:
+        raise ValueError("a cache is 4-D")
+    nb, a, c, d = k_cache.shape
+    return (nb, a, c, d) if layout == "nhd" else (nb, c, a, d)
+
+
+def _kv_code(k_cache: torch.Tensor, layout: str) -> int:
+    """The dtype argument for a call that takes the cache: element type plus layout flag."""
+    return _kv_dtype(k_cache) | (LAYOUT_HND if layout == "hnd" else 0)
+
+
 def new_error_flag(device) -> torch.Tensor:
     """A zeroed int32 device word for the kernels' index/timeout flags."""
     return torch.zeros(1, dtype=torch.int32, device=device)
@@ -132,10 +152,10 @@ def new_error_flag(device) -> torch.Tensor:
 
 def append(k_new: torch.Tensor, v_new: torch.Tensor, k_cache: torch.Tensor,
            v_cache: torch.Tensor, slot_mapping: torch.Tensor,
-           err_flag: Optional[torch.Tensor] = None, stream=None) -> None:
+           err_flag: Optional[torch.Tensor] = None, stream=None, layout: str = "nhd") -> None:
     """Scatters k_new/v_new [T, H_kv, d] into the caches at ``slot_mapping`` (int64 [T])."""
     lib = load()
-    nb, bs, h_kv, d = k_cache.shape
+    nb, bs, h_kv, d = _cache_dims(k_cache, layout)
     if v_cache.shape != k_cache.shape or k_new.shape[1:] != (h_kv, d) or \
             v_new.shape != k_new.shape or slot_mapping.shape != (k_new.shape[0],):
         raise ValueError("inconsistent append shapes")
@@ -143,7 +163,7 @@ def append(k_new: torch.Tensor, v_new: torch.Tensor, k_cache: torch.Tensor,
     st = lib.pkv_append(_dev(k_new, "k_new", dt), _dev(v_new, "v_new", dt),
                         _dev(k_cache, "k_cache", dt), _dev(v_cache, "v_cache", dt),
                         _dev(slot_mapping, "slot_mapping", torch.int64), k_new.shape[0], nb, bs,
-                        h_kv, d, _kv_dtype(k_cache), _opt(err_flag, "err_flag"),
+                        h_kv, d, _kv_code(k_cache, layout), _opt(err_flag, "err_flag"),
                         _stream(stream, k_cache.device))
     _check(st, "pkv_append")
 
@@ -173,7 +193,8 @@ def decode_attention(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tens
                      max_context_len: int, scale: Optional[float] = None, num_splits: int = 0,
                      out: Optional[torch.Tensor] = None,
                      workspace: Optional[torch.Tensor] = None,
-                     err_flag: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+                     err_flag: Optional[torch.Tensor] = None, stream=None,
+                     layout: str = "nhd") -> torch.Tensor:
     """softmax(q K^T * scale) V per sequence and query head over the paged cache.
 
     q [B, H_q, d]; caches [num_blocks, bs, H_kv, d]; block_tables int32
@@ -182,7 +203,7 @@ def decode_attention(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tens
     """
     lib = load()
     b, h_q, d = q.shape
-    nb, bs, h_kv, d2 = k_cache.shape
+    nb, bs, h_kv, d2 = _cache_dims(k_cache, layout)
     if d2 != d or v_cache.shape != k_cache.shape or block_tables.dim() != 2 or \
             block_tables.shape[0] != b or context_lens.shape != (b,):
         raise ValueError("inconsistent decode shapes")
@@ -201,7 +222,7 @@ def decode_attention(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tens
         _dev(v_cache, "v_cache", dt), _dev(block_tables, "block_tables", torch.int32),
         block_tables.shape[1], _dev(context_lens, "context_lens", torch.int32),
         int(max_context_len), b, nb, bs, h_q, h_kv, d, float(scale), int(num_splits), ws_ptr,
-        ws_bytes, _kv_dtype(k_cache), _opt(err_flag, "err_flag"), _stream(stream, q.device))
+        ws_bytes, _kv_code(k_cache, layout), _opt(err_flag, "err_flag"), _stream(stream, q.device))
     _check(st, "pkv_decode_attention")
     return out
 
@@ -212,13 +233,14 @@ def append_decode_attention(q: torch.Tensor, k_new: torch.Tensor, v_new: torch.T
                             max_context_len: int, scale: Optional[float] = None,
                             num_splits: int = 0, out: Optional[torch.Tensor] = None,
                             workspace: Optional[torch.Tensor] = None,
-                            err_flag: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+                            err_flag: Optional[torch.Tensor] = None, stream=None,
+                            layout: str = "nhd") -> torch.Tensor:
     """One decode step in one launch: sequence b's new token (k_new[b], v_new[b],
     [B, H_kv, d]) is written at position context_lens[b] - 1 of its block table,
     then ``decode_attention`` runs over the updated cache."""
     lib = load()
     b, h_q, d = q.shape
-    nb, bs, h_kv, d2 = k_cache.shape
+    nb, bs, h_kv, d2 = _cache_dims(k_cache, layout)
     if d2 != d or v_cache.shape != k_cache.shape or block_tables.dim() != 2 or \
             block_tables.shape[0] != b or context_lens.shape != (b,) or \
             k_new.shape != (b, h_kv, d) or v_new.shape != (b, h_kv, d):
@@ -238,7 +260,7 @@ def append_decode_attention(q: torch.Tensor, k_new: torch.Tensor, v_new: torch.T
         _dev(k_cache, "k_cache", dt), _dev(v_cache, "v_cache", dt),
         _dev(block_tables, "block_tables", torch.int32), block_tables.shape[1],
         _dev(context_lens, "context_lens", torch.int32), int(max_context_len), b, nb, bs, h_q,
-        h_kv, d, float(scale), int(num_splits), ws_ptr, ws_bytes, _kv_dtype(k_cache),
+        h_kv, d, float(scale), int(num_splits), ws_ptr, ws_bytes, _kv_code(k_cache, layout),
         _opt(err_flag, "err_flag"), _stream(stream, q.device))
     _check(st, "pkv_append_decode_attention")
     return out
@@ -264,7 +286,7 @@ def decode_attention_prefix_shared(q: torch.Tensor, k_cache: torch.Tensor, v_cac
                                    out: Optional[torch.Tensor] = None,
                                    workspace: Optional[torch.Tensor] = None,
                                    err_flag: Optional[torch.Tensor] = None,
-                                   stream=None) -> torch.Tensor:
+                                   stream=None, layout: str = "nhd") -> torch.Tensor:
     """``decode_attention`` for batches whose sequences share prompt-prefix blocks.
 
     group_start int32 [G+1] and group_prefix_len int32 [G] (device) describe
@@ -273,7 +295,7 @@ def decode_attention_prefix_shared(q: torch.Tensor, k_cache: torch.Tensor, v_cac
     """
     lib = load()
     b, h_q, d = q.shape
-    nb, bs, h_kv, d2 = k_cache.shape
+    nb, bs, h_kv, d2 = _cache_dims(k_cache, layout)
     ng = group_prefix_len.shape[0]
     if d2 != d or v_cache.shape != k_cache.shape or block_tables.dim() != 2 or \
             block_tables.shape[0] != b or context_lens.shape != (b,) or \
@@ -296,7 +318,7 @@ def decode_attention_prefix_shared(q: torch.Tensor, k_cache: torch.Tensor, v_cac
         _dev(group_start, "group_start", torch.int32),
         _dev(group_prefix_len, "group_prefix_len", torch.int32), int(max_group_size),
         int(max_prefix_len), _dev(workspace, "workspace"),
-        workspace.numel() * workspace.element_size(), _kv_dtype(k_cache),
+        workspace.numel() * workspace.element_size(), _kv_code(k_cache, layout),
         _opt(err_flag, "err_flag"), _stream(stream, q.device))
     _check(st, "pkv_decode_attention_prefix_shared")
     return out
@@ -317,7 +339,8 @@ def multi_query_attention(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch
                           max_context_len: int, scale: Optional[float] = None,
                           out: Optional[torch.Tensor] = None,
                           workspace: Optional[torch.Tensor] = None,
-                          err_flag: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+                          err_flag: Optional[torch.Tensor] = None, stream=None,
+                          layout: str = "nhd") -> torch.Tensor:
     """Causal attention of q_len new query tokens per sequence over the paged cache.
 
     q [B, q_len, H_q, d]; context_lens counts the cached tokens including the
@@ -326,7 +349,7 @@ def multi_query_attention(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch
     """
     lib = load()
     b, q_len, h_q, d = q.shape
-    nb, bs, h_kv, d2 = k_cache.shape
+    nb, bs, h_kv, d2 = _cache_dims(k_cache, layout)
     if d2 != d or v_cache.shape != k_cache.shape or block_tables.dim() != 2 or \
             block_tables.shape[0] != b or context_lens.shape != (b,):
         raise ValueError("inconsistent multi-query shapes")
@@ -344,7 +367,7 @@ def multi_query_attention(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch
         block_tables.shape[1], _dev(context_lens, "context_lens", torch.int32),
         int(max_context_len), b, q_len, nb, bs, h_q, h_kv, d, float(scale),
         _dev(workspace, "workspace"), workspace.numel() * workspace.element_size(),
-        _kv_dtype(k_cache), _opt(err_flag, "err_flag"), _stream(stream, q.device))
+        _kv_code(k_cache, layout), _opt(err_flag, "err_flag"), _stream(stream, q.device))
     _check(st, "pkv_multi_query_attention")
     return out
 
@@ -356,7 +379,8 @@ def decode_attention_noalloc(q: torch.Tensor, k_cache: torch.Tensor, v_cache: to
                              block_tables: torch.Tensor, context_lens: torch.Tensor,
                              max_context_len: int, out: torch.Tensor,
                              scale: Optional[float] = None, num_splits: int = 0,
-                             err_flag: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+                             err_flag: Optional[torch.Tensor] = None, stream=None,
+                             layout: str = "nhd") -> torch.Tensor:
     """``decode_attention`` for callers that cannot allocate device memory.
 
     Same result, but the split-K scratch is a fixed 8 MiB array inside the
@@ -368,7 +392,7 @@ def decode_attention_noalloc(q: torch.Tensor, k_cache: torch.Tensor, v_cache: to
     """
     lib = load()
     b, h_q, d = q.shape
-    nb, bs, h_kv, d2 = k_cache.shape
+    nb, bs, h_kv, d2 = _cache_dims(k_cache, layout)
     if d2 != d or v_cache.shape != k_cache.shape or block_tables.dim() != 2 or \
             block_tables.shape[0] != b or context_lens.shape != (b,) or out.shape != q.shape:
         raise ValueError("inconsistent decode shapes")
@@ -380,7 +404,7 @@ def decode_attention_noalloc(q: torch.Tensor, k_cache: torch.Tensor, v_cache: to
         _dev(v_cache, "v_cache", dt), _dev(block_tables, "block_tables", torch.int32),
         block_tables.shape[1], _dev(context_lens, "context_lens", torch.int32),
         int(max_context_len), b, nb, bs, h_q, h_kv, d, float(scale), int(num_splits),
-        _kv_dtype(k_cache), _opt(err_flag, "err_flag"), _stream(stream, q.device))
+        _kv_code(k_cache, layout), _opt(err_flag, "err_flag"), _stream(stream, q.device))
     _check(st, "pkv_decode_attention_noalloc")
     return out
 
@@ -405,10 +429,10 @@ def merge(partial_o: torch.Tensor, partial_lse: torch.Tensor, out_dtype=torch.bf
 def gather(k_cache: torch.Tensor, v_cache: torch.Tensor, block_tables: torch.Tensor,
            context_lens: torch.Tensor, max_context_len: int,
            k_out: Optional[torch.Tensor] = None, v_out: Optional[torch.Tensor] = None,
-           err_flag: Optional[torch.Tensor] = None, stream=None):
+           err_flag: Optional[torch.Tensor] = None, stream=None, layout: str = "nhd"):
     """Contiguous copies [B, max_context_len, H_kv, d] of each sequence's cached K and V."""
     lib = load()
-    nb, bs, h_kv, d = k_cache.shape
+    nb, bs, h_kv, d = _cache_dims(k_cache, layout)
     b = block_tables.shape[0]
     shape = (b, max_context_len, h_kv, d)
     if k_out is None:
@@ -420,7 +444,7 @@ def gather(k_cache: torch.Tensor, v_cache: torch.Tensor, block_tables: torch.Ten
                         _dev(k_cache, "k_cache", dt), _dev(v_cache, "v_cache", dt),
                         _dev(block_tables, "block_tables", torch.int32), block_tables.shape[1],
                         _dev(context_lens, "context_lens", torch.int32), int(max_context_len),
-                        b, nb, bs, h_kv, d, _kv_dtype(k_cache), _opt(err_flag, "err_flag"),
+                        b, nb, bs, h_kv, d, _kv_code(k_cache, layout), _opt(err_flag, "err_flag"),
                         _stream(stream, k_cache.device))
     _check(st, "pkv_gather")
     return k_out, v_out

@@ -5,18 +5,31 @@
 // s % block_size (gsyq.cn essay §三.2 get_kv_cache; tutorial chapter 12
 // PagedKVCache.update; LLM-101-CN "推理优化" KVCachePool.write_tokens).
 // One CTA per token; the token's K and V rows ([num_kv_heads][head_dim], a
-// multiple of 16 bytes) are moved with 16-byte vector loads and stores.
+// multiple of 16 bytes) are moved with 16-byte vector loads and stores.  In a
+// head-major cache ([num_blocks][num_kv_heads][block_size][head_dim]) head g
+// of the token lands in the (block, g) tile at row offset.
 #include <climits>
 
 #include "pkv_common.cuh"
 
 namespace pkv {
 
+// Offset (in 16-byte vectors) of vector c of a token's [num_kv_heads][head_dim]
+// row at `slot` of the cache.
+__device__ __forceinline__ int64_t cache_vec(int64_t slot, int c, int row_vecs, int head_vecs,
+                                             int num_kv_heads, int block_size, bool hnd) {
+    if (!hnd) return slot * row_vecs + c;
+    const int64_t blk = slot / block_size;
+    const int off = (int)(slot - blk * block_size);
+    const int g = c / head_vecs;
+    return ((blk * num_kv_heads + g) * block_size + off) * head_vecs + (c - g * head_vecs);
+}
+
 __global__ void __launch_bounds__(128)
 append_kernel(const uint4* __restrict__ k_new, const uint4* __restrict__ v_new,
               uint4* __restrict__ k_cache, uint4* __restrict__ v_cache,
               const int64_t* __restrict__ slot_mapping, int64_t num_slots, int row_vecs,
-              int32_t* err_flag) {
+              int head_vecs, int num_kv_heads, int block_size, bool hnd, int32_t* err_flag) {
     // Launched as a programmatic dependent: let the next kernel (the decode)
     // get scheduled now, then wait for the previous one before touching memory.
     asm volatile("griddepcontrol.launch_dependents;" :::);
@@ -28,16 +41,15 @@ append_kernel(const uint4* __restrict__ k_new, const uint4* __restrict__ v_new,
         if (threadIdx.x == 0) flag_error(err_flag, PKV_EFLAG_SLOT);
         return;
     }
-    // [num_blocks][block_size] flattens to the slot index itself.
+    // Token-major: [num_blocks][block_size] flattens to the slot index itself.
     const uint4* ks = k_new + (int64_t)i * row_vecs;
     const uint4* vs = v_new + (int64_t)i * row_vecs;
-    uint4* kd = k_cache + slot * row_vecs;
-    uint4* vd = v_cache + slot * row_vecs;
     for (int c = threadIdx.x; c < row_vecs; c += blockDim.x) {
+        const int64_t d = cache_vec(slot, c, row_vecs, head_vecs, num_kv_heads, block_size, hnd);
         uint4 a = __ldg(ks + c);
         uint4 b = __ldg(vs + c);
-        kd[c] = a;
-        vd[c] = b;
+        k_cache[d] = a;
+        v_cache[d] = b;
     }
 }
 
@@ -48,7 +60,8 @@ gather_kernel(uint4* __restrict__ k_out, uint4* __restrict__ v_out,
               const uint4* __restrict__ k_cache, const uint4* __restrict__ v_cache,
               const int32_t* __restrict__ block_tables, int max_blocks_per_seq,
               const int32_t* __restrict__ context_lens, int max_context_len, int num_blocks,
-              int block_size, int row_vecs, int32_t* err_flag) {
+              int block_size, int row_vecs, int head_vecs, int num_kv_heads, bool hnd,
+              int32_t* err_flag) {
     const int page = blockIdx.x;
     const int b = blockIdx.y;
     int n = __ldg(context_lens + b);
@@ -69,7 +82,8 @@ gather_kernel(uint4* __restrict__ k_out, uint4* __restrict__ v_out,
     for (int c = threadIdx.x; c < total; c += blockDim.x) {
         const int t = t0 + c / row_vecs;
         const int v = c % row_vecs;
-        const int64_t src = ((int64_t)blk * block_size + (t - t0)) * row_vecs + v;
+        const int64_t src = cache_vec((int64_t)blk * block_size + (t - t0), v, row_vecs,
+                                      head_vecs, num_kv_heads, block_size, hnd);
         const int64_t dst = ((int64_t)b * max_context_len + t) * row_vecs + v;
         k_out[dst] = __ldg(k_cache + src);
         v_out[dst] = __ldg(v_cache + src);
@@ -84,6 +98,7 @@ extern "C" pkv_status pkv_append(const void* k_new, const void* v_new, void* k_c
                                  void* v_cache, const int64_t* slot_mapping, int num_tokens,
                                  int num_blocks, int block_size, int num_kv_heads, int head_dim,
                                  pkv_dtype dtype, int32_t* err_flag, void* stream) {
+    const bool hnd = take_layout(dtype);
     if (num_tokens < 0 || num_blocks <= 0 || block_size <= 0 || num_kv_heads <= 0 ||
         head_dim <= 0 || (dtype != PKV_FP16 && dtype != PKV_BF16))
         return PKV_ERR_INVALID_ARG;
@@ -94,6 +109,7 @@ extern "C" pkv_status pkv_append(const void* k_new, const void* v_new, void* k_c
         return PKV_ERR_INVALID_ARG;
     const int64_t row_bytes = (int64_t)num_kv_heads * head_dim * 2;
     if (row_bytes % 16 != 0 || row_bytes / 16 > INT_MAX) return PKV_ERR_UNSUPPORTED;
+    if (hnd && (head_dim * 2) % 16 != 0) return PKV_ERR_UNSUPPORTED;
     const int row_vecs = (int)(row_bytes / 16);
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(num_tokens);
@@ -106,7 +122,8 @@ extern "C" pkv_status pkv_append(const void* k_new, const void* v_new, void* k_c
     cfg.numAttrs = 1;
     const cudaError_t e = cudaLaunchKernelEx(
         &cfg, append_kernel, (const uint4*)k_new, (const uint4*)v_new, (uint4*)k_cache,
-        (uint4*)v_cache, slot_mapping, (int64_t)num_blocks * block_size, row_vecs, err_flag);
+        (uint4*)v_cache, slot_mapping, (int64_t)num_blocks * block_size, row_vecs, head_dim / 8,
+        num_kv_heads, block_size, hnd, err_flag);
     if (e != cudaSuccess) {
         cudaGetLastError();
         return PKV_ERR_CUDA;
@@ -120,6 +137,7 @@ extern "C" pkv_status pkv_gather(void* k_out, void* v_out, const void* k_cache,
                                  int max_context_len, int num_seqs, int num_blocks,
                                  int block_size, int num_kv_heads, int head_dim, pkv_dtype dtype,
                                  int32_t* err_flag, void* stream) {
+    const bool hnd = take_layout(dtype);
     if (num_seqs < 0 || max_context_len < 0 || max_blocks_per_seq <= 0 || num_blocks <= 0 ||
         block_size <= 0 || num_kv_heads <= 0 || head_dim <= 0 ||
         (dtype != PKV_FP16 && dtype != PKV_BF16))
@@ -133,13 +151,14 @@ extern "C" pkv_status pkv_gather(void* k_out, void* v_out, const void* k_cache,
         return PKV_ERR_INVALID_ARG;
     const int64_t row_bytes = (int64_t)num_kv_heads * head_dim * 2;
     if (row_bytes % 16 != 0 || row_bytes / 16 > INT_MAX) return PKV_ERR_UNSUPPORTED;
+    if (hnd && (head_dim * 2) % 16 != 0) return PKV_ERR_UNSUPPORTED;
     const int pages = (max_context_len + block_size - 1) / block_size;
     if (num_seqs > 65535) return PKV_ERR_UNSUPPORTED;
     dim3 grid(pages, num_seqs);
     gather_kernel<<<grid, 128, 0, (cudaStream_t)stream>>>(
         (uint4*)k_out, (uint4*)v_out, (const uint4*)k_cache, (const uint4*)v_cache, block_tables,
         max_blocks_per_seq, context_lens, max_context_len, num_blocks, block_size,
-        (int)(row_bytes / 16), err_flag);
+        (int)(row_bytes / 16), head_dim / 8, num_kv_heads, hnd, err_flag);
     return cudaGetLastError() == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
 }
 

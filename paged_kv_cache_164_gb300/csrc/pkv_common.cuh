@@ -60,7 +60,16 @@ __device__ __forceinline__ void load_as_float(const T* ptr, float (&out)[N]) {
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 inline bool supported_head_dim(int d) { return d == 64 || d == 128; }
-inline bool supported_block_size(int bs) { return bs == 16 || bs == 32; }
+inline bool supported_block_size(int bs) { return bs == 16 || bs == 32 || bs == 64 || bs == 128; }
+
+// The dtype argument of a call that takes the cache: the element type, with
+// PKV_LAYOUT_HND OR-ed in for head-major caches.  Strips the flag and tells
+// whether it was set.
+inline bool take_layout(pkv_dtype& dtype) {
+    const int v = static_cast<int>(dtype);
+    dtype = static_cast<pkv_dtype>(v & ~PKV_LAYOUT_HND);
+    return (v & PKV_LAYOUT_HND) != 0;
+}
 
 constexpr int kMaxGroup = 16;  // query heads per KV head served by one CTA
 

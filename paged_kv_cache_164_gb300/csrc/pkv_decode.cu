@@ -79,9 +79,10 @@ struct DecodeParams {
     int num_q_heads;
     int group;           // query heads per KV head
     int num_splits;
-    int chunk_tokens;    // tokens per partition (a multiple of block_size and of 16)
+    int chunk_tokens;    // tokens per partition (a multiple of 16)
     int num_kv_heads;
     int max_context_len;
+    bool hnd;            // head-major cache layout
     float scale_log2;    // scale * log2(e)
 };
 
@@ -112,6 +113,17 @@ __device__ __forceinline__ float2 unpack2(uint32_t x, __nv_bfloat16) {
 }
 __device__ __forceinline__ float2 unpack2(uint32_t x, __half) {
     return __half22float2(*reinterpret_cast<__half2*>(&x));
+}
+
+// 16-token box of K or V for KV head g at token offset toff of block blk,
+// 64-dim region starting at dim c0, in either cache layout.
+__device__ __forceinline__ void load_kv_box(uint32_t dst, const CUtensorMap* map, uint32_t bar,
+                                            int c0, int g, int toff, int blk, bool hnd,
+                                            uint64_t policy) {
+    if (hnd)
+        ptx::tma_load_4d(dst, map, bar, c0, toff, g, blk, policy);
+    else
+        ptx::tma_load_4d(dst, map, bar, c0, g, toff, blk, policy);
 }
 
 // Bounded wait on an mbarrier phase.  Returns false (after raising the CTA's
@@ -324,7 +336,8 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
     // warp fetches the block-table slice at the same time as the length.
     const int t_begin = start + split * p.chunk_tokens;
     const int page0 = t_begin / bs;
-    const int max_pages = min(p.max_blocks_per_seq - page0, p.chunk_tokens / bs + 1);
+    // pages a partition can touch: it may start and end mid-page
+    const int max_pages = min(p.max_blocks_per_seq - page0, (p.chunk_tokens + bs - 1) / bs + 1);
     const int32_t* row = p.block_tables + (int64_t)b * p.max_blocks_per_seq + page0;
     int blk_r[3] = {-1, -1, -1};
     if (warp == kConsumerWarps) {
@@ -355,7 +368,8 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
             const int c = tid % (D / 8);  // 16-byte chunk of the row
             const int64_t src = ((int64_t)b * p.num_kv_heads + g) * (D / 8) + c;
             const int64_t dst =
-                (((int64_t)blk * bs + pos % bs) * p.num_kv_heads + g) * (D / 8) + c;
+                (p.hnd ? ((int64_t)blk * p.num_kv_heads + g) * bs + pos % bs
+                       : ((int64_t)blk * bs + pos % bs) * p.num_kv_heads + g) * (D / 8) + c;
             const uint4 v = __ldg(static_cast<const uint4*>(is_v ? p.v_new : p.k_new) + src);
             static_cast<uint4*>(is_v ? p.v_cache : p.k_cache)[dst] = v;
             ptx::fence_proxy_async_global();
@@ -414,10 +428,10 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
                     ptx::mbar_arrive_expect_tx(fb, Cfg::kStageBytes);
 #pragma unroll
                     for (int r = 0; r < Cfg::kRegions; ++r) {
-                        ptx::tma_load_4d(kdst + r * Cfg::kRegionBytes, &tm_k, fb, r * 64, g, toff,
-                                         blk, policy);
-                        ptx::tma_load_4d(kdst + Cfg::kHalfBytes + r * Cfg::kRegionBytes, &tm_v, fb,
-                                         r * 64, g, toff, blk, policy);
+                        load_kv_box(kdst + r * Cfg::kRegionBytes, &tm_k, fb, r * 64, g, toff,
+                                    blk, p.hnd, policy);
+                        load_kv_box(kdst + Cfg::kHalfBytes + r * Cfg::kRegionBytes, &tm_v, fb,
+                                    r * 64, g, toff, blk, p.hnd, policy);
                     }
                 } else {
                     ptx::mbar_arrive(fb);  // nothing to load: the consumer masks the stage
@@ -626,6 +640,7 @@ struct PrefixParams {
     int prefix_chunk;     // prefix tokens per partition (a multiple of 64 and of block_size)
     int cap;              // context clamp
     int q_len;            // 0: shared prefixes; > 0: multi-query (q_len query tokens per sequence)
+    bool hnd;             // head-major cache layout
     float scale_log2;
 };
 
@@ -886,8 +901,8 @@ prefix_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
             if (blk >= 0) {
                 const uint32_t off = (is_v ? Cfg::kHalfBytes : 0) + rr * Cfg::kKVRegionBytes +
                                      bx * kStageTokens * 128;
-                ptx::tma_load_4d(kdst + off, is_v ? &tm_v : &tm_k, fb, rr * 64, g, tok0 % bs, blk,
-                                 policy);
+                load_kv_box(kdst + off, is_v ? &tm_v : &tm_k, fb, rr * 64, g, tok0 % bs, blk,
+                            p.hnd, policy);
             }
             issued = j + 1;
         }
@@ -1400,52 +1415,54 @@ static pkv_status check_shapes(int num_seqs, int num_q_heads, int num_kv_heads, 
     return PKV_OK;
 }
 
-// Partitions: each is a whole number of pages, at most kMaxChunkPages; the
-// automatic plan sizes them so that, at the longest context, the CTAs fill
-// whole waves of resident CTAs (see the loop), without cutting partitions
-// below 256 tokens.
+// Partitions: whole 16-token stages, whatever the page size; the automatic
+// plan sizes them so that, at the longest context, the CTAs fill whole waves
+// of resident CTAs (see the loop), between 256 and 1024 tokens.
 static pkv_status make_plan(int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
                             int block_size, int max_context_len, int num_splits, Plan* plan) {
     pkv_status st = check_shapes(num_seqs, num_q_heads, num_kv_heads, head_dim, block_size,
                                  max_context_len, num_splits);
     if (st != PKV_OK) return st;
-    const int max_pages = std::max(1, (max_context_len + block_size - 1) / block_size);
-    int chunk_pages;
+    // Partitions are whole 16-token stages (a stage box may start anywhere in a
+    // page), at most kMaxChunkPages pages long so a partition's slice of the
+    // block table, starting mid-page, fits kMaxChunkPages + 1 entries.
+    const int max_stages = std::max(1, (max_context_len + kStageTokens - 1) / kStageTokens);
+    const int cap_stages = kMaxChunkPages * block_size / kStageTokens;
+    int chunk_stages;
     if (num_splits == 0) {
         const int sms = current_sm_count();
         if (sms <= 0) return PKV_ERR_CUDA;
-        // Whole pages from 256 tokens up to kMaxChunkPages pages.  Among those
-        // partition counts, the fewest whose CTAs (at the longest context) fill
-        // their last wave of resident CTAs to 95%, else the best filled one:
-        // equal-length CTAs run in lock-step waves, so a partly empty last wave
-        // leaves SMs idle.
+        // From 256 to 1024 tokens.  Among those partition counts, the fewest
+        // whose CTAs (at the longest context) fill their last wave of resident
+        // CTAs to 95%, else the best filled one: equal-length CTAs run in
+        // lock-step waves, so a partly empty last wave leaves SMs idle.
         const int64_t units = (int64_t)std::max(1, num_seqs) * num_kv_heads;
         const double slots = 3.0 * sms;
-        const int min_pages = std::max(1, 256 / block_size);
-        const int lo = std::max(1, (max_pages + kMaxChunkPages - 1) / kMaxChunkPages);
-        const int hi = std::max(lo, std::min(PKV_MAX_SPLITS, (max_pages + min_pages - 1) / min_pages));
+        const int min_chunk = 256 / kStageTokens, max_chunk = std::min(1024 / kStageTokens, cap_stages);
+        const int lo = std::max(1, (max_stages + max_chunk - 1) / max_chunk);
+        const int hi = std::max(lo, std::min(PKV_MAX_SPLITS, (max_stages + min_chunk - 1) / min_chunk));
         double best_eff = -1.0;
-        chunk_pages = (max_pages + lo - 1) / lo;
+        chunk_stages = (max_stages + lo - 1) / lo;
         for (int s = lo; s <= hi; ++s) {
-            const int cp = (max_pages + s - 1) / s;
-            const int splits = (max_pages + cp - 1) / cp;
+            const int cs = (max_stages + s - 1) / s;
+            const int splits = (max_stages + cs - 1) / cs;
             if (splits != s) continue;  // the same partition as a smaller count
             const double waves = (double)units * splits / slots;
             const double eff = waves / std::ceil(waves);
             if (eff > best_eff + 1e-9) {
                 best_eff = eff;
-                chunk_pages = cp;
+                chunk_stages = cs;
             }
             if (eff >= 0.95) {
-                chunk_pages = cp;
+                chunk_stages = cs;
                 break;
             }
         }
     } else {
-        chunk_pages = (max_pages + num_splits - 1) / num_splits;
+        chunk_stages = (max_stages + num_splits - 1) / num_splits;
     }
-    chunk_pages = std::min(std::max(chunk_pages, 1), kMaxChunkPages);
-    const int chunk = chunk_pages * block_size;
+    chunk_stages = std::min(std::max(chunk_stages, 1), cap_stages);
+    const int chunk = chunk_stages * kStageTokens;
     const int64_t splits64 = std::max<int64_t>(1, ((int64_t)max_context_len + chunk - 1) / chunk);
     if (splits64 > PKV_MAX_SPLITS) return PKV_ERR_UNSUPPORTED;  // context too long for the plan
     const int splits = (int)splits64;
@@ -1473,19 +1490,23 @@ static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
     return fn;
 }
 
-// Tensor map over a cache [num_blocks][block_size][H_kv][D]: dims (innermost
-// first) D, H_kv, block_size, num_blocks; box 64 dims x 1 head x 16 tokens x
-// 1 block, 128-byte swizzle.
+// Tensor map over a token-major cache [num_blocks][block_size][H_kv][D]: dims
+// (innermost first) D, H_kv, block_size, num_blocks; box 64 dims x 1 head x 16
+// tokens x 1 block.  Head major [num_blocks][H_kv][block_size][D]: dims D,
+// block_size, H_kv, num_blocks; box 64 dims x 16 tokens x 1 head x 1 block.
+// 128-byte swizzle either way, so a box lands as 16 rows of 128 bytes.
 static bool make_cache_map(CUtensorMap* map, const void* base, pkv_dtype dtype, int num_blocks,
-                           int block_size, int num_kv_heads, int head_dim) {
+                           int block_size, int num_kv_heads, int head_dim, bool hnd) {
     PFN_cuTensorMapEncodeTiled_v12000 fn = encode_fn();
     if (fn == nullptr) return false;
     const cuuint64_t e = 2;
-    cuuint64_t dims[4] = {(cuuint64_t)head_dim, (cuuint64_t)num_kv_heads, (cuuint64_t)block_size,
-                          (cuuint64_t)num_blocks};
-    cuuint64_t strides[3] = {(cuuint64_t)head_dim * e, (cuuint64_t)num_kv_heads * head_dim * e,
-                             (cuuint64_t)block_size * num_kv_heads * head_dim * e};
-    cuuint32_t box[4] = {64, 1, (cuuint32_t)kStageTokens, 1};
+    const cuuint64_t inner = hnd ? (cuuint64_t)block_size : (cuuint64_t)num_kv_heads;
+    const cuuint64_t outer = hnd ? (cuuint64_t)num_kv_heads : (cuuint64_t)block_size;
+    cuuint64_t dims[4] = {(cuuint64_t)head_dim, inner, outer, (cuuint64_t)num_blocks};
+    cuuint64_t strides[3] = {(cuuint64_t)head_dim * e, inner * head_dim * e,
+                             outer * inner * head_dim * e};
+    cuuint32_t box[4] = {64, hnd ? (cuuint32_t)kStageTokens : 1u,
+                         hnd ? 1u : (cuuint32_t)kStageTokens, 1};
     cuuint32_t estr[4] = {1, 1, 1, 1};
     CUresult r = fn(map, dtype == PKV_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
                                            : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
@@ -1688,6 +1709,7 @@ static pkv_status decode_impl(void* out, const void* q, const void* k_new, const
                               int num_q_heads, int num_kv_heads, int head_dim, float scale,
                               int num_splits, void* workspace, size_t workspace_bytes,
                               pkv_dtype dtype, int32_t* err_flag, void* stream) {
+    const bool hnd = take_layout(dtype);
     pkv_status st = check_shapes(num_seqs, num_q_heads, num_kv_heads, head_dim, block_size,
                                  max_context_len, num_splits);
     if (st != PKV_OK) return st;
@@ -1714,8 +1736,8 @@ static pkv_status decode_impl(void* out, const void* q, const void* k_new, const
     if (workspace != nullptr && !aligned16(workspace)) return PKV_ERR_INVALID_ARG;
 
     CUtensorMap mk, mv;
-    if (!make_cache_map(&mk, k_cache, dtype, num_blocks, block_size, num_kv_heads, head_dim) ||
-        !make_cache_map(&mv, v_cache, dtype, num_blocks, block_size, num_kv_heads, head_dim))
+    if (!make_cache_map(&mk, k_cache, dtype, num_blocks, block_size, num_kv_heads, head_dim, hnd) ||
+        !make_cache_map(&mv, v_cache, dtype, num_blocks, block_size, num_kv_heads, head_dim, hnd))
         return PKV_ERR_CUDA;
 
     DecodeParams p = {};
@@ -1743,6 +1765,7 @@ static pkv_status decode_impl(void* out, const void* q, const void* k_new, const
     p.v_new = v_new;
     p.k_cache = k_cache;
     p.v_cache = v_cache;
+    p.hnd = hnd;
     if (plan.num_splits > 1) {
         p.partial_o = static_cast<float*>(workspace);
         p.partial_lse = p.partial_o + (size_t)num_seqs * num_q_heads * plan.num_splits * head_dim;
@@ -1873,6 +1896,7 @@ extern "C" pkv_status pkv_decode_attention_prefix_shared(
     int num_kv_heads, int head_dim, float scale, int num_groups, const int32_t* group_start,
     const int32_t* group_prefix_len, int max_group_size, int max_prefix_len, void* workspace,
     size_t workspace_bytes, pkv_dtype dtype, int32_t* err_flag, void* stream) {
+    const bool hnd = take_layout(dtype);
     pkv_status st = check_shapes(num_seqs, num_q_heads, num_kv_heads, head_dim, block_size,
                                  max_context_len, 0);
     if (st != PKV_OK) return st;
@@ -1897,8 +1921,8 @@ extern "C" pkv_status pkv_decode_attention_prefix_shared(
     if (workspace_bytes < pp.workspace_bytes) return PKV_ERR_WORKSPACE;
 
     CUtensorMap mk, mv;
-    if (!make_cache_map(&mk, k_cache, dtype, num_blocks, block_size, num_kv_heads, head_dim) ||
-        !make_cache_map(&mv, v_cache, dtype, num_blocks, block_size, num_kv_heads, head_dim))
+    if (!make_cache_map(&mk, k_cache, dtype, num_blocks, block_size, num_kv_heads, head_dim, hnd) ||
+        !make_cache_map(&mv, v_cache, dtype, num_blocks, block_size, num_kv_heads, head_dim, hnd))
         return PKV_ERR_CUDA;
 
     float* partial_o = static_cast<float*>(workspace);
@@ -1970,6 +1994,7 @@ extern "C" pkv_status pkv_decode_attention_prefix_shared(
     pr.max_prefix_len = max_prefix_len;
     pr.prefix_chunk = pp.prefix_chunk;
     pr.cap = cap;
+    pr.hnd = hnd;
     pr.scale_log2 = scale * kLog2e;
     const dim3 pgrid(pp.row_tiles, std::max(1, num_groups * num_kv_heads),
                      std::max(1, pp.prefix_parts));
@@ -2006,6 +2031,7 @@ extern "C" pkv_status pkv_decode_attention_prefix_shared(
     p.chunk_tokens = pp.suffix.chunk_tokens;
     p.num_kv_heads = num_kv_heads;
     p.max_context_len = max_context_len;
+    p.hnd = hnd;
     p.scale_log2 = scale * kLog2e;
     const dim3 grid((unsigned)num_items);
     e = dtype == PKV_FP16 ? launch_decode<__half>(mk, mv, p, head_dim, grid, s)
@@ -2054,6 +2080,7 @@ extern "C" pkv_status pkv_multi_query_attention(
     int max_context_len, int num_seqs, int q_len, int num_blocks, int block_size,
     int num_q_heads, int num_kv_heads, int head_dim, float scale, void* workspace,
     size_t workspace_bytes, pkv_dtype dtype, int32_t* err_flag, void* stream) {
+    const bool hnd = take_layout(dtype);
     if ((dtype != PKV_FP16 && dtype != PKV_BF16) || max_blocks_per_seq <= 0 || num_blocks <= 0 ||
         !std::isfinite(scale) || q_len <= 0)
         return PKV_ERR_INVALID_ARG;
@@ -2075,8 +2102,8 @@ extern "C" pkv_status pkv_multi_query_attention(
     if (workspace_bytes < mq.workspace_bytes) return PKV_ERR_WORKSPACE;
 
     CUtensorMap mk, mv;
-    if (!make_cache_map(&mk, k_cache, dtype, num_blocks, block_size, num_kv_heads, head_dim) ||
-        !make_cache_map(&mv, v_cache, dtype, num_blocks, block_size, num_kv_heads, head_dim))
+    if (!make_cache_map(&mk, k_cache, dtype, num_blocks, block_size, num_kv_heads, head_dim, hnd) ||
+        !make_cache_map(&mv, v_cache, dtype, num_blocks, block_size, num_kv_heads, head_dim, hnd))
         return PKV_ERR_CUDA;
     float* partial_o = static_cast<float*>(workspace);
     float* partial_lse = partial_o + (size_t)num_seqs * q_len * num_q_heads * mq.parts * head_dim;
@@ -2103,6 +2130,7 @@ extern "C" pkv_status pkv_multi_query_attention(
     pr.prefix_chunk = mq.chunk;
     pr.cap = cap;
     pr.q_len = q_len;
+    pr.hnd = hnd;
     pr.scale_log2 = scale * kLog2e;
     const dim3 pgrid(mq.row_tiles, num_seqs * num_kv_heads, mq.parts);
     cudaError_t e;

@@ -74,6 +74,9 @@ def test_decode_rejects_bad_arguments_without_launching(lib):
     assert _decode(lib, dt=3) == 1
     assert _decode(lib, scale=float("nan")) == 1
     assert _decode(lib, B=0) == 0                 # empty batch is a no-op
+    assert _decode(lib, dt=0x200) == 1            # an unknown flag in the dtype argument
+    assert _decode(lib, dt=pkv.LAYOUT_HND, B=0) == 0   # the head-major flag is accepted
+    assert _decode(lib, bs=128, d=96) == 2        # 128-token pages are fine, head_dim 96 is not
 
 
 def test_workspace_size_rejects_bad_arguments(lib):

@@ -268,6 +268,12 @@ def make_workload(name_or_spec, device="cpu", poison: bool = False, with_values:
                     group_start=gstart, group_prefix_len=gplen)
 
 
+def to_head_major(cache: torch.Tensor) -> torch.Tensor:
+    """The same cache in the head-major page layout: [blocks][bs][H_kv][d] ->
+    [blocks][H_kv][bs][d] (a permutation of the values, nothing else)."""
+    return cache.permute(0, 2, 1, 3).contiguous()
+
+
 def make_queries(w: Workload, q_len: int, seed: int) -> torch.Tensor:
     """Seeded N(0,1) queries [B, q_len, H_q, d] in the workload's dtype and device
     (several new query tokens per sequence: a prefill chunk or drafted tokens)."""
