@@ -3,7 +3,8 @@
 A plain, slow, obviously correct CPU implementation (fp64) of what the CUDA
 library computes: the append (scatter through ``slot_mapping``), the gather
 through the block table, decode attention ``softmax(q K^T * scale) V`` with
-GQA, causal multi-query attention (several new query tokens per sequence),
+GQA, causal multi-query attention (several new query tokens per sequence), the
+E4M3 (FP8) cache codes with their quantising append and decode attention,
 the pages' per-page partials and their online-softmax combine, and the
 log-sum-exp merge of split partials.
 
@@ -21,10 +22,14 @@ from .reference import (  # noqa: F401
     DTYPE_CODES,
     append,
     combine_result,
+    append_fp8,
     decode_attention,
+    decode_attention_fp8,
+    decode_e4m3,
     decode_attention_np,
     decode_attention_pagewise,
     decode_values,
+    encode_e4m3,
     gather_kv,
     kv_cache_bytes,
     merge_lse,

@@ -43,6 +43,17 @@ def load_library(path: str) -> ctypes.CDLL:
     lib.oracle_decode_attention.restype = i
     lib.oracle_append.argtypes = [p, p, p, p, p, i, i, i, i, i]
     lib.oracle_append.restype = i
+    lib.oracle_decode_e4m3.argtypes = [p, p, ctypes.c_int64]
+    lib.oracle_decode_e4m3.restype = None
+    lib.oracle_encode_e4m3.argtypes = [p, p, ctypes.c_int64]
+    lib.oracle_encode_e4m3.restype = None
+    lib.oracle_append_fp8.argtypes = [p, p, p, p, p, i, i, i, i, i, ctypes.c_float,
+                                      ctypes.c_float, i]
+    lib.oracle_append_fp8.restype = i
+    lib.oracle_decode_attention_fp8.argtypes = [p, p, p, p, p, i, p, i, i, i, i, i, i,
+                                                ctypes.c_double, ctypes.c_double,
+                                                ctypes.c_double, i]
+    lib.oracle_decode_attention_fp8.restype = i
     lib.oracle_num_threads.argtypes = []
     lib.oracle_num_threads.restype = i
     return lib
@@ -196,6 +207,69 @@ def multi_query_attention(q: np.ndarray, k_cache: np.ndarray, v_cache: np.ndarra
                             np.maximum(limits, 0).reshape(-1).astype(np.int32), scale, dtype,
                             lib=lib)
     return rows.reshape(num_seqs, q_len, h_q, d)
+
+
+def decode_e4m3(codes: np.ndarray, lib: ctypes.CDLL = None) -> np.ndarray:
+    """Exact float64 values of E4M3 codes (1 sign, 4 exponent bits with bias 7,
+    3 fraction bits, no infinities, S.1111.111 = NaN): the oracle's own decoder."""
+    c = np.ascontiguousarray(codes, dtype=np.uint8)
+    out = np.empty(c.shape, dtype=np.float64)
+    (lib or _lib()).oracle_decode_e4m3(_ptr(out), _ptr(c), int(c.size))
+    return out
+
+
+def encode_e4m3(x: np.ndarray, lib: ctypes.CDLL = None) -> np.ndarray:
+    """E4M3 codes of float32 values: round to nearest, ties to even, saturating
+    at +-448 (NaN gives 0x7F)."""
+    f = np.ascontiguousarray(x, dtype=np.float32)
+    out = np.empty(f.shape, dtype=np.uint8)
+    (lib or _lib()).oracle_encode_e4m3(_ptr(out), _ptr(f), int(f.size))
+    return out
+
+
+def append_fp8(k_cache: np.ndarray, v_cache: np.ndarray, k_new: np.ndarray, v_new: np.ndarray,
+               slot_mapping: np.ndarray, k_scale: float, v_scale: float, dtype: str,
+               lib: ctypes.CDLL = None) -> int:
+    """Quantising host scatter, in place, into uint8 E4M3 caches
+    [num_blocks, bs, H_kv, d]: element x of the new K row is stored as
+    E4M3(x / k_scale), the quotient in fp32 (vLLM deep dive, 3.3 FP8 inference:
+    E4M3 with the range held by a scale; 2.2: KV-cache write fused with
+    quantisation).  Returns 0, or -2 if a slot lies beyond the pool."""
+    kn, vn = _bits(k_new), _bits(v_new)
+    sm = np.ascontiguousarray(slot_mapping, dtype=np.int64)
+    nb, bs, h_kv, d = k_cache.shape
+    assert k_cache.dtype == np.uint8 and k_cache.flags.c_contiguous
+    return (lib or _lib()).oracle_append_fp8(
+        _ptr(k_cache), _ptr(v_cache), _ptr(kn), _ptr(vn), _ptr(sm), int(sm.shape[0]), nb, bs,
+        h_kv, d, float(k_scale), float(v_scale), DTYPE_CODES[dtype])
+
+
+def decode_attention_fp8(q: np.ndarray, k_cache: np.ndarray, v_cache: np.ndarray,
+                         block_tables: np.ndarray, context_lens: np.ndarray, scale: float,
+                         k_scale: float, v_scale: float, dtype: str,
+                         lib: ctypes.CDLL = None) -> np.ndarray:
+    """Decode attention over E4M3 caches (uint8 [num_blocks, bs, H_kv, d]) whose
+    values are code * k_scale and code * v_scale; q uint16 of ``dtype``.
+    Otherwise as ``decode_attention``.  Returns float64 [B, H_q, d]."""
+    q = _bits(q)
+    kc = np.ascontiguousarray(k_cache, dtype=np.uint8)
+    vc = np.ascontiguousarray(v_cache, dtype=np.uint8)
+    bt = np.ascontiguousarray(block_tables, dtype=np.int32)
+    cl = np.ascontiguousarray(context_lens, dtype=np.int32)
+    num_seqs, h_q, d = q.shape
+    num_blocks, bs, h_kv, d2 = kc.shape
+    if d2 != d or vc.shape != kc.shape or cl.shape != (num_seqs,):
+        raise ValueError("inconsistent shapes")
+    out = np.empty((num_seqs, h_q, d), dtype=np.float64)
+    rc = (lib or _lib()).oracle_decode_attention_fp8(
+        _ptr(out), _ptr(q), _ptr(kc), _ptr(vc), _ptr(bt), int(bt.shape[1]), _ptr(cl), num_seqs,
+        num_blocks, bs, h_q, h_kv, d, float(scale), float(k_scale), float(v_scale),
+        DTYPE_CODES[dtype])
+    if rc == -1:
+        raise ValueError("invalid arguments")
+    if rc == -2:
+        raise ValueError("block id out of range")
+    return out
 
 
 def decode_attention_np(q: np.ndarray, k_cache: np.ndarray, v_cache: np.ndarray,

@@ -448,3 +448,91 @@ def test_multi_query_last_token_sees_whole_context_first_sees_less():
                                     w.spec.dtype)
     assert np.array_equal(mq[:, -1], full)
     assert np.array_equal(mq[:, 0], first)
+
+
+# ---------------------------------------------------------------- FP8 (E4M3) cache
+
+def test_e4m3_decoder_matches_library_float8():
+    codes = np.arange(256, dtype=np.uint8)
+    ours = oracle.decode_e4m3(codes)
+    lib = torch.from_numpy(codes).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    nan = np.isnan(lib)
+    assert np.array_equal(np.isnan(ours), nan) and nan.sum() == 2   # 0x7F and 0xFF
+    assert np.array_equal(ours[~nan], lib[~nan])
+    assert ours[0x7E] == 448.0 and ours[0x01] == 2.0 ** -9 and ours[0x08] == 2.0 ** -6
+
+
+def test_e4m3_encoder_round_trips_and_matches_library_rounding():
+    codes = np.array([c for c in range(256) if c not in (0x7F, 0xFF)], dtype=np.uint8)
+    values = oracle.decode_e4m3(codes).astype(np.float32)
+    back = oracle.encode_e4m3(values)
+    # every finite code comes back (0x80, negative zero, stays negative zero)
+    assert np.array_equal(back, codes)
+    g = torch.Generator().manual_seed(5)
+    x = (torch.randn(200000, generator=g) * torch.exp2(torch.randint(-12, 9, (200000,),
+                                                                       generator=g).float()))
+    x = x.clamp(-448, 448)
+    ours = oracle.encode_e4m3(x.numpy())
+    lib = x.to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    assert np.array_equal(ours, lib)
+
+
+def test_e4m3_encoder_ties_saturation_and_nan():
+    f = np.float32
+    cases = {
+        1.0625: 0x38,        # halfway 1.0 (0x38) / 1.125 (0x39): to the even code
+        1.1875: 0x3A,        # halfway 1.125 / 1.25: to 1.25 (0x3A, even)
+        2.0 ** -10: 0x00,    # halfway 0 / 2^-9: to zero (even)
+        3 * 2.0 ** -10: 0x02,  # halfway 2^-9 / 2^-8: to 2^-8 (code 2, even)
+        464.0: 0x7E,         # halfway 448 / (480, not a value): saturates
+        1.0e6: 0x7E, -1.0e6: 0xFE,
+        float("inf"): 0x7E, float("-inf"): 0xFE,
+    }
+    x = np.array(list(cases), dtype=f)
+    assert list(oracle.encode_e4m3(x)) == list(cases.values())
+    assert oracle.encode_e4m3(np.array([np.nan], dtype=f))[0] == 0x7F
+
+
+@pytest.mark.parametrize("dtype", ["fp16", "bf16"])
+def test_append_fp8_matches_independent_quantisation(dtype):
+    c = make_append_case(50, 8, 16, 4, 64, dtype, seed=9)
+    k_new, v_new = c["k_new"], c["v_new"]
+    slots = c["slot_mapping"].numpy()
+    k_scale, v_scale = 0.0123, 0.0311
+    kc = np.full((8, 16, 4, 64), 0x5A, dtype=np.uint8)
+    vc = kc.copy()
+    assert oracle.append_fp8(kc, vc, bits(k_new), bits(v_new), slots, k_scale, v_scale,
+                             dtype) == 0
+    ks = torch.full((8 * 16, 4, 64), 0x5A, dtype=torch.uint8)
+    vs = ks.clone()
+    for i, s in enumerate(slots):
+        if s < 0:
+            continue
+        ks[s] = (k_new[i].float() / torch.tensor(k_scale, dtype=torch.float32)).clamp(
+            -448, 448).to(torch.float8_e4m3fn).view(torch.uint8)
+        vs[s] = (v_new[i].float() / torch.tensor(v_scale, dtype=torch.float32)).clamp(
+            -448, 448).to(torch.float8_e4m3fn).view(torch.uint8)
+    assert np.array_equal(kc.reshape(8 * 16, 4, 64), ks.numpy())
+    assert np.array_equal(vc.reshape(8 * 16, 4, 64), vs.numpy())
+
+
+def test_decode_attention_fp8_equals_dense_attention_on_dequantized_values():
+    w = make_workload("c3", num_seqs=3, num_q_heads=8, num_kv_heads=2, head_dim=64,
+                      lengths=("uniform", 5, 90), max_len_cap=96, seed=17)
+    k_scale, v_scale = 5.0 / 448, 4.0 / 448
+    kc = oracle.encode_e4m3(w.k_cache.float().numpy() / np.float32(k_scale))
+    vc = oracle.encode_e4m3(w.v_cache.float().numpy() / np.float32(v_scale))
+    bt, cl = w.block_tables.numpy(), w.context_lens.numpy()
+    got = oracle.decode_attention_fp8(bits(w.q), kc, vc, bt, cl, w.scale, k_scale, v_scale,
+                                      w.spec.dtype)
+    kd = oracle.decode_e4m3(kc) * k_scale
+    vd = oracle.decode_e4m3(vc) * v_scale
+    qd = oracle.decode_values(bits(w.q), w.spec.dtype)
+    group = w.spec.num_q_heads // w.spec.num_kv_heads
+    for b in range(w.spec.num_seqs):
+        n = int(cl[b])
+        for h in range(w.spec.num_q_heads):
+            k, v = oracle.gather_kv(kd, vd, bt, n, b, h // group)
+            s = torch.from_numpy(qd[b, h] @ k.T * w.scale)
+            ref = (torch.softmax(s, dim=0) @ torch.from_numpy(v)).numpy()
+            assert np.allclose(got[b, h], ref, rtol=1e-12, atol=1e-14)
