@@ -86,16 +86,17 @@ def _peaks():
         return FALLBACK_HBM_GBS, "fallback"
 
 
-def step_bytes(w, q_len: int = 1) -> dict:
-    """Algorithmic bytes of one step of workload ``w`` (all 16-bit values: 2 bytes),
-    with ``q_len`` query tokens per sequence (1: decode)."""
+def step_bytes(w, q_len: int = 1, kv_bytes: int = 2) -> dict:
+    """Algorithmic bytes of one step of workload ``w`` (16-bit q, out and new
+    tokens; ``kv_bytes`` per cached K/V element), with ``q_len`` query tokens
+    per sequence (1: decode)."""
     import torch
     e = 2
     s = w.spec
     lens = w.context_lens.cpu().long()
     bt = w.block_tables.cpu().long()
     bs = s.block_size
-    row = s.num_kv_heads * s.head_dim * e            # one token's K (or V) row
+    row = s.num_kv_heads * s.head_dim * kv_bytes     # one cached token's K (or V) row
     logical_tokens = int(lens.sum())
     # unique physical slots read (shared prefix pages count once per step)
     slots = []
@@ -109,7 +110,8 @@ def step_bytes(w, q_len: int = 1) -> dict:
     meta = pages * 4 + s.num_seqs * 4
     decode = 2 * unique_tokens * row + qo + meta
     decode_logical = 2 * logical_tokens * row + qo + meta
-    append = 4 * s.num_seqs * row + 8 * s.num_seqs   # read k_new, v_new; write both; slots
+    new_row = s.num_kv_heads * s.head_dim * e
+    append = 2 * s.num_seqs * (new_row + row) + 8 * s.num_seqs   # read new K/V, write both; slots
     flops = 4 * logical_tokens * q_len * s.num_q_heads * s.head_dim
     return dict(decode=decode, decode_logical=decode_logical, append=append,
                 step=decode + append, kv_unique=2 * unique_tokens * row, flops=flops,
@@ -329,7 +331,19 @@ def run_gpu(args):
     mq = args.q_len > 0
     if mq:
         w.q = make_queries(w, args.q_len, seed=s.seed + 101)
-    nbytes = step_bytes(w, args.q_len if mq else 1)
+    # --kv fp8: the cache as E4M3 codes with one scale for K and one for V
+    fp8 = args.kv == "fp8"
+    if fp8:
+        if mq or args.fused or s.shared_prefix_groups and args.prefix_sharing:
+            raise SystemExit("--kv fp8 times the plain decode path only "
+                             "(add --no-prefix-sharing for shared-prefix workloads)")
+        k_scale = float(w.k_cache.float().abs().max()) / 448.0
+        v_scale = float(w.v_cache.float().abs().max()) / 448.0
+        w.k_cache = (w.k_cache.float() / k_scale).clamp(-448, 448).to(
+            torch.float8_e4m3fn).view(torch.uint8)
+        w.v_cache = (w.v_cache.float() / v_scale).clamp(-448, 448).to(
+            torch.float8_e4m3fn).view(torch.uint8)
+    nbytes = step_bytes(w, args.q_len if mq else 1, 1 if fp8 else 2)
     mcl = w.max_context_len
     # Workloads whose sequences share prefix blocks use the shared-prefix decode
     # (each group's prefix read once for all members) unless told otherwise.
@@ -359,7 +373,11 @@ def run_gpu(args):
                          (1 if fused else 2) + (1 if splits > 1 else 0))
 
     def decode_call(q, block_tables, context_lens):
-        if mq:
+        if fp8:
+            pkv.decode_attention_fp8(q, w.k_cache, w.v_cache, block_tables, context_lens, mcl,
+                                     k_scale, v_scale, scale=w.scale, num_splits=args.splits,
+                                     out=out, workspace=workspace, err_flag=flag, layout=layout)
+        elif mq:
             pkv.multi_query_attention(q, w.k_cache, w.v_cache, block_tables, context_lens, mcl,
                                       scale=w.scale, out=out, workspace=workspace, err_flag=flag,
                                       layout=layout)
@@ -373,6 +391,14 @@ def run_gpu(args):
                                  scale=w.scale, num_splits=args.splits, out=out,
                                  workspace=workspace, err_flag=flag, layout=layout)
 
+    def append_call(k_new, v_new, slot_mapping):
+        if fp8:
+            pkv.append_fp8(k_new, v_new, w.k_cache, w.v_cache, slot_mapping, k_scale, v_scale,
+                           err_flag=flag, layout=layout)
+        else:
+            pkv.append(k_new, v_new, w.k_cache, w.v_cache, slot_mapping, err_flag=flag,
+                       layout=layout)
+
     def step():
         if fused:
             pkv.append_decode_attention(w.q, w.k_new, w.v_new, w.k_cache, w.v_cache,
@@ -380,8 +406,7 @@ def run_gpu(args):
                                         num_splits=args.splits, out=out, workspace=workspace,
                                         err_flag=flag, layout=layout)
             return
-        pkv.append(w.k_new, w.v_new, w.k_cache, w.v_cache, w.slot_mapping, err_flag=flag,
-                   layout=layout)
+        append_call(w.k_new, w.v_new, w.slot_mapping)
         decode_call(w.q, w.block_tables, w.context_lens)
 
     for _ in range(args.warmup):
@@ -459,8 +484,7 @@ def run_gpu(args):
     def e2e_step():
         for k, t in host.items():
             dev_in[k].copy_(t, non_blocking=True)
-        pkv.append(dev_in["k_new"], dev_in["v_new"], w.k_cache, w.v_cache,
-                   dev_in["slot_mapping"], err_flag=flag, layout=layout)
+        append_call(dev_in["k_new"], dev_in["v_new"], dev_in["slot_mapping"])
         decode_call(dev_in["q"], dev_in["block_tables"], dev_in["context_lens"])
         out_h.copy_(out, non_blocking=True)
 
@@ -491,7 +515,8 @@ def run_gpu(args):
     traffic = None
     rec = NCU_TRAFFIC.get(args.config)
     if rec and rec.get("digest") == _kernel_digest() and rec.get("splits") == splits and \
-            rec.get("shared") == shared and not mq and layout == "nhd" and not args.block_size:
+            rec.get("shared") == shared and not mq and layout == "nhd" and not args.block_size \
+            and not fp8:
         traffic = rec["bytes"]
 
     cpu = None
@@ -505,7 +530,7 @@ def run_gpu(args):
         "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": ws,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 5),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": s.dtype, "data": "synthetic",
+        "dtype": f"e4m3 KV, {s.dtype} q" if fp8 else s.dtype, "data": "synthetic",
         "config": {"workload": args.config, "description": WORKLOAD_TEXT[args.config],
                    "num_seqs": s.num_seqs, "num_q_heads": s.num_q_heads,
                    "num_kv_heads": s.num_kv_heads, "head_dim": s.head_dim,
@@ -514,7 +539,7 @@ def run_gpu(args):
                    "shared_prefix_decode": shared,
                    "q_len": args.q_len if mq else 1,
                    "fused_append": fused, "cuda_graph": bool(args.graph),
-                   "layout": layout,
+                   "layout": layout, "kv_cache": "e4m3" if fp8 else s.dtype,
                    "kv_bytes_unique": nbytes["kv_unique"],
                    "decode_bytes_per_step": nbytes["decode"],
                    "decode_bytes_logical": nbytes["decode_logical"],
@@ -552,6 +577,8 @@ def main(argv=None):
     ap.add_argument("--impl", choices=["mine", "reference"], default="mine")
     ap.add_argument("--config", default="c2", choices=sorted(WORKLOAD_TEXT))
     ap.add_argument("--splits", type=int, default=0, help="KV partitions (0 = automatic)")
+    ap.add_argument("--kv", choices=["16bit", "fp8"], default="16bit",
+                    help="cache element type: the workload's 16-bit type or E4M3 codes")
     ap.add_argument("--layout", choices=["nhd", "hnd"], default="nhd",
                     help="page layout: token major [blocks][bs][H_kv][d] or head major "
                          "[blocks][H_kv][bs][d]")

@@ -148,6 +148,39 @@ pkv_status pkv_decode_attention(void* out, const void* q, const void* k_cache,
                                 void* stream);
 
 /*
+ * FP8 (E4M3) KV cache ([vllm-06] 3.3 FP8 inference: E4M3 for inference, the
+ * value range held by a scale; 2.2 kernel fusion: the KV-cache write fused
+ * with quantisation).  The caches hold E4M3 codes, one byte per element, in
+ * either layout; one fp32 scale for K and one for V (finite, > 0): a code c
+ * stands for the value c * k_scale (c * v_scale).  E4M3: 1 sign bit, 4
+ * exponent bits (bias 7), 3 fraction bits, no infinities, S.1111.111 = NaN,
+ * largest finite value 448.
+ *
+ * pkv_append_fp8: pkv_append with quantisation: element x of a new K row is
+ *   stored as E4M3(x / k_scale), the quotient rounded to fp32 and then to the
+ *   nearest E4M3 value (ties to even), saturating at +-448; likewise V.
+ *   k_new, v_new are 16-bit values of dtype (which may carry PKV_LAYOUT_HND);
+ *   the caches must be 8-byte aligned; head_dim a multiple of 8.
+ * pkv_decode_attention_fp8: pkv_decode_attention over E4M3 caches; q and out
+ *   are dtype; head_dim 128 only; workspace as pkv_decode_workspace_size.
+ *   Each code is converted exactly (every E4M3 value is an fp16 and a bf16
+ *   value); k_scale enters the scores, v_scale the output.
+ */
+pkv_status pkv_append_fp8(const void* k_new, const void* v_new, void* k_cache, void* v_cache,
+                          const int64_t* slot_mapping, int num_tokens, int num_blocks,
+                          int block_size, int num_kv_heads, int head_dim, float k_scale,
+                          float v_scale, pkv_dtype dtype, int32_t* err_flag, void* stream);
+
+pkv_status pkv_decode_attention_fp8(void* out, const void* q, const void* k_cache,
+                                    const void* v_cache, const int32_t* block_tables,
+                                    int max_blocks_per_seq, const int32_t* context_lens,
+                                    int max_context_len, int num_seqs, int num_blocks,
+                                    int block_size, int num_q_heads, int num_kv_heads,
+                                    int head_dim, float scale, float k_scale, float v_scale,
+                                    int num_splits, void* workspace, size_t workspace_bytes,
+                                    pkv_dtype dtype, int32_t* err_flag, void* stream);
+
+/*
  * One decode step in one launch: the append of one new token per sequence
  * followed by decode attention, with the append done by the decode kernel
  * itself (the pages list KV-cache writes among the ops worth fusing into

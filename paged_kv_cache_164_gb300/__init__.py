@@ -66,6 +66,9 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
                                          i, p, p]
     lib.pkv_append_decode_attention.argtypes = [p, p, p, p, p, p, p, i, p, i, i, i, i, i, i, i,
                                                 f, i, p, sz, i, p, p]
+    lib.pkv_append_fp8.argtypes = [p, p, p, p, p, i, i, i, i, i, f, f, i, p, p]
+    lib.pkv_decode_attention_fp8.argtypes = [p, p, p, p, p, i, p, i, i, i, i, i, i, i, f, f, f, i,
+                                             p, sz, i, p, p]
     lib.pkv_decode_attention_noalloc.argtypes = [p, p, p, p, p, i, p, i, i, i, i, i, i, i, f,
                                                  i, i, p, p]
     lib.pkv_prefix_shared_workspace_size.argtypes = [i, i, i, i, i, i, i, i, i]
@@ -84,7 +87,7 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.pkv_max_group_size.argtypes = []
     lib.pkv_selftest_wait_timeout.argtypes = [p, ctypes.c_ulonglong, p]
     for name in ("pkv_append", "pkv_decode_attention", "pkv_decode_attention_noalloc",
-                 "pkv_append_decode_attention",
+                 "pkv_append_decode_attention", "pkv_append_fp8", "pkv_decode_attention_fp8",
                  "pkv_decode_attention_prefix_shared", "pkv_multi_query_attention",
                  "pkv_merge", "pkv_gather", "pkv_selftest_wait_timeout",
                  "pkv_check_error", "pkv_max_group_size"):
@@ -263,6 +266,66 @@ def append_decode_attention(q: torch.Tensor, k_new: torch.Tensor, v_new: torch.T
         h_kv, d, float(scale), int(num_splits), ws_ptr, ws_bytes, _kv_code(k_cache, layout),
         _opt(err_flag, "err_flag"), _stream(stream, q.device))
     _check(st, "pkv_append_decode_attention")
+    return out
+
+
+def append_fp8(k_new: torch.Tensor, v_new: torch.Tensor, k_cache: torch.Tensor,
+               v_cache: torch.Tensor, slot_mapping: torch.Tensor, k_scale: float, v_scale: float,
+               err_flag: Optional[torch.Tensor] = None, stream=None,
+               layout: str = "nhd") -> None:
+    """Quantising append into uint8 E4M3 caches: element x of a new K row is
+    stored as E4M3(x / k_scale) (nearest, ties to even, saturating at +-448)."""
+    lib = load()
+    if k_cache.dtype != torch.uint8 or v_cache.dtype != torch.uint8:
+        raise TypeError("E4M3 caches are uint8 tensors of codes")
+    nb, bs, h_kv, d = _cache_dims(k_cache, layout)
+    if v_cache.shape != k_cache.shape or k_new.shape[1:] != (h_kv, d) or \
+            v_new.shape != k_new.shape or slot_mapping.shape != (k_new.shape[0],):
+        raise ValueError("inconsistent fp8 append shapes")
+    st = lib.pkv_append_fp8(_dev(k_new, "k_new"), _dev(v_new, "v_new"),
+                            _dev(k_cache, "k_cache"), _dev(v_cache, "v_cache"),
+                            _dev(slot_mapping, "slot_mapping", torch.int64), k_new.shape[0], nb,
+                            bs, h_kv, d, float(k_scale), float(v_scale),
+                            _kv_code(k_new, layout), _opt(err_flag, "err_flag"),
+                            _stream(stream, k_cache.device))
+    _check(st, "pkv_append_fp8")
+
+
+def decode_attention_fp8(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
+                         block_tables: torch.Tensor, context_lens: torch.Tensor,
+                         max_context_len: int, k_scale: float, v_scale: float,
+                         scale: Optional[float] = None, num_splits: int = 0,
+                         out: Optional[torch.Tensor] = None,
+                         workspace: Optional[torch.Tensor] = None,
+                         err_flag: Optional[torch.Tensor] = None, stream=None,
+                         layout: str = "nhd") -> torch.Tensor:
+    """``decode_attention`` over uint8 E4M3 caches whose codes stand for
+    code * k_scale and code * v_scale; q (and out) fp16 or bf16; head_dim 128."""
+    lib = load()
+    if k_cache.dtype != torch.uint8 or v_cache.dtype != torch.uint8:
+        raise TypeError("E4M3 caches are uint8 tensors of codes")
+    b, h_q, d = q.shape
+    nb, bs, h_kv, d2 = _cache_dims(k_cache, layout)
+    if d2 != d or v_cache.shape != k_cache.shape or block_tables.dim() != 2 or \
+            block_tables.shape[0] != b or context_lens.shape != (b,):
+        raise ValueError("inconsistent fp8 decode shapes")
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    if out is None:
+        out = torch.empty_like(q)
+    need = workspace_size(b, h_q, h_kv, d, bs, max_context_len, num_splits)
+    if workspace is None and need > 0:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    ws_ptr = ctypes.c_void_p(0) if workspace is None else _dev(workspace, "workspace")
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    st = lib.pkv_decode_attention_fp8(
+        _dev(out, "out", q.dtype), _dev(q, "q"), _dev(k_cache, "k_cache"),
+        _dev(v_cache, "v_cache"), _dev(block_tables, "block_tables", torch.int32),
+        block_tables.shape[1], _dev(context_lens, "context_lens", torch.int32),
+        int(max_context_len), b, nb, bs, h_q, h_kv, d, float(scale), float(k_scale),
+        float(v_scale), int(num_splits), ws_ptr, ws_bytes, _kv_code(q, layout),
+        _opt(err_flag, "err_flag"), _stream(stream, q.device))
+    _check(st, "pkv_decode_attention_fp8")
     return out
 
 

@@ -9,6 +9,9 @@
 // head-major cache ([num_blocks][num_kv_heads][block_size][head_dim]) head g
 // of the token lands in the (block, g) tile at row offset.
 #include <climits>
+#include <cmath>
+
+#include <cuda_fp8.h>
 
 #include "pkv_common.cuh"
 
@@ -87,6 +90,56 @@ gather_kernel(uint4* __restrict__ k_out, uint4* __restrict__ v_out,
         const int64_t dst = ((int64_t)b * max_context_len + t) * row_vecs + v;
         k_out[dst] = __ldg(k_cache + src);
         v_out[dst] = __ldg(v_cache + src);
+    }
+}
+
+// Quantising append into an E4M3 cache (vLLM deep dive, 3.3 FP8 inference:
+// E4M3 with the range held by a scale; 2.2: the KV-cache write fused with
+// quantisation): element x of token i's K row is stored as E4M3(x / k_scale),
+// the quotient rounded to fp32 and then to the nearest E4M3 value (ties to
+// even), saturating at +-448; likewise V.  One CTA per token, eight elements
+// (16 input bytes, 8 output bytes) per thread and step.
+template <typename T>
+__global__ void __launch_bounds__(128)
+append_fp8_kernel(const uint4* __restrict__ k_new, const uint4* __restrict__ v_new,
+                  uint8_t* __restrict__ k_cache, uint8_t* __restrict__ v_cache,
+                  const int64_t* __restrict__ slot_mapping, int64_t num_slots, int num_kv_heads,
+                  int head_dim, int block_size, bool hnd, float k_scale, float v_scale,
+                  int32_t* err_flag) {
+    asm volatile("griddepcontrol.launch_dependents;" :::);
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    const int i = blockIdx.x;
+    const int64_t slot = __ldg(slot_mapping + i);
+    if (slot < 0) return;  // padding
+    if (slot >= num_slots) {
+        if (threadIdx.x == 0) flag_error(err_flag, PKV_EFLAG_SLOT);
+        return;
+    }
+    const int row = num_kv_heads * head_dim;
+    const int64_t blk = slot / block_size;
+    const int off = (int)(slot - blk * block_size);
+    for (int c = threadIdx.x; c < row / 8; c += blockDim.x) {
+        const int e = c * 8;              // element of the [heads][dim] row
+        const int g = e / head_dim;
+        const int64_t dst = hnd ? ((blk * num_kv_heads + g) * block_size + off) * head_dim +
+                                      (e - g * head_dim)
+                                : slot * row + e;
+#pragma unroll
+        for (int which = 0; which < 2; ++which) {
+            const uint4 raw = __ldg((which ? v_new : k_new) + ((int64_t)i * row + e) / 8);
+            const float sc = which ? v_scale : k_scale;
+            const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
+            uint32_t outw[2] = {0u, 0u};
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const float2 x = pair_to_float2(w[j], T());
+                const float2 f = make_float2(__fdiv_rn(x.x, sc), __fdiv_rn(x.y, sc));
+                const uint32_t two = __nv_cvt_float2_to_fp8x2(f, __NV_SATFINITE, __NV_E4M3);
+                outw[j / 2] |= two << (16 * (j % 2));
+            }
+            *reinterpret_cast<uint2*>((which ? v_cache : k_cache) + dst) =
+                make_uint2(outw[0], outw[1]);
+        }
     }
 }
 
@@ -189,3 +242,48 @@ extern "C" const char* pkv_status_string(pkv_status status) {
 }
 
 extern "C" int pkv_max_group_size(void) { return kMaxGroup; }
+
+extern "C" pkv_status pkv_append_fp8(const void* k_new, const void* v_new, void* k_cache,
+                                     void* v_cache, const int64_t* slot_mapping, int num_tokens,
+                                     int num_blocks, int block_size, int num_kv_heads,
+                                     int head_dim, float k_scale, float v_scale, pkv_dtype dtype,
+                                     int32_t* err_flag, void* stream) {
+    const bool hnd = take_layout(dtype);
+    if (num_tokens < 0 || num_blocks <= 0 || block_size <= 0 || num_kv_heads <= 0 ||
+        head_dim <= 0 || (dtype != PKV_FP16 && dtype != PKV_BF16) || !std::isfinite(k_scale) ||
+        !std::isfinite(v_scale) || k_scale <= 0.f || v_scale <= 0.f)
+        return PKV_ERR_INVALID_ARG;
+    if (head_dim % 8 != 0) return PKV_ERR_UNSUPPORTED;
+    if (num_tokens == 0) return PKV_OK;
+    if (!k_new || !v_new || !k_cache || !v_cache || !slot_mapping) return PKV_ERR_INVALID_ARG;
+    if (!aligned16(k_new) || !aligned16(v_new) || (reinterpret_cast<uintptr_t>(k_cache) & 7u) ||
+        (reinterpret_cast<uintptr_t>(v_cache) & 7u) ||
+        (reinterpret_cast<uintptr_t>(slot_mapping) & 7u))
+        return PKV_ERR_INVALID_ARG;
+    if ((int64_t)num_kv_heads * head_dim > INT_MAX / 2) return PKV_ERR_UNSUPPORTED;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(num_tokens);
+    cfg.blockDim = dim3(128);
+    cfg.stream = (cudaStream_t)stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    const int64_t slots = (int64_t)num_blocks * block_size;
+    const cudaError_t e =
+        dtype == PKV_FP16
+            ? cudaLaunchKernelEx(&cfg, append_fp8_kernel<__half>, (const uint4*)k_new,
+                                 (const uint4*)v_new, (uint8_t*)k_cache, (uint8_t*)v_cache,
+                                 slot_mapping, slots, num_kv_heads, head_dim, block_size, hnd,
+                                 k_scale, v_scale, err_flag)
+            : cudaLaunchKernelEx(&cfg, append_fp8_kernel<__nv_bfloat16>, (const uint4*)k_new,
+                                 (const uint4*)v_new, (uint8_t*)k_cache, (uint8_t*)v_cache,
+                                 slot_mapping, slots, num_kv_heads, head_dim, block_size, hnd,
+                                 k_scale, v_scale, err_flag);
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return PKV_ERR_CUDA;
+    }
+    return PKV_OK;
+}

@@ -33,6 +33,7 @@
 #include <cmath>
 #include <mutex>
 
+#include <cuda_fp8.h>
 #include <cudaTypedefs.h>
 
 #include "pkv_common.cuh"
@@ -46,13 +47,17 @@ constexpr int kThreads = (kConsumerWarps + 1) * 32;
 constexpr int kMaxChunkPages = 64;    // pages per partition (block-table slice in smem)
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s per wait before giving up
 
-template <int D>
+// Shared-memory geometry of a decode stage: K then V of 16 tokens, as 128-byte
+// swizzled rows per column block (64 dims of a 16-bit cache, 128 of an E4M3 one).
+template <int D, bool F8 = false>
 struct Tile {
-    static constexpr int kRegions = D / 64;                   // 64-dim (128-byte) column blocks
+    static constexpr int kElemBytes = F8 ? 1 : 2;
+    static constexpr int kRegionElems = 128 / kElemBytes;     // elements per 128-byte row
+    static constexpr int kRegions = D / kRegionElems;         // column blocks
     static constexpr int kRegionBytes = kStageTokens * 128;   // 16 rows of 128 bytes, swizzled
     static constexpr int kHalfBytes = kRegions * kRegionBytes;  // K (or V) of one stage
     static constexpr int kStageBytes = 2 * kHalfBytes;
-    static constexpr int kStages = D == 128 ? 8 : 16;         // ring depth: 64 KB either way
+    static constexpr int kStages = 65536 / kStageBytes;       // ring depth: 64 KB
     static constexpr int kRingBytes = kStages * kStageBytes;
     static constexpr int kSmemBytes = 1024 /*align*/ + kRingBytes + 2 * kStages * 8 +
                                       (kMaxChunkPages + 1) * 4 + 16;
@@ -83,7 +88,8 @@ struct DecodeParams {
     int num_kv_heads;
     int max_context_len;
     bool hnd;            // head-major cache layout
-    float scale_log2;    // scale * log2(e)
+    float scale_log2;    // scale * log2(e) (times the K scale of an E4M3 cache)
+    float v_scale;       // value of one V unit: 1, or the V scale of an E4M3 cache
 };
 
 // Context length of sequence b as the kernels use it: negative or too long
@@ -144,6 +150,18 @@ __device__ __forceinline__ bool wait_phase(uint32_t bar, uint32_t parity, volati
     }
 }
 
+// Two E4M3 codes (the first in the low byte) as a pair of T, exactly: every
+// E4M3 value is an fp16 (and a bf16) value.
+__device__ __forceinline__ uint32_t e4m3x2_to(uint32_t v, __half) {
+    const __half2_raw h = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(v & 0xffffu), __NV_E4M3);
+    return (uint32_t)h.x | ((uint32_t)h.y << 16);
+}
+__device__ __forceinline__ uint32_t e4m3x2_to(uint32_t v, __nv_bfloat16) {
+    const __half2_raw h = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(v & 0xffffu), __NV_E4M3);
+    const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&h));
+    return pack2(f.x, f.y, __nv_bfloat16());
+}
+
 // One 16-token stage of K and V, staged in shared memory (128-byte swizzled
 // rows of 64 dims, K then V), against the query columns held in `qb`:
 // S^T = K Q^T on the tensor cores, the base-2 online-softmax update of
@@ -153,7 +171,17 @@ __device__ __forceinline__ bool wait_phase(uint32_t bar, uint32_t parity, volati
 // (0..15) of the stage takes part only when i < nvalid, and, with ROW_LIMITS,
 // only for the columns c with tok0 + i < lim[nt][c]; V rows of tokens at
 // i >= nvalid are zeroed in registers so unused slots never reach the output.
-template <typename T, int D, int NT, bool ROW_LIMITS>
+//
+// F8: the stage holds E4M3 codes, one 128-byte row per token (128 dims).  An
+// ldmatrix of 16-bit units then yields four consecutive dims of a token per
+// register; converted to T pairs they feed the same products with the dims
+// of each 16-dim block permuted (k-slots 2tq, 2tq+1 <- dims 4tq, 4tq+1 and
+// 2tq+8, 2tq+9 <- 4tq+2, 4tq+3), which qb must follow.  For V, the transposed
+// 16-bit units hold a pair of dims for two tokens; split into even and odd
+// dims they make the A operand with the rows of each 16-dim block permuted
+// (row r <- dim 2r for r < 8, dim 2(r-8)+1 for r >= 8): o comes out in that
+// order.
+template <typename T, int D, int NT, bool ROW_LIMITS, bool F8 = false>
 __device__ __forceinline__ void stage_update(uint32_t kbase, uint32_t vbase, int nvalid, int tok0,
                                              const int (&lim)[NT][2],
                                              const uint32_t (&qb)[NT][D / 16][2],
@@ -179,15 +207,39 @@ __device__ __forceinline__ void stage_update(uint32_t kbase, uint32_t vbase, int
     for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
         for (int c = 0; c < 4; ++c) s[nt][c] = 0.f;
+    if constexpr (F8) {
+        static_assert(D == 128, "an E4M3 stage row holds 128 dims");
+        // matrices: (tokens 0-7, block 2j), (8-15, 2j), (0-7, 2j+1), (8-15, 2j+1)
+        const int row = (mi & 1) * 8 + r8;
 #pragma unroll
-    for (int ks = 0; ks < KSTEPS; ++ks) {
-        const int chunk = ks * 2 + k_csel;
-        const uint32_t addr =
-            kbase + (chunk >> 3) * kRegionBytes + k_tok * 128 + (((chunk & 7) ^ r8) << 4);
-        uint32_t a[4];
-        ptx::ldmatrix_x4(a, addr);
+        for (int j = 0; j < D / 32; ++j) {
+            const int chunk = 2 * j + (mi >> 1);
+            uint32_t r[4];
+            ptx::ldmatrix_x4(r, kbase + row * 128 + ((chunk ^ r8) << 4));
 #pragma unroll
-        for (int nt = 0; nt < NT; ++nt) ptx::mma_16816<T>(s[nt], a, qb[nt][ks][0], qb[nt][ks][1]);
+            for (int h = 0; h < 2; ++h) {
+                uint32_t a[4];
+                a[0] = e4m3x2_to(r[2 * h], T());
+                a[1] = e4m3x2_to(r[2 * h + 1], T());
+                a[2] = e4m3x2_to(r[2 * h] >> 16, T());
+                a[3] = e4m3x2_to(r[2 * h + 1] >> 16, T());
+#pragma unroll
+                for (int nt = 0; nt < NT; ++nt)
+                    ptx::mma_16816<T>(s[nt], a, qb[nt][2 * j + h][0], qb[nt][2 * j + h][1]);
+            }
+        }
+    } else {
+#pragma unroll
+        for (int ks = 0; ks < KSTEPS; ++ks) {
+            const int chunk = ks * 2 + k_csel;
+            const uint32_t addr =
+                kbase + (chunk >> 3) * kRegionBytes + k_tok * 128 + (((chunk & 7) ^ r8) << 4);
+            uint32_t a[4];
+            ptx::ldmatrix_x4(a, addr);
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt)
+                ptx::mma_16816<T>(s[nt], a, qb[nt][ks][0], qb[nt][ks][1]);
+        }
     }
 
     // Online softmax in base 2.  s[nt][0]: (token gq, column 2tq), [1]: (gq, 2tq+1),
@@ -250,13 +302,7 @@ __device__ __forceinline__ void stage_update(uint32_t kbase, uint32_t vbase, int
         vmask_hi =
             (2 * tq + 8 < nvalid ? 0x0000ffffu : 0u) | (2 * tq + 9 < nvalid ? 0xffff0000u : 0u);
     }
-#pragma unroll
-    for (int mt = 0; mt < KSTEPS; ++mt) {
-        const int chunk = mt * 2 + v_csel;
-        const uint32_t addr =
-            vbase + (chunk >> 3) * kRegionBytes + v_tok * 128 + (((chunk & 7) ^ r8) << 4);
-        uint32_t a[4];
-        ptx::ldmatrix_x4_trans(a, addr);
+    auto accumulate = [&](int mt, uint32_t (&a)[4]) {
         a[0] &= vmask_lo;
         a[1] &= vmask_lo;
         a[2] &= vmask_hi;
@@ -270,15 +316,45 @@ __device__ __forceinline__ void stage_update(uint32_t kbase, uint32_t vbase, int
             ptx::mma_16816<T>(o[nt][mt], a, pb_hi[nt][0], pb_hi[nt][1]);
             ptx::mma_16816<T>(o[nt][mt], a, pb_lo[nt][0], pb_lo[nt][1]);
         }
+    };
+    if constexpr (F8) {
+        const int row = (mi & 1) * 8 + r8;
+#pragma unroll
+        for (int j = 0; j < D / 32; ++j) {
+            const int chunk = 2 * j + (mi >> 1);
+            uint32_t r[4];
+            ptx::ldmatrix_x4_trans(r, vbase + row * 128 + ((chunk ^ r8) << 4));
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                // r[2h]: tokens 2tq, 2tq+1; r[2h+1]: tokens 2tq+8, 2tq+9; bytes (dim 2gq,
+                // token a), (dim 2gq+1, token a), (dim 2gq, token b), (dim 2gq+1, token b)
+                uint32_t a[4];
+                a[0] = e4m3x2_to(__byte_perm(r[2 * h], 0u, 0x0020), T());      // even dim
+                a[1] = e4m3x2_to(__byte_perm(r[2 * h], 0u, 0x0031), T());      // odd dim
+                a[2] = e4m3x2_to(__byte_perm(r[2 * h + 1], 0u, 0x0020), T());
+                a[3] = e4m3x2_to(__byte_perm(r[2 * h + 1], 0u, 0x0031), T());
+                accumulate(2 * j + h, a);
+            }
+        }
+    } else {
+#pragma unroll
+        for (int mt = 0; mt < KSTEPS; ++mt) {
+            const int chunk = mt * 2 + v_csel;
+            const uint32_t addr =
+                vbase + (chunk >> 3) * kRegionBytes + v_tok * 128 + (((chunk & 7) ^ r8) << 4);
+            uint32_t a[4];
+            ptx::ldmatrix_x4_trans(a, addr);
+            accumulate(mt, a);
+        }
     }
 }
 
-// NT = number of 8-head groups (1: G <= 8, 2: G <= 16).
-template <typename T, int D, int NT>
+// NT = number of 8-head groups (1: G <= 8, 2: G <= 16); F8: E4M3 cache codes.
+template <typename T, int D, int NT, bool F8 = false>
 __global__ void __launch_bounds__(kThreads, 3)
 decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
               const DecodeParams p) {
-    using Cfg = Tile<D>;
+    using Cfg = Tile<D, F8>;
     constexpr int S = Cfg::kStages;
     constexpr int KSTEPS = D / 16;   // k-steps of S^T = K Q^T, also m-tiles of O^T
 
@@ -428,10 +504,10 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
                     ptx::mbar_arrive_expect_tx(fb, Cfg::kStageBytes);
 #pragma unroll
                     for (int r = 0; r < Cfg::kRegions; ++r) {
-                        load_kv_box(kdst + r * Cfg::kRegionBytes, &tm_k, fb, r * 64, g, toff,
-                                    blk, p.hnd, policy);
+                        load_kv_box(kdst + r * Cfg::kRegionBytes, &tm_k, fb,
+                                    r * Cfg::kRegionElems, g, toff, blk, p.hnd, policy);
                         load_kv_box(kdst + Cfg::kHalfBytes + r * Cfg::kRegionBytes, &tm_v, fb,
-                                    r * 64, g, toff, blk, p.hnd, policy);
+                                    r * Cfg::kRegionElems, g, toff, blk, p.hnd, policy);
                     }
                 } else {
                     ptx::mbar_arrive(fb);  // nothing to load: the consumer masks the stage
@@ -457,7 +533,8 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
     float o[NT][KSTEPS][4];    // O^T tiles: 16 dims x 8 heads each
     float m0[NT], m1[NT], l0[NT], l1[NT];  // heads 2tq and 2tq+1 of each 8-head group
     if (warp < kConsumerWarps) {
-        // Q^T operand fragments (B of S^T = K Q^T): head nt*8 + gq, dims 2tq.. of each k-step.
+        // Q^T operand fragments (B of S^T = K Q^T): head nt*8 + gq, dims 2tq.. of each
+        // k-step (for an E4M3 cache, dims 4tq.. and 4tq+2.., the K fragments' order).
         uint32_t qb[NT][KSTEPS][2];
         const T* qbase = static_cast<const T*>(p.q) + ((int64_t)b * p.num_q_heads + g * p.group) * D;
 #pragma unroll
@@ -467,8 +544,10 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
 #pragma unroll
             for (int ks = 0; ks < KSTEPS; ++ks) {
                 const bool ok = head < p.group;
-                qb[nt][ks][0] = ok ? __ldg(qrow + (ks * 16 + 2 * tq) / 2) : 0u;
-                qb[nt][ks][1] = ok ? __ldg(qrow + (ks * 16 + 8 + 2 * tq) / 2) : 0u;
+                const int d0 = F8 ? ks * 16 + 4 * tq : ks * 16 + 2 * tq;
+                const int d1 = F8 ? d0 + 2 : d0 + 8;
+                qb[nt][ks][0] = ok ? __ldg(qrow + d0 / 2) : 0u;
+                qb[nt][ks][1] = ok ? __ldg(qrow + d1 / 2) : 0u;
             }
             m0[nt] = m1[nt] = -INFINITY;
             l0[nt] = l1[nt] = 0.f;
@@ -491,8 +570,9 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
             const int nvalid = blk >= 0 ? min(kStageTokens, t_end - tok0) : 0;
             if (nvalid > 0) {
                 const uint32_t kbase = ring_addr + slot * Cfg::kStageBytes;
-                stage_update<T, D, NT, false>(kbase, kbase + Cfg::kHalfBytes, nvalid, 0, no_limit, qb,
-                                              o, m0, m1, l0, l1, p.scale_log2, lane);
+                stage_update<T, D, NT, false, F8>(kbase, kbase + Cfg::kHalfBytes, nvalid, 0,
+                                                  no_limit, qb, o, m0, m1, l0, l1, p.scale_log2,
+                                                  lane);
             }
             __syncwarp();
             if (lane == 0) ptx::mbar_arrive(ptx::smem_addr(&empty_bar[slot]));
@@ -529,10 +609,14 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
             float* w1 = w0 + OSTRIDE;
 #pragma unroll
             for (int mt = 0; mt < KSTEPS; ++mt) {
-                w0[mt * 16 + gq] = o[nt][mt][0];
-                w1[mt * 16 + gq] = o[nt][mt][1];
-                w0[mt * 16 + gq + 8] = o[nt][mt][2];
-                w1[mt * 16 + gq + 8] = o[nt][mt][3];
+                // fragment rows gq and gq+8 of block mt are dims gq, gq+8 (16-bit cache)
+                // or 2gq, 2gq+1 (E4M3 cache)
+                const int da = F8 ? mt * 16 + 2 * gq : mt * 16 + gq;
+                const int db = F8 ? da + 1 : da + 8;
+                w0[da] = o[nt][mt][0];
+                w1[da] = o[nt][mt][1];
+                w0[db] = o[nt][mt][2];
+                w1[db] = o[nt][mt][3];
             }
         }
         ptx::named_barrier_sync(1, kConsumerWarps * 32);
@@ -555,7 +639,7 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
                 c[w] = (mx == -INFINITY || mw == -INFINITY) ? 0.f : exp2f(mw - mx);
                 den = fmaf(sm_l[w * HP + h], c[w], den);
             }
-            const float inv = den > 0.f ? 1.f / den : 0.f;
+            const float inv = den > 0.f ? p.v_scale / den : 0.f;
 #pragma unroll
             for (int w = 0; w < kConsumerWarps; ++w) sm_f[h * kConsumerWarps + w] = c[w] * inv;
             sm_lse[h] = den > 0.f ? (mx + log2f(den)) * kLn2 : -INFINITY;
@@ -1496,19 +1580,21 @@ static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 // block_size, H_kv, num_blocks; box 64 dims x 16 tokens x 1 head x 1 block.
 // 128-byte swizzle either way, so a box lands as 16 rows of 128 bytes.
 static bool make_cache_map(CUtensorMap* map, const void* base, pkv_dtype dtype, int num_blocks,
-                           int block_size, int num_kv_heads, int head_dim, bool hnd) {
+                           int block_size, int num_kv_heads, int head_dim, bool hnd,
+                           bool f8 = false) {
     PFN_cuTensorMapEncodeTiled_v12000 fn = encode_fn();
     if (fn == nullptr) return false;
-    const cuuint64_t e = 2;
+    const cuuint64_t e = f8 ? 1 : 2;
     const cuuint64_t inner = hnd ? (cuuint64_t)block_size : (cuuint64_t)num_kv_heads;
     const cuuint64_t outer = hnd ? (cuuint64_t)num_kv_heads : (cuuint64_t)block_size;
     cuuint64_t dims[4] = {(cuuint64_t)head_dim, inner, outer, (cuuint64_t)num_blocks};
     cuuint64_t strides[3] = {(cuuint64_t)head_dim * e, inner * head_dim * e,
                              outer * inner * head_dim * e};
-    cuuint32_t box[4] = {64, hnd ? (cuuint32_t)kStageTokens : 1u,
+    cuuint32_t box[4] = {(cuuint32_t)(128 / e), hnd ? (cuuint32_t)kStageTokens : 1u,
                          hnd ? 1u : (cuuint32_t)kStageTokens, 1};
     cuuint32_t estr[4] = {1, 1, 1, 1};
-    CUresult r = fn(map, dtype == PKV_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+    CUresult r = fn(map, f8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8
+                       : dtype == PKV_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
                                            : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
                     4, const_cast<void*>(base), dims, strides, box, estr,
                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -1516,21 +1602,21 @@ static bool make_cache_map(CUtensorMap* map, const void* base, pkv_dtype dtype, 
     return r == CUDA_SUCCESS;
 }
 
-template <typename T, int D, int NT>
+template <typename T, int D, int NT, bool F8>
 static cudaError_t launch_decode_t(const CUtensorMap& mk, const CUtensorMap& mv,
                                    const DecodeParams& p, dim3 grid, cudaStream_t stream) {
-    auto kern = decode_kernel<T, D, NT>;
+    auto kern = decode_kernel<T, D, NT, F8>;
     static std::once_flag once;
     static cudaError_t attr_err = cudaSuccess;
     std::call_once(once, [&] {
         attr_err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                        Tile<D>::kSmemBytes);
+                                        Tile<D, F8>::kSmemBytes);
     });
     if (attr_err != cudaSuccess) return attr_err;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = grid;
     cfg.blockDim = dim3(kThreads);
-    cfg.dynamicSmemBytes = Tile<D>::kSmemBytes;
+    cfg.dynamicSmemBytes = Tile<D, F8>::kSmemBytes;
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -1540,16 +1626,20 @@ static cudaError_t launch_decode_t(const CUtensorMap& mk, const CUtensorMap& mv,
     return cudaLaunchKernelEx(&cfg, kern, mk, mv, p);
 }
 
+// f8: an E4M3 cache (head_dim 128 only).
 template <typename T>
 static cudaError_t launch_decode(const CUtensorMap& mk, const CUtensorMap& mv,
                                  const DecodeParams& p, int head_dim, dim3 grid,
-                                 cudaStream_t stream) {
+                                 cudaStream_t stream, bool f8 = false) {
     const bool wide = p.group > 8;
+    if (f8)
+        return wide ? launch_decode_t<T, 128, 2, true>(mk, mv, p, grid, stream)
+                    : launch_decode_t<T, 128, 1, true>(mk, mv, p, grid, stream);
     if (head_dim == 64)
-        return wide ? launch_decode_t<T, 64, 2>(mk, mv, p, grid, stream)
-                    : launch_decode_t<T, 64, 1>(mk, mv, p, grid, stream);
-    return wide ? launch_decode_t<T, 128, 2>(mk, mv, p, grid, stream)
-                : launch_decode_t<T, 128, 1>(mk, mv, p, grid, stream);
+        return wide ? launch_decode_t<T, 64, 2, false>(mk, mv, p, grid, stream)
+                    : launch_decode_t<T, 64, 1, false>(mk, mv, p, grid, stream);
+    return wide ? launch_decode_t<T, 128, 2, false>(mk, mv, p, grid, stream)
+                : launch_decode_t<T, 128, 1, false>(mk, mv, p, grid, stream);
 }
 
 template <typename T>
@@ -1708,7 +1798,8 @@ static pkv_status decode_impl(void* out, const void* q, const void* k_new, const
                               int max_context_len, int num_seqs, int num_blocks, int block_size,
                               int num_q_heads, int num_kv_heads, int head_dim, float scale,
                               int num_splits, void* workspace, size_t workspace_bytes,
-                              pkv_dtype dtype, int32_t* err_flag, void* stream) {
+                              pkv_dtype dtype, int32_t* err_flag, void* stream, bool f8 = false,
+                              float k_scale = 1.f, float v_scale = 1.f) {
     const bool hnd = take_layout(dtype);
     pkv_status st = check_shapes(num_seqs, num_q_heads, num_kv_heads, head_dim, block_size,
                                  max_context_len, num_splits);
@@ -1726,6 +1817,10 @@ static pkv_status decode_impl(void* out, const void* q, const void* k_new, const
     if ((k_new == nullptr) != (v_new == nullptr) ||
         (k_new != nullptr && (!aligned16(k_new) || !aligned16(v_new))))
         return PKV_ERR_INVALID_ARG;
+    if (f8 && (head_dim != 128 || k_new != nullptr)) return PKV_ERR_UNSUPPORTED;
+    if (f8 && (!std::isfinite(k_scale) || !std::isfinite(v_scale) || k_scale <= 0.f ||
+               v_scale <= 0.f))
+        return PKV_ERR_INVALID_ARG;
     if ((int64_t)max_blocks_per_seq * block_size > INT_MAX) return PKV_ERR_UNSUPPORTED;
     Plan plan;
     st = make_plan(num_seqs, num_q_heads, num_kv_heads, head_dim, block_size, max_context_len,
@@ -1736,8 +1831,10 @@ static pkv_status decode_impl(void* out, const void* q, const void* k_new, const
     if (workspace != nullptr && !aligned16(workspace)) return PKV_ERR_INVALID_ARG;
 
     CUtensorMap mk, mv;
-    if (!make_cache_map(&mk, k_cache, dtype, num_blocks, block_size, num_kv_heads, head_dim, hnd) ||
-        !make_cache_map(&mv, v_cache, dtype, num_blocks, block_size, num_kv_heads, head_dim, hnd))
+    if (!make_cache_map(&mk, k_cache, dtype, num_blocks, block_size, num_kv_heads, head_dim, hnd,
+                        f8) ||
+        !make_cache_map(&mv, v_cache, dtype, num_blocks, block_size, num_kv_heads, head_dim, hnd,
+                        f8))
         return PKV_ERR_CUDA;
 
     DecodeParams p = {};
@@ -1755,7 +1852,8 @@ static pkv_status decode_impl(void* out, const void* q, const void* k_new, const
     p.chunk_tokens = plan.chunk_tokens;
     p.num_kv_heads = num_kv_heads;
     p.max_context_len = max_context_len;
-    p.scale_log2 = scale * kLog2e;
+    p.scale_log2 = scale * k_scale * kLog2e;
+    p.v_scale = v_scale;
     p.partial_o = nullptr;
     p.partial_lse = nullptr;
     p.seq_info = nullptr;
@@ -1772,8 +1870,9 @@ static pkv_status decode_impl(void* out, const void* q, const void* k_new, const
     }
     cudaStream_t s = (cudaStream_t)stream;
     dim3 grid(num_kv_heads, num_seqs, plan.num_splits);
-    cudaError_t e = dtype == PKV_FP16 ? launch_decode<__half>(mk, mv, p, head_dim, grid, s)
-                                      : launch_decode<__nv_bfloat16>(mk, mv, p, head_dim, grid, s);
+    cudaError_t e = dtype == PKV_FP16
+                        ? launch_decode<__half>(mk, mv, p, head_dim, grid, s, f8)
+                        : launch_decode<__nv_bfloat16>(mk, mv, p, head_dim, grid, s, f8);
     if (e != cudaSuccess) {
         cudaGetLastError();
         return PKV_ERR_CUDA;
@@ -1815,6 +1914,19 @@ extern "C" pkv_status pkv_decode_attention(void* out, const void* q, const void*
                        max_context_len, num_seqs, num_blocks, block_size, num_q_heads,
                        num_kv_heads, head_dim, scale, num_splits, workspace, workspace_bytes,
                        dtype, err_flag, stream);
+}
+
+extern "C" pkv_status pkv_decode_attention_fp8(
+    void* out, const void* q, const void* k_cache, const void* v_cache,
+    const int32_t* block_tables, int max_blocks_per_seq, const int32_t* context_lens,
+    int max_context_len, int num_seqs, int num_blocks, int block_size, int num_q_heads,
+    int num_kv_heads, int head_dim, float scale, float k_scale, float v_scale, int num_splits,
+    void* workspace, size_t workspace_bytes, pkv_dtype dtype, int32_t* err_flag, void* stream) {
+    return decode_impl(out, q, nullptr, nullptr, const_cast<void*>(k_cache),
+                       const_cast<void*>(v_cache), block_tables, max_blocks_per_seq, context_lens,
+                       max_context_len, num_seqs, num_blocks, block_size, num_q_heads,
+                       num_kv_heads, head_dim, scale, num_splits, workspace, workspace_bytes,
+                       dtype, err_flag, stream, true, k_scale, v_scale);
 }
 
 extern "C" pkv_status pkv_append_decode_attention(
@@ -2033,6 +2145,7 @@ extern "C" pkv_status pkv_decode_attention_prefix_shared(
     p.max_context_len = max_context_len;
     p.hnd = hnd;
     p.scale_log2 = scale * kLog2e;
+    p.v_scale = 1.f;
     const dim3 grid((unsigned)num_items);
     e = dtype == PKV_FP16 ? launch_decode<__half>(mk, mv, p, head_dim, grid, s)
                           : launch_decode<__nv_bfloat16>(mk, mv, p, head_dim, grid, s);

@@ -274,6 +274,16 @@ def to_head_major(cache: torch.Tensor) -> torch.Tensor:
     return cache.permute(0, 2, 1, 3).contiguous()
 
 
+def make_fp8_codes(shape, seed: int, device="cpu") -> torch.Tensor:
+    """Seeded E4M3 bit patterns (uint8) of normal values with |value| in
+    [2^-6, 2^3): random sign, exponent field 1..9, any fraction; never NaN."""
+    g = torch.Generator().manual_seed(seed * 7919 + 31)
+    sign = torch.randint(0, 2, shape, generator=g, dtype=torch.int32) << 7
+    expo = torch.randint(1, 10, shape, generator=g, dtype=torch.int32) << 3
+    frac = torch.randint(0, 8, shape, generator=g, dtype=torch.int32)
+    return (sign | expo | frac).to(torch.uint8).to(device)
+
+
 def make_queries(w: Workload, q_len: int, seed: int) -> torch.Tensor:
     """Seeded N(0,1) queries [B, q_len, H_q, d] in the workload's dtype and device
     (several new query tokens per sequence: a prefill chunk or drafted tokens)."""
