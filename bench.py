@@ -365,11 +365,11 @@ def run_gpu(args):
     workspace = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device=device)
     out = torch.empty_like(w.q)
     flag = pkv.new_error_flag(device)
-    # append, decode, merge when split; the shared-prefix path: append, plan,
-    # prefix, decode, merge
+    # append, decode, merge when split; the shared-prefix path: append, prefix
+    # (with the plan as one of its CTAs), decode, merge
     # --fused: the append is done by the decode kernel (plain path only)
     fused = args.fused and not mq and not shared
-    launches_per_step = (3 if mq else 5 if shared else
+    launches_per_step = (3 if mq else 4 if shared else
                          (1 if fused else 2) + (1 if splits > 1 else 0))
 
     def decode_call(q, block_tables, context_lens):
@@ -553,7 +553,7 @@ def run_gpu(args):
                      "unit": "GB/s", "frac": round(decode_gbs / peak, 4),
                      "traffic": traffic,
                      "kernel": ("prefix_kernel in multi-query mode (tcgen05) + merge_kernel" if mq
-                                else "plan_kernel + prefix_kernel + decode_kernel + merge_kernel"
+                                else "prefix_kernel (with the plan CTA) + decode_kernel + merge_kernel"
                                 if shared else "decode_kernel + merge_kernel")
                      + " (one attention call, back to back)",
                      "peak_source": f"{peak_src} hbm_gbs"},

@@ -701,6 +701,37 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
 // below 256 and the final normalisation uses the same reference, so the
 // result is the same softmax.
 
+// ---------------------------------------------------------------------------
+// Shared-prefix decode: the plan
+// ---------------------------------------------------------------------------
+// One CTA writes, for every sequence, its (shared-prefix tokens, prefix
+// partials) record and the compact list of the suffix partitions that hold
+// tokens, unit by unit ((sequence, KV head) pairs, KV head fastest).  The
+// decode grid is sized for the longest sequence; with the list, only real
+// partitions get a CTA and the rest of the grid exits at once.  The plan runs
+// as an extra CTA of the prefix kernel's launch (it needs nothing the prefix
+// CTAs compute), so it costs neither a launch nor a serial step.
+
+struct PlanParams {
+    const int32_t* context_lens;
+    const int32_t* group_start;
+    const int32_t* group_prefix_len;
+    int2* seq_info;   // [B] out
+    int2* items;      // out: (unit, partition)
+    int* item_count;  // out
+    int32_t* err_flag;
+    int num_seqs;
+    int num_kv_heads;
+    int num_groups;
+    int max_group_size;
+    int max_prefix_len;
+    int block_size;
+    int max_blocks_per_seq;
+    int prefix_chunk;
+    int chunk_tokens;
+    int cap;
+};
+
 struct PrefixParams {
     const void* q;
     const int32_t* block_tables;
@@ -726,6 +757,8 @@ struct PrefixParams {
     int q_len;            // 0: shared prefixes; > 0: multi-query (q_len query tokens per sequence)
     bool hnd;             // head-major cache layout
     float scale_log2;
+    bool with_plan;       // grid z slice 0 is the plan (its CTA (0, 0, 0)); partitions follow
+    PlanParams plan;
 };
 
 constexpr int kPrefixTileRows = 128;     // query rows per CTA (MMA M)
@@ -812,6 +845,79 @@ __device__ __forceinline__ void split_hi_lo(float p0, float p1, uint32_t& hi, ui
     lo = pack2(p0 - back.x, p1 - back.y, __half());
 }
 
+// The plan, run by one CTA of any width (a multiple of 32, at most 1024).
+// scratch: 33 ints of shared memory.
+__device__ void plan_cta(const PlanParams& p, int* scratch) {
+    int* warp_sum = scratch;  // [32] exclusive prefix of the warp totals
+    int* base = scratch + 32;
+    const int tid = threadIdx.x;
+    const int lane = tid & 31;
+    const int warp = tid >> 5;
+    const int nthreads = blockDim.x;
+    const int nwarps = nthreads >> 5;
+
+    // 1. per-sequence prefix records (a search of group_start)
+    for (int b = tid; b < p.num_seqs; b += nthreads) {
+        int2 info = make_int2(0, 0);
+        if (p.num_groups > 0) {
+            int lo = 0, hi = p.num_groups - 1;  // last group with group_start <= b
+            while (lo < hi) {
+                const int mid = (lo + hi + 1) >> 1;
+                if (p.group_start[mid] <= b) lo = mid; else hi = mid - 1;
+            }
+            int first, last, plen;
+            if (group_valid(p.group_start, p.group_prefix_len, lo, p.num_seqs, p.max_group_size,
+                            p.max_prefix_len, p.block_size, p.max_blocks_per_seq, first, last,
+                            plen) &&
+                first <= b && b < last)
+                info = make_int2(plen, (plen + p.prefix_chunk - 1) / p.prefix_chunk);
+            else
+                flag_error(p.err_flag, PKV_EFLAG_GROUP);
+        }
+        p.seq_info[b] = info;
+    }
+    if (tid == 0) *base = 0;
+    __syncthreads();
+
+    // 2. the suffix partitions with tokens, unit by unit (block-wide scans)
+    const int units = p.num_seqs * p.num_kv_heads;
+    for (int u0 = 0; u0 < units; u0 += nthreads) {
+        const int u = u0 + tid;
+        int cnt = 0;
+        if (u < units) {
+            const int b = u / p.num_kv_heads;
+            const int2 info = p.seq_info[b];
+            const int n = clamped_len(p.context_lens[b], p.cap);
+            cnt = suffix_partitions(max(0, n - info.x), info.y, p.chunk_tokens);
+        }
+        int incl = cnt;  // inclusive warp scan
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            const int v = __shfl_up_sync(0xffffffffu, incl, off);
+            if (lane >= off) incl += v;
+        }
+        if (lane == 31) warp_sum[warp] = incl;
+        __syncthreads();
+        if (warp == 0) {
+            const int w = lane < nwarps ? warp_sum[lane] : 0;
+            int wi = w;
+#pragma unroll
+            for (int off = 1; off < 32; off <<= 1) {
+                const int v = __shfl_up_sync(0xffffffffu, wi, off);
+                if (lane >= off) wi += v;
+            }
+            if (lane < nwarps) warp_sum[lane] = wi - w;
+        }
+        __syncthreads();
+        const int pos = *base + warp_sum[warp] + incl - cnt;
+        for (int j = 0; j < cnt; ++j) p.items[pos + j] = make_int2(u, j);
+        __syncthreads();
+        if (tid == nthreads - 1) *base = pos + cnt;
+        __syncthreads();
+    }
+    if (tid == 0) *p.item_count = *base;
+}
+
 template <typename T, int D>
 __global__ void __launch_bounds__(kPrefixThreads, 1)
 prefix_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
@@ -844,7 +950,7 @@ prefix_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
     const int rt = blockIdx.x;                     // tile of 128 query rows
     const int g = blockIdx.y % p.num_kv_heads;     // KV head
     const int grp = blockIdx.y / p.num_kv_heads;   // group (shared prefix) or sequence (multi-query)
-    const int part = blockIdx.z;                   // partition of the tokens
+    const int part = blockIdx.z - (p.with_plan ? 1 : 0);  // partition of the tokens
     const int tid = threadIdx.x;
     const int warp = tid >> 5;
     const int lane = tid & 31;
@@ -852,6 +958,11 @@ prefix_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
 
     ptx::launch_dependents();
     ptx::grid_dependency_wait();
+
+    if (part < 0) {  // the plan slice
+        if (blockIdx.x == 0 && blockIdx.y == 0) plan_cta(p.plan, reinterpret_cast<int*>(smem));
+        return;
+    }
 
     // The CTA's query rows and tokens.  Shared prefix (q_len == 0): row r is
     // query head g*group + r % group of member first + r / group of group grp,
@@ -1227,117 +1338,17 @@ prefix_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
     }
 }
 
-// ---------------------------------------------------------------------------
-// Shared-prefix decode: the plan kernel
-// ---------------------------------------------------------------------------
-// One CTA writes, for every sequence, its (shared-prefix tokens, prefix
-// partials) record and the compact list of the suffix partitions that hold
-// tokens, unit by unit ((sequence, KV head) pairs, KV head fastest).  The
-// decode grid is sized for the longest sequence; with the list, only real
-// partitions get a CTA and the rest of the grid exits at once.
-
-struct PlanParams {
-    const int32_t* context_lens;
-    const int32_t* group_start;
-    const int32_t* group_prefix_len;
-    int2* seq_info;   // [B] out
-    int2* items;      // out: (unit, partition)
-    int* item_count;  // out
-    int32_t* err_flag;
-    int num_seqs;
-    int num_kv_heads;
-    int num_groups;
-    int max_group_size;
-    int max_prefix_len;
-    int block_size;
-    int max_blocks_per_seq;
-    int prefix_chunk;
-    int chunk_tokens;
-    int cap;
-};
-
-constexpr int kPlanThreads = 1024;
-
-__global__ void __launch_bounds__(kPlanThreads) plan_kernel(const PlanParams p) {
-    __shared__ int warp_sum[kPlanThreads / 32];
-    __shared__ int base;
-    const int tid = threadIdx.x;
-    const int lane = tid & 31;
-    const int warp = tid >> 5;
-    ptx::launch_dependents();
-    ptx::grid_dependency_wait();
-
-    // 1. per-sequence prefix records (a search of group_start)
-    for (int b = tid; b < p.num_seqs; b += kPlanThreads) {
-        int2 info = make_int2(0, 0);
-        if (p.num_groups > 0) {
-            int lo = 0, hi = p.num_groups - 1;  // last group with group_start <= b
-            while (lo < hi) {
-                const int mid = (lo + hi + 1) >> 1;
-                if (p.group_start[mid] <= b) lo = mid; else hi = mid - 1;
-            }
-            int first, last, plen;
-            if (group_valid(p.group_start, p.group_prefix_len, lo, p.num_seqs, p.max_group_size,
-                            p.max_prefix_len, p.block_size, p.max_blocks_per_seq, first, last,
-                            plen) &&
-                first <= b && b < last)
-                info = make_int2(plen, (plen + p.prefix_chunk - 1) / p.prefix_chunk);
-            else
-                flag_error(p.err_flag, PKV_EFLAG_GROUP);
-        }
-        p.seq_info[b] = info;
-    }
-    if (tid == 0) base = 0;
-    __syncthreads();
-
-    // 2. the suffix partitions with tokens, unit by unit (block-wide scans)
-    const int units = p.num_seqs * p.num_kv_heads;
-    for (int u0 = 0; u0 < units; u0 += kPlanThreads) {
-        const int u = u0 + tid;
-        int cnt = 0;
-        if (u < units) {
-            const int b = u / p.num_kv_heads;
-            const int2 info = p.seq_info[b];
-            const int n = clamped_len(p.context_lens[b], p.cap);
-            cnt = suffix_partitions(max(0, n - info.x), info.y, p.chunk_tokens);
-        }
-        int incl = cnt;  // inclusive warp scan
-#pragma unroll
-        for (int off = 1; off < 32; off <<= 1) {
-            const int v = __shfl_up_sync(0xffffffffu, incl, off);
-            if (lane >= off) incl += v;
-        }
-        if (lane == 31) warp_sum[warp] = incl;
-        __syncthreads();
-        if (warp == 0) {
-            const int w = warp_sum[lane];
-            int wi = w;
-#pragma unroll
-            for (int off = 1; off < 32; off <<= 1) {
-                const int v = __shfl_up_sync(0xffffffffu, wi, off);
-                if (lane >= off) wi += v;
-            }
-            warp_sum[lane] = wi - w;  // exclusive prefix of the warp totals
-        }
-        __syncthreads();
-        const int pos = base + warp_sum[warp] + incl - cnt;
-        for (int j = 0; j < cnt; ++j) p.items[pos + j] = make_int2(u, j);
-        __syncthreads();
-        if (tid == kPlanThreads - 1) base = pos + cnt;
-        __syncthreads();
-    }
-    if (tid == 0) *p.item_count = base;
-}
-
-// Merge of split partials (log-sum-exp rule): one CTA per (query head,
-// sequence).  Its threads cover the head's dims four at a time and, across
-// thread groups, interleaved subsets of the partitions; the groups' sums meet
-// in shared memory.  With context_lens given (the decode path), a sequence
-// whose context fitted a single partition was written by the decode kernel and
-// is skipped, and only the partitions that hold tokens are read.  Multi-query
-// rows (q_len > 0) are always merged, from the partitions of their sequence's
-// context.  Without context_lens (pkv_merge), every row merges all num_splits
-// partials.
+// Merge of split partials (log-sum-exp rule): one warp per (row of q, query
+// head), four rows per CTA.  Each lane owns float4 columns of the head (lane,
+// lane + 32, ...) and weighs every partition itself: w_p = e^(lse_p - m*),
+// out = sum_p w_p O_p / sum_p w_p; m* and sum_p w_p come from lane-strided
+// sums and shuffles.  No shared memory and no CTA barrier: rows are short,
+// and the merge of a call is a few thousand of them.  With context_lens given
+// (the decode path), a sequence whose context fitted a single partition was
+// written by the decode kernel and is skipped, and only the partitions that
+// hold tokens are read.  Multi-query rows (q_len > 0) are always merged, from
+// the partitions of their sequence's context.  Without context_lens
+// (pkv_merge), every row merges all num_splits partials.
 struct MergeParams {
     void* out;
     const float* partial_o;
@@ -1348,24 +1359,26 @@ struct MergeParams {
     int num_kv_heads;
     int group;                    // query heads per KV head
     int num_splits;
-    int head_dim;                 // a multiple of 4, at most 4 * kMergeThreads
+    int head_dim;                 // a multiple of 4, at most 512
     int chunk_tokens;
     int cap;                      // context clamp, as in the decode kernel
     int q_len;                    // > 0: multi-query rows (sequence, query token); every row merged
+    int64_t rows;                 // (row of q, query head) pairs
 };
 
-constexpr int kMergeThreads = 128;
+constexpr int kMergeRowsPerCta = 4;
+constexpr int kMergeThreads = kMergeRowsPerCta * 32;
+constexpr int kMergeMaxHeadDim = 512;
 
 template <typename T>
 __global__ void __launch_bounds__(kMergeThreads)
 merge_kernel(const MergeParams p) {
-    __shared__ float4 part[kMergeThreads];
-    __shared__ float s_mx, s_inv;
-    const int h = blockIdx.x;
-    const int b = blockIdx.y;  // row of q: a sequence, or (sequence, query token) for multi-query
-    const int tid = threadIdx.x;
+    const int lane = threadIdx.x & 31;
+    const int64_t row = (int64_t)blockIdx.x * kMergeRowsPerCta + (threadIdx.x >> 5);
     ptx::launch_dependents();
     ptx::grid_dependency_wait();
+    if (row >= p.rows) return;
+    const int b = (int)(row / p.num_q_heads);  // row of q: a sequence, or (sequence, query token)
     int ns = p.num_splits;
     if (p.q_len > 0) {
         // multi-query partials: the partitions of the sequence's context
@@ -1382,62 +1395,44 @@ merge_kernel(const MergeParams p) {
         ns = slot0 + suffix_partitions(max(0, n - start), slot0, p.chunk_tokens);
         if (slot0 == 0 && ns <= 1) return;  // written directly by the decode kernel
     }
-    const int64_t row = (int64_t)b * p.num_q_heads + h;
     const float* lse = p.partial_lse + row * p.num_splits;
-    if (tid < 32) {  // m* = max_p lse_p and 1 / sum_p e^(lse_p - m*)
-        float mx = -INFINITY;
-        for (int sp = tid; sp < ns; sp += 32) mx = fmaxf(mx, lse[sp]);
+    // m* = max_p lse_p and 1 / sum_p e^(lse_p - m*)
+    float mx = -INFINITY;
+    for (int sp = lane; sp < ns; sp += 32) mx = fmaxf(mx, lse[sp]);
 #pragma unroll
-        for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
-        float den = 0.f;
-        if (mx != -INFINITY)
-            for (int sp = tid; sp < ns; sp += 32) {
-                const float ls = lse[sp];
-                if (ls != -INFINITY) den += exp2f((ls - mx) * kLog2e);
-            }
-#pragma unroll
-        for (int off = 16; off > 0; off >>= 1) den += __shfl_xor_sync(0xffffffffu, den, off);
-        if (tid == 0) {
-            s_mx = mx;
-            s_inv = den > 0.f ? 1.f / den : 0.f;
-        }
-    }
-    __syncthreads();
-    const int cols = p.head_dim / 4;          // float4 columns
-    const int groups = kMergeThreads / cols;  // partition subsets
-    const int col = tid % cols;
-    const int grp = tid / cols;
-    const float mx = s_mx;
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (grp < groups && mx != -INFINITY) {
-        const float* po = p.partial_o + row * p.num_splits * p.head_dim + col * 4;
-        for (int sp = grp; sp < ns; sp += groups) {
+    for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+    float den = 0.f;
+    if (mx != -INFINITY)
+        for (int sp = lane; sp < ns; sp += 32) {
             const float ls = lse[sp];
-            if (ls == -INFINITY) continue;  // an empty partition may hold anything
-            const float wgt = exp2f((ls - mx) * kLog2e);
-            const float4 v = *reinterpret_cast<const float4*>(po + (int64_t)sp * p.head_dim);
-            acc.x = fmaf(wgt, v.x, acc.x);
-            acc.y = fmaf(wgt, v.y, acc.y);
-            acc.z = fmaf(wgt, v.z, acc.z);
-            acc.w = fmaf(wgt, v.w, acc.w);
+            if (ls != -INFINITY) den += exp2f((ls - mx) * kLog2e);
         }
-    }
-    part[tid] = acc;
-    __syncthreads();
-    if (tid < cols) {
-        float4 sum = part[tid];
-        for (int gi = 1; gi < groups; ++gi) {
-            const float4 v = part[gi * cols + tid];
-            sum.x += v.x;
-            sum.y += v.y;
-            sum.z += v.z;
-            sum.w += v.w;
-        }
-        const float inv = s_inv;
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) den += __shfl_xor_sync(0xffffffffu, den, off);
+    const float inv = den > 0.f ? 1.f / den : 0.f;
+    const int cols = p.head_dim / 4;
+    const float* po = p.partial_o + row * p.num_splits * p.head_dim;
+    T* out = static_cast<T*>(p.out) + row * p.head_dim;
+#pragma unroll
+    for (int k = 0; k < kMergeMaxHeadDim / 128; ++k) {
+        const int c = lane + 32 * k;
+        if (c >= cols) break;
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (mx != -INFINITY)
+            for (int sp = 0; sp < ns; ++sp) {
+                const float ls = lse[sp];
+                if (ls == -INFINITY) continue;  // an empty partition may hold anything
+                const float wgt = exp2f((ls - mx) * kLog2e);
+                const float4 v = *reinterpret_cast<const float4*>(po + (int64_t)sp * p.head_dim + c * 4);
+                acc.x = fmaf(wgt, v.x, acc.x);
+                acc.y = fmaf(wgt, v.y, acc.y);
+                acc.z = fmaf(wgt, v.z, acc.z);
+                acc.w = fmaf(wgt, v.w, acc.w);
+            }
         uint2 packed;
-        packed.x = pack2(sum.x * inv, sum.y * inv, T());
-        packed.y = pack2(sum.z * inv, sum.w * inv, T());
-        *reinterpret_cast<uint2*>(static_cast<T*>(p.out) + row * p.head_dim + tid * 4) = packed;
+        packed.x = pack2(acc.x * inv, acc.y * inv, T());
+        packed.y = pack2(acc.z * inv, acc.w * inv, T());
+        *reinterpret_cast<uint2*>(out + c * 4) = packed;
     }
 }
 
@@ -1644,8 +1639,12 @@ static cudaError_t launch_decode(const CUtensorMap& mk, const CUtensorMap& mv,
 
 template <typename T>
 static cudaError_t launch_merge(const MergeParams& p, int groups, int seqs, cudaStream_t stream) {
+    MergeParams q = p;
+    q.rows = (int64_t)groups * seqs;
+    const int64_t ctas = (q.rows + kMergeRowsPerCta - 1) / kMergeRowsPerCta;
+    if (ctas > INT_MAX) return cudaErrorInvalidValue;
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(groups, seqs);
+    cfg.gridDim = dim3((unsigned)std::max<int64_t>(1, ctas));
     cfg.blockDim = dim3(kMergeThreads);
     cfg.dynamicSmemBytes = 0;
     cfg.stream = stream;
@@ -1654,7 +1653,7 @@ static cudaError_t launch_merge(const MergeParams& p, int groups, int seqs, cuda
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, merge_kernel<T>, p);
+    return cudaLaunchKernelEx(&cfg, merge_kernel<T>, q);
 }
 
 template <typename T, int D>
@@ -1956,7 +1955,7 @@ extern "C" pkv_status pkv_merge(void* out, const float* partial_o, const float* 
     if ((reinterpret_cast<uintptr_t>(out) & 7u) || (reinterpret_cast<uintptr_t>(partial_o) & 15u) ||
         (reinterpret_cast<uintptr_t>(partial_lse) & 3u))
         return PKV_ERR_INVALID_ARG;
-    if (head_dim % 4 != 0 || head_dim > 4 * kMergeThreads) return PKV_ERR_UNSUPPORTED;
+    if (head_dim % 4 != 0 || head_dim > kMergeMaxHeadDim) return PKV_ERR_UNSUPPORTED;
     if (num_seqs > 65535) return PKV_ERR_UNSUPPORTED;
     MergeParams mp = {};
     mp.out = out;
@@ -2048,7 +2047,8 @@ extern "C" pkv_status pkv_decode_attention_prefix_shared(
     const int cap = std::min(max_blocks_per_seq * block_size, max_context_len);
     cudaStream_t s = (cudaStream_t)stream;
 
-    // 1. every sequence's prefix record and the list of suffix partitions with tokens
+    // every sequence's prefix record and the list of suffix partitions with
+    // tokens: the plan, run by the prefix launch's extra CTA
     PlanParams pl = {};
     pl.context_lens = context_lens;
     pl.group_start = group_start;
@@ -2067,23 +2067,8 @@ extern "C" pkv_status pkv_decode_attention_prefix_shared(
     pl.prefix_chunk = pp.prefix_chunk;
     pl.chunk_tokens = pp.suffix.chunk_tokens;
     pl.cap = cap;
-    {
-        cudaLaunchConfig_t cfg = {};
-        cfg.gridDim = dim3(1);
-        cfg.blockDim = dim3(kPlanThreads);
-        cfg.stream = s;
-        cudaLaunchAttribute attr[1];
-        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-        attr[0].val.programmaticStreamSerializationAllowed = 1;
-        cfg.attrs = attr;
-        cfg.numAttrs = 1;
-        if (cudaLaunchKernelEx(&cfg, plan_kernel, pl) != cudaSuccess) {
-            cudaGetLastError();
-            return PKV_ERR_CUDA;
-        }
-    }
 
-    // 2. prefix partials of every group (tcgen05)
+    // 1. the plan and the prefix partials of every group (tcgen05)
     PrefixParams pr = {};
     pr.q = q;
     pr.block_tables = block_tables;
@@ -2108,8 +2093,9 @@ extern "C" pkv_status pkv_decode_attention_prefix_shared(
     pr.cap = cap;
     pr.hnd = hnd;
     pr.scale_log2 = scale * kLog2e;
-    const dim3 pgrid(pp.row_tiles, std::max(1, num_groups * num_kv_heads),
-                     std::max(1, pp.prefix_parts));
+    pr.with_plan = true;
+    pr.plan = pl;
+    const dim3 pgrid(pp.row_tiles, std::max(1, num_groups * num_kv_heads), pp.prefix_parts + 1);
     cudaError_t e;
     if (head_dim == 64)
         e = dtype == PKV_FP16 ? launch_prefix_t<__half, 64>(mk, mv, pr, pgrid, s)
@@ -2122,7 +2108,7 @@ extern "C" pkv_status pkv_decode_attention_prefix_shared(
         return PKV_ERR_CUDA;
     }
 
-    // 3. suffix partials (or the whole answer for sequences without a prefix)
+    // 2. suffix partials (or the whole answer for sequences without a prefix)
     DecodeParams p = {};
     p.out = out;
     p.q = q;
@@ -2154,7 +2140,7 @@ extern "C" pkv_status pkv_decode_attention_prefix_shared(
         return PKV_ERR_CUDA;
     }
 
-    // 4. merge
+    // 3. merge
     MergeParams mp = {};
     mp.out = out;
     mp.partial_o = partial_o;
