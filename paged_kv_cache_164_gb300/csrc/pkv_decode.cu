@@ -371,6 +371,7 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
     const int warp = tid >> 5;
     const int lane = tid & 31;
     const int bs = p.block_size;
+    const int bs_shift = __ffs(bs) - 1;  // block sizes are powers of two
 
     // Let the merge kernel (launched as a programmatic dependent) get scheduled
     // as soon as every CTA of this grid has started; it waits for our results.
@@ -496,10 +497,10 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
                                 p.err_flag))
                     break;
                 const int tok0 = t_begin + i * kStageTokens;
-                const int blk = table[tok0 / bs - page0];
+                const int blk = table[(tok0 >> bs_shift) - page0];
                 const uint32_t fb = ptx::smem_addr(&full_bar[slot]);
                 if (blk >= 0) {
-                    const int toff = tok0 % bs;
+                    const int toff = tok0 & (bs - 1);
                     const uint32_t kdst = ring_addr + slot * Cfg::kStageBytes;
                     ptx::mbar_arrive_expect_tx(fb, Cfg::kStageBytes);
 #pragma unroll
@@ -566,7 +567,7 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
             if (!wait_phase(ptx::smem_addr(&full_bar[slot]), (i / S) & 1, abort_flag, p.err_flag))
                 break;
             const int tok0 = t_begin + i * kStageTokens;
-            const int blk = table[tok0 / bs - page0];
+            const int blk = table[(tok0 >> bs_shift) - page0];
             const int nvalid = blk >= 0 ? min(kStageTokens, t_end - tok0) : 0;
             if (nvalid > 0) {
                 const uint32_t kbase = ring_addr + slot * Cfg::kStageBytes;
@@ -692,13 +693,17 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
 //   softmax          one thread per query row, reading its row of S directly
 //   O += P V         M=128, N=D, 16-token steps; P enters as hi + lo 16-bit
 //                    terms (as in the decode kernel); O stays in tensor memory
-// Warp 4 streams K/V tiles by TMA into a 4-stage ring, warp 5 owns the tensor
-// memory and one of its lanes issues the MMAs, warps 0-3 run the softmax and
-// write the rows' normalised O and log-sum-exp as their prefix partials.  S is
+// Warp 8 streams K/V tiles by TMA into a 4-stage ring, warp 9 owns the tensor
+// memory and one of its lanes issues the MMAs, warps 0-7 run the softmax: two
+// threads per query row, one for tokens 0-31 of every tile, one for tokens
+// 32-63.  The two halves are independent online softmaxes with accumulators
+// O_a and O_b of their own in tensor memory (O_a += P[:, 0:32] V[0:32], O_b +=
+// P[:, 32:64] V[32:64]); they meet once, at the end, where the rows' normalised
+// O and log-sum-exp are combined and written as partials.  S is
 // double-buffered, so S of the next tile is computed during this tile's
-// softmax.  A row's reference max is raised (and its O rescaled in tensor
-// memory) only when the running max exceeds it by more than 2^8; P stays
-// below 256 and the final normalisation uses the same reference, so the
+// softmax.  A half's reference max is raised (and its O rescaled in tensor
+// memory) only when its running max exceeds it by more than 2^8; P stays
+// below 256 and the final normalisation uses the same references, so the
 // result is the same softmax.
 
 // ---------------------------------------------------------------------------
@@ -764,7 +769,7 @@ struct PrefixParams {
 constexpr int kPrefixTileRows = 128;     // query rows per CTA (MMA M)
 constexpr int kPrefixTileTokens = 64;    // tokens per tile (N of S, K of O)
 constexpr int kPrefixStages = 4;
-constexpr int kPrefixSoftmaxWarps = 4;   // one thread per query row
+constexpr int kPrefixSoftmaxWarps = 8;   // two threads per query row (token halves)
 constexpr int kPrefixThreads = (kPrefixSoftmaxWarps + 2) * 32;
 constexpr int kPrefixTmaWarp = kPrefixSoftmaxWarps;
 constexpr int kPrefixMmaWarp = kPrefixSoftmaxWarps + 1;
@@ -779,13 +784,16 @@ struct PrefixTile {
     static constexpr int kHalfBytes = kRegions * kKVRegionBytes;       // K (or V) of one tile
     static constexpr int kStageBytes = 2 * kHalfBytes;
     static constexpr int kPBytes = kPrefixTileRows * kPrefixTileTokens * 2;  // P hi (or lo)
+    static constexpr int kXchBytes = 2 * kPrefixTileRows * 8;  // (m, l) per row and half
     // full[stages], empty[stages], s_full[2], p_ready, o_done, q_ready, drain
     static constexpr int kBarriers = 2 * kPrefixStages + 6;
     static constexpr int kSmemBytes = 1024 + kQBytes + kPrefixStages * kStageBytes + 2 * kPBytes +
-                                      kBarriers * 8 + (kMaxChunkPages + 1) * 4 + 64;
-    static constexpr uint32_t kTmemCols = 256;  // S0, S1 (64 columns each), O (D columns)
-    static constexpr uint32_t kColO = 2 * kPrefixTileTokens;
-    static_assert(kColO + D <= kTmemCols, "tensor memory layout");
+                                      kXchBytes + kBarriers * 8 + (kMaxChunkPages + 1) * 4 + 64;
+    // S0, S1 (64 columns each), O_a, O_b (D columns each)
+    static constexpr uint32_t kColOa = 2 * kPrefixTileTokens;
+    static constexpr uint32_t kColOb = kColOa + D;
+    static constexpr uint32_t kTmemCols = kColOb + D <= 256 ? 256 : 512;
+    static_assert(kColOb + D <= kTmemCols, "tensor memory layout");
 };
 
 // Instruction descriptor of tcgen05.mma kind::f16: fp32 accumulator, A and B
@@ -934,7 +942,8 @@ prefix_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
     uint8_t* sq = smem;                          // Q: [region][128 rows][128 B], swizzled
     uint8_t* ring = sq + Cfg::kQBytes;           // stages of K [region][64][128 B], then V
     uint8_t* sp = ring + NS * Cfg::kStageBytes;  // P hi, then P lo: [128 rows][128 B], swizzled
-    uint64_t* bars = reinterpret_cast<uint64_t*>(sp + 2 * Cfg::kPBytes);
+    float2* xch = reinterpret_cast<float2*>(sp + 2 * Cfg::kPBytes);  // [half][row] (m, l)
+    uint64_t* bars = reinterpret_cast<uint64_t*>(sp + 2 * Cfg::kPBytes + Cfg::kXchBytes);
     uint64_t* full_bar = bars;
     uint64_t* empty_bar = bars + NS;
     uint64_t* s_full = bars + 2 * NS;  // [2]
@@ -955,6 +964,7 @@ prefix_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
     const int warp = tid >> 5;
     const int lane = tid & 31;
     const int bs = p.block_size;
+    const int bs_shift = __ffs(bs) - 1;  // block sizes are powers of two
 
     ptx::launch_dependents();
     ptx::grid_dependency_wait();
@@ -994,8 +1004,10 @@ prefix_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
     const int page0 = t_begin / bs;
 
     // This thread's query row (softmax warps): its row of q and of the
-    // partials ([rows of q][H_q]), and its context limit.
-    const int r = row0 + tid;
+    // partials ([rows of q][H_q]), its context limit, and its token half.
+    const int srow = 32 * (warp % 4) + lane;  // row within the tile = tensor-memory lane
+    const int half = warp / 4;                // tokens 32*half .. 32*half+31 of every tile
+    const int r = row0 + srow;
     const bool row_ok = warp < kPrefixSoftmaxWarps && r < rows;
     const int head = g * p.group + (row_ok ? r % p.group : 0);
     int64_t qrow;
@@ -1084,7 +1096,7 @@ prefix_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
             const uint32_t kdst = ring_addr + slot * Cfg::kStageBytes;
             const uint32_t fb = ptx::smem_addr(&full_bar[slot]);
             const int tok0 = t_begin + j * TT + bx * kStageTokens;
-            const int blk = lane < kLoads && tok0 < t_end ? table[tok0 / bs - page0] : -1;
+            const int blk = lane < kLoads && tok0 < t_end ? table[(tok0 >> bs_shift) - page0] : -1;
             const uint32_t loads = __ballot_sync(0xffffffffu, blk >= 0);
             if (lane == 0) {
                 if (loads == 0)
@@ -1096,7 +1108,7 @@ prefix_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
             if (blk >= 0) {
                 const uint32_t off = (is_v ? Cfg::kHalfBytes : 0) + rr * Cfg::kKVRegionBytes +
                                      bx * kStageTokens * 128;
-                load_kv_box(kdst + off, is_v ? &tm_v : &tm_k, fb, rr * 64, g, tok0 % bs, blk,
+                load_kv_box(kdst + off, is_v ? &tm_v : &tm_k, fb, rr * 64, g, tok0 & (bs - 1), blk,
                             p.hnd, policy);
             }
             issued = j + 1;
@@ -1148,11 +1160,14 @@ prefix_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
                 const uint32_t vb = ring_addr + (j % NS) * Cfg::kStageBytes + Cfg::kHalfBytes;
 #pragma unroll
                 for (int kt = 0; kt < TT / 16; ++kt) {
+                    // tokens 0-31 accumulate into O_a, tokens 32-63 into O_b
+                    const uint32_t acc = tmem + (kt < TT / 32 ? Cfg::kColOa : Cfg::kColOb);
+                    const uint32_t keep = (j > 0 || kt % (TT / 32) > 0) ? 1u : 0u;
                     const uint64_t b = ptx::smem_desc_sw128(vb + kt * 16 * 128, Cfg::kKVRegionBytes, 1024);
                     const uint64_t a_hi = ptx::smem_desc_sw128(p_addr + kt * 32, 16, 1024);
                     const uint64_t a_lo = ptx::smem_desc_sw128(p_addr + Cfg::kPBytes + kt * 32, 16, 1024);
-                    ptx::tc_mma_f16(tmem + Cfg::kColO, a_hi, b, idesc_o, (j > 0 || kt > 0) ? 1u : 0u);
-                    ptx::tc_mma_f16(tmem + Cfg::kColO, a_lo, b, idesc_o, 1u);
+                    ptx::tc_mma_f16(acc, a_hi, b, idesc_o, keep);
+                    ptx::tc_mma_f16(acc, a_lo, b, idesc_o, 1u);
                 }
                 ptx::tc_commit(ptx::smem_addr(o_done));
                 ptx::tc_commit(ptx::smem_addr(&empty_bar[j % NS]));
@@ -1167,21 +1182,26 @@ prefix_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
         }
     } else {
         // ------------------------------------------------------------ softmax rows
-        // This row of Q into shared memory (16-byte chunk c of a 128-byte row
-        // lands at chunk c ^ (row % 8): the 128-byte swizzle of the MMA operand).
+        constexpr int HT = TT / 2;              // tokens per half of a tile
+        constexpr int HB = HT / kStageTokens;   // 16-token boxes per half
+        // This thread's half of its row of Q into shared memory (16-byte chunk
+        // c of a 128-byte row lands at chunk c ^ (row % 8): the 128-byte
+        // swizzle of the MMA operand).
         {
             const uint4* src = reinterpret_cast<const uint4*>(static_cast<const T*>(p.q) + qrow * D);
 #pragma unroll
-            for (int c = 0; c < D / 8; ++c) {
+            for (int k = 0; k < D / 16; ++k) {
+                const int c = half * (D / 16) + k;
                 const uint4 v = row_ok ? __ldg(src + c) : make_uint4(0u, 0u, 0u, 0u);
-                *reinterpret_cast<uint4*>(sq + (c / 8) * Cfg::kQRegionBytes + tid * 128 +
-                                          (((c % 8) ^ (tid & 7)) << 4)) = v;
+                *reinterpret_cast<uint4*>(sq + (c / 8) * Cfg::kQRegionBytes + srow * 128 +
+                                          (((c % 8) ^ (srow & 7)) << 4)) = v;
             }
             ptx::fence_proxy_async_smem();
             ptx::mbar_arrive(ptx::smem_addr(q_ready));
         }
-        const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
-        float m_ref = -INFINITY;  // reference max of this row's P (log2 domain)
+        const uint32_t lane_base = (uint32_t)(32 * (warp % 4)) << 16;
+        const uint32_t col_o = half ? Cfg::kColOb : Cfg::kColOa;  // this half's accumulator
+        float m_ref = -INFINITY;  // reference max of this half's P (log2 domain)
         float l = 0.f;
         bool ok = true;
         for (int j = 0; j < ntiles; ++j) {
@@ -1191,44 +1211,45 @@ prefix_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
                 break;
             }
             ptx::tc_fence_after_sync();
-            uint32_t sv[TT];
-            ptx::tmem_ld32(tmem + lane_base + (j % 2) * TT, *reinterpret_cast<uint32_t(*)[32]>(sv));
-            ptx::tmem_ld32(tmem + lane_base + (j % 2) * TT + 32,
-                           *reinterpret_cast<uint32_t(*)[32]>(sv + 32));
+            uint32_t sv[HT];
+            ptx::tmem_ld32(tmem + lane_base + (j % 2) * TT + half * HT,
+                           *reinterpret_cast<uint32_t(*)[32]>(sv));
             const int tile0 = t_begin + j * TT;
-            // Tokens of this row: present (a valid block, before t_end) and within its context.
+            const int h0 = tile0 + half * HT;  // first token of this half
+            // Tokens present (a valid block, before t_end), per 16-token box of the tile.
             int nvalid[TT / kStageTokens];
-            bool complete = tile0 + TT <= lim;
 #pragma unroll
             for (int bx = 0; bx < TT / kStageTokens; ++bx) {
                 const int tok0 = tile0 + bx * kStageTokens;
-                nvalid[bx] = (tok0 < t_end && table[tok0 / bs - page0] >= 0)
+                nvalid[bx] = (tok0 < t_end && table[(tok0 >> bs_shift) - page0] >= 0)
                                  ? min(kStageTokens, t_end - tok0)
                                  : 0;
-                complete &= nvalid[bx] == kStageTokens;
             }
-            float sc[TT];
+            bool complete = h0 + HT <= lim;
 #pragma unroll
-            for (int i = 0; i < TT; ++i) sc[i] = __uint_as_float(sv[i]) * p.scale_log2;
+            for (int bx = 0; bx < HB; ++bx) complete &= nvalid[half * HB + bx] == kStageTokens;
+            float sc[HT];
+#pragma unroll
+            for (int i = 0; i < HT; ++i) sc[i] = __uint_as_float(sv[i]) * p.scale_log2;
             if (!complete) {
 #pragma unroll
-                for (int i = 0; i < TT; ++i)
-                    if (!((i % kStageTokens) < nvalid[i / kStageTokens] && tile0 + i < lim))
+                for (int i = 0; i < HT; ++i)
+                    if (!((i % kStageTokens) < nvalid[half * HB + i / kStageTokens] && h0 + i < lim))
                         sc[i] = -INFINITY;
             }
-            // row max, as a tree
-            float red[TT / 2];
+            // max, as a tree
+            float red[HT / 2];
 #pragma unroll
-            for (int i = 0; i < TT / 2; ++i) red[i] = fmaxf(sc[i], sc[i + TT / 2]);
+            for (int i = 0; i < HT / 2; ++i) red[i] = fmaxf(sc[i], sc[i + HT / 2]);
 #pragma unroll
-            for (int w = TT / 4; w > 0; w >>= 1)
+            for (int w = HT / 4; w > 0; w >>= 1)
 #pragma unroll
                 for (int i = 0; i < w; ++i) red[i] = fmaxf(red[i], red[i + w]);
             const float mx = red[0];
             float alpha = 1.f;
             bool rescale = false;
             if (m_ref == -INFINITY) {
-                m_ref = mx;  // O and l are still zero for this row
+                m_ref = mx;  // O and l of this half are still zero for this row
             } else if (mx > m_ref + kRescaleLog2) {
                 alpha = ptx::ex2_approx(m_ref - mx);
                 m_ref = mx;
@@ -1236,12 +1257,12 @@ prefix_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
             }
             const float ref = m_ref == -INFINITY ? 0.f : m_ref;
 #pragma unroll
-            for (int i = 0; i < TT; ++i) sc[i] = ptx::ex2_approx(sc[i] - ref);
-            // row sum, as a tree
+            for (int i = 0; i < HT; ++i) sc[i] = ptx::ex2_approx(sc[i] - ref);
+            // sum, as a tree
 #pragma unroll
-            for (int i = 0; i < TT / 2; ++i) red[i] = sc[i] + sc[i + TT / 2];
+            for (int i = 0; i < HT / 2; ++i) red[i] = sc[i] + sc[i + HT / 2];
 #pragma unroll
-            for (int w = TT / 4; w > 0; w >>= 1)
+            for (int w = HT / 4; w > 0; w >>= 1)
 #pragma unroll
                 for (int i = 0; i < w; ++i) red[i] += red[i + w];
             l = l * alpha + red[0];
@@ -1256,24 +1277,22 @@ prefix_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
 #pragma unroll
                 for (int c = 0; c < D / 32; ++c) {
                     uint32_t ov[32];
-                    const uint32_t ta = tmem + lane_base + Cfg::kColO + c * 32;
+                    const uint32_t ta = tmem + lane_base + col_o + c * 32;
                     ptx::tmem_ld32(ta, ov);
 #pragma unroll
                     for (int i = 0; i < 32; ++i) ov[i] = __float_as_uint(__uint_as_float(ov[i]) * alpha);
                     ptx::tmem_st32(ta, ov);
                 }
             }
-            // P as hi + lo 16-bit terms, this row's 128 bytes of each (swizzled).
+            // P as hi + lo 16-bit terms: this half's 64 bytes of the row in each (swizzled).
 #pragma unroll
-            for (int c = 0; c < TT / 8; ++c) {
+            for (int k = 0; k < HT / 8; ++k) {
+                const int c = half * (HT / 8) + k;  // 16-byte chunk of the 128-byte row
                 uint32_t hi[4], lo[4];
 #pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const float p0 = sc[c * 8 + 2 * e];
-                    const float p1 = sc[c * 8 + 2 * e + 1];
-                    split_hi_lo(p0, p1, hi[e], lo[e], T());
-                }
-                const int off = tid * 128 + ((c ^ (tid & 7)) << 4);
+                for (int e = 0; e < 4; ++e) split_hi_lo(sc[k * 8 + 2 * e], sc[k * 8 + 2 * e + 1],
+                                                        hi[e], lo[e], T());
+                const int off = srow * 128 + ((c ^ (srow & 7)) << 4);
                 *reinterpret_cast<uint4*>(sp + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
                 *reinterpret_cast<uint4*>(sp + Cfg::kPBytes + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
             }
@@ -1298,34 +1317,50 @@ prefix_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
         }
         if (ok && ntiles > 0)
             ok = warp_wait_phase(ptx::smem_addr(o_done), (ntiles - 1) & 1, abort_flag, p.err_flag);
-        if (ok) {
-            // Epilogue: this row's normalised O and log-sum-exp as prefix partial `part`.
+        // The two halves of each row meet: every softmax thread passes this
+        // barrier exactly once, aborted or not.
+        xch[half * kPrefixTileRows + srow] = make_float2(m_ref, l);
+        ptx::named_barrier_sync(1, kPrefixSoftmaxWarps * 32);
+        if (ok && !*abort_flag) {
+            // Epilogue: O = (2^(m_a - M) O_a + 2^(m_b - M) O_b) / L with M the larger
+            // reference and L = 2^(m_a - M) l_a + 2^(m_b - M) l_b; this thread
+            // writes columns half*D/2 .. half*D/2 + D/2 - 1 of its row, as prefix
+            // partial `part`, and (half 0) the log-sum-exp.
             ptx::tc_fence_after_sync();
-            const float inv = l > 0.f ? 1.f / l : 0.f;
+            const float2 ha = xch[srow];
+            const float2 hb = xch[kPrefixTileRows + srow];
+            const float mm = fmaxf(ha.x, hb.x);
+            const float fa = ha.x == -INFINITY ? 0.f : ptx::ex2_approx(ha.x - mm);
+            const float fb = hb.x == -INFINITY ? 0.f : ptx::ex2_approx(hb.x - mm);
+            const float L = ha.y * fa + hb.y * fb;
+            const float inv = L > 0.f ? 1.f / L : 0.f;
             const int64_t prow = qrow * p.num_splits + part;
-            float* dst = p.partial_o + prow * D;
+            float* dst = p.partial_o + prow * D + half * (D / 2);
 #pragma unroll
-            for (int c = 0; c < D / 32; ++c) {
-                uint32_t ov[32];
+            for (int c = 0; c < D / 64; ++c) {
+                uint32_t oa[32], ob[32];
                 if (ntiles > 0) {
-                    ptx::tmem_ld32(tmem + lane_base + Cfg::kColO + c * 32, ov);
+                    const uint32_t cbase = tmem + lane_base + half * (D / 2) + c * 32;
+                    ptx::tmem_ld32(cbase + Cfg::kColOa, oa);
+                    ptx::tmem_ld32(cbase + Cfg::kColOb, ob);
                 } else {
 #pragma unroll
-                    for (int i = 0; i < 32; ++i) ov[i] = 0u;
+                    for (int i = 0; i < 32; ++i) oa[i] = ob[i] = 0u;
                 }
                 if (row_ok) {
 #pragma unroll
                     for (int i = 0; i < 32; i += 4) {
                         float4 v;
-                        v.x = l > 0.f ? __uint_as_float(ov[i]) * inv : 0.f;
-                        v.y = l > 0.f ? __uint_as_float(ov[i + 1]) * inv : 0.f;
-                        v.z = l > 0.f ? __uint_as_float(ov[i + 2]) * inv : 0.f;
-                        v.w = l > 0.f ? __uint_as_float(ov[i + 3]) * inv : 0.f;
+                        v.x = L > 0.f ? (__uint_as_float(oa[i]) * fa + __uint_as_float(ob[i]) * fb) * inv : 0.f;
+                        v.y = L > 0.f ? (__uint_as_float(oa[i + 1]) * fa + __uint_as_float(ob[i + 1]) * fb) * inv : 0.f;
+                        v.z = L > 0.f ? (__uint_as_float(oa[i + 2]) * fa + __uint_as_float(ob[i + 2]) * fb) * inv : 0.f;
+                        v.w = L > 0.f ? (__uint_as_float(oa[i + 3]) * fa + __uint_as_float(ob[i + 3]) * fb) * inv : 0.f;
                         *reinterpret_cast<float4*>(dst + c * 32 + i) = v;
                     }
                 }
             }
-            if (row_ok) p.partial_lse[prow] = l > 0.f ? (m_ref + log2f(l)) * kLn2 : -INFINITY;
+            if (row_ok && half == 0)
+                p.partial_lse[prow] = L > 0.f ? (mm + log2f(L)) * kLn2 : -INFINITY;
         }
     }
 
