@@ -486,11 +486,15 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
     const uint32_t ring_addr = ptx::smem_addr(ring);
 
     // ---------------------------------------------------------------- producer
+    // Lane j of the producer warp fills the slots of stages j, j + P, j + 2P, ...
+    // (P = kConsumerWarps, the stages consumer warp j takes), so one warp
+    // instruction waits for, and issues the copies of, P stages.
+    static_assert(S % kConsumerWarps == 0, "each producer lane keeps to its own ring slots");
     if (warp == kConsumerWarps) {
-        if (lane == 0) {
+        if (lane < kConsumerWarps) {
             const uint64_t policy = ptx::l2_policy_evict_first();
-            int issued = 0;
-            for (int i = 0; i < nstages; ++i) {
+            int issued = 0;  // one past this lane's last stage issued
+            for (int i = lane; i < nstages; i += kConsumerWarps) {
                 const int slot = i % S;
                 if (i >= S &&
                     !wait_phase(ptx::smem_addr(&empty_bar[slot]), ((i / S) - 1) & 1, abort_flag,
@@ -516,8 +520,9 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
                 issued = i + 1;
             }
             if (*abort_flag) {
-                // Wait (bounded) for this CTA's copies still in flight before leaving.
-                for (int i = max(0, issued - S); i < issued; ++i) {
+                // Wait (bounded) for this lane's copies still in flight before leaving.
+                for (int i = lane; i < issued; i += kConsumerWarps) {
+                    if (i < issued - S) continue;
                     const uint32_t fb = ptx::smem_addr(&full_bar[i % S]);
                     const uint64_t t0 = ptx::globaltimer();
                     while (!ptx::mbar_try_wait(fb, (i / S) & 1) &&
