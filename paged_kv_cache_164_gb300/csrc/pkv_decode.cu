@@ -32,6 +32,7 @@
 #include <climits>
 #include <cmath>
 #include <mutex>
+#include <type_traits>
 
 #include <cuda_fp8.h>
 #include <cudaTypedefs.h>
@@ -209,8 +210,14 @@ __device__ __forceinline__ void stage_update(uint32_t kbase, uint32_t vbase, int
         for (int c = 0; c < 4; ++c) s[nt][c] = 0.f;
     if constexpr (F8) {
         static_assert(D == 128, "an E4M3 stage row holds 128 dims");
-        // matrices: (tokens 0-7, block 2j), (8-15, 2j), (0-7, 2j+1), (8-15, 2j+1)
+        // matrices: (tokens 0-7, block 2j), (8-15, 2j), (0-7, 2j+1), (8-15, 2j+1).
+        // Odd 16-dim blocks accumulate apart (s2) to halve the dependent MMA chain.
         const int row = (mi & 1) * 8 + r8;
+        float s2[NT][4];
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+            for (int c = 0; c < 4; ++c) s2[nt][c] = 0.f;
 #pragma unroll
         for (int j = 0; j < D / 32; ++j) {
             const int chunk = 2 * j + (mi >> 1);
@@ -225,9 +232,14 @@ __device__ __forceinline__ void stage_update(uint32_t kbase, uint32_t vbase, int
                 a[3] = e4m3x2_to(r[2 * h + 1] >> 16, T());
 #pragma unroll
                 for (int nt = 0; nt < NT; ++nt)
-                    ptx::mma_16816<T>(s[nt], a, qb[nt][2 * j + h][0], qb[nt][2 * j + h][1]);
+                    ptx::mma_16816<T>(h ? s2[nt] : s[nt], a, qb[nt][2 * j + h][0],
+                                      qb[nt][2 * j + h][1]);
             }
         }
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+            for (int c = 0; c < 4; ++c) s[nt][c] += s2[nt][c];
     } else {
 #pragma unroll
         for (int ks = 0; ks < KSTEPS; ++ks) {
@@ -294,59 +306,82 @@ __device__ __forceinline__ void stage_update(uint32_t kbase, uint32_t vbase, int
         pb_lo[nt][1] = ptx::movmatrix_trans(l23);
     }
 
-    // O^T = alpha * O^T + V^T P^T
-    uint32_t vmask_lo = 0xffffffffu, vmask_hi = 0xffffffffu;
-    if (nvalid < kStageTokens) {
-        // A fragments of V^T hold tokens 2tq, 2tq+1 (a0, a1) and 2tq+8, 2tq+9 (a2, a3)
-        vmask_lo = (2 * tq < nvalid ? 0x0000ffffu : 0u) | (2 * tq + 1 < nvalid ? 0xffff0000u : 0u);
-        vmask_hi =
-            (2 * tq + 8 < nvalid ? 0x0000ffffu : 0u) | (2 * tq + 9 < nvalid ? 0xffff0000u : 0u);
+    // O^T = alpha * O^T + V^T P^T.  The rescale is skipped when no column's max
+    // moved (alpha = 1 everywhere, the common case once the max has settled).
+    bool moved = false;
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) moved |= (alpha0[nt] != 1.f) | (alpha1[nt] != 1.f);
+    if (__any_sync(0xffffffffu, moved)) {
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+            for (int mt = 0; mt < KSTEPS; ++mt) {
+                o[nt][mt][0] *= alpha0[nt];
+                o[nt][mt][1] *= alpha1[nt];
+                o[nt][mt][2] *= alpha0[nt];
+                o[nt][mt][3] *= alpha1[nt];
+            }
     }
-    auto accumulate = [&](int mt, uint32_t (&a)[4]) {
-        a[0] &= vmask_lo;
-        a[1] &= vmask_lo;
-        a[2] &= vmask_hi;
-        a[3] &= vmask_hi;
-#pragma unroll
-        for (int nt = 0; nt < NT; ++nt) {
-            o[nt][mt][0] *= alpha0[nt];
-            o[nt][mt][1] *= alpha1[nt];
-            o[nt][mt][2] *= alpha0[nt];
-            o[nt][mt][3] *= alpha1[nt];
-            ptx::mma_16816<T>(o[nt][mt], a, pb_hi[nt][0], pb_hi[nt][1]);
-            ptx::mma_16816<T>(o[nt][mt], a, pb_lo[nt][0], pb_lo[nt][1]);
+    // V rows of tokens at i >= nvalid are zeroed in the A fragments (only a
+    // ragged stage pays for the masks).
+    auto v_pass = [&](auto ragged_tag) {
+        constexpr bool RAGGED = decltype(ragged_tag)::value;
+        uint32_t vmask_lo = 0xffffffffu, vmask_hi = 0xffffffffu;
+        if constexpr (RAGGED) {
+            // A fragments of V^T hold tokens 2tq, 2tq+1 (a0, a1) and 2tq+8, 2tq+9 (a2, a3)
+            vmask_lo = (2 * tq < nvalid ? 0x0000ffffu : 0u) |
+                       (2 * tq + 1 < nvalid ? 0xffff0000u : 0u);
+            vmask_hi = (2 * tq + 8 < nvalid ? 0x0000ffffu : 0u) |
+                       (2 * tq + 9 < nvalid ? 0xffff0000u : 0u);
         }
-    };
-    if constexpr (F8) {
-        const int row = (mi & 1) * 8 + r8;
+        auto accumulate = [&](int mt, uint32_t (&a)[4]) {
+            if constexpr (RAGGED) {
+                a[0] &= vmask_lo;
+                a[1] &= vmask_lo;
+                a[2] &= vmask_hi;
+                a[3] &= vmask_hi;
+            }
 #pragma unroll
-        for (int j = 0; j < D / 32; ++j) {
-            const int chunk = 2 * j + (mi >> 1);
-            uint32_t r[4];
-            ptx::ldmatrix_x4_trans(r, vbase + row * 128 + ((chunk ^ r8) << 4));
+            for (int nt = 0; nt < NT; ++nt) {
+                ptx::mma_16816<T>(o[nt][mt], a, pb_hi[nt][0], pb_hi[nt][1]);
+                ptx::mma_16816<T>(o[nt][mt], a, pb_lo[nt][0], pb_lo[nt][1]);
+            }
+        };
+        if constexpr (F8) {
+            const int row = (mi & 1) * 8 + r8;
 #pragma unroll
-            for (int h = 0; h < 2; ++h) {
-                // r[2h]: tokens 2tq, 2tq+1; r[2h+1]: tokens 2tq+8, 2tq+9; bytes (dim 2gq,
-                // token a), (dim 2gq+1, token a), (dim 2gq, token b), (dim 2gq+1, token b)
+            for (int j = 0; j < D / 32; ++j) {
+                const int chunk = 2 * j + (mi >> 1);
+                uint32_t r[4];
+                ptx::ldmatrix_x4_trans(r, vbase + row * 128 + ((chunk ^ r8) << 4));
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    // r[2h]: tokens 2tq, 2tq+1; r[2h+1]: tokens 2tq+8, 2tq+9; bytes (dim 2gq,
+                    // token a), (dim 2gq+1, token a), (dim 2gq, token b), (dim 2gq+1, token b)
+                    uint32_t a[4];
+                    a[0] = e4m3x2_to(__byte_perm(r[2 * h], 0u, 0x0020), T());      // even dim
+                    a[1] = e4m3x2_to(__byte_perm(r[2 * h], 0u, 0x0031), T());      // odd dim
+                    a[2] = e4m3x2_to(__byte_perm(r[2 * h + 1], 0u, 0x0020), T());
+                    a[3] = e4m3x2_to(__byte_perm(r[2 * h + 1], 0u, 0x0031), T());
+                    accumulate(2 * j + h, a);
+                }
+            }
+        } else {
+#pragma unroll
+            for (int mt = 0; mt < KSTEPS; ++mt) {
+                const int chunk = mt * 2 + v_csel;
+                const uint32_t addr = vbase + (chunk >> 3) * kRegionBytes + v_tok * 128 +
+                                      (((chunk & 7) ^ r8) << 4);
                 uint32_t a[4];
-                a[0] = e4m3x2_to(__byte_perm(r[2 * h], 0u, 0x0020), T());      // even dim
-                a[1] = e4m3x2_to(__byte_perm(r[2 * h], 0u, 0x0031), T());      // odd dim
-                a[2] = e4m3x2_to(__byte_perm(r[2 * h + 1], 0u, 0x0020), T());
-                a[3] = e4m3x2_to(__byte_perm(r[2 * h + 1], 0u, 0x0031), T());
-                accumulate(2 * j + h, a);
+                ptx::ldmatrix_x4_trans(a, addr);
+                accumulate(mt, a);
             }
         }
-    } else {
-#pragma unroll
-        for (int mt = 0; mt < KSTEPS; ++mt) {
-            const int chunk = mt * 2 + v_csel;
-            const uint32_t addr =
-                vbase + (chunk >> 3) * kRegionBytes + v_tok * 128 + (((chunk & 7) ^ r8) << 4);
-            uint32_t a[4];
-            ptx::ldmatrix_x4_trans(a, addr);
-            accumulate(mt, a);
-        }
-    }
+    };
+    if (nvalid < kStageTokens)
+        v_pass(std::true_type{});
+    else
+        v_pass(std::false_type{});
 }
 
 // NT = number of 8-head groups (1: G <= 8, 2: G <= 16); F8: E4M3 cache codes.
