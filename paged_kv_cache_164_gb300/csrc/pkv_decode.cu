@@ -58,7 +58,10 @@ struct Tile {
     static constexpr int kRegionBytes = kStageTokens * 128;   // 16 rows of 128 bytes, swizzled
     static constexpr int kHalfBytes = kRegions * kRegionBytes;  // K (or V) of one stage
     static constexpr int kStageBytes = 2 * kHalfBytes;
-    static constexpr int kStages = 65536 / kStageBytes;       // ring depth: 64 KB
+    // Ring depth: 64 KB (three CTAs an SM); 48 KB for E4M3 stages, whose
+    // kernel (at one 8-column group) holds four CTAs an SM to hide the longer
+    // per-stage arithmetic behind more warps.
+    static constexpr int kStages = (F8 ? 49152 : 65536) / kStageBytes;
     static constexpr int kRingBytes = kStages * kStageBytes;
     static constexpr int kSmemBytes = 1024 /*align*/ + kRingBytes + 2 * kStages * 8 +
                                       (kMaxChunkPages + 1) * 4 + 16;
@@ -386,7 +389,7 @@ __device__ __forceinline__ void stage_update(uint32_t kbase, uint32_t vbase, int
 
 // NT = number of 8-head groups (1: G <= 8, 2: G <= 16); F8: E4M3 cache codes.
 template <typename T, int D, int NT, bool F8 = false>
-__global__ void __launch_bounds__(kThreads, 3)
+__global__ void __launch_bounds__(kThreads, (F8 && NT == 1) ? 4 : 3)
 decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
               const DecodeParams p) {
     using Cfg = Tile<D, F8>;
@@ -1590,6 +1593,8 @@ static pkv_status make_plan(int num_seqs, int num_q_heads, int num_kv_heads, int
         // whose CTAs (at the longest context) fill their last wave of resident
         // CTAs to 95%, else the best filled one: equal-length CTAs run in
         // lock-step waves, so a partly empty last wave leaves SMs idle.
+        // (Three resident CTAs an SM, the 16-bit kernel's; the E4M3 kernel's
+        // fourth is left out so that workspace sizes do not depend on the cache.)
         const int64_t units = (int64_t)std::max(1, num_seqs) * num_kv_heads;
         const double slots = 3.0 * sms;
         const int min_chunk = 256 / kStageTokens, max_chunk = std::min(1024 / kStageTokens, cap_stages);
