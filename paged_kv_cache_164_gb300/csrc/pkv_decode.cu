@@ -527,7 +527,10 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
     // Lane j of the producer warp fills the slots of stages j, j + P, j + 2P, ...
     // (P = kConsumerWarps, the stages consumer warp j takes), so one warp
     // instruction waits for, and issues the copies of, P stages.
-    static_assert(S % kConsumerWarps == 0, "each producer lane keeps to its own ring slots");
+    // S a multiple of the consumer warps: every slot then has one consumer warp
+    // (and one producer lane), so no warp can wait on a slot's next phase while
+    // its current one is still pending (a parity wait would pass at once).
+    static_assert(S % kConsumerWarps == 0, "each ring slot has one consumer warp");
     if (warp == kConsumerWarps) {
         if (lane < kConsumerWarps) {
             const uint64_t policy = ptx::l2_policy_evict_first();
@@ -630,6 +633,9 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
     // Reuses the ring (every copy has landed and been consumed).
     constexpr int HP = NT * 8;        // heads per warp state
     constexpr int OSTRIDE = D + 4;    // padded row of the per-warp O tile (conflict-free writes)
+    static_assert((kConsumerWarps * HP * OSTRIDE + 3 * kConsumerWarps * HP + HP) * 4 <=
+                      Cfg::kRingBytes,
+                  "the combine buffers fit in the ring they reuse");
     float* sm_o = reinterpret_cast<float*>(ring);                 // [warps][HP][OSTRIDE]
     float* sm_m = sm_o + kConsumerWarps * HP * OSTRIDE;           // [warps][HP]
     float* sm_l = sm_m + kConsumerWarps * HP;                     // [warps][HP]
