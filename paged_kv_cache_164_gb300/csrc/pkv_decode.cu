@@ -975,7 +975,15 @@ __device__ void plan_cta(const PlanParams& p, int* scratch) {
     if (tid == 0) *p.item_count = *base;
 }
 
-template <typename T, int D>
+// DUP (at most 64 query rows in the CTA): rows 64-127 of the tile repeat rows
+// 0-63, so every query row has four threads, one per 16-token quarter of each
+// tile, on all four SM sub-partitions (a warp reaches only its own quarter of
+// the tensor-memory lanes).  P rows 0-63 carry tokens 0-31 and zeros for
+// 32-63, rows 64-127 the reverse; O_a takes the 16-token steps 0 and 2 and O_b
+// steps 1 and 3, so each accumulator lane sums exactly one thread's quarter.
+// Lanes r and r + 64 then hold two independent partial softmaxes of the same
+// row, written as partial slots 2 * partition and 2 * partition + 1.
+template <typename T, int D, bool DUP = false>
 __global__ void __launch_bounds__(kPrefixThreads, 1)
 prefix_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
               const PrefixParams p) {
@@ -1056,7 +1064,8 @@ prefix_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
     // partials ([rows of q][H_q]), its context limit, and its token half.
     const int srow = 32 * (warp % 4) + lane;  // row within the tile = tensor-memory lane
     const int half = warp / 4;                // tokens 32*half .. 32*half+31 of every tile
-    const int r = row0 + srow;
+    const int dcopy = DUP ? (srow >> 6) : 0;  // DUP: which copy of the row this lane holds
+    const int r = row0 + (DUP ? (srow & 63) : srow);
     const bool row_ok = warp < kPrefixSoftmaxWarps && r < rows;
     const int head = g * p.group + (row_ok ? r % p.group : 0);
     int64_t qrow;
@@ -1209,9 +1218,12 @@ prefix_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
                 const uint32_t vb = ring_addr + (j % NS) * Cfg::kStageBytes + Cfg::kHalfBytes;
 #pragma unroll
                 for (int kt = 0; kt < TT / 16; ++kt) {
-                    // tokens 0-31 accumulate into O_a, tokens 32-63 into O_b
-                    const uint32_t acc = tmem + (kt < TT / 32 ? Cfg::kColOa : Cfg::kColOb);
-                    const uint32_t keep = (j > 0 || kt % (TT / 32) > 0) ? 1u : 0u;
+                    // tokens 0-31 accumulate into O_a, tokens 32-63 into O_b; with
+                    // DUP the even 16-token steps into O_a, the odd ones into O_b
+                    const bool to_a = DUP ? (kt % 2 == 0) : (kt < TT / 32);
+                    const uint32_t acc = tmem + (to_a ? Cfg::kColOa : Cfg::kColOb);
+                    const uint32_t keep =
+                        (j > 0 || (DUP ? kt >= 2 : kt % (TT / 32) > 0)) ? 1u : 0u;
                     const uint64_t b = ptx::smem_desc_sw128(vb + kt * 16 * 128, Cfg::kKVRegionBytes, 1024);
                     const uint64_t a_hi = ptx::smem_desc_sw128(p_addr + kt * 32, 16, 1024);
                     const uint64_t a_lo = ptx::smem_desc_sw128(p_addr + Cfg::kPBytes + kt * 32, 16, 1024);
@@ -1231,8 +1243,10 @@ prefix_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
         }
     } else {
         // ------------------------------------------------------------ softmax rows
-        constexpr int HT = TT / 2;              // tokens per half of a tile
-        constexpr int HB = HT / kStageTokens;   // 16-token boxes per half
+        constexpr int HT = DUP ? TT / 4 : TT / 2;  // tokens per thread and tile
+        constexpr int HB = HT / kStageTokens;      // 16-token boxes per thread
+        // this thread's tokens of every tile: unit `unit` of HT tokens
+        const int unit = DUP ? 2 * dcopy + half : half;
         // This thread's half of its row of Q into shared memory (16-byte chunk
         // c of a 128-byte row lands at chunk c ^ (row % 8): the 128-byte
         // swizzle of the MMA operand).
@@ -1244,6 +1258,17 @@ prefix_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
                 const uint4 v = row_ok ? __ldg(src + c) : make_uint4(0u, 0u, 0u, 0u);
                 *reinterpret_cast<uint4*>(sq + (c / 8) * Cfg::kQRegionBytes + srow * 128 +
                                           (((c % 8) ^ (srow & 7)) << 4)) = v;
+            }
+            if constexpr (DUP) {
+                // The other copy's quarter of this P row stays zero (hi and lo).
+                const int zu = 2 * (1 - dcopy) + half;
+#pragma unroll
+                for (int k = 0; k < HT / 8; ++k) {
+                    const int c = zu * (HT / 8) + k;
+                    const int off = srow * 128 + ((c ^ (srow & 7)) << 4);
+                    *reinterpret_cast<uint4*>(sp + off) = make_uint4(0u, 0u, 0u, 0u);
+                    *reinterpret_cast<uint4*>(sp + Cfg::kPBytes + off) = make_uint4(0u, 0u, 0u, 0u);
+                }
             }
             ptx::fence_proxy_async_smem();
             ptx::mbar_arrive(ptx::smem_addr(q_ready));
@@ -1261,10 +1286,12 @@ prefix_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
             }
             ptx::tc_fence_after_sync();
             uint32_t sv[HT];
-            ptx::tmem_ld32(tmem + lane_base + (j % 2) * TT + half * HT,
-                           *reinterpret_cast<uint32_t(*)[32]>(sv));
+            if constexpr (HT == 32)
+                ptx::tmem_ld32(tmem + lane_base + (j % 2) * TT + unit * HT, sv);
+            else
+                ptx::tmem_ld16(tmem + lane_base + (j % 2) * TT + unit * HT, sv);
             const int tile0 = t_begin + j * TT;
-            const int h0 = tile0 + half * HT;  // first token of this half
+            const int h0 = tile0 + unit * HT;  // first token of this thread's unit
             // Tokens present (a valid block, before t_end), per 16-token box of the tile.
             int nvalid[TT / kStageTokens];
 #pragma unroll
@@ -1276,14 +1303,14 @@ prefix_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
             }
             bool complete = h0 + HT <= lim;
 #pragma unroll
-            for (int bx = 0; bx < HB; ++bx) complete &= nvalid[half * HB + bx] == kStageTokens;
+            for (int bx = 0; bx < HB; ++bx) complete &= nvalid[unit * HB + bx] == kStageTokens;
             float sc[HT];
 #pragma unroll
             for (int i = 0; i < HT; ++i) sc[i] = __uint_as_float(sv[i]) * p.scale_log2;
             if (!complete) {
 #pragma unroll
                 for (int i = 0; i < HT; ++i)
-                    if (!((i % kStageTokens) < nvalid[half * HB + i / kStageTokens] && h0 + i < lim))
+                    if (!((i % kStageTokens) < nvalid[unit * HB + i / kStageTokens] && h0 + i < lim))
                         sc[i] = -INFINITY;
             }
             // max, as a tree
@@ -1333,10 +1360,10 @@ prefix_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
                     ptx::tmem_st32(ta, ov);
                 }
             }
-            // P as hi + lo 16-bit terms: this half's 64 bytes of the row in each (swizzled).
+            // P as hi + lo 16-bit terms: this unit's bytes of the row in each (swizzled).
 #pragma unroll
             for (int k = 0; k < HT / 8; ++k) {
-                const int c = half * (HT / 8) + k;  // 16-byte chunk of the 128-byte row
+                const int c = unit * (HT / 8) + k;  // 16-byte chunk of the 128-byte row
                 uint32_t hi[4], lo[4];
 #pragma unroll
                 for (int e = 0; e < 4; ++e) split_hi_lo(sc[k * 8 + 2 * e], sc[k * 8 + 2 * e + 1],
@@ -1383,7 +1410,7 @@ prefix_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
             const float fb = hb.x == -INFINITY ? 0.f : ptx::ex2_approx(hb.x - mm);
             const float L = ha.y * fa + hb.y * fb;
             const float inv = L > 0.f ? 1.f / L : 0.f;
-            const int64_t prow = qrow * p.num_splits + part;
+            const int64_t prow = qrow * p.num_splits + (DUP ? 2 * part + dcopy : part);
             float* dst = p.partial_o + prow * D + half * (D / 2);
 #pragma unroll
             for (int c = 0; c < D / 64; ++c) {
@@ -1447,6 +1474,7 @@ struct MergeParams {
     int chunk_tokens;
     int cap;                      // context clamp, as in the decode kernel
     int q_len;                    // > 0: multi-query rows (sequence, query token); every row merged
+    int mq_slots;                 // multi-query: partial slots per context partition (1 or 2)
     int64_t rows;                 // (row of q, query head) pairs
 };
 
@@ -1467,7 +1495,7 @@ merge_kernel(const MergeParams p) {
     if (p.q_len > 0) {
         // multi-query partials: the partitions of the sequence's context
         const int n = clamped_len(__ldg(p.context_lens + b / p.q_len), p.cap);
-        ns = (n + p.chunk_tokens - 1) / p.chunk_tokens;
+        ns = (n + p.chunk_tokens - 1) / p.chunk_tokens * p.mq_slots;
     } else if (p.context_lens != nullptr) {
         int start = 0, slot0 = 0;
         if (p.seq_info != nullptr) {
@@ -1742,10 +1770,10 @@ static cudaError_t launch_merge(const MergeParams& p, int groups, int seqs, cuda
     return cudaLaunchKernelEx(&cfg, merge_kernel<T>, q);
 }
 
-template <typename T, int D>
+template <typename T, int D, bool DUP = false>
 static cudaError_t launch_prefix_t(const CUtensorMap& mk, const CUtensorMap& mv,
                                    const PrefixParams& p, dim3 grid, cudaStream_t stream) {
-    auto kern = prefix_kernel<T, D>;
+    auto kern = prefix_kernel<T, D, DUP>;
     static std::once_flag once;
     static cudaError_t attr_err = cudaSuccess;
     std::call_once(once, [&] {
@@ -1819,6 +1847,8 @@ struct MultiQueryPlan {
     int chunk;
     int parts;
     int row_tiles;
+    bool dup;      // at most 64 query rows per (sequence, KV head): two partials per partition
+    int slots;     // partial slots per row: parts, or 2 * parts with dup
     size_t workspace_bytes;
 };
 
@@ -1846,8 +1876,11 @@ static pkv_status make_mq_plan(int num_seqs, int q_len, int num_q_heads, int num
     mp->chunk = chunk_tiles * kPrefixTileTokens;
     mp->parts = std::max(1, (max_context_len + mp->chunk - 1) / mp->chunk);
     if (mp->parts > PKV_MAX_SPLITS || mp->parts > 65535) return PKV_ERR_UNSUPPORTED;
+    mp->dup = rows <= kPrefixTileRows / 2;
+    mp->slots = mp->parts * (mp->dup ? 2 : 1);
+    if (mp->slots > 65535) return PKV_ERR_UNSUPPORTED;
     mp->workspace_bytes =
-        (size_t)num_seqs * q_len * num_q_heads * mp->parts * (head_dim + 1) * sizeof(float) + 256;
+        (size_t)num_seqs * q_len * num_q_heads * mp->slots * (head_dim + 1) * sizeof(float) + 256;
     return PKV_OK;
 }
 
@@ -2291,7 +2324,7 @@ extern "C" pkv_status pkv_multi_query_attention(
         !make_cache_map(&mv, v_cache, dtype, num_blocks, block_size, num_kv_heads, head_dim, hnd))
         return PKV_ERR_CUDA;
     float* partial_o = static_cast<float*>(workspace);
-    float* partial_lse = partial_o + (size_t)num_seqs * q_len * num_q_heads * mq.parts * head_dim;
+    float* partial_lse = partial_o + (size_t)num_seqs * q_len * num_q_heads * mq.slots * head_dim;
     const int cap = std::min(max_blocks_per_seq * block_size, max_context_len);
     const int group = num_q_heads / num_kv_heads;
     cudaStream_t s = (cudaStream_t)stream;
@@ -2311,7 +2344,7 @@ extern "C" pkv_status pkv_multi_query_attention(
     pr.num_q_heads = num_q_heads;
     pr.num_kv_heads = num_kv_heads;
     pr.group = group;
-    pr.num_splits = mq.parts;
+    pr.num_splits = mq.slots;
     pr.prefix_chunk = mq.chunk;
     pr.cap = cap;
     pr.q_len = q_len;
@@ -2319,12 +2352,20 @@ extern "C" pkv_status pkv_multi_query_attention(
     pr.scale_log2 = scale * kLog2e;
     const dim3 pgrid(mq.row_tiles, num_seqs * num_kv_heads, mq.parts);
     cudaError_t e;
-    if (head_dim == 64)
+    if (mq.dup) {
+        if (head_dim == 64)
+            e = dtype == PKV_FP16 ? launch_prefix_t<__half, 64, true>(mk, mv, pr, pgrid, s)
+                                  : launch_prefix_t<__nv_bfloat16, 64, true>(mk, mv, pr, pgrid, s);
+        else
+            e = dtype == PKV_FP16 ? launch_prefix_t<__half, 128, true>(mk, mv, pr, pgrid, s)
+                                  : launch_prefix_t<__nv_bfloat16, 128, true>(mk, mv, pr, pgrid, s);
+    } else if (head_dim == 64) {
         e = dtype == PKV_FP16 ? launch_prefix_t<__half, 64>(mk, mv, pr, pgrid, s)
                               : launch_prefix_t<__nv_bfloat16, 64>(mk, mv, pr, pgrid, s);
-    else
+    } else {
         e = dtype == PKV_FP16 ? launch_prefix_t<__half, 128>(mk, mv, pr, pgrid, s)
                               : launch_prefix_t<__nv_bfloat16, 128>(mk, mv, pr, pgrid, s);
+    }
     if (e != cudaSuccess) {
         cudaGetLastError();
         return PKV_ERR_CUDA;
@@ -2339,11 +2380,12 @@ extern "C" pkv_status pkv_multi_query_attention(
     mp.num_q_heads = num_q_heads;
     mp.num_kv_heads = num_kv_heads;
     mp.group = group;
-    mp.num_splits = mq.parts;
+    mp.num_splits = mq.slots;
     mp.head_dim = head_dim;
     mp.chunk_tokens = mq.chunk;
     mp.cap = cap;
     mp.q_len = q_len;
+    mp.mq_slots = mq.dup ? 2 : 1;
     e = dtype == PKV_FP16 ? launch_merge<__half>(mp, num_q_heads, num_seqs * q_len, s)
                           : launch_merge<__nv_bfloat16>(mp, num_q_heads, num_seqs * q_len, s);
     if (e != cudaSuccess) {

@@ -30,6 +30,12 @@ CASES = {
     "bs32_d64_q3": dict(name="c5_bs32", q_len=3, num_seqs=5, head_dim=64,
                         lengths=("uniform", 20, 400), max_len_cap=416, shared_prefix_groups=0,
                         seed=65),
+    # 64 rows per (sequence, KV head) run the four-threads-per-row layout, 72
+    # rows the two-threads-per-row one: both sides of the switch
+    "gqa8_q8_rows64_long": dict(name="c3", q_len=8, num_seqs=3, lengths=("uniform", 1500, 2600),
+                                max_len_cap=2688, seed=66),
+    "gqa8_q9_rows72": dict(name="c3", q_len=9, num_seqs=3, lengths=("uniform", 60, 900),
+                           max_len_cap=960, seed=67),
 }
 
 
