@@ -832,13 +832,13 @@ struct PrefixTile {
     static constexpr int kKVRegionBytes = kPrefixTileTokens * 128;     // 64 tokens x 64 dims
     static constexpr int kHalfBytes = kRegions * kKVRegionBytes;       // K (or V) of one tile
     static constexpr int kStageBytes = 2 * kHalfBytes;
-    static constexpr int kPBytes = kPrefixTileRows * kPrefixTileTokens * 2;  // P hi (or lo)
     static constexpr int kXchBytes = 2 * kPrefixTileRows * 8;  // (m, l) per row and half
-    // full[stages], empty[stages], s_full[2], p_ready, o_done, q_ready, drain
-    static constexpr int kBarriers = 2 * kPrefixStages + 6;
-    static constexpr int kSmemBytes = 1024 + kQBytes + kPrefixStages * kStageBytes + 2 * kPBytes +
-                                      kXchBytes + kBarriers * 8 + (kMaxChunkPages + 1) * 4 + 64;
-    // S0, S1 (64 columns each), O_a, O_b (D columns each)
+    // full[stages], empty[stages], s_full[2], p_ready, o_done[2], q_ready, drain
+    static constexpr int kBarriers = 2 * kPrefixStages + 7;
+    static constexpr int kSmemBytes = 1024 + kQBytes + kPrefixStages * kStageBytes + kXchBytes +
+                                      kBarriers * 8 + (kMaxChunkPages + 1) * 4 + 64;
+    // S0, S1 (64 columns each; P of the tile overwrites its S as hi/lo 16-bit
+    // pairs), O_a, O_b (D columns each)
     static constexpr uint32_t kColOa = 2 * kPrefixTileTokens;
     static constexpr uint32_t kColOb = kColOa + D;
     static constexpr uint32_t kTmemCols = kColOb + D <= 256 ? 256 : 512;
@@ -998,15 +998,14 @@ prefix_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
                                                ~uintptr_t(1023));
     uint8_t* sq = smem;                          // Q: [region][128 rows][128 B], swizzled
     uint8_t* ring = sq + Cfg::kQBytes;           // stages of K [region][64][128 B], then V
-    uint8_t* sp = ring + NS * Cfg::kStageBytes;  // P hi, then P lo: [128 rows][128 B], swizzled
-    float2* xch = reinterpret_cast<float2*>(sp + 2 * Cfg::kPBytes);  // [half][row] (m, l)
-    uint64_t* bars = reinterpret_cast<uint64_t*>(sp + 2 * Cfg::kPBytes + Cfg::kXchBytes);
+    float2* xch = reinterpret_cast<float2*>(ring + NS * Cfg::kStageBytes);  // [half][row] (m, l)
+    uint64_t* bars = reinterpret_cast<uint64_t*>(ring + NS * Cfg::kStageBytes + Cfg::kXchBytes);
     uint64_t* full_bar = bars;
     uint64_t* empty_bar = bars + NS;
     uint64_t* s_full = bars + 2 * NS;  // [2]
     uint64_t* p_ready = s_full + 2;
-    uint64_t* o_done = p_ready + 1;
-    uint64_t* q_ready = o_done + 1;
+    uint64_t* o_done = p_ready + 1;  // [2]: O += P V of even / odd tiles done
+    uint64_t* q_ready = o_done + 2;
     uint64_t* drain = q_ready + 1;
     int* table = reinterpret_cast<int*>(bars + Cfg::kBarriers);
     volatile int* abort_flag = table + kMaxChunkPages + 1;
@@ -1088,7 +1087,8 @@ prefix_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
         ptx::mbar_init(ptx::smem_addr(&s_full[0]), 1);
         ptx::mbar_init(ptx::smem_addr(&s_full[1]), 1);
         ptx::mbar_init(ptx::smem_addr(p_ready), kPrefixSoftmaxWarps * 32);
-        ptx::mbar_init(ptx::smem_addr(o_done), 1);
+        ptx::mbar_init(ptx::smem_addr(&o_done[0]), 1);
+        ptx::mbar_init(ptx::smem_addr(&o_done[1]), 1);
         ptx::mbar_init(ptx::smem_addr(q_ready), kPrefixSoftmaxWarps * 32);
         ptx::mbar_init(ptx::smem_addr(drain), 1);
         *abort_flag = 0;
@@ -1131,7 +1131,6 @@ prefix_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
     const int ntiles = (t_end - t_begin + TT - 1) / TT;
     const uint32_t ring_addr = ptx::smem_addr(ring);
     const uint32_t q_addr = ptx::smem_addr(sq);
-    const uint32_t p_addr = ptx::smem_addr(sp);
 
     if (warp == kPrefixTmaWarp) {
         // ------------------------------------------------------------ producer
@@ -1216,6 +1215,7 @@ prefix_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
                 }
                 ptx::tc_fence_after_sync();
                 const uint32_t vb = ring_addr + (j % NS) * Cfg::kStageBytes + Cfg::kHalfBytes;
+                constexpr int HTK = DUP ? TT / 4 : TT / 2;  // tokens per softmax thread
 #pragma unroll
                 for (int kt = 0; kt < TT / 16; ++kt) {
                     // tokens 0-31 accumulate into O_a, tokens 32-63 into O_b; with
@@ -1225,12 +1225,13 @@ prefix_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
                     const uint32_t keep =
                         (j > 0 || (DUP ? kt >= 2 : kt % (TT / 32) > 0)) ? 1u : 0u;
                     const uint64_t b = ptx::smem_desc_sw128(vb + kt * 16 * 128, Cfg::kKVRegionBytes, 1024);
-                    const uint64_t a_hi = ptx::smem_desc_sw128(p_addr + kt * 32, 16, 1024);
-                    const uint64_t a_lo = ptx::smem_desc_sw128(p_addr + Cfg::kPBytes + kt * 32, 16, 1024);
-                    ptx::tc_mma_f16(acc, a_hi, b, idesc_o, keep);
-                    ptx::tc_mma_f16(acc, a_lo, b, idesc_o, 1u);
+                    // tokens 16kt.. of P: unit u's hi pairs at u*HTK, lo pairs HTK/2 on
+                    const int u = kt * 16 / HTK;
+                    const uint32_t a_hi = tmem + (j % 2) * TT + u * HTK + (kt * 16 % HTK) / 2;
+                    ptx::tc_mma_f16_ts(acc, a_hi, b, idesc_o, keep);
+                    ptx::tc_mma_f16_ts(acc, a_hi + HTK / 2, b, idesc_o, 1u);
                 }
-                ptx::tc_commit(ptx::smem_addr(o_done));
+                ptx::tc_commit(ptx::smem_addr(&o_done[j % 2]));
                 ptx::tc_commit(ptx::smem_addr(&empty_bar[j % NS]));
                 if (j + 2 < ntiles) ok = issue_s(j + 2);
             }
@@ -1258,17 +1259,6 @@ prefix_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
                 const uint4 v = row_ok ? __ldg(src + c) : make_uint4(0u, 0u, 0u, 0u);
                 *reinterpret_cast<uint4*>(sq + (c / 8) * Cfg::kQRegionBytes + srow * 128 +
                                           (((c % 8) ^ (srow & 7)) << 4)) = v;
-            }
-            if constexpr (DUP) {
-                // The other copy's quarter of this P row stays zero (hi and lo).
-                const int zu = 2 * (1 - dcopy) + half;
-#pragma unroll
-                for (int k = 0; k < HT / 8; ++k) {
-                    const int c = zu * (HT / 8) + k;
-                    const int off = srow * 128 + ((c ^ (srow & 7)) << 4);
-                    *reinterpret_cast<uint4*>(sp + off) = make_uint4(0u, 0u, 0u, 0u);
-                    *reinterpret_cast<uint4*>(sp + Cfg::kPBytes + off) = make_uint4(0u, 0u, 0u, 0u);
-                }
             }
             ptx::fence_proxy_async_smem();
             ptx::mbar_arrive(ptx::smem_addr(q_ready));
@@ -1342,14 +1332,16 @@ prefix_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
 #pragma unroll
                 for (int i = 0; i < w; ++i) red[i] += red[i + w];
             l = l * alpha + red[0];
-            // P and O are free once the previous tile's O += P V has completed.
-            if (j > 0 && !warp_wait_phase(ptx::smem_addr(o_done), (j - 1) & 1, abort_flag,
-                                          p.err_flag)) {
-                ok = false;
-                break;
-            }
-            ptx::tc_fence_after_sync();
+            // O is rescaled only once the previous tile's O += P V has completed
+            // (o_done alternates between two barriers, so the parity wait can
+            // never meet a phase two behind: S(j) completing implies P V(j-2) has).
             if (__any_sync(0xffffffffu, rescale)) {
+                if (j > 0 && !warp_wait_phase(ptx::smem_addr(&o_done[(j - 1) % 2]),
+                                              ((j - 1) / 2) & 1, abort_flag, p.err_flag)) {
+                    ok = false;
+                    break;
+                }
+                ptx::tc_fence_after_sync();
 #pragma unroll
                 for (int c = 0; c < D / 32; ++c) {
                     uint32_t ov[32];
@@ -1360,17 +1352,27 @@ prefix_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
                     ptx::tmem_st32(ta, ov);
                 }
             }
-            // P as hi + lo 16-bit terms: this unit's bytes of the row in each (swizzled).
+            // P as hi + lo 16-bit terms over this thread's own S columns of the
+            // tile's buffer (already read): the HT/2 columns of hi pairs, then
+            // the HT/2 of lo pairs; the MMA takes them as its A operand.
+            {
+                uint32_t pv[HT];
 #pragma unroll
-            for (int k = 0; k < HT / 8; ++k) {
-                const int c = unit * (HT / 8) + k;  // 16-byte chunk of the 128-byte row
-                uint32_t hi[4], lo[4];
+                for (int e = 0; e < HT / 2; ++e)
+                    split_hi_lo(sc[2 * e], sc[2 * e + 1], pv[e], pv[HT / 2 + e], T());
+                const uint32_t pcol = tmem + lane_base + (j % 2) * TT + unit * HT;
+                if constexpr (HT == 32)
+                    ptx::tmem_st32(pcol, pv);
+                else
+                    ptx::tmem_st16(pcol, pv);
+                if constexpr (DUP) {
+                    // The other copy's unit of this lane (S values no thread reads)
+                    // must be zero for the steps that bring it into this lane's O.
+                    uint32_t z[16];
 #pragma unroll
-                for (int e = 0; e < 4; ++e) split_hi_lo(sc[k * 8 + 2 * e], sc[k * 8 + 2 * e + 1],
-                                                        hi[e], lo[e], T());
-                const int off = srow * 128 + ((c ^ (srow & 7)) << 4);
-                *reinterpret_cast<uint4*>(sp + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
-                *reinterpret_cast<uint4*>(sp + Cfg::kPBytes + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+                    for (int e = 0; e < 16; ++e) z[e] = 0u;
+                    ptx::tmem_st16(tmem + lane_base + (j % 2) * TT + (2 * (1 - dcopy) + half) * HT, z);
+                }
             }
             // V rows of tokens that were not loaded hold stale or uninitialised
             // bytes: zero them so 0 * V stays 0.
@@ -1392,7 +1394,8 @@ prefix_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
             ptx::mbar_arrive(ptx::smem_addr(p_ready));
         }
         if (ok && ntiles > 0)
-            ok = warp_wait_phase(ptx::smem_addr(o_done), (ntiles - 1) & 1, abort_flag, p.err_flag);
+            ok = warp_wait_phase(ptx::smem_addr(&o_done[(ntiles - 1) % 2]), ((ntiles - 1) / 2) & 1,
+                                 abort_flag, p.err_flag);
         // The two halves of each row meet: every softmax thread passes this
         // barrier exactly once, aborted or not.
         xch[half * kPrefixTileRows + srow] = make_float2(m_ref, l);
