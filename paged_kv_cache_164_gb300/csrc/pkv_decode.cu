@@ -833,8 +833,8 @@ struct PrefixTile {
     static constexpr int kHalfBytes = kRegions * kKVRegionBytes;       // K (or V) of one tile
     static constexpr int kStageBytes = 2 * kHalfBytes;
     static constexpr int kXchBytes = 2 * kPrefixTileRows * 8;  // (m, l) per row and half
-    // full[stages], empty[stages], s_full[2], p_ready, o_done[2], q_ready, drain
-    static constexpr int kBarriers = 2 * kPrefixStages + 7;
+    // full[stages], empty[stages], s_full[2], p_ready[2], o_done[2], q_ready, drain
+    static constexpr int kBarriers = 2 * kPrefixStages + 8;
     static constexpr int kSmemBytes = 1024 + kQBytes + kPrefixStages * kStageBytes + kXchBytes +
                                       kBarriers * 8 + (kMaxChunkPages + 1) * 4 + 64;
     // S0, S1 (64 columns each; P of the tile overwrites its S as hi/lo 16-bit
@@ -1002,9 +1002,13 @@ prefix_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
     uint64_t* bars = reinterpret_cast<uint64_t*>(ring + NS * Cfg::kStageBytes + Cfg::kXchBytes);
     uint64_t* full_bar = bars;
     uint64_t* empty_bar = bars + NS;
+    // Tile j uses S/P buffer j % 2 with its own s_full and p_ready barriers: a
+    // softmax thread passes S(j+1) only after P V(j-1) was issued, i.e. after
+    // p_ready of buffer (j+1) % 2 completed for tile j-1, so its arrival for
+    // tile j+1 never lands in an earlier tile's phase.
     uint64_t* s_full = bars + 2 * NS;  // [2]
-    uint64_t* p_ready = s_full + 2;
-    uint64_t* o_done = p_ready + 1;  // [2]: O += P V of even / odd tiles done
+    uint64_t* p_ready = s_full + 2;    // [2]
+    uint64_t* o_done = p_ready + 2;  // [2]: O += P V of even / odd tiles done
     uint64_t* q_ready = o_done + 2;
     uint64_t* drain = q_ready + 1;
     int* table = reinterpret_cast<int*>(bars + Cfg::kBarriers);
@@ -1086,7 +1090,8 @@ prefix_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
         }
         ptx::mbar_init(ptx::smem_addr(&s_full[0]), 1);
         ptx::mbar_init(ptx::smem_addr(&s_full[1]), 1);
-        ptx::mbar_init(ptx::smem_addr(p_ready), kPrefixSoftmaxWarps * 32);
+        ptx::mbar_init(ptx::smem_addr(&p_ready[0]), kPrefixSoftmaxWarps * 32);
+        ptx::mbar_init(ptx::smem_addr(&p_ready[1]), kPrefixSoftmaxWarps * 32);
         ptx::mbar_init(ptx::smem_addr(&o_done[0]), 1);
         ptx::mbar_init(ptx::smem_addr(&o_done[1]), 1);
         ptx::mbar_init(ptx::smem_addr(q_ready), kPrefixSoftmaxWarps * 32);
@@ -1094,7 +1099,15 @@ prefix_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
         *abort_flag = 0;
         ptx::fence_barrier_init();
     }
+    // The softmax threads' halves of their query rows, loaded before the barrier
+    // below so the load overlaps the block-table read (stored to shared memory
+    // after it).
+    uint4 qv[D / 16];
     if (warp < kPrefixSoftmaxWarps) {
+        const uint4* src = reinterpret_cast<const uint4*>(static_cast<const T*>(p.q) + qrow * D);
+#pragma unroll
+        for (int k = 0; k < D / 16; ++k)
+            qv[k] = row_ok ? __ldg(src + half * (D / 16) + k) : make_uint4(0u, 0u, 0u, 0u);
         int m = lim;
 #pragma unroll
         for (int off = 16; off > 0; off >>= 1) m = max(m, __shfl_xor_sync(0xffffffffu, m, off));
@@ -1209,7 +1222,8 @@ prefix_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
             for (int j = 0; j < 2 && j < ntiles && ok; ++j) ok = issue_s(j);
             for (int j = 0; j < ntiles && ok; ++j) {
                 // O += P(j) V(j) once the softmax has written P(j)
-                if (!wait_phase(ptx::smem_addr(p_ready), j & 1, abort_flag, p.err_flag)) {
+                if (!wait_phase(ptx::smem_addr(&p_ready[j % 2]), (j / 2) & 1, abort_flag,
+                                p.err_flag)) {
                     ok = false;
                     break;
                 }
@@ -1252,13 +1266,11 @@ prefix_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
         // c of a 128-byte row lands at chunk c ^ (row % 8): the 128-byte
         // swizzle of the MMA operand).
         {
-            const uint4* src = reinterpret_cast<const uint4*>(static_cast<const T*>(p.q) + qrow * D);
 #pragma unroll
             for (int k = 0; k < D / 16; ++k) {
                 const int c = half * (D / 16) + k;
-                const uint4 v = row_ok ? __ldg(src + c) : make_uint4(0u, 0u, 0u, 0u);
                 *reinterpret_cast<uint4*>(sq + (c / 8) * Cfg::kQRegionBytes + srow * 128 +
-                                          (((c % 8) ^ (srow & 7)) << 4)) = v;
+                                          (((c % 8) ^ (srow & 7)) << 4)) = qv[k];
             }
             ptx::fence_proxy_async_smem();
             ptx::mbar_arrive(ptx::smem_addr(q_ready));
@@ -1391,7 +1403,7 @@ prefix_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
             }
             ptx::fence_proxy_async_smem();
             ptx::tc_fence_before_sync();
-            ptx::mbar_arrive(ptx::smem_addr(p_ready));
+            ptx::mbar_arrive(ptx::smem_addr(&p_ready[j % 2]));
         }
         if (ok && ntiles > 0)
             ok = warp_wait_phase(ptx::smem_addr(&o_done[(ntiles - 1) % 2]), ((ntiles - 1) / 2) & 1,
