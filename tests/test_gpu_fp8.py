@@ -121,3 +121,29 @@ def test_fp8_full_size_llama70b_layer_sampled():
                                          1.0 / np.sqrt(s.head_dim), k_scale, v_scale, "bf16")
     assert_attention_close(out[torch.as_tensor(seqs, device="cuda")], expect, "c3 fp8")
     assert torch.isfinite(out).all()
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "fp16"])
+def test_fp8_decode_subnormal_codes(dtype):
+    # K and V hold only E4M3 subnormal codes (exponent field 0) and zeros, with
+    # scales that make their values O(1): every product goes through the
+    # conversion of subnormal codes, so one that lost them would be far off.
+    w = make_workload("c3", device="cuda", with_values=False, num_seqs=3,
+                      lengths=("uniform", 100, 420), max_len_cap=448, seed=98, dtype=dtype)
+    s = w.spec
+    kc = make_fp8_codes((w.num_blocks, s.block_size, s.num_kv_heads, s.head_dim), seed=99,
+                        device="cuda", exponents=(0, 1))
+    vc = make_fp8_codes(kc.shape, seed=100, device="cuda", exponents=(0, 1))
+    g = torch.Generator(device="cuda").manual_seed(101)
+    tdt = torch.bfloat16 if dtype == "bf16" else torch.float16
+    q = torch.randn((s.num_seqs, s.num_q_heads, s.head_dim), generator=g, device="cuda",
+                    dtype=torch.float32).to(tdt)
+    k_scale, v_scale = 64.0, 48.0     # code values m * 2^-9 become m / 8 and 3m / 32
+    flag = pkv.new_error_flag("cuda")
+    out = pkv.decode_attention_fp8(q, kc, vc, w.block_tables, w.context_lens, w.max_context_len,
+                                   k_scale, v_scale, err_flag=flag)
+    assert pkv.check_error(flag) == 0
+    expect = oracle.decode_attention_fp8(bits(q), kc.cpu().numpy(), vc.cpu().numpy(),
+                                         w.block_tables.cpu().numpy(), w.context_lens.cpu().numpy(),
+                                         1.0 / np.sqrt(s.head_dim), k_scale, v_scale, dtype)
+    assert_attention_close(out, expect, f"subnormal codes {dtype}")

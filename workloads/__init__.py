@@ -274,12 +274,14 @@ def to_head_major(cache: torch.Tensor) -> torch.Tensor:
     return cache.permute(0, 2, 1, 3).contiguous()
 
 
-def make_fp8_codes(shape, seed: int, device="cpu") -> torch.Tensor:
-    """Seeded E4M3 bit patterns (uint8) of normal values with |value| in
-    [2^-6, 2^3): random sign, exponent field 1..9, any fraction; never NaN."""
+def make_fp8_codes(shape, seed: int, device="cpu", exponents=(1, 10)) -> torch.Tensor:
+    """Seeded E4M3 bit patterns (uint8): random sign, exponent field drawn from
+    range(*exponents), any fraction; never NaN.  The default gives normal values
+    with |value| in [2^-6, 2^3); exponents=(0, 1) gives only subnormal codes
+    (and zeros), |value| = fraction * 2^-9."""
     g = torch.Generator().manual_seed(seed * 7919 + 31)
     sign = torch.randint(0, 2, shape, generator=g, dtype=torch.int32) << 7
-    expo = torch.randint(1, 10, shape, generator=g, dtype=torch.int32) << 3
+    expo = torch.randint(exponents[0], exponents[1], shape, generator=g, dtype=torch.int32) << 3
     frac = torch.randint(0, 8, shape, generator=g, dtype=torch.int32)
     return (sign | expo | frac).to(torch.uint8).to(device)
 
