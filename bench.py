@@ -55,14 +55,14 @@ WORKLOAD_TEXT = {
 # measured on (digest of csrc/), else reported as null.
 NCU_TRAFFIC = {
     # ncu --metrics dram__bytes_read.sum,dram__bytes_write.sum -k regex:decode_kernel -s 4 -c 1
-    "c2": {"digest": "4e4d3d04dbeb29e0", "splits": 4, "shared": False,
-           "bytes": 2312733696 + 4395008},
-    "c3": {"digest": "4e4d3d04dbeb29e0", "splits": 7, "shared": False,
-           "bytes": 537528064 + 5481472},
+    "c2": {"digest": "3cb5a85afd5afd79", "splits": 4, "shared": False,
+           "bytes": 2312808448 + 4363520},
+    "c3": {"digest": "3cb5a85afd5afd79", "splits": 7, "shared": False,
+           "bytes": 537524224 + 5497856},
     # shared-prefix path: decode_kernel (suffixes) + prefix_kernel (one --set full
     # capture); the merge kernel's few MB are not included
-    "c5": {"digest": "4e4d3d04dbeb29e0", "splits": 16, "shared": True,
-           "bytes": (1531714560 + 5743104) + (35776768 + 101376)},
+    "c5": {"digest": "3cb5a85afd5afd79", "splits": 16, "shared": True,
+           "bytes": (1531731456 + 5720832) + (35770880 + 102656)},
 }
 
 
