@@ -91,19 +91,23 @@ pkv_status pkv_append(const void* k_new, const void* v_new, void* k_cache, void*
                       int32_t* err_flag, void* stream);
 
 /*
- * Bytes of device workspace pkv_decode_attention needs for these arguments on
- * the current device (the split-K plan depends on the device's SM count).
- * Returns 0 when no workspace is needed and SIZE_MAX when the arguments are
- * invalid or the device cannot be queried.
+ * Bytes of device workspace pkv_decode_attention (and pkv_decode_attention_fp8)
+ * needs for these arguments on the current device (the split-K plan depends on
+ * the device's SM count; the automatic plan picks, among partitions of 256 to
+ * 1024 tokens, the count with the least estimated time: waves of resident CTAs,
+ * rounded up, times the partition's tokens plus a fixed per-CTA start; the
+ * E4M3 kernel, with more resident CTAs per SM, may pick another count, and
+ * this size covers both).  Returns 0 when no workspace is needed and SIZE_MAX
+ * when the arguments are invalid or the device cannot be queried.
  */
 size_t pkv_decode_workspace_size(int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
                                  int block_size, int max_context_len, int num_splits);
 
 /*
  * The number of KV partitions per sequence (split-K) pkv_decode_attention
- * uses for these arguments on the current device: >= 1, or -1 when the
- * arguments are invalid or the device cannot be queried.  num_splits as in
- * pkv_decode_attention (0 = automatic).
+ * uses for these arguments on the current device (16-bit caches): >= 1, or -1
+ * when the arguments are invalid or the device cannot be queried.  num_splits
+ * as in pkv_decode_attention (0 = automatic).
  */
 int pkv_decode_num_splits(int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
                           int block_size, int max_context_len, int num_splits);

@@ -1622,10 +1622,13 @@ static pkv_status check_shapes(int num_seqs, int num_q_heads, int num_kv_heads, 
 }
 
 // Partitions: whole 16-token stages, whatever the page size; the automatic
-// plan sizes them so that, at the longest context, the CTAs fill whole waves
-// of resident CTAs (see the loop), between 256 and 1024 tokens.
+// plan sizes them from 256 to 1024 tokens by an estimate of the time (see the
+// loop).  ctas_per_sm: the decode kernel's resident CTAs an SM (3, or 4 for
+// the E4M3 kernel at one 8-column group).
+constexpr double kCtaStartTokens = 384.0;  // a CTA's fixed start, in tokens streamed
 static pkv_status make_plan(int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
-                            int block_size, int max_context_len, int num_splits, Plan* plan) {
+                            int block_size, int max_context_len, int num_splits, Plan* plan,
+                            int ctas_per_sm = 3) {
     pkv_status st = check_shapes(num_seqs, num_q_heads, num_kv_heads, head_dim, block_size,
                                  max_context_len, num_splits);
     if (st != PKV_OK) return st;
@@ -1638,32 +1641,33 @@ static pkv_status make_plan(int num_seqs, int num_q_heads, int num_kv_heads, int
     if (num_splits == 0) {
         const int sms = current_sm_count();
         if (sms <= 0) return PKV_ERR_CUDA;
-        // From 256 to 1024 tokens.  Among those partition counts, the fewest
-        // whose CTAs (at the longest context) fill their last wave of resident
-        // CTAs to 95%, else the best filled one: equal-length CTAs run in
-        // lock-step waves, so a partly empty last wave leaves SMs idle.
-        // (Three resident CTAs an SM, the 16-bit kernel's; the E4M3 kernel's
-        // fourth is left out so that workspace sizes do not depend on the cache.)
+        // From 256 to 1024 tokens.  Equal-length CTAs (at the longest
+        // context) run in waves of resident CTAs; every wave costs its
+        // partition's tokens plus a CTA's fixed start (context length and
+        // block-table reads, the first copy round trip), kCtaStartTokens in
+        // tokens streamed.  The count with the least (waves rounded up) x
+        // (tokens + start) wins, the fewest partitions among equals.  A
+        // partly filled last wave costs less than this counts (fewer CTAs on
+        // an SM still draw most of its bandwidth), more waves cost their
+        // starts: measured on the Llama-70B layer (32 x 4096 tokens, GQA-8),
+        // 5 partitions (2.8 waves) ran at 89.6 % of peak, the 7 of a
+        // fill-the-last-wave rule (3.9 waves) at 86.9 %.
         const int64_t units = (int64_t)std::max(1, num_seqs) * num_kv_heads;
-        const double slots = 3.0 * sms;
+        const double slots = (double)ctas_per_sm * sms;
         const int min_chunk = 256 / kStageTokens, max_chunk = std::min(1024 / kStageTokens, cap_stages);
         const int lo = std::max(1, (max_stages + max_chunk - 1) / max_chunk);
         const int hi = std::max(lo, std::min(PKV_MAX_SPLITS, (max_stages + min_chunk - 1) / min_chunk));
-        double best_eff = -1.0;
+        double best = 0.0;
         chunk_stages = (max_stages + lo - 1) / lo;
         for (int s = lo; s <= hi; ++s) {
             const int cs = (max_stages + s - 1) / s;
             const int splits = (max_stages + cs - 1) / cs;
             if (splits != s) continue;  // the same partition as a smaller count
-            const double waves = (double)units * splits / slots;
-            const double eff = waves / std::ceil(waves);
-            if (eff > best_eff + 1e-9) {
-                best_eff = eff;
+            const double waves = std::ceil((double)units * splits / slots);
+            const double cost = waves * (cs * kStageTokens + kCtaStartTokens);
+            if (s == lo || cost < best - 1e-9) {
+                best = cost;
                 chunk_stages = cs;
-            }
-            if (eff >= 0.95) {
-                chunk_stages = cs;
-                break;
             }
         }
     } else {
@@ -1906,11 +1910,15 @@ using namespace pkv;
 extern "C" size_t pkv_decode_workspace_size(int num_seqs, int num_q_heads, int num_kv_heads,
                                             int head_dim, int block_size, int max_context_len,
                                             int num_splits) {
-    Plan plan;
+    // Enough for the 16-bit kernel's plan and the E4M3 kernel's (whose
+    // automatic plan counts four resident CTAs an SM).
+    Plan plan, plan4;
     if (make_plan(num_seqs, num_q_heads, num_kv_heads, head_dim, block_size, max_context_len,
-                  num_splits, &plan) != PKV_OK)
+                  num_splits, &plan) != PKV_OK ||
+        make_plan(num_seqs, num_q_heads, num_kv_heads, head_dim, block_size, max_context_len,
+                  num_splits, &plan4, 4) != PKV_OK)
         return SIZE_MAX;
-    return plan.workspace_bytes;
+    return std::max(plan.workspace_bytes, plan4.workspace_bytes);
 }
 
 extern "C" int pkv_decode_num_splits(int num_seqs, int num_q_heads, int num_kv_heads,
@@ -1957,7 +1965,7 @@ static pkv_status decode_impl(void* out, const void* q, const void* k_new, const
     if ((int64_t)max_blocks_per_seq * block_size > INT_MAX) return PKV_ERR_UNSUPPORTED;
     Plan plan;
     st = make_plan(num_seqs, num_q_heads, num_kv_heads, head_dim, block_size, max_context_len,
-                   num_splits, &plan);
+                   num_splits, &plan, f8 && num_q_heads / num_kv_heads <= 8 ? 4 : 3);
     if (st != PKV_OK) return st;
     if (plan.workspace_bytes > 0 && (workspace == nullptr || workspace_bytes < plan.workspace_bytes))
         return PKV_ERR_WORKSPACE;
