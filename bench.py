@@ -351,7 +351,7 @@ def run_gpu(args):
     # Host-side bounds of the group metadata, read once (each read syncs the device).
     max_group_size, max_prefix_len = w.max_group_size, w.max_prefix_len
     splits = pkv.decode_num_splits(s.num_seqs, s.num_q_heads, s.num_kv_heads, s.head_dim,
-                                   s.block_size, mcl, args.splits)
+                                   s.block_size, mcl, args.splits, kv=args.kv)
     if mq:
         ws_bytes = pkv.multi_query_workspace_size(s.num_seqs, args.q_len, s.num_q_heads,
                                                   s.num_kv_heads, s.head_dim, s.block_size, mcl)

@@ -112,6 +112,11 @@ size_t pkv_decode_workspace_size(int num_seqs, int num_q_heads, int num_kv_heads
 int pkv_decode_num_splits(int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
                           int block_size, int max_context_len, int num_splits);
 
+/* The same for pkv_decode_attention_fp8 (E4M3 caches), whose kernel holds more
+ * CTAs per SM, so its automatic plan may pick another count. */
+int pkv_decode_num_splits_fp8(int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
+                              int block_size, int max_context_len, int num_splits);
+
 /*
  * Decode attention: one query token per sequence against its paged context.
  *

@@ -62,6 +62,8 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.pkv_decode_workspace_size.restype = sz
     lib.pkv_decode_num_splits.argtypes = [i, i, i, i, i, i, i]
     lib.pkv_decode_num_splits.restype = i
+    lib.pkv_decode_num_splits_fp8.argtypes = [i, i, i, i, i, i, i]
+    lib.pkv_decode_num_splits_fp8.restype = i
     lib.pkv_decode_attention.argtypes = [p, p, p, p, p, i, p, i, i, i, i, i, i, i, f, i, p, sz,
                                          i, p, p]
     lib.pkv_append_decode_attention.argtypes = [p, p, p, p, p, p, p, i, p, i, i, i, i, i, i, i,
@@ -182,10 +184,13 @@ def workspace_size(num_seqs: int, num_q_heads: int, num_kv_heads: int, head_dim:
 
 
 def decode_num_splits(num_seqs: int, num_q_heads: int, num_kv_heads: int, head_dim: int,
-                      block_size: int, max_context_len: int, num_splits: int = 0) -> int:
-    """KV partitions per sequence ``decode_attention`` uses on the current device."""
-    n = load().pkv_decode_num_splits(num_seqs, num_q_heads, num_kv_heads, head_dim, block_size,
-                                     max_context_len, num_splits)
+                      block_size: int, max_context_len: int, num_splits: int = 0,
+                      kv: str = "16bit") -> int:
+    """KV partitions per sequence ``decode_attention`` (kv="16bit") or
+    ``decode_attention_fp8`` (kv="fp8") uses on the current device."""
+    lib = load()
+    fn = lib.pkv_decode_num_splits_fp8 if kv == "fp8" else lib.pkv_decode_num_splits
+    n = fn(num_seqs, num_q_heads, num_kv_heads, head_dim, block_size, max_context_len, num_splits)
     if n < 0:
         raise PkvError(1, "pkv_decode_num_splits")
     return int(n)

@@ -1931,6 +1931,17 @@ extern "C" int pkv_decode_num_splits(int num_seqs, int num_q_heads, int num_kv_h
     return plan.num_splits;
 }
 
+extern "C" int pkv_decode_num_splits_fp8(int num_seqs, int num_q_heads, int num_kv_heads,
+                                         int head_dim, int block_size, int max_context_len,
+                                         int num_splits) {
+    Plan plan;
+    if (make_plan(num_seqs, num_q_heads, num_kv_heads, head_dim, block_size, max_context_len,
+                  num_splits, &plan, num_q_heads > 0 && num_kv_heads > 0 &&
+                                         num_q_heads / num_kv_heads <= 8 ? 4 : 3) != PKV_OK)
+        return -1;
+    return plan.num_splits;
+}
+
 // The plain decode, with the new tokens' K/V appended by the decode kernel
 // itself when k_new / v_new are given.
 static pkv_status decode_impl(void* out, const void* q, const void* k_new, const void* v_new,

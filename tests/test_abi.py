@@ -88,6 +88,8 @@ def test_workspace_size_rejects_bad_arguments(lib):
     assert lib.pkv_decode_num_splits(2, 4, 2, 64, 16, 64, 3) == 2   # 4 pages -> 2 chunks of 2
     assert lib.pkv_decode_num_splits(2, 4, 2, 64, 16, 64, 2000) == -1
     assert lib.pkv_decode_num_splits(2, 4, 2, 64, 16, 64, 8) == 4     # no more than the pages
+    assert lib.pkv_decode_num_splits_fp8(2, 4, 2, 64, 16, 64, 3) == 2
+    assert lib.pkv_decode_num_splits_fp8(2, 4, 2, 64, 16, 64, 2000) == -1
 
 
 def _multi_query(lib, **kw):
