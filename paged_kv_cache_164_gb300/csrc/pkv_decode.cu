@@ -824,7 +824,7 @@ constexpr int kPrefixTmaWarp = kPrefixSoftmaxWarps;
 constexpr int kPrefixMmaWarp = kPrefixSoftmaxWarps + 1;
 constexpr float kRescaleLog2 = 8.f;      // P values stay below 2^8 between rescales
 
-template <int D>
+template <int D, int NSTG = kPrefixStages, bool ONE_ACC = false>
 struct PrefixTile {
     static constexpr int kRegions = D / 64;                            // 128-byte column blocks
     static constexpr int kQRegionBytes = kPrefixTileRows * 128;
@@ -834,15 +834,16 @@ struct PrefixTile {
     static constexpr int kStageBytes = 2 * kHalfBytes;
     static constexpr int kXchBytes = 2 * kPrefixTileRows * 8;  // (m, l) per row and half
     // full[stages], empty[stages], s_full[2], p_ready[2], o_done[2], q_ready, drain
-    static constexpr int kBarriers = 2 * kPrefixStages + 8;
-    static constexpr int kSmemBytes = 1024 + kQBytes + kPrefixStages * kStageBytes + kXchBytes +
+    static constexpr int kBarriers = 2 * NSTG + 8;
+    static constexpr int kSmemBytes = 1024 + kQBytes + NSTG * kStageBytes + kXchBytes +
                                       kBarriers * 8 + (kMaxChunkPages + 1) * 4 + 64;
     // S0, S1 (64 columns each; P of the tile overwrites its S as hi/lo 16-bit
-    // pairs), O_a, O_b (D columns each)
+    // pairs), O_a, O_b (D columns each; with ONE_ACC only O_a)
     static constexpr uint32_t kColOa = 2 * kPrefixTileTokens;
     static constexpr uint32_t kColOb = kColOa + D;
-    static constexpr uint32_t kTmemCols = kColOb + D <= 256 ? 256 : 512;
-    static_assert(kColOb + D <= kTmemCols, "tensor memory layout");
+    static constexpr uint32_t kTmemEnd = ONE_ACC ? kColOa + D : kColOb + D;
+    static constexpr uint32_t kTmemCols = kTmemEnd <= 256 ? 256 : 512;
+    static_assert(kTmemEnd <= kTmemCols, "tensor memory layout");
 };
 
 // Instruction descriptor of tcgen05.mma kind::f16: fp32 accumulator, A and B
@@ -975,20 +976,29 @@ __device__ void plan_cta(const PlanParams& p, int* scratch) {
     if (tid == 0) *p.item_count = *base;
 }
 
-// DUP (at most 64 query rows in the CTA): rows 64-127 of the tile repeat rows
-// 0-63, so every query row has four threads, one per 16-token quarter of each
-// tile, on all four SM sub-partitions (a warp reaches only its own quarter of
-// the tensor-memory lanes).  P rows 0-63 carry tokens 0-31 and zeros for
-// 32-63, rows 64-127 the reverse; O_a takes the 16-token steps 0 and 2 and O_b
-// steps 1 and 3, so each accumulator lane sums exactly one thread's quarter.
-// Lanes r and r + 64 then hold two independent partial softmaxes of the same
-// row, written as partial slots 2 * partition and 2 * partition + 1.
-template <typename T, int D, bool DUP = false>
-__global__ void __launch_bounds__(kPrefixThreads, 1)
+// MODE 0: up to 128 query rows, two softmax threads per row (token halves).
+// MODE 1 and 2 (at most 64 query rows in the CTA): rows 64-127 of the tile
+// repeat rows 0-63, so the rows' softmax runs on all four SM sub-partitions
+// (a warp reaches only its own quarter of the tensor-memory lanes).  P rows
+// 0-63 carry tokens 0-31 and zeros for 32-63, rows 64-127 the reverse, and
+// lanes r and r + 64 hold two independent partial softmaxes of the same row,
+// written as partial slots 2 * partition and 2 * partition + 1.
+//   MODE 1: eight softmax warps, four threads per row (one per 16-token
+//   quarter of each tile); O_a takes the 16-token steps 0 and 2 and O_b steps
+//   1 and 3, so each accumulator lane sums exactly one thread's quarter.
+//   MODE 2: four softmax warps, one thread per row copy (32 tokens of each
+//   tile) and one accumulator; with a 2-stage ring and 256 tensor-memory
+//   columns two CTAs share an SM, so one's start and per-tile chain overlap
+//   the other's.
+template <typename T, int D, int MODE = 0>
+__global__ void __launch_bounds__((MODE == 2 ? 4 : kPrefixSoftmaxWarps) * 32 + 64, MODE == 2 ? 2 : 1)
 prefix_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
               const PrefixParams p) {
-    using Cfg = PrefixTile<D>;
-    constexpr int NS = kPrefixStages;
+    constexpr bool DUP = MODE != 0;
+    constexpr bool PAIR = MODE == 2;
+    constexpr int SW = PAIR ? 4 : kPrefixSoftmaxWarps;  // softmax warps; then the TMA and MMA warps
+    constexpr int NS = PAIR ? 2 : kPrefixStages;
+    using Cfg = PrefixTile<D, NS, PAIR>;
     constexpr int R = Cfg::kRegions;
     constexpr int KSTEPS = D / 16;
     constexpr int TT = kPrefixTileTokens;
@@ -1014,7 +1024,7 @@ prefix_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
     int* table = reinterpret_cast<int*>(bars + Cfg::kBarriers);
     volatile int* abort_flag = table + kMaxChunkPages + 1;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(table + kMaxChunkPages + 2);
-    int* warp_lim = table + kMaxChunkPages + 3;  // [kPrefixSoftmaxWarps]
+    int* warp_lim = table + kMaxChunkPages + 3;  // [SW]
 
     const int rt = blockIdx.x;                     // tile of 128 query rows
     const int g = blockIdx.y % p.num_kv_heads;     // KV head
@@ -1069,7 +1079,7 @@ prefix_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
     const int half = warp / 4;                // tokens 32*half .. 32*half+31 of every tile
     const int dcopy = DUP ? (srow >> 6) : 0;  // DUP: which copy of the row this lane holds
     const int r = row0 + (DUP ? (srow & 63) : srow);
-    const bool row_ok = warp < kPrefixSoftmaxWarps && r < rows;
+    const bool row_ok = warp < SW && r < rows;
     const int head = g * p.group + (row_ok ? r % p.group : 0);
     int64_t qrow;
     int lim = 0;
@@ -1090,11 +1100,11 @@ prefix_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
         }
         ptx::mbar_init(ptx::smem_addr(&s_full[0]), 1);
         ptx::mbar_init(ptx::smem_addr(&s_full[1]), 1);
-        ptx::mbar_init(ptx::smem_addr(&p_ready[0]), kPrefixSoftmaxWarps * 32);
-        ptx::mbar_init(ptx::smem_addr(&p_ready[1]), kPrefixSoftmaxWarps * 32);
+        ptx::mbar_init(ptx::smem_addr(&p_ready[0]), SW * 32);
+        ptx::mbar_init(ptx::smem_addr(&p_ready[1]), SW * 32);
         ptx::mbar_init(ptx::smem_addr(&o_done[0]), 1);
         ptx::mbar_init(ptx::smem_addr(&o_done[1]), 1);
-        ptx::mbar_init(ptx::smem_addr(q_ready), kPrefixSoftmaxWarps * 32);
+        ptx::mbar_init(ptx::smem_addr(q_ready), SW * 32);
         ptx::mbar_init(ptx::smem_addr(drain), 1);
         *abort_flag = 0;
         ptx::fence_barrier_init();
@@ -1102,17 +1112,18 @@ prefix_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
     // The softmax threads' halves of their query rows, loaded before the barrier
     // below so the load overlaps the block-table read (stored to shared memory
     // after it).
-    uint4 qv[D / 16];
-    if (warp < kPrefixSoftmaxWarps) {
+    constexpr int QV = PAIR ? D / 8 : D / 16;  // 16-byte pieces per thread (whole row, or half)
+    uint4 qv[QV];
+    if (warp < SW) {
         const uint4* src = reinterpret_cast<const uint4*>(static_cast<const T*>(p.q) + qrow * D);
 #pragma unroll
-        for (int k = 0; k < D / 16; ++k)
-            qv[k] = row_ok ? __ldg(src + half * (D / 16) + k) : make_uint4(0u, 0u, 0u, 0u);
+        for (int k = 0; k < QV; ++k)
+            qv[k] = row_ok ? __ldg(src + half * QV + k) : make_uint4(0u, 0u, 0u, 0u);
         int m = lim;
 #pragma unroll
         for (int off = 16; off > 0; off >>= 1) m = max(m, __shfl_xor_sync(0xffffffffu, m, off));
         if (lane == 0) warp_lim[warp] = m;
-    } else if (warp == kPrefixTmaWarp) {
+    } else if (warp == SW) {
         // The partition's slice of the block table (from the first member's row).
         const int npages = (t_chunk_end + bs - 1) / bs - page0;
         const int32_t* trow = p.block_tables + (int64_t)first * p.max_blocks_per_seq + page0;
@@ -1139,13 +1150,13 @@ prefix_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
     // Tokens past every row's context take no part for any row of this CTA: not read.
     int max_lim = 0;
 #pragma unroll
-    for (int w = 0; w < kPrefixSoftmaxWarps; ++w) max_lim = max(max_lim, warp_lim[w]);
+    for (int w = 0; w < SW; ++w) max_lim = max(max_lim, warp_lim[w]);
     const int t_end = min(t_chunk_end, max(t_begin, max_lim));
     const int ntiles = (t_end - t_begin + TT - 1) / TT;
     const uint32_t ring_addr = ptx::smem_addr(ring);
     const uint32_t q_addr = ptx::smem_addr(sq);
 
-    if (warp == kPrefixTmaWarp) {
+    if (warp == SW) {
         // ------------------------------------------------------------ producer
         // The tile's box loads (16-token page box x 64-dim region x K/V) are
         // spread over the warp's lanes: one thread issuing them in turn is the
@@ -1192,7 +1203,7 @@ prefix_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
                 }
             }
         }
-    } else if (warp == kPrefixMmaWarp) {
+    } else if (warp == (SW + 1)) {
         // ------------------------------------------------------------ MMA issuer
         if (lane == 0) {
             constexpr uint32_t fmt = F16Format<T>::value;
@@ -1200,12 +1211,9 @@ prefix_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
             constexpr uint32_t idesc_o = mma_idesc(fmt, kPrefixTileRows, D, true);
             bool ok = wait_phase(ptx::smem_addr(q_ready), 0, abort_flag, p.err_flag);
             if (ok) ptx::tc_fence_after_sync();
-            // S(j) = Q K(j)^T into S buffer j % 2
-            auto issue_s = [&](int j) -> bool {
+            // S(j) = Q K(j)^T into S buffer j % 2 (tile j's K/V have landed)
+            auto issue_s = [&](int j) {
                 const int slot = j % NS;
-                if (!wait_phase(ptx::smem_addr(&full_bar[slot]), (j / NS) & 1, abort_flag,
-                                p.err_flag))
-                    return false;
                 ptx::tc_fence_after_sync();
                 const uint32_t kb = ring_addr + slot * Cfg::kStageBytes;
 #pragma unroll
@@ -1217,27 +1225,21 @@ prefix_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
                     ptx::tc_mma_f16(tmem + (j % 2) * TT, a, b, idesc_s, ks > 0 ? 1u : 0u);
                 }
                 ptx::tc_commit(ptx::smem_addr(&s_full[j % 2]));
-                return true;
             };
-            for (int j = 0; j < 2 && j < ntiles && ok; ++j) ok = issue_s(j);
-            for (int j = 0; j < ntiles && ok; ++j) {
-                // O += P(j) V(j) once the softmax has written P(j)
-                if (!wait_phase(ptx::smem_addr(&p_ready[j % 2]), (j / 2) & 1, abort_flag,
-                                p.err_flag)) {
-                    ok = false;
-                    break;
-                }
+            // O += P(j) V(j) (the softmax has written P(j))
+            auto issue_pv = [&](int j) {
                 ptx::tc_fence_after_sync();
                 const uint32_t vb = ring_addr + (j % NS) * Cfg::kStageBytes + Cfg::kHalfBytes;
-                constexpr int HTK = DUP ? TT / 4 : TT / 2;  // tokens per softmax thread
+                constexpr int HTK = MODE == 1 ? TT / 4 : TT / 2;  // tokens per softmax thread
 #pragma unroll
                 for (int kt = 0; kt < TT / 16; ++kt) {
-                    // tokens 0-31 accumulate into O_a, tokens 32-63 into O_b; with
-                    // DUP the even 16-token steps into O_a, the odd ones into O_b
-                    const bool to_a = DUP ? (kt % 2 == 0) : (kt < TT / 32);
+                    // tokens 0-31 accumulate into O_a, tokens 32-63 into O_b; MODE 1:
+                    // the even 16-token steps into O_a, the odd ones into O_b;
+                    // MODE 2: every step into the one accumulator
+                    const bool to_a = PAIR || (DUP ? (kt % 2 == 0) : (kt < TT / 32));
                     const uint32_t acc = tmem + (to_a ? Cfg::kColOa : Cfg::kColOb);
                     const uint32_t keep =
-                        (j > 0 || (DUP ? kt >= 2 : kt % (TT / 32) > 0)) ? 1u : 0u;
+                        (j > 0 || (PAIR ? kt > 0 : DUP ? kt >= 2 : kt % (TT / 32) > 0)) ? 1u : 0u;
                     const uint64_t b = ptx::smem_desc_sw128(vb + kt * 16 * 128, Cfg::kKVRegionBytes, 1024);
                     // tokens 16kt.. of P: unit u's hi pairs at u*HTK, lo pairs HTK/2 on
                     const int u = kt * 16 / HTK;
@@ -1247,7 +1249,58 @@ prefix_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
                 }
                 ptx::tc_commit(ptx::smem_addr(&o_done[j % 2]));
                 ptx::tc_commit(ptx::smem_addr(&empty_bar[j % NS]));
-                if (j + 2 < ntiles) ok = issue_s(j + 2);
+            };
+            if constexpr (PAIR) {
+                // With a 2-stage ring, S(j+2) often waits for its copy: one thread
+                // issues both kinds as their inputs become ready, so a product
+                // whose P is written never queues behind it.  S(j) may start once
+                // P V(j-2), the last reader of its buffer, is issued (the tensor
+                // core runs them in order).
+                int next_s = 0, next_pv = 0;
+                uint64_t t_last = ptx::globaltimer();
+                while (ok && next_pv < ntiles) {
+                    bool moved = false;
+                    if (next_pv < next_s &&
+                        ptx::mbar_try_wait(ptx::smem_addr(&p_ready[next_pv % 2]), (next_pv / 2) & 1)) {
+                        issue_pv(next_pv++);
+                        moved = true;
+                    }
+                    if (next_s < ntiles && next_s < next_pv + 2 &&
+                        ptx::mbar_try_wait(ptx::smem_addr(&full_bar[next_s % NS]), (next_s / NS) & 1)) {
+                        issue_s(next_s++);
+                        moved = true;
+                    }
+                    if (moved) {
+                        t_last = ptx::globaltimer();
+                    } else if (*abort_flag) {
+                        ok = false;
+                    } else if (ptx::globaltimer() - t_last > kWaitLimitNs) {
+                        *abort_flag = 1;
+                        flag_error(p.err_flag, PKV_EFLAG_TIMEOUT);
+                        ok = false;
+                    }
+                }
+            } else {
+                auto wait_s = [&](int j) {
+                    return wait_phase(ptx::smem_addr(&full_bar[j % NS]), (j / NS) & 1, abort_flag,
+                                      p.err_flag);
+                };
+                for (int j = 0; j < 2 && j < ntiles && ok; ++j) {
+                    ok = wait_s(j);
+                    if (ok) issue_s(j);
+                }
+                for (int j = 0; j < ntiles && ok; ++j) {
+                    if (!wait_phase(ptx::smem_addr(&p_ready[j % 2]), (j / 2) & 1, abort_flag,
+                                    p.err_flag)) {
+                        ok = false;
+                        break;
+                    }
+                    issue_pv(j);
+                    if (j + 2 < ntiles) {
+                        ok = wait_s(j + 2);
+                        if (ok) issue_s(j + 2);
+                    }
+                }
             }
             // every MMA has completed before the tensor memory is released
             ptx::tc_commit(ptx::smem_addr(drain));
@@ -1258,17 +1311,17 @@ prefix_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
         }
     } else {
         // ------------------------------------------------------------ softmax rows
-        constexpr int HT = DUP ? TT / 4 : TT / 2;  // tokens per thread and tile
+        constexpr int HT = MODE == 1 ? TT / 4 : TT / 2;  // tokens per thread and tile
         constexpr int HB = HT / kStageTokens;      // 16-token boxes per thread
         // this thread's tokens of every tile: unit `unit` of HT tokens
-        const int unit = DUP ? 2 * dcopy + half : half;
+        const int unit = PAIR ? dcopy : DUP ? 2 * dcopy + half : half;
         // This thread's half of its row of Q into shared memory (16-byte chunk
         // c of a 128-byte row lands at chunk c ^ (row % 8): the 128-byte
         // swizzle of the MMA operand).
         {
 #pragma unroll
-            for (int k = 0; k < D / 16; ++k) {
-                const int c = half * (D / 16) + k;
+            for (int k = 0; k < QV; ++k) {
+                const int c = half * QV + k;
                 *reinterpret_cast<uint4*>(sq + (c / 8) * Cfg::kQRegionBytes + srow * 128 +
                                           (((c % 8) ^ (srow & 7)) << 4)) = qv[k];
             }
@@ -1276,7 +1329,7 @@ prefix_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
             ptx::mbar_arrive(ptx::smem_addr(q_ready));
         }
         const uint32_t lane_base = (uint32_t)(32 * (warp % 4)) << 16;
-        const uint32_t col_o = half ? Cfg::kColOb : Cfg::kColOa;  // this half's accumulator
+        const uint32_t col_o = (half && !PAIR) ? Cfg::kColOb : Cfg::kColOa;  // this thread's accumulator
         float m_ref = -INFINITY;  // reference max of this half's P (log2 domain)
         float l = 0.f;
         bool ok = true;
@@ -1380,10 +1433,15 @@ prefix_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
                 if constexpr (DUP) {
                     // The other copy's unit of this lane (S values no thread reads)
                     // must be zero for the steps that bring it into this lane's O.
-                    uint32_t z[16];
+                    uint32_t z[HT];
 #pragma unroll
-                    for (int e = 0; e < 16; ++e) z[e] = 0u;
-                    ptx::tmem_st16(tmem + lane_base + (j % 2) * TT + (2 * (1 - dcopy) + half) * HT, z);
+                    for (int e = 0; e < HT; ++e) z[e] = 0u;
+                    const int zu = PAIR ? 1 - dcopy : 2 * (1 - dcopy) + half;
+                    const uint32_t zcol = tmem + lane_base + (j % 2) * TT + zu * HT;
+                    if constexpr (HT == 32)
+                        ptx::tmem_st32(zcol, z);
+                    else
+                        ptx::tmem_st16(zcol, z);
                 }
             }
             // V rows of tokens that were not loaded hold stale or uninitialised
@@ -1393,7 +1451,7 @@ prefix_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
             for (int bx = 0; bx < TT / kStageTokens; ++bx) partial |= nvalid[bx] < kStageTokens;
             if (partial) {
                 uint8_t* vst = ring + (j % NS) * Cfg::kStageBytes + Cfg::kHalfBytes;
-                for (int idx = tid; idx < TT * R * 8; idx += kPrefixSoftmaxWarps * 32) {
+                for (int idx = tid; idx < TT * R * 8; idx += SW * 32) {
                     const int row = idx / (R * 8);
                     const int rem = idx - row * (R * 8);
                     if (row % kStageTokens >= nvalid[row / kStageTokens])
@@ -1411,8 +1469,40 @@ prefix_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
         // The two halves of each row meet: every softmax thread passes this
         // barrier exactly once, aborted or not.
         xch[half * kPrefixTileRows + srow] = make_float2(m_ref, l);
-        ptx::named_barrier_sync(1, kPrefixSoftmaxWarps * 32);
-        if (ok && !*abort_flag) {
+        ptx::named_barrier_sync(1, SW * 32);
+        if constexpr (PAIR) {
+            if (ok && !*abort_flag) {
+                // Each lane's partial softmax on its own: O / l and its log-sum-exp,
+                // as partial slot 2 * part + copy.
+                ptx::tc_fence_after_sync();
+                const float inv = l > 0.f ? 1.f / l : 0.f;
+                const int64_t prow = qrow * p.num_splits + 2 * part + dcopy;
+                float* dst = p.partial_o + prow * D;
+#pragma unroll
+                for (int c = 0; c < D / 32; ++c) {
+                    uint32_t ov[32];
+                    if (ntiles > 0) {
+                        ptx::tmem_ld32(tmem + lane_base + Cfg::kColOa + c * 32, ov);
+                    } else {
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) ov[i] = 0u;
+                    }
+                    if (row_ok) {
+#pragma unroll
+                        for (int i = 0; i < 32; i += 4) {
+                            float4 v;
+                            v.x = __uint_as_float(ov[i]) * inv;
+                            v.y = __uint_as_float(ov[i + 1]) * inv;
+                            v.z = __uint_as_float(ov[i + 2]) * inv;
+                            v.w = __uint_as_float(ov[i + 3]) * inv;
+                            *reinterpret_cast<float4*>(dst + c * 32 + i) = v;
+                        }
+                    }
+                }
+                if (row_ok)
+                    p.partial_lse[prow] = l > 0.f ? (m_ref + log2f(l)) * kLn2 : -INFINITY;
+            }
+        } else if (ok && !*abort_flag) {
             // Epilogue: O = (2^(m_a - M) O_a + 2^(m_b - M) O_b) / L with M the larger
             // reference and L = 2^(m_a - M) l_a + 2^(m_b - M) l_b; this thread
             // writes columns half*D/2 .. half*D/2 + D/2 - 1 of its row, as prefix
@@ -1457,7 +1547,7 @@ prefix_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
 
     ptx::tc_fence_before_sync();
     __syncthreads();
-    if (warp == kPrefixMmaWarp) {
+    if (warp == (SW + 1)) {
         __syncwarp();
         ptx::tc_fence_after_sync();
         ptx::tmem_dealloc(tmem, Cfg::kTmemCols);
@@ -1789,21 +1879,22 @@ static cudaError_t launch_merge(const MergeParams& p, int groups, int seqs, cuda
     return cudaLaunchKernelEx(&cfg, merge_kernel<T>, q);
 }
 
-template <typename T, int D, bool DUP = false>
+template <typename T, int D, int MODE = 0>
 static cudaError_t launch_prefix_t(const CUtensorMap& mk, const CUtensorMap& mv,
                                    const PrefixParams& p, dim3 grid, cudaStream_t stream) {
-    auto kern = prefix_kernel<T, D, DUP>;
+    auto kern = prefix_kernel<T, D, MODE>;
+    using Cfg = PrefixTile<D, MODE == 2 ? 2 : kPrefixStages, MODE == 2>;
     static std::once_flag once;
     static cudaError_t attr_err = cudaSuccess;
     std::call_once(once, [&] {
         attr_err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                        PrefixTile<D>::kSmemBytes);
+                                        Cfg::kSmemBytes);
     });
     if (attr_err != cudaSuccess) return attr_err;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = grid;
-    cfg.blockDim = dim3(kPrefixThreads);
-    cfg.dynamicSmemBytes = PrefixTile<D>::kSmemBytes;
+    cfg.blockDim = dim3(((MODE == 2 ? 4 : kPrefixSoftmaxWarps) + 2) * 32);
+    cfg.dynamicSmemBytes = Cfg::kSmemBytes;
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -1862,6 +1953,12 @@ static pkv_status make_prefix_plan(int num_seqs, int num_q_heads, int num_kv_hea
 // Plan of a multi-query call: 128-row tiles of (query token, query head) rows
 // per (sequence, KV head); the context in partitions of whole 64-token tiles,
 // as many as give about one CTA per SM, at most kMaxChunkPages pages each.
+// The multi-query kernel for at most 64 query rows per (sequence, KV head):
+// MODE 2 (one thread per row copy, two CTAs an SM) or MODE 1 (four threads
+// per row, one CTA an SM).
+constexpr int kMqDupMode = 2;
+constexpr int kMqDupCtasPerSm = kMqDupMode == 2 ? 2 : 1;
+
 struct MultiQueryPlan {
     int chunk;
     int parts;
@@ -1886,8 +1983,9 @@ static pkv_status make_mq_plan(int num_seqs, int q_len, int num_q_heads, int num
         return PKV_ERR_UNSUPPORTED;
     const int sms = current_sm_count();
     if (sms <= 0) return PKV_ERR_CUDA;
+    mp->dup = rows <= kPrefixTileRows / 2;
     const int64_t units = std::max<int64_t>(1, (int64_t)num_seqs * num_kv_heads * mp->row_tiles);
-    const int64_t want = std::max<int64_t>(1, sms / units);
+    const int64_t want = std::max<int64_t>(1, (int64_t)sms * (mp->dup ? kMqDupCtasPerSm : 1) / units);
     const int tiles = std::max(1, (max_context_len + kPrefixTileTokens - 1) / kPrefixTileTokens);
     const int max_tiles = kMaxChunkPages * block_size / kPrefixTileTokens;
     const int chunk_tiles =
@@ -1895,7 +1993,6 @@ static pkv_status make_mq_plan(int num_seqs, int q_len, int num_q_heads, int num
     mp->chunk = chunk_tiles * kPrefixTileTokens;
     mp->parts = std::max(1, (max_context_len + mp->chunk - 1) / mp->chunk);
     if (mp->parts > PKV_MAX_SPLITS || mp->parts > 65535) return PKV_ERR_UNSUPPORTED;
-    mp->dup = rows <= kPrefixTileRows / 2;
     mp->slots = mp->parts * (mp->dup ? 2 : 1);
     if (mp->slots > 65535) return PKV_ERR_UNSUPPORTED;
     mp->workspace_bytes =
@@ -2388,11 +2485,11 @@ extern "C" pkv_status pkv_multi_query_attention(
     cudaError_t e;
     if (mq.dup) {
         if (head_dim == 64)
-            e = dtype == PKV_FP16 ? launch_prefix_t<__half, 64, true>(mk, mv, pr, pgrid, s)
-                                  : launch_prefix_t<__nv_bfloat16, 64, true>(mk, mv, pr, pgrid, s);
+            e = dtype == PKV_FP16 ? launch_prefix_t<__half, 64, kMqDupMode>(mk, mv, pr, pgrid, s)
+                                  : launch_prefix_t<__nv_bfloat16, 64, kMqDupMode>(mk, mv, pr, pgrid, s);
         else
-            e = dtype == PKV_FP16 ? launch_prefix_t<__half, 128, true>(mk, mv, pr, pgrid, s)
-                                  : launch_prefix_t<__nv_bfloat16, 128, true>(mk, mv, pr, pgrid, s);
+            e = dtype == PKV_FP16 ? launch_prefix_t<__half, 128, kMqDupMode>(mk, mv, pr, pgrid, s)
+                                  : launch_prefix_t<__nv_bfloat16, 128, kMqDupMode>(mk, mv, pr, pgrid, s);
     } else if (head_dim == 64) {
         e = dtype == PKV_FP16 ? launch_prefix_t<__half, 64>(mk, mv, pr, pgrid, s)
                               : launch_prefix_t<__nv_bfloat16, 64>(mk, mv, pr, pgrid, s);
