@@ -976,26 +976,22 @@ __device__ void plan_cta(const PlanParams& p, int* scratch) {
     if (tid == 0) *p.item_count = *base;
 }
 
-// MODE 0: up to 128 query rows, two softmax threads per row (token halves).
-// MODE 1 and 2 (at most 64 query rows in the CTA): rows 64-127 of the tile
-// repeat rows 0-63, so the rows' softmax runs on all four SM sub-partitions
-// (a warp reaches only its own quarter of the tensor-memory lanes).  P rows
-// 0-63 carry tokens 0-31 and zeros for 32-63, rows 64-127 the reverse, and
-// lanes r and r + 64 hold two independent partial softmaxes of the same row,
-// written as partial slots 2 * partition and 2 * partition + 1.
-//   MODE 1: eight softmax warps, four threads per row (one per 16-token
-//   quarter of each tile); O_a takes the 16-token steps 0 and 2 and O_b steps
-//   1 and 3, so each accumulator lane sums exactly one thread's quarter.
-//   MODE 2: four softmax warps, one thread per row copy (32 tokens of each
-//   tile) and one accumulator; with a 2-stage ring and 256 tensor-memory
-//   columns two CTAs share an SM, so one's start and per-tile chain overlap
-//   the other's.
+// MODE 0: up to 128 query rows, two softmax threads per row (token halves),
+// accumulators O_a and O_b.
+// MODE 1 (at most 64 query rows in the CTA): rows 64-127 of the tile repeat
+// rows 0-63, so the rows' softmax runs on all four SM sub-partitions (a warp
+// reaches only its own quarter of the tensor-memory lanes); lane r's thread
+// takes tokens 0-31 of each tile and lane r + 64's tokens 32-63.  P rows 0-63
+// carry tokens 0-31 and zeros for 32-63, rows 64-127 the reverse, so one
+// accumulator holds two independent partial softmaxes of each row (lanes r
+// and r + 64), written as partial slots 2 * partition and 2 * partition + 1.
+// Four softmax warps, 256 tensor-memory columns and a 2-stage ring: two CTAs
+// share an SM, so one's start and per-tile chain overlap the other's.
 template <typename T, int D, int MODE = 0>
-__global__ void __launch_bounds__((MODE == 2 ? 4 : kPrefixSoftmaxWarps) * 32 + 64, MODE == 2 ? 2 : 1)
+__global__ void __launch_bounds__((MODE == 1 ? 4 : kPrefixSoftmaxWarps) * 32 + 64, MODE == 1 ? 2 : 1)
 prefix_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
               const PrefixParams p) {
-    constexpr bool DUP = MODE != 0;
-    constexpr bool PAIR = MODE == 2;
+    constexpr bool PAIR = MODE == 1;
     constexpr int SW = PAIR ? 4 : kPrefixSoftmaxWarps;  // softmax warps; then the TMA and MMA warps
     constexpr int NS = PAIR ? 2 : kPrefixStages;
     using Cfg = PrefixTile<D, NS, PAIR>;
@@ -1077,8 +1073,8 @@ prefix_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
     // partials ([rows of q][H_q]), its context limit, and its token half.
     const int srow = 32 * (warp % 4) + lane;  // row within the tile = tensor-memory lane
     const int half = warp / 4;                // tokens 32*half .. 32*half+31 of every tile
-    const int dcopy = DUP ? (srow >> 6) : 0;  // DUP: which copy of the row this lane holds
-    const int r = row0 + (DUP ? (srow & 63) : srow);
+    const int dcopy = PAIR ? (srow >> 6) : 0;  // MODE 1: which copy of the row this lane holds
+    const int r = row0 + (PAIR ? (srow & 63) : srow);
     const bool row_ok = warp < SW && r < rows;
     const int head = g * p.group + (row_ok ? r % p.group : 0);
     int64_t qrow;
@@ -1230,16 +1226,14 @@ prefix_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
             auto issue_pv = [&](int j) {
                 ptx::tc_fence_after_sync();
                 const uint32_t vb = ring_addr + (j % NS) * Cfg::kStageBytes + Cfg::kHalfBytes;
-                constexpr int HTK = MODE == 1 ? TT / 4 : TT / 2;  // tokens per softmax thread
+                constexpr int HTK = TT / 2;  // tokens per softmax thread
 #pragma unroll
                 for (int kt = 0; kt < TT / 16; ++kt) {
                     // tokens 0-31 accumulate into O_a, tokens 32-63 into O_b; MODE 1:
-                    // the even 16-token steps into O_a, the odd ones into O_b;
-                    // MODE 2: every step into the one accumulator
-                    const bool to_a = PAIR || (DUP ? (kt % 2 == 0) : (kt < TT / 32));
+                    // every step into the one accumulator
+                    const bool to_a = PAIR || kt < TT / 32;
                     const uint32_t acc = tmem + (to_a ? Cfg::kColOa : Cfg::kColOb);
-                    const uint32_t keep =
-                        (j > 0 || (PAIR ? kt > 0 : DUP ? kt >= 2 : kt % (TT / 32) > 0)) ? 1u : 0u;
+                    const uint32_t keep = (j > 0 || (PAIR ? kt > 0 : kt % (TT / 32) > 0)) ? 1u : 0u;
                     const uint64_t b = ptx::smem_desc_sw128(vb + kt * 16 * 128, Cfg::kKVRegionBytes, 1024);
                     // tokens 16kt.. of P: unit u's hi pairs at u*HTK, lo pairs HTK/2 on
                     const int u = kt * 16 / HTK;
@@ -1311,10 +1305,10 @@ prefix_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
         }
     } else {
         // ------------------------------------------------------------ softmax rows
-        constexpr int HT = MODE == 1 ? TT / 4 : TT / 2;  // tokens per thread and tile
-        constexpr int HB = HT / kStageTokens;      // 16-token boxes per thread
+        constexpr int HT = TT / 2;              // tokens per thread and tile
+        constexpr int HB = HT / kStageTokens;   // 16-token boxes per thread
         // this thread's tokens of every tile: unit `unit` of HT tokens
-        const int unit = PAIR ? dcopy : DUP ? 2 * dcopy + half : half;
+        const int unit = PAIR ? dcopy : half;
         // This thread's half of its row of Q into shared memory (16-byte chunk
         // c of a 128-byte row lands at chunk c ^ (row % 8): the 128-byte
         // swizzle of the MMA operand).
@@ -1341,10 +1335,7 @@ prefix_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
             }
             ptx::tc_fence_after_sync();
             uint32_t sv[HT];
-            if constexpr (HT == 32)
-                ptx::tmem_ld32(tmem + lane_base + (j % 2) * TT + unit * HT, sv);
-            else
-                ptx::tmem_ld16(tmem + lane_base + (j % 2) * TT + unit * HT, sv);
+            ptx::tmem_ld32(tmem + lane_base + (j % 2) * TT + unit * HT, sv);
             const int tile0 = t_begin + j * TT;
             const int h0 = tile0 + unit * HT;  // first token of this thread's unit
             // Tokens present (a valid block, before t_end), per 16-token box of the tile.
@@ -1425,23 +1416,14 @@ prefix_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
 #pragma unroll
                 for (int e = 0; e < HT / 2; ++e)
                     split_hi_lo(sc[2 * e], sc[2 * e + 1], pv[e], pv[HT / 2 + e], T());
-                const uint32_t pcol = tmem + lane_base + (j % 2) * TT + unit * HT;
-                if constexpr (HT == 32)
-                    ptx::tmem_st32(pcol, pv);
-                else
-                    ptx::tmem_st16(pcol, pv);
-                if constexpr (DUP) {
-                    // The other copy's unit of this lane (S values no thread reads)
+                ptx::tmem_st32(tmem + lane_base + (j % 2) * TT + unit * HT, pv);
+                if constexpr (PAIR) {
+                    // The other copy's half of this lane (S values no thread reads)
                     // must be zero for the steps that bring it into this lane's O.
                     uint32_t z[HT];
 #pragma unroll
                     for (int e = 0; e < HT; ++e) z[e] = 0u;
-                    const int zu = PAIR ? 1 - dcopy : 2 * (1 - dcopy) + half;
-                    const uint32_t zcol = tmem + lane_base + (j % 2) * TT + zu * HT;
-                    if constexpr (HT == 32)
-                        ptx::tmem_st32(zcol, z);
-                    else
-                        ptx::tmem_st16(zcol, z);
+                    ptx::tmem_st32(tmem + lane_base + (j % 2) * TT + (1 - dcopy) * HT, z);
                 }
             }
             // V rows of tokens that were not loaded hold stale or uninitialised
@@ -1515,7 +1497,7 @@ prefix_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
             const float fb = hb.x == -INFINITY ? 0.f : ptx::ex2_approx(hb.x - mm);
             const float L = ha.y * fa + hb.y * fb;
             const float inv = L > 0.f ? 1.f / L : 0.f;
-            const int64_t prow = qrow * p.num_splits + (DUP ? 2 * part + dcopy : part);
+            const int64_t prow = qrow * p.num_splits + part;
             float* dst = p.partial_o + prow * D + half * (D / 2);
 #pragma unroll
             for (int c = 0; c < D / 64; ++c) {
@@ -1883,7 +1865,7 @@ template <typename T, int D, int MODE = 0>
 static cudaError_t launch_prefix_t(const CUtensorMap& mk, const CUtensorMap& mv,
                                    const PrefixParams& p, dim3 grid, cudaStream_t stream) {
     auto kern = prefix_kernel<T, D, MODE>;
-    using Cfg = PrefixTile<D, MODE == 2 ? 2 : kPrefixStages, MODE == 2>;
+    using Cfg = PrefixTile<D, MODE == 1 ? 2 : kPrefixStages, MODE == 1>;
     static std::once_flag once;
     static cudaError_t attr_err = cudaSuccess;
     std::call_once(once, [&] {
@@ -1893,7 +1875,7 @@ static cudaError_t launch_prefix_t(const CUtensorMap& mk, const CUtensorMap& mv,
     if (attr_err != cudaSuccess) return attr_err;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = grid;
-    cfg.blockDim = dim3(((MODE == 2 ? 4 : kPrefixSoftmaxWarps) + 2) * 32);
+    cfg.blockDim = dim3(((MODE == 1 ? 4 : kPrefixSoftmaxWarps) + 2) * 32);
     cfg.dynamicSmemBytes = Cfg::kSmemBytes;
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];
@@ -1954,10 +1936,9 @@ static pkv_status make_prefix_plan(int num_seqs, int num_q_heads, int num_kv_hea
 // per (sequence, KV head); the context in partitions of whole 64-token tiles,
 // as many as give about one CTA per SM, at most kMaxChunkPages pages each.
 // The multi-query kernel for at most 64 query rows per (sequence, KV head):
-// MODE 2 (one thread per row copy, two CTAs an SM) or MODE 1 (four threads
-// per row, one CTA an SM).
-constexpr int kMqDupMode = 2;
-constexpr int kMqDupCtasPerSm = kMqDupMode == 2 ? 2 : 1;
+// MODE 1, two CTAs an SM.
+constexpr int kMqDupMode = 1;
+constexpr int kMqDupCtasPerSm = 2;
 
 struct MultiQueryPlan {
     int chunk;
