@@ -985,16 +985,20 @@ __device__ void plan_cta(const PlanParams& p, int* scratch) {
 // carry tokens 0-31 and zeros for 32-63, rows 64-127 the reverse, so one
 // accumulator holds two independent partial softmaxes of each row (lanes r
 // and r + 64), written as partial slots 2 * partition and 2 * partition + 1.
-// Four softmax warps, 256 tensor-memory columns and a 2-stage ring: two CTAs
-// share an SM, so one's start and per-tile chain overlap the other's.
+// MODE 2: up to 128 query rows, one softmax thread per row taking all 64
+// tokens of each tile, one accumulator.
+// MODES 1 and 2 run four softmax warps, 256 tensor-memory columns and a
+// 2-stage ring: two CTAs share an SM, so one's start and per-tile chain
+// overlap the other's.
 template <typename T, int D, int MODE = 0>
-__global__ void __launch_bounds__((MODE == 1 ? 4 : kPrefixSoftmaxWarps) * 32 + 64, MODE == 1 ? 2 : 1)
+__global__ void __launch_bounds__((MODE != 0 ? 4 : kPrefixSoftmaxWarps) * 32 + 64, MODE != 0 ? 2 : 1)
 prefix_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
               const PrefixParams p) {
-    constexpr bool PAIR = MODE == 1;
-    constexpr int SW = PAIR ? 4 : kPrefixSoftmaxWarps;  // softmax warps; then the TMA and MMA warps
-    constexpr int NS = PAIR ? 2 : kPrefixStages;
-    using Cfg = PrefixTile<D, NS, PAIR>;
+    constexpr bool ONE = MODE != 0;   // one thread per lane, one accumulator, two CTAs an SM
+    constexpr bool PAIR = MODE == 1;  // rows 64-127 repeat rows 0-63
+    constexpr int SW = ONE ? 4 : kPrefixSoftmaxWarps;  // softmax warps; then the TMA and MMA warps
+    constexpr int NS = ONE ? 2 : kPrefixStages;
+    using Cfg = PrefixTile<D, NS, ONE>;
     constexpr int R = Cfg::kRegions;
     constexpr int KSTEPS = D / 16;
     constexpr int TT = kPrefixTileTokens;
@@ -1108,7 +1112,7 @@ prefix_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
     // The softmax threads' halves of their query rows, loaded before the barrier
     // below so the load overlaps the block-table read (stored to shared memory
     // after it).
-    constexpr int QV = PAIR ? D / 8 : D / 16;  // 16-byte pieces per thread (whole row, or half)
+    constexpr int QV = ONE ? D / 8 : D / 16;  // 16-byte pieces per thread (whole row, or half)
     uint4 qv[QV];
     if (warp < SW) {
         const uint4* src = reinterpret_cast<const uint4*>(static_cast<const T*>(p.q) + qrow * D);
@@ -1226,14 +1230,14 @@ prefix_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
             auto issue_pv = [&](int j) {
                 ptx::tc_fence_after_sync();
                 const uint32_t vb = ring_addr + (j % NS) * Cfg::kStageBytes + Cfg::kHalfBytes;
-                constexpr int HTK = TT / 2;  // tokens per softmax thread
+                constexpr int HTK = MODE == 2 ? TT : TT / 2;  // tokens per softmax thread
 #pragma unroll
                 for (int kt = 0; kt < TT / 16; ++kt) {
-                    // tokens 0-31 accumulate into O_a, tokens 32-63 into O_b; MODE 1:
-                    // every step into the one accumulator
-                    const bool to_a = PAIR || kt < TT / 32;
+                    // tokens 0-31 accumulate into O_a, tokens 32-63 into O_b; MODES 1
+                    // and 2: every step into the one accumulator
+                    const bool to_a = ONE || kt < TT / 32;
                     const uint32_t acc = tmem + (to_a ? Cfg::kColOa : Cfg::kColOb);
-                    const uint32_t keep = (j > 0 || (PAIR ? kt > 0 : kt % (TT / 32) > 0)) ? 1u : 0u;
+                    const uint32_t keep = (j > 0 || (ONE ? kt > 0 : kt % (TT / 32) > 0)) ? 1u : 0u;
                     const uint64_t b = ptx::smem_desc_sw128(vb + kt * 16 * 128, Cfg::kKVRegionBytes, 1024);
                     // tokens 16kt.. of P: unit u's hi pairs at u*HTK, lo pairs HTK/2 on
                     const int u = kt * 16 / HTK;
@@ -1244,7 +1248,7 @@ prefix_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
                 ptx::tc_commit(ptx::smem_addr(&o_done[j % 2]));
                 ptx::tc_commit(ptx::smem_addr(&empty_bar[j % NS]));
             };
-            if constexpr (PAIR) {
+            if constexpr (ONE) {
                 // With a 2-stage ring, S(j+2) often waits for its copy: one thread
                 // issues both kinds as their inputs become ready, so a product
                 // whose P is written never queues behind it.  S(j) may start once
@@ -1305,10 +1309,10 @@ prefix_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
         }
     } else {
         // ------------------------------------------------------------ softmax rows
-        constexpr int HT = TT / 2;              // tokens per thread and tile
-        constexpr int HB = HT / kStageTokens;   // 16-token boxes per thread
+        constexpr int HT = MODE == 2 ? TT : TT / 2;  // tokens per thread and tile
+        constexpr int HB = HT / kStageTokens;         // 16-token boxes per thread
         // this thread's tokens of every tile: unit `unit` of HT tokens
-        const int unit = PAIR ? dcopy : half;
+        const int unit = PAIR ? dcopy : MODE == 2 ? 0 : half;
         // This thread's half of its row of Q into shared memory (16-byte chunk
         // c of a 128-byte row lands at chunk c ^ (row % 8): the 128-byte
         // swizzle of the MMA operand).
@@ -1323,7 +1327,7 @@ prefix_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
             ptx::mbar_arrive(ptx::smem_addr(q_ready));
         }
         const uint32_t lane_base = (uint32_t)(32 * (warp % 4)) << 16;
-        const uint32_t col_o = (half && !PAIR) ? Cfg::kColOb : Cfg::kColOa;  // this thread's accumulator
+        const uint32_t col_o = (half && !ONE) ? Cfg::kColOb : Cfg::kColOa;  // this thread's accumulator
         float m_ref = -INFINITY;  // reference max of this half's P (log2 domain)
         float l = 0.f;
         bool ok = true;
@@ -1335,7 +1339,10 @@ prefix_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
             }
             ptx::tc_fence_after_sync();
             uint32_t sv[HT];
-            ptx::tmem_ld32(tmem + lane_base + (j % 2) * TT + unit * HT, sv);
+#pragma unroll
+            for (int h = 0; h < HT / 32; ++h)
+                ptx::tmem_ld32(tmem + lane_base + (j % 2) * TT + unit * HT + h * 32,
+                               *reinterpret_cast<uint32_t(*)[32]>(sv + h * 32));
             const int tile0 = t_begin + j * TT;
             const int h0 = tile0 + unit * HT;  // first token of this thread's unit
             // Tokens present (a valid block, before t_end), per 16-token box of the tile.
@@ -1416,7 +1423,10 @@ prefix_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
 #pragma unroll
                 for (int e = 0; e < HT / 2; ++e)
                     split_hi_lo(sc[2 * e], sc[2 * e + 1], pv[e], pv[HT / 2 + e], T());
-                ptx::tmem_st32(tmem + lane_base + (j % 2) * TT + unit * HT, pv);
+#pragma unroll
+                for (int h = 0; h < HT / 32; ++h)
+                    ptx::tmem_st32(tmem + lane_base + (j % 2) * TT + unit * HT + h * 32,
+                                   *reinterpret_cast<const uint32_t(*)[32]>(pv + h * 32));
                 if constexpr (PAIR) {
                     // The other copy's half of this lane (S values no thread reads)
                     // must be zero for the steps that bring it into this lane's O.
@@ -1452,13 +1462,13 @@ prefix_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
         // barrier exactly once, aborted or not.
         xch[half * kPrefixTileRows + srow] = make_float2(m_ref, l);
         ptx::named_barrier_sync(1, SW * 32);
-        if constexpr (PAIR) {
+        if constexpr (ONE) {
             if (ok && !*abort_flag) {
                 // Each lane's partial softmax on its own: O / l and its log-sum-exp,
-                // as partial slot 2 * part + copy.
+                // as partial slot part (MODE 1: 2 * part + copy).
                 ptx::tc_fence_after_sync();
                 const float inv = l > 0.f ? 1.f / l : 0.f;
-                const int64_t prow = qrow * p.num_splits + 2 * part + dcopy;
+                const int64_t prow = qrow * p.num_splits + (PAIR ? 2 * part + dcopy : part);
                 float* dst = p.partial_o + prow * D;
 #pragma unroll
                 for (int c = 0; c < D / 32; ++c) {
@@ -1865,7 +1875,7 @@ template <typename T, int D, int MODE = 0>
 static cudaError_t launch_prefix_t(const CUtensorMap& mk, const CUtensorMap& mv,
                                    const PrefixParams& p, dim3 grid, cudaStream_t stream) {
     auto kern = prefix_kernel<T, D, MODE>;
-    using Cfg = PrefixTile<D, MODE == 1 ? 2 : kPrefixStages, MODE == 1>;
+    using Cfg = PrefixTile<D, MODE != 0 ? 2 : kPrefixStages, MODE != 0>;
     static std::once_flag once;
     static cudaError_t attr_err = cudaSuccess;
     std::call_once(once, [&] {
@@ -1875,7 +1885,7 @@ static cudaError_t launch_prefix_t(const CUtensorMap& mk, const CUtensorMap& mv,
     if (attr_err != cudaSuccess) return attr_err;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = grid;
-    cfg.blockDim = dim3(((MODE == 1 ? 4 : kPrefixSoftmaxWarps) + 2) * 32);
+    cfg.blockDim = dim3(((MODE != 0 ? 4 : kPrefixSoftmaxWarps) + 2) * 32);
     cfg.dynamicSmemBytes = Cfg::kSmemBytes;
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];
@@ -1885,6 +1895,16 @@ static cudaError_t launch_prefix_t(const CUtensorMap& mk, const CUtensorMap& mv,
     cfg.numAttrs = 1;
     return cudaLaunchKernelEx(&cfg, kern, mk, mv, p);
 }
+
+// Modes of the tcgen05 kernel per path: multi-query with at most 64 query
+// rows per (sequence, KV head) MODE 1, with more MODE 2 (one CTA per 128 rows,
+// two CTAs an SM: C4 q_len 16 42.7 -> 45.2 % against MODE 0); shared prefixes
+// MODE 0 (MODE 2 ran C5 at 80.2 % against 81.7 %).
+constexpr int kMqDupMode = 1;
+constexpr int kMqFullMode = 2;
+constexpr int kPrefixMode = 0;
+constexpr int ctas_per_sm_of_mode(int mode) { return mode != 0 ? 2 : 1; }
+constexpr int kMqDupCtasPerSm = ctas_per_sm_of_mode(kMqDupMode);
 
 // Plan of a shared-prefix call: the suffixes planned like a plain decode; the
 // prefix in partitions of whole 64-token tiles, as many as give about one
@@ -1914,7 +1934,7 @@ static pkv_status make_prefix_plan(int num_seqs, int num_q_heads, int num_kv_hea
     const int sms = current_sm_count();
     if (sms <= 0) return PKV_ERR_CUDA;
     const int64_t units = std::max<int64_t>(1, (int64_t)num_groups * num_kv_heads * pp->row_tiles);
-    const int64_t want = std::max<int64_t>(1, sms / units);
+    const int64_t want = std::max<int64_t>(1, (int64_t)sms * ctas_per_sm_of_mode(kPrefixMode) / units);
     const int tiles = (max_prefix_len + kPrefixTileTokens - 1) / kPrefixTileTokens;
     const int max_tiles = kMaxChunkPages * block_size / kPrefixTileTokens;
     const int chunk_tiles =
@@ -1935,11 +1955,6 @@ static pkv_status make_prefix_plan(int num_seqs, int num_q_heads, int num_kv_hea
 // Plan of a multi-query call: 128-row tiles of (query token, query head) rows
 // per (sequence, KV head); the context in partitions of whole 64-token tiles,
 // as many as give about one CTA per SM, at most kMaxChunkPages pages each.
-// The multi-query kernel for at most 64 query rows per (sequence, KV head):
-// MODE 1, two CTAs an SM.
-constexpr int kMqDupMode = 1;
-constexpr int kMqDupCtasPerSm = 2;
-
 struct MultiQueryPlan {
     int chunk;
     int parts;
@@ -1966,7 +1981,8 @@ static pkv_status make_mq_plan(int num_seqs, int q_len, int num_q_heads, int num
     if (sms <= 0) return PKV_ERR_CUDA;
     mp->dup = rows <= kPrefixTileRows / 2;
     const int64_t units = std::max<int64_t>(1, (int64_t)num_seqs * num_kv_heads * mp->row_tiles);
-    const int64_t want = std::max<int64_t>(1, (int64_t)sms * (mp->dup ? kMqDupCtasPerSm : 1) / units);
+    const int64_t want = std::max<int64_t>(
+        1, (int64_t)sms * (mp->dup ? kMqDupCtasPerSm : ctas_per_sm_of_mode(kMqFullMode)) / units);
     const int tiles = std::max(1, (max_context_len + kPrefixTileTokens - 1) / kPrefixTileTokens);
     const int max_tiles = kMaxChunkPages * block_size / kPrefixTileTokens;
     const int chunk_tiles =
@@ -2329,11 +2345,11 @@ extern "C" pkv_status pkv_decode_attention_prefix_shared(
     const dim3 pgrid(pp.row_tiles, std::max(1, num_groups * num_kv_heads), pp.prefix_parts + 1);
     cudaError_t e;
     if (head_dim == 64)
-        e = dtype == PKV_FP16 ? launch_prefix_t<__half, 64>(mk, mv, pr, pgrid, s)
-                              : launch_prefix_t<__nv_bfloat16, 64>(mk, mv, pr, pgrid, s);
+        e = dtype == PKV_FP16 ? launch_prefix_t<__half, 64, kPrefixMode>(mk, mv, pr, pgrid, s)
+                              : launch_prefix_t<__nv_bfloat16, 64, kPrefixMode>(mk, mv, pr, pgrid, s);
     else
-        e = dtype == PKV_FP16 ? launch_prefix_t<__half, 128>(mk, mv, pr, pgrid, s)
-                              : launch_prefix_t<__nv_bfloat16, 128>(mk, mv, pr, pgrid, s);
+        e = dtype == PKV_FP16 ? launch_prefix_t<__half, 128, kPrefixMode>(mk, mv, pr, pgrid, s)
+                              : launch_prefix_t<__nv_bfloat16, 128, kPrefixMode>(mk, mv, pr, pgrid, s);
     if (e != cudaSuccess) {
         cudaGetLastError();
         return PKV_ERR_CUDA;
@@ -2472,11 +2488,11 @@ extern "C" pkv_status pkv_multi_query_attention(
             e = dtype == PKV_FP16 ? launch_prefix_t<__half, 128, kMqDupMode>(mk, mv, pr, pgrid, s)
                                   : launch_prefix_t<__nv_bfloat16, 128, kMqDupMode>(mk, mv, pr, pgrid, s);
     } else if (head_dim == 64) {
-        e = dtype == PKV_FP16 ? launch_prefix_t<__half, 64>(mk, mv, pr, pgrid, s)
-                              : launch_prefix_t<__nv_bfloat16, 64>(mk, mv, pr, pgrid, s);
+        e = dtype == PKV_FP16 ? launch_prefix_t<__half, 64, kMqFullMode>(mk, mv, pr, pgrid, s)
+                              : launch_prefix_t<__nv_bfloat16, 64, kMqFullMode>(mk, mv, pr, pgrid, s);
     } else {
-        e = dtype == PKV_FP16 ? launch_prefix_t<__half, 128>(mk, mv, pr, pgrid, s)
-                              : launch_prefix_t<__nv_bfloat16, 128>(mk, mv, pr, pgrid, s);
+        e = dtype == PKV_FP16 ? launch_prefix_t<__half, 128, kMqFullMode>(mk, mv, pr, pgrid, s)
+                              : launch_prefix_t<__nv_bfloat16, 128, kMqFullMode>(mk, mv, pr, pgrid, s);
     }
     if (e != cudaSuccess) {
         cudaGetLastError();
