@@ -474,6 +474,17 @@ def run_gpu(args):
     d1.record(stream)
     torch.cuda.synchronize(device)
     decode_ms = d0.elapsed_time(d1) / args.steps
+    # The append alone (the scatter of the step's new K/V rows), timed the same way.
+    for _ in range(3):
+        append_call(w.k_new, w.v_new, w.slot_mapping)
+    a0 = torch.cuda.Event(enable_timing=True)
+    a1 = torch.cuda.Event(enable_timing=True)
+    a0.record(stream)
+    for _ in range(args.steps):
+        append_call(w.k_new, w.v_new, w.slot_mapping)
+    a1.record(stream)
+    torch.cuda.synchronize(device)
+    append_ms = a0.elapsed_time(a1) / args.steps
     ms_local = total_ms / args.steps
     ms_step = reduce_over_ranks(ms_local, "max", device)
     bytes_all = reduce_over_ranks(float(nbytes["step"]), "sum", device)
@@ -604,6 +615,8 @@ def run_gpu(args):
         "pct_of_peak": round(100.0 * value / (peak * ws), 2),
         "tokens_per_s": round(tokens_all / (ms_step * 1e-3), 1),
         "decode_ms": round(decode_ms, 5),
+        "append_ms": round(append_ms, 5),
+        "append_gbs": round(nbytes["append"] / (append_ms * 1e-3) / 1e9, 2),
         "roofline": {"bound": "hbm", "achieved": round(decode_gbs, 2), "peak": peak,
                      "unit": "GB/s", "frac": round(decode_gbs / peak, 4),
                      "traffic": traffic,
