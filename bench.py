@@ -55,14 +55,14 @@ WORKLOAD_TEXT = {
 # measured on (digest of csrc/), else reported as null.
 NCU_TRAFFIC = {
     # ncu --metrics dram__bytes_read.sum,dram__bytes_write.sum -k regex:decode_kernel -s 4 -c 1
-    "c2": {"digest": "3cb5a85afd5afd79", "splits": 4, "shared": False,
-           "bytes": 2312808448 + 4363520},
-    "c3": {"digest": "3cb5a85afd5afd79", "splits": 7, "shared": False,
-           "bytes": 537524224 + 5497856},
+    "c2": {"digest": "41e6202e98344c7b", "splits": 4, "shared": False,
+           "bytes": 2312625920 + 4671232},
+    "c3": {"digest": "41e6202e98344c7b", "splits": 5, "shared": False,
+           "bytes": 537495552 + 4641280},
     # shared-prefix path: decode_kernel (suffixes) + prefix_kernel (one --set full
     # capture); the merge kernel's few MB are not included
-    "c5": {"digest": "3cb5a85afd5afd79", "splits": 16, "shared": True,
-           "bytes": (1531731456 + 5720832) + (35770880 + 102656)},
+    "c5": {"digest": "41e6202e98344c7b", "splits": 16, "shared": True,
+           "bytes": (1531715584 + 5754624) + (35772672 + 98816)},
 }
 
 
