@@ -739,21 +739,25 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
 // real contraction, so it runs on tcgen05.  One CTA takes 128 query rows and
 // one prefix partition, in tiles of 64 tokens:
 //   S = Q K^T        tcgen05.mma M=128, N=64, 16-dim steps; S in tensor memory
-//   softmax          one thread per query row, reading its row of S directly
+//   softmax          threads reading their rows of S directly
 //   O += P V         M=128, N=D, 16-token steps; P enters as hi + lo 16-bit
-//                    terms (as in the decode kernel); O stays in tensor memory
-// Warp 8 streams K/V tiles by TMA into a 4-stage ring, warp 9 owns the tensor
-// memory and one of its lanes issues the MMAs, warps 0-7 run the softmax: two
-// threads per query row, one for tokens 0-31 of every tile, one for tokens
-// 32-63.  The two halves are independent online softmaxes with accumulators
-// O_a and O_b of their own in tensor memory (O_a += P[:, 0:32] V[0:32], O_b +=
-// P[:, 32:64] V[32:64]); they meet once, at the end, where the rows' normalised
-// O and log-sum-exp are combined and written as partials.  S is
-// double-buffered, so S of the next tile is computed during this tile's
-// softmax.  A half's reference max is raised (and its O rescaled in tensor
-// memory) only when its running max exceeds it by more than 2^8; P stays
-// below 256 and the final normalisation uses the same references, so the
-// result is the same softmax.
+//                    terms (as in the decode kernel), written by the softmax
+//                    over its S and read as the A operand from tensor memory;
+//                    O stays in tensor memory
+// In MODE 0 (this path) warp 8 streams K/V tiles by TMA into a 4-stage ring,
+// warp 9 owns the tensor memory and one of its lanes issues the MMAs, warps
+// 0-7 run the softmax: two threads per query row, one for tokens 0-31 of every
+// tile, one for tokens 32-63.  The two halves are independent online softmaxes
+// with accumulators O_a and O_b of their own in tensor memory (O_a += P[:, 0:32]
+// V[0:32], O_b += P[:, 32:64] V[32:64]); they meet once, at the end, where the
+// rows' normalised O and log-sum-exp are combined and written as partials.  S
+// (and P over it) is double-buffered, so S of the next tile is computed during
+// this tile's softmax.  A half's reference max is raised (and its O rescaled in
+// tensor memory) only when its running max exceeds it by more than 2^8; P
+// stays below 256 and the final normalisation uses the same references, so
+// the result is the same softmax.  The multi-query path uses the same kernel
+// in MODES 1 and 2 (one softmax thread per tensor-memory lane, two CTAs an SM;
+// see prefix_kernel).
 
 // ---------------------------------------------------------------------------
 // Shared-prefix decode: the plan
