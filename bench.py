@@ -361,6 +361,9 @@ def run_gpu(args):
     splits = pkv.decode_num_splits(s.num_seqs, s.num_q_heads, s.num_kv_heads, s.head_dim,
                                    s.block_size, mcl, args.splits, kv=args.kv)
     if mq:
+        # at most 16 query rows per (sequence, KV head): the decode kernel
+        mq_kernel, mq_parts = pkv.multi_query_plan(s.num_seqs, args.q_len, s.num_q_heads,
+                                                   s.num_kv_heads, s.head_dim, s.block_size, mcl)
         ws_bytes = pkv.multi_query_workspace_size(s.num_seqs, args.q_len, s.num_q_heads,
                                                   s.num_kv_heads, s.head_dim, s.block_size, mcl)
     elif shared:
@@ -377,8 +380,10 @@ def run_gpu(args):
     # (with the plan as one of its CTAs), decode, merge
     # --fused: the append is done by the decode kernel (plain path only)
     fused = args.fused and not mq and not shared
-    launches_per_step = (3 if mq else 4 if shared else
-                         (1 if fused else 2) + (1 if splits > 1 else 0))
+    if mq:
+        launches_per_step = 2 + (1 if mq_kernel == "tcgen05" or mq_parts > 1 else 0)
+    else:
+        launches_per_step = (4 if shared else (1 if fused else 2) + (1 if splits > 1 else 0))
 
     def decode_call(q, block_tables, context_lens, out=out):
         if fp8:
@@ -601,7 +606,7 @@ def run_gpu(args):
                    "num_seqs": s.num_seqs, "num_q_heads": s.num_q_heads,
                    "num_kv_heads": s.num_kv_heads, "head_dim": s.head_dim,
                    "block_size": s.block_size, "context_tokens": int(w.context_lens.sum()),
-                   "max_context_len": mcl, "num_splits": splits, "accumulate": "fp32",
+                   "max_context_len": mcl, "num_splits": mq_parts if mq else splits, "accumulate": "fp32",
                    "shared_prefix_decode": shared,
                    "q_len": args.q_len if mq else 1,
                    "fused_append": fused, "cuda_graph": bool(args.graph),
@@ -620,7 +625,10 @@ def run_gpu(args):
         "roofline": {"bound": "hbm", "achieved": round(decode_gbs, 2), "peak": peak,
                      "unit": "GB/s", "frac": round(decode_gbs / peak, 4),
                      "traffic": traffic,
-                     "kernel": ("prefix_kernel in multi-query mode (tcgen05) + merge_kernel" if mq
+                     "kernel": (("prefix_kernel in multi-query mode (tcgen05) + merge_kernel"
+                                 if mq_kernel == "tcgen05" else
+                                 "decode_kernel in multi-query mode"
+                                 + (" + merge_kernel" if mq_parts > 1 else "")) if mq
                                 else "prefix_kernel (with the plan CTA) + decode_kernel + merge_kernel"
                                 if shared else "decode_kernel + merge_kernel")
                      + " (one attention call, back to back)",

@@ -313,12 +313,28 @@ pkv_status pkv_decode_attention_prefix_shared(
  *   pkv_multi_query_workspace_size(...) bytes (contents on entry do not matter)
  * Limits: num_seqs * num_kv_heads and num_seqs * q_len at most 65535.
  * The (query token, query head) rows of one KV head form a dense matrix that
- * meets every context token, so the products run on the tensor cores
- * (tcgen05, 128 rows per CTA, accumulators in tensor memory), split over
- * context partitions and merged by log-sum-exp as in pkv_merge.
+ * meets every context token.  With at most pkv_max_group_size() rows per
+ * (sequence, KV head) (q_len * num_q_heads / num_kv_heads: verifying a few
+ * drafted tokens, or a small GQA group) the decode kernel serves them as it
+ * serves the heads of a GQA group, streaming the context once at the HBM
+ * rate, with per-row causal limits on the last positions.  With more rows the
+ * products run on the tensor cores (tcgen05, 128 rows per CTA, accumulators
+ * in tensor memory).  Either way the context is split into partitions whose
+ * partials are merged by log-sum-exp as in pkv_merge.
  */
 size_t pkv_multi_query_workspace_size(int num_seqs, int q_len, int num_q_heads, int num_kv_heads,
                                       int head_dim, int block_size, int max_context_len);
+
+/*
+ * The kernel a pkv_multi_query_attention call with these arguments runs on
+ * the current device: 1 for the decode kernel, 0 for the tensor-core kernel,
+ * -1 when the arguments are invalid or the device cannot be queried.  When
+ * num_partitions is not null it receives the context partitions (partial
+ * slots per row are the same, or twice as many on the tensor-core kernel with
+ * at most 64 rows per (sequence, KV head)).
+ */
+int pkv_multi_query_plan(int num_seqs, int q_len, int num_q_heads, int num_kv_heads,
+                         int head_dim, int block_size, int max_context_len, int* num_partitions);
 
 pkv_status pkv_multi_query_attention(
     void* out, const void* q, const void* k_cache, const void* v_cache,

@@ -79,6 +79,7 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
                                                        i, p, p, i, i, p, sz, i, p, p]
     lib.pkv_multi_query_workspace_size.argtypes = [i, i, i, i, i, i, i]
     lib.pkv_multi_query_workspace_size.restype = sz
+    lib.pkv_multi_query_plan.argtypes = [i, i, i, i, i, i, i, ctypes.POINTER(ctypes.c_int)]
     lib.pkv_multi_query_attention.argtypes = [p, p, p, p, p, i, p, i, i, i, i, i, i, i, i, f, p,
                                               sz, i, p, p]
     lib.pkv_merge.argtypes = [p, p, p, i, i, i, i, i, p]
@@ -92,7 +93,7 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
                  "pkv_append_decode_attention", "pkv_append_fp8", "pkv_decode_attention_fp8",
                  "pkv_decode_attention_prefix_shared", "pkv_multi_query_attention",
                  "pkv_merge", "pkv_gather", "pkv_selftest_wait_timeout",
-                 "pkv_check_error", "pkv_max_group_size"):
+                 "pkv_check_error", "pkv_max_group_size", "pkv_multi_query_plan"):
         getattr(lib, name).restype = i
     _lib = lib
     return lib
@@ -390,6 +391,19 @@ def decode_attention_prefix_shared(q: torch.Tensor, k_cache: torch.Tensor, v_cac
         _opt(err_flag, "err_flag"), _stream(stream, q.device))
     _check(st, "pkv_decode_attention_prefix_shared")
     return out
+
+
+def multi_query_plan(num_seqs: int, q_len: int, num_q_heads: int, num_kv_heads: int,
+                     head_dim: int, block_size: int, max_context_len: int) -> tuple:
+    """(kernel, context partitions) of a ``multi_query_attention`` call on the
+    current device: kernel "decode" (at most ``pkv_max_group_size()``, 16, query
+    rows per sequence and KV head) or "tcgen05"."""
+    parts = ctypes.c_int(0)
+    r = load().pkv_multi_query_plan(num_seqs, q_len, num_q_heads, num_kv_heads, head_dim,
+                                    block_size, max_context_len, ctypes.byref(parts))
+    if r < 0:
+        raise PkvError(1, "pkv_multi_query_plan")
+    return ("decode" if r == 1 else "tcgen05"), int(parts.value)
 
 
 def multi_query_workspace_size(num_seqs: int, q_len: int, num_q_heads: int, num_kv_heads: int,

@@ -91,6 +91,7 @@ struct DecodeParams {
     int chunk_tokens;    // tokens per partition (a multiple of 16)
     int num_kv_heads;
     int max_context_len;
+    int q_len;           // > 0 (multi-query): columns are (query token, head), causal
     bool hnd;            // head-major cache layout
     float scale_log2;    // scale * log2(e) (times the K scale of an E4M3 cache)
     float v_scale;       // value of one V unit: 1, or the V scale of an E4M3 cache
@@ -387,8 +388,12 @@ __device__ __forceinline__ void stage_update(uint32_t kbase, uint32_t vbase, int
         v_pass(std::false_type{});
 }
 
-// NT = number of 8-head groups (1: G <= 8, 2: G <= 16); F8: E4M3 cache codes.
-template <typename T, int D, int NT, bool F8 = false>
+// NT = number of 8-column groups (1: up to 8 query rows, 2: up to 16); F8:
+// E4M3 cache codes.  MQ: multi-query, the columns are the (query token i,
+// query head) rows of a chunk of q_len tokens (i * group + head in group), and
+// column i sees positions < n - q_len + 1 + i; only the stages that reach past
+// n - q_len + 1 apply the per-column limits.
+template <typename T, int D, int NT, bool F8 = false, bool MQ = false>
 __global__ void __launch_bounds__(kThreads, (F8 && NT == 1) ? 4 : 3)
 decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
               const DecodeParams p) {
@@ -460,7 +465,8 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
         for (int r = 0; r < 3; ++r)
             if (lane + 32 * r < max_pages) blk_r[r] = __ldg(row + lane + 32 * r);
     }
-    if ((n_raw < 0 || n_raw > cap) && split == 0 && g == 0 && tid == 0)
+    if ((n_raw < 0 || n_raw > cap || (MQ && n_raw < p.q_len)) && split == 0 && g == 0 &&
+        tid == 0)
         flag_error(p.err_flag, PKV_EFLAG_CONTEXT_LEN);
     const int n = clamped_len(n_raw, cap);
     const int suffix = max(0, n - start);
@@ -580,17 +586,23 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
     float o[NT][KSTEPS][4];    // O^T tiles: 16 dims x 8 heads each
     float m0[NT], m1[NT], l0[NT], l1[NT];  // heads 2tq and 2tq+1 of each 8-head group
     if (warp < kConsumerWarps) {
-        // Q^T operand fragments (B of S^T = K Q^T): head nt*8 + gq, dims 2tq.. of each
-        // k-step (for an E4M3 cache, dims 4tq.. and 4tq+2.., the K fragments' order).
+        // Q^T operand fragments (B of S^T = K Q^T): column nt*8 + gq, dims 2tq.. of
+        // each k-step (for an E4M3 cache, dims 4tq.. and 4tq+2.., the K fragments'
+        // order).  A column is a head of the group, or (MQ) a (query token, head).
         uint32_t qb[NT][KSTEPS][2];
-        const T* qbase = static_cast<const T*>(p.q) + ((int64_t)b * p.num_q_heads + g * p.group) * D;
+        const int ncols = MQ ? p.q_len * p.group : p.group;
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt) {
-            const int head = nt * 8 + gq;
-            const uint32_t* qrow = reinterpret_cast<const uint32_t*>(qbase + head * D);
+            const int col = nt * 8 + gq;
+            const bool ok = col < ncols;
+            const int cc = ok ? col : 0;
+            const int64_t qr = MQ ? ((int64_t)b * p.q_len + cc / p.group) * p.num_q_heads +
+                                        g * p.group + cc % p.group
+                                  : (int64_t)b * p.num_q_heads + g * p.group + cc;
+            const uint32_t* qrow =
+                reinterpret_cast<const uint32_t*>(static_cast<const T*>(p.q) + qr * D);
 #pragma unroll
             for (int ks = 0; ks < KSTEPS; ++ks) {
-                const bool ok = head < p.group;
                 const int d0 = F8 ? ks * 16 + 4 * tq : ks * 16 + 2 * tq;
                 const int d1 = F8 ? d0 + 2 : d0 + 8;
                 qb[nt][ks][0] = ok ? __ldg(qrow + d0 / 2) : 0u;
@@ -607,6 +619,20 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
         int no_limit[NT][2];
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt) no_limit[nt][0] = no_limit[nt][1] = INT_MAX;
+        // MQ: the causal limits of this thread's fragment columns 2tq and 2tq+1
+        // (columns past the rows in use get the largest limit: their q is zero
+        // and their results are not written), and the first position that some
+        // column does not see.
+        int lim[NT][2];
+        int causal0 = INT_MAX;
+        if constexpr (MQ) {
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+                for (int k = 0; k < 2; ++k)
+                    lim[nt][k] = max(0, n - p.q_len + 1 + (nt * 8 + 2 * tq + k) / p.group);
+            causal0 = n - p.q_len + 1;
+        }
 
         for (int i = warp; i < nstages; i += kConsumerWarps) {
             const int slot = i % S;
@@ -617,9 +643,14 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
             const int nvalid = blk >= 0 ? min(kStageTokens, t_end - tok0) : 0;
             if (nvalid > 0) {
                 const uint32_t kbase = ring_addr + slot * Cfg::kStageBytes;
-                stage_update<T, D, NT, false, F8>(kbase, kbase + Cfg::kHalfBytes, nvalid, 0,
-                                                  no_limit, qb, o, m0, m1, l0, l1, p.scale_log2,
-                                                  lane);
+                if (MQ && tok0 + kStageTokens > causal0)
+                    stage_update<T, D, NT, true, F8>(kbase, kbase + Cfg::kHalfBytes, nvalid, tok0,
+                                                     lim, qb, o, m0, m1, l0, l1, p.scale_log2,
+                                                     lane);
+                else
+                    stage_update<T, D, NT, false, F8>(kbase, kbase + Cfg::kHalfBytes, nvalid, 0,
+                                                      no_limit, qb, o, m0, m1, l0, l1,
+                                                      p.scale_log2, lane);
             }
             __syncwarp();
             if (lane == 0) ptx::mbar_arrive(ptx::smem_addr(&empty_bar[slot]));
@@ -671,9 +702,9 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
         }
         ptx::named_barrier_sync(1, kConsumerWarps * 32);
 
-        // Per-head combine factors, once per head: c_w = e^(m_w - m*) / L with
-        // L = sum_w e^(m_w - m*) l_w, and the head's log-sum-exp.
-        const int G = p.group;
+        // Per-column combine factors, once per column: c_w = e^(m_w - m*) / L with
+        // L = sum_w e^(m_w - m*) l_w, and the column's log-sum-exp.
+        const int G = MQ ? p.q_len * p.group : p.group;
         float* sm_f = sm_l + kConsumerWarps * HP;   // [HP][warps]
         float* sm_lse = sm_f + HP * kConsumerWarps; // [HP]
         if (tid < G) {
@@ -710,16 +741,19 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
                 acc.z = fmaf(v.z, f, acc.z);
                 acc.w = fmaf(v.w, f, acc.w);
             }
-            const int hq = g * G + h;
+            // (row of q, query head) of the column: rows of q are sequences, or
+            // (sequence, query token) with MQ
+            const int64_t orow = MQ ? ((int64_t)b * p.q_len + h / p.group) * p.num_q_heads +
+                                          g * p.group + h % p.group
+                                    : (int64_t)b * p.num_q_heads + g * G + h;
             if (direct) {
-                T* out = static_cast<T*>(p.out) + ((int64_t)b * p.num_q_heads + hq) * D + j;
+                T* out = static_cast<T*>(p.out) + orow * D + j;
                 uint2 packed;
                 packed.x = pack2(acc.x, acc.y, T());
                 packed.y = pack2(acc.z, acc.w, T());
                 *reinterpret_cast<uint2*>(out) = packed;
             } else {
-                const int64_t prow =
-                    ((int64_t)b * p.num_q_heads + hq) * p.num_splits + slot0 + split;
+                const int64_t prow = orow * p.num_splits + slot0 + split;
                 *reinterpret_cast<float4*>(p.partial_o + prow * D + j) = acc;
                 if (j == 0) p.partial_lse[prow] = sm_lse[h];
             }
@@ -1558,9 +1592,11 @@ prefix_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
 // and the merge of a call is a few thousand of them.  With context_lens given
 // (the decode path), a sequence whose context fitted a single partition was
 // written by the decode kernel and is skipped, and only the partitions that
-// hold tokens are read.  Multi-query rows (q_len > 0) are always merged, from
-// the partitions of their sequence's context.  Without context_lens
-// (pkv_merge), every row merges all num_splits partials.
+// hold tokens are read.  Multi-query rows (q_len > 0) are merged from the
+// partitions of their sequence's context; with mq_direct (the decode kernel's
+// multi-query form) a context that fitted one partition was written directly
+// and is skipped.  Without context_lens (pkv_merge), every row merges all
+// num_splits partials.
 struct MergeParams {
     void* out;
     const float* partial_o;
@@ -1574,8 +1610,9 @@ struct MergeParams {
     int head_dim;                 // a multiple of 4, at most 512
     int chunk_tokens;
     int cap;                      // context clamp, as in the decode kernel
-    int q_len;                    // > 0: multi-query rows (sequence, query token); every row merged
+    int q_len;                    // > 0: multi-query rows (sequence, query token)
     int mq_slots;                 // multi-query: partial slots per context partition (1 or 2)
+    bool mq_direct;               // multi-query partials of the decode kernel (single ones direct)
     int64_t rows;                 // (row of q, query head) pairs
 };
 
@@ -1596,7 +1633,12 @@ merge_kernel(const MergeParams p) {
     if (p.q_len > 0) {
         // multi-query partials: the partitions of the sequence's context
         const int n = clamped_len(__ldg(p.context_lens + b / p.q_len), p.cap);
-        ns = (n + p.chunk_tokens - 1) / p.chunk_tokens * p.mq_slots;
+        if (p.mq_direct) {
+            ns = suffix_partitions(n, 0, p.chunk_tokens);
+            if (ns <= 1) return;  // written directly by the decode kernel
+        } else {
+            ns = (n + p.chunk_tokens - 1) / p.chunk_tokens * p.mq_slots;
+        }
     } else if (p.context_lens != nullptr) {
         int start = 0, slot0 = 0;
         if (p.seq_info != nullptr) {
@@ -1816,10 +1858,10 @@ static bool make_cache_map(CUtensorMap* map, const void* base, pkv_dtype dtype, 
     return r == CUDA_SUCCESS;
 }
 
-template <typename T, int D, int NT, bool F8>
+template <typename T, int D, int NT, bool F8, bool MQ = false>
 static cudaError_t launch_decode_t(const CUtensorMap& mk, const CUtensorMap& mv,
                                    const DecodeParams& p, dim3 grid, cudaStream_t stream) {
-    auto kern = decode_kernel<T, D, NT, F8>;
+    auto kern = decode_kernel<T, D, NT, F8, MQ>;
     static std::once_flag once;
     static cudaError_t attr_err = cudaSuccess;
     std::call_once(once, [&] {
@@ -1854,6 +1896,19 @@ static cudaError_t launch_decode(const CUtensorMap& mk, const CUtensorMap& mv,
                     : launch_decode_t<T, 64, 1, false>(mk, mv, p, grid, stream);
     return wide ? launch_decode_t<T, 128, 2, false>(mk, mv, p, grid, stream)
                 : launch_decode_t<T, 128, 1, false>(mk, mv, p, grid, stream);
+}
+
+// Multi-query rows on the decode kernel: q_len * group <= 16 columns.
+template <typename T>
+static cudaError_t launch_decode_mq(const CUtensorMap& mk, const CUtensorMap& mv,
+                                    const DecodeParams& p, int head_dim, dim3 grid,
+                                    cudaStream_t stream) {
+    const bool wide = p.q_len * p.group > 8;
+    if (head_dim == 64)
+        return wide ? launch_decode_t<T, 64, 2, false, true>(mk, mv, p, grid, stream)
+                    : launch_decode_t<T, 64, 1, false, true>(mk, mv, p, grid, stream);
+    return wide ? launch_decode_t<T, 128, 2, false, true>(mk, mv, p, grid, stream)
+                : launch_decode_t<T, 128, 1, false, true>(mk, mv, p, grid, stream);
 }
 
 template <typename T>
@@ -1956,10 +2011,14 @@ static pkv_status make_prefix_plan(int num_seqs, int num_q_heads, int num_kv_hea
     return PKV_OK;
 }
 
-// Plan of a multi-query call: 128-row tiles of (query token, query head) rows
-// per (sequence, KV head); the context in partitions of whole 64-token tiles,
+// Plan of a multi-query call.  At most kMaxGroup (query token, query head)
+// rows per (sequence, KV head) (speculative verification of a few tokens, a
+// small GQA group or MHA): the decode kernel with those rows as its columns,
+// planned like a decode.  More rows: 128-row tiles per (sequence, KV head) on
+// the tensor-core kernel; the context in partitions of whole 64-token tiles,
 // as many as give about one CTA per SM, at most kMaxChunkPages pages each.
 struct MultiQueryPlan {
+    bool on_decode;  // the decode kernel's multi-query form
     int chunk;
     int parts;
     int row_tiles;
@@ -1981,6 +2040,23 @@ static pkv_status make_mq_plan(int num_seqs, int q_len, int num_q_heads, int num
     if ((int64_t)num_seqs * num_kv_heads > 65535 || mp->row_tiles > 65535 ||
         (int64_t)num_seqs * q_len > 65535)
         return PKV_ERR_UNSUPPORTED;
+    mp->on_decode = rows <= kMaxGroup;
+    if (mp->on_decode) {
+        Plan dp;
+        st = make_plan(num_seqs, num_q_heads, num_kv_heads, head_dim, block_size,
+                       max_context_len, 0, &dp);
+        if (st != PKV_OK) return st;
+        mp->dup = false;
+        mp->chunk = dp.chunk_tokens;
+        mp->parts = dp.num_splits;
+        mp->slots = dp.num_splits;
+        mp->workspace_bytes =
+            (mp->parts > 1
+                 ? (size_t)num_seqs * q_len * num_q_heads * mp->slots * (head_dim + 1) * sizeof(float)
+                 : 0) +
+            256;
+        return PKV_OK;
+    }
     const int sms = current_sm_count();
     if (sms <= 0) return PKV_ERR_CUDA;
     mp->dup = rows <= kPrefixTileRows / 2;
@@ -2424,6 +2500,17 @@ extern "C" size_t pkv_multi_query_workspace_size(int num_seqs, int q_len, int nu
     return mp.workspace_bytes;
 }
 
+extern "C" int pkv_multi_query_plan(int num_seqs, int q_len, int num_q_heads, int num_kv_heads,
+                                    int head_dim, int block_size, int max_context_len,
+                                    int* num_partitions) {
+    MultiQueryPlan mp;
+    if (make_mq_plan(num_seqs, q_len, num_q_heads, num_kv_heads, head_dim, block_size,
+                     max_context_len, &mp) != PKV_OK)
+        return -1;
+    if (num_partitions != nullptr) *num_partitions = mp.parts;
+    return mp.on_decode ? 1 : 0;
+}
+
 extern "C" pkv_status pkv_multi_query_attention(
     void* out, const void* q, const void* k_cache, const void* v_cache,
     const int32_t* block_tables, int max_blocks_per_seq, const int32_t* context_lens,
@@ -2460,6 +2547,65 @@ extern "C" pkv_status pkv_multi_query_attention(
     const int cap = std::min(max_blocks_per_seq * block_size, max_context_len);
     const int group = num_q_heads / num_kv_heads;
     cudaStream_t s = (cudaStream_t)stream;
+    cudaError_t e;
+
+    if (mq.on_decode) {
+        // 1. every row's attention (contexts of one partition) or its partials
+        DecodeParams p = {};
+        p.out = out;
+        p.q = q;
+        p.block_tables = block_tables;
+        p.context_lens = context_lens;
+        p.err_flag = err_flag;
+        p.max_blocks_per_seq = max_blocks_per_seq;
+        p.num_blocks = num_blocks;
+        p.block_size = block_size;
+        p.num_q_heads = num_q_heads;
+        p.group = group;
+        p.num_splits = mq.parts;
+        p.chunk_tokens = mq.chunk;
+        p.num_kv_heads = num_kv_heads;
+        p.max_context_len = max_context_len;
+        p.q_len = q_len;
+        p.hnd = hnd;
+        p.scale_log2 = scale * kLog2e;
+        p.v_scale = 1.f;
+        if (mq.parts > 1) {
+            p.partial_o = partial_o;
+            p.partial_lse = partial_lse;
+        }
+        const dim3 grid(num_kv_heads, num_seqs, mq.parts);
+        e = dtype == PKV_FP16 ? launch_decode_mq<__half>(mk, mv, p, head_dim, grid, s)
+                              : launch_decode_mq<__nv_bfloat16>(mk, mv, p, head_dim, grid, s);
+        if (e != cudaSuccess) {
+            cudaGetLastError();
+            return PKV_ERR_CUDA;
+        }
+        if (mq.parts == 1) return PKV_OK;
+        // 2. merge the rows of contexts longer than one partition
+        MergeParams mp = {};
+        mp.out = out;
+        mp.partial_o = partial_o;
+        mp.partial_lse = partial_lse;
+        mp.context_lens = context_lens;
+        mp.num_q_heads = num_q_heads;
+        mp.num_kv_heads = num_kv_heads;
+        mp.group = group;
+        mp.num_splits = mq.parts;
+        mp.head_dim = head_dim;
+        mp.chunk_tokens = mq.chunk;
+        mp.cap = cap;
+        mp.q_len = q_len;
+        mp.mq_slots = 1;
+        mp.mq_direct = true;
+        e = dtype == PKV_FP16 ? launch_merge<__half>(mp, num_q_heads, num_seqs * q_len, s)
+                              : launch_merge<__nv_bfloat16>(mp, num_q_heads, num_seqs * q_len, s);
+        if (e != cudaSuccess) {
+            cudaGetLastError();
+            return PKV_ERR_CUDA;
+        }
+        return PKV_OK;
+    }
 
     // 1. partials of every (query token, query head) row per context partition (tcgen05)
     PrefixParams pr = {};
@@ -2483,7 +2629,6 @@ extern "C" pkv_status pkv_multi_query_attention(
     pr.hnd = hnd;
     pr.scale_log2 = scale * kLog2e;
     const dim3 pgrid(mq.row_tiles, num_seqs * num_kv_heads, mq.parts);
-    cudaError_t e;
     if (mq.dup) {
         if (head_dim == 64)
             e = dtype == PKV_FP16 ? launch_prefix_t<__half, 64, kMqDupMode>(mk, mv, pr, pgrid, s)

@@ -90,6 +90,10 @@ def test_workspace_size_rejects_bad_arguments(lib):
     assert lib.pkv_decode_num_splits(2, 4, 2, 64, 16, 64, 8) == 4     # no more than the pages
     assert lib.pkv_decode_num_splits_fp8(2, 4, 2, 64, 16, 64, 3) == 2
     assert lib.pkv_decode_num_splits_fp8(2, 4, 2, 64, 16, 64, 2000) == -1
+    parts = ctypes.c_int(0)
+    assert lib.pkv_multi_query_plan(2, 0, 4, 2, 64, 16, 64, ctypes.byref(parts)) == -1  # q_len 0
+    assert lib.pkv_multi_query_plan(2, 4, 4, 2, 96, 16, 64, None) == -1  # head_dim 96
+    assert lib.pkv_multi_query_plan(2, 4, 5, 2, 64, 16, 64, None) == -1  # heads not a multiple
 
 
 def _multi_query(lib, **kw):

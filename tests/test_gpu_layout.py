@@ -98,13 +98,14 @@ def test_shared_prefix_on_head_major_cache_with_64_token_pages():
     assert_attention_close(out, expect, "shared prefix, head-major, bs 64")
 
 
-def test_multi_query_on_head_major_cache_with_128_token_pages():
+@pytest.mark.parametrize("q_len", [6, 2])  # 48 rows: tensor-core kernel; 16: decode kernel
+def test_multi_query_on_head_major_cache_with_128_token_pages(q_len):
     case = dict(DECODE["gqa8_bf16_bs128"])
     w = make_workload(case.pop("name"), device="cuda", poison=True, **case)
     _, kc, vc = oracle_after_append(w)
     kh, vh = to_head_major(w.k_cache), to_head_major(w.v_cache)
     pkv.append(w.k_new, w.v_new, kh, vh, w.slot_mapping, layout="hnd")
-    q = make_queries(w, 6, seed=15)
+    q = make_queries(w, q_len, seed=15)
     flag = pkv.new_error_flag("cuda")
     out = pkv.multi_query_attention(q, kh, vh, w.block_tables, w.context_lens, w.max_context_len,
                                     scale=w.scale, err_flag=flag, layout="hnd")

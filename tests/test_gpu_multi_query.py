@@ -36,6 +36,17 @@ CASES = {
                                 max_len_cap=2688, seed=66),
     "gqa8_q9_rows72": dict(name="c3", q_len=9, num_seqs=3, lengths=("uniform", 60, 900),
                            max_len_cap=960, seed=67),
+    # At most 16 (query token, head) rows per (sequence, KV head) run on the
+    # decode kernel (rows as its columns): one and two 8-column groups, one
+    # partition (direct output) and several (partials + merge); 17 rows are
+    # the tensor-core kernel's again.
+    "mha_q4_split_merge": dict(name="c2", q_len=4, num_seqs=3, num_q_heads=4, num_kv_heads=4,
+                               lengths=("uniform", 1500, 4000), max_len_cap=4096, seed=68),
+    "gqa8_q2_rows16": dict(name="c3", q_len=2, num_seqs=3, lengths=("uniform", 100, 1800),
+                           max_len_cap=1856, seed=69),
+    "gqa2_q8_fp16_d64_rows16": dict(name="c1", q_len=8),
+    "mha_q17_rows17": dict(name="c2", q_len=17, num_seqs=2, num_q_heads=4, num_kv_heads=4,
+                           lengths=("uniform", 30, 400), max_len_cap=448, seed=70),
 }
 
 
@@ -123,3 +134,35 @@ def test_full_size_llama70b_layer_speculative_verify_sampled():
                                           w.spec.dtype)
     assert_attention_close(out[torch.as_tensor(seqs, device="cuda")], expect, "c3 q_len 8")
     assert torch.isfinite(out).all()
+
+
+def test_full_size_llama7b_layer_four_token_verify_sampled():
+    """C2 (Llama-7B MHA layer, 64 sequences of 512-4096 tokens) with 4 query
+    tokens per sequence: 4 rows per (sequence, KV head), the decode kernel's
+    multi-query form, checked on sampled sequences."""
+    w = make_workload("c2", device="cuda")
+    kc, vc = _appended(w)
+    q_len = 4
+    q = make_queries(w, q_len, seed=16)
+    flag = pkv.new_error_flag("cuda")
+    out = pkv.multi_query_attention(q, w.k_cache, w.v_cache, w.block_tables, w.context_lens,
+                                    w.max_context_len, scale=w.scale, err_flag=flag)
+    assert pkv.check_error(flag) == 0
+    cl = w.context_lens.cpu().numpy()
+    seqs = np.array([int(np.argmin(cl)), 17, 40, int(np.argmax(cl))])
+    expect = oracle.multi_query_attention(bits(q)[seqs], kc, vc,
+                                          w.block_tables.cpu().numpy()[seqs], cl[seqs], w.scale,
+                                          w.spec.dtype)
+    assert_attention_close(out[torch.as_tensor(seqs, device="cuda")], expect, "c2 q_len 4")
+    assert torch.isfinite(out).all()
+
+
+def test_rows_per_kv_head_choose_the_kernel():
+    """Up to 16 (query token, head) rows per (sequence, KV head) go to the decode
+    kernel, planned like a decode; more go to the tensor-core kernel."""
+    kernel, parts = pkv.multi_query_plan(64, 4, 32, 32, 128, 16, 4096)
+    assert kernel == "decode"
+    assert parts == pkv.decode_num_splits(64, 32, 32, 128, 16, 4096)
+    assert pkv.multi_query_plan(32, 2, 64, 8, 128, 16, 4096)[0] == "decode"    # 16 rows
+    assert pkv.multi_query_plan(32, 3, 64, 8, 128, 16, 4096)[0] == "tcgen05"   # 24 rows
+    assert pkv.multi_query_plan(2, 17, 4, 4, 128, 16, 448)[0] == "tcgen05"     # 17 rows
