@@ -789,9 +789,10 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
 // this tile's softmax.  A half's reference max is raised (and its O rescaled in
 // tensor memory) only when its running max exceeds it by more than 2^8; P
 // stays below 256 and the final normalisation uses the same references, so
-// the result is the same softmax.  The multi-query path uses the same kernel
-// in MODES 1 and 2 (one softmax thread per tensor-memory lane, two CTAs an SM;
-// see prefix_kernel).
+// the result is the same softmax.  Multi-query calls with more than 16 rows per
+// (sequence, KV head) use the same kernel in MODES 1 and 2 (one softmax thread
+// per tensor-memory lane, two CTAs an SM; see prefix_kernel); smaller ones run
+// on the decode kernel.
 
 // ---------------------------------------------------------------------------
 // Shared-prefix decode: the plan
