@@ -91,10 +91,10 @@ struct DecodeParams {
     int chunk_tokens;    // tokens per partition (a multiple of 16)
     int num_kv_heads;
     int max_context_len;
-    int q_len;           // > 0 (multi-query): columns are (query token, head), causal
     bool hnd;            // head-major cache layout
     float scale_log2;    // scale * log2(e) (times the K scale of an E4M3 cache)
     float v_scale;       // value of one V unit: 1, or the V scale of an E4M3 cache
+    int q_len;           // > 0 (multi-query): columns are (query token, head), causal
 };
 
 // Context length of sequence b as the kernels use it: negative or too long
@@ -591,18 +591,21 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
         // order).  A column is a head of the group, or (MQ) a (query token, head).
         uint32_t qb[NT][KSTEPS][2];
         const int ncols = MQ ? p.q_len * p.group : p.group;
+        // the first row of the CTA's block of q: head g*group of the sequence (MQ:
+        // of its first query token)
+        const T* qbase = static_cast<const T*>(p.q) +
+                         ((int64_t)b * (MQ ? p.q_len : 1) * p.num_q_heads + g * p.group) * D;
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt) {
             const int col = nt * 8 + gq;
-            const bool ok = col < ncols;
-            const int cc = ok ? col : 0;
-            const int64_t qr = MQ ? ((int64_t)b * p.q_len + cc / p.group) * p.num_q_heads +
-                                        g * p.group + cc % p.group
-                                  : (int64_t)b * p.num_q_heads + g * p.group + cc;
-            const uint32_t* qrow =
-                reinterpret_cast<const uint32_t*>(static_cast<const T*>(p.q) + qr * D);
+            // rows of q after the first: the column's head, or (MQ) its query
+            // token's rows of all heads plus its head
+            const int cc = MQ && col >= ncols ? 0 : col;
+            const int off = MQ ? (cc / p.group) * p.num_q_heads + cc % p.group : col;
+            const uint32_t* qrow = reinterpret_cast<const uint32_t*>(qbase + off * D);
 #pragma unroll
             for (int ks = 0; ks < KSTEPS; ++ks) {
+                const bool ok = col < ncols;
                 const int d0 = F8 ? ks * 16 + 4 * tq : ks * 16 + 2 * tq;
                 const int d1 = F8 ? d0 + 2 : d0 + 8;
                 qb[nt][ks][0] = ok ? __ldg(qrow + d0 / 2) : 0u;
@@ -743,9 +746,10 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
             }
             // (row of q, query head) of the column: rows of q are sequences, or
             // (sequence, query token) with MQ
-            const int64_t orow = MQ ? ((int64_t)b * p.q_len + h / p.group) * p.num_q_heads +
-                                          g * p.group + h % p.group
-                                    : (int64_t)b * p.num_q_heads + g * G + h;
+            const int64_t orow =
+                MQ ? ((int64_t)b * p.q_len + h / p.group) * p.num_q_heads + g * p.group +
+                         h % p.group
+                   : (int64_t)b * p.num_q_heads + (g * G + h);
             if (direct) {
                 T* out = static_cast<T*>(p.out) + orow * D + j;
                 uint2 packed;
