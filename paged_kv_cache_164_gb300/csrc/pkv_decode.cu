@@ -861,6 +861,9 @@ struct PrefixParams {
 constexpr int kPrefixTileRows = 128;     // query rows per CTA (MMA M)
 constexpr int kPrefixTileTokens = 64;    // tokens per tile (N of S, K of O)
 constexpr int kPrefixStages = 4;
+// Multi-query modes: ring stages (Q lives in tensor memory, so the ring takes
+// the shared memory two CTAs an SM leave).
+template <int D> constexpr int mq_stages() { return D == 64 ? 6 : 3; }
 constexpr int kPrefixSoftmaxWarps = 8;   // two threads per query row (token halves)
 constexpr int kPrefixThreads = (kPrefixSoftmaxWarps + 2) * 32;
 constexpr int kPrefixTmaWarp = kPrefixSoftmaxWarps;
@@ -871,7 +874,9 @@ template <int D, int NSTG = kPrefixStages, bool ONE_ACC = false>
 struct PrefixTile {
     static constexpr int kRegions = D / 64;                            // 128-byte column blocks
     static constexpr int kQRegionBytes = kPrefixTileRows * 128;
-    static constexpr int kQBytes = kRegions * kQRegionBytes;
+    // ONE_ACC (multi-query modes): Q is the A operand of S from tensor memory,
+    // none of it in shared memory
+    static constexpr int kQBytes = ONE_ACC ? 0 : kRegions * kQRegionBytes;
     static constexpr int kKVRegionBytes = kPrefixTileTokens * 128;     // 64 tokens x 64 dims
     static constexpr int kHalfBytes = kRegions * kKVRegionBytes;       // K (or V) of one tile
     static constexpr int kStageBytes = 2 * kHalfBytes;
@@ -881,12 +886,15 @@ struct PrefixTile {
     static constexpr int kSmemBytes = 1024 + kQBytes + NSTG * kStageBytes + kXchBytes +
                                       kBarriers * 8 + (kMaxChunkPages + 1) * 4 + 64;
     // S0, S1 (64 columns each; P of the tile overwrites its S as hi/lo 16-bit
-    // pairs), O_a, O_b (D columns each; with ONE_ACC only O_a)
+    // pairs), O_a, O_b (D columns each).  ONE_ACC: one S/P buffer, Q as 16-bit
+    // pairs (D/2 columns) where S1 would be, and only O_a.
+    static constexpr uint32_t kColQ = kPrefixTileTokens;
     static constexpr uint32_t kColOa = 2 * kPrefixTileTokens;
     static constexpr uint32_t kColOb = kColOa + D;
     static constexpr uint32_t kTmemEnd = ONE_ACC ? kColOa + D : kColOb + D;
     static constexpr uint32_t kTmemCols = kTmemEnd <= 256 ? 256 : 512;
     static_assert(kTmemEnd <= kTmemCols, "tensor memory layout");
+    static_assert(!ONE_ACC || kColQ + D / 2 <= kColOa, "Q fits between S and O");
 };
 
 // Instruction descriptor of tcgen05.mma kind::f16: fp32 accumulator, A and B
@@ -1040,7 +1048,8 @@ prefix_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
     constexpr bool ONE = MODE != 0;   // one thread per lane, one accumulator, two CTAs an SM
     constexpr bool PAIR = MODE == 1;  // rows 64-127 repeat rows 0-63
     constexpr int SW = ONE ? 4 : kPrefixSoftmaxWarps;  // softmax warps; then the TMA and MMA warps
-    constexpr int NS = ONE ? 2 : kPrefixStages;
+    constexpr int NS = ONE ? mq_stages<D>() : kPrefixStages;
+    constexpr int NSB = ONE ? 1 : 2;  // S/P buffers: tile j uses buffer j % NSB
     using Cfg = PrefixTile<D, NS, ONE>;
     constexpr int R = Cfg::kRegions;
     constexpr int KSTEPS = D / 16;
@@ -1055,7 +1064,9 @@ prefix_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
     uint64_t* bars = reinterpret_cast<uint64_t*>(ring + NS * Cfg::kStageBytes + Cfg::kXchBytes);
     uint64_t* full_bar = bars;
     uint64_t* empty_bar = bars + NS;
-    // Tile j uses S/P buffer j % 2 with its own s_full and p_ready barriers: a
+    // MODE 0: tile j uses S/P buffer j % 2 with its own s_full and p_ready
+    // barriers (MODES 1-2: the one buffer and barrier 0, S(j) issued after
+    // P V(j-1), so S(j) completing implies P V(j-1) has).  MODE 0: a
     // softmax thread passes S(j+1) only after P V(j-1) was issued, i.e. after
     // p_ready of buffer (j+1) % 2 completed for tile j-1, so its arrival for
     // tile j+1 never lands in an earlier tile's phase.
@@ -1198,6 +1209,8 @@ prefix_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
     const int ntiles = (t_end - t_begin + TT - 1) / TT;
     const uint32_t ring_addr = ptx::smem_addr(ring);
     const uint32_t q_addr = ptx::smem_addr(sq);
+    auto sbuf = [](int j) { return j % NSB; };          // S/P buffer of tile j
+    auto sphase = [](int j) { return (j / NSB) & 1; };  // its barriers' phase parity
 
     if (warp == SW) {
         // ------------------------------------------------------------ producer
@@ -1262,12 +1275,18 @@ prefix_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
 #pragma unroll
                 for (int ks = 0; ks < KSTEPS; ++ks) {
                     const uint32_t koff = (ks / 4) * Cfg::kQRegionBytes + (ks % 4) * 32;
-                    const uint64_t a = ptx::smem_desc_sw128(q_addr + koff, 16, 1024);
                     const uint64_t b = ptx::smem_desc_sw128(
                         kb + (ks / 4) * Cfg::kKVRegionBytes + (ks % 4) * 32, 16, 1024);
-                    ptx::tc_mma_f16(tmem + (j % 2) * TT, a, b, idesc_s, ks > 0 ? 1u : 0u);
+                    if constexpr (ONE) {
+                        // A = Q from tensor memory: 16 dims = 8 columns a step
+                        ptx::tc_mma_f16_ts(tmem, tmem + Cfg::kColQ + ks * 8, b, idesc_s,
+                                           ks > 0 ? 1u : 0u);
+                    } else {
+                        const uint64_t a = ptx::smem_desc_sw128(q_addr + koff, 16, 1024);
+                        ptx::tc_mma_f16(tmem + (j % 2) * TT, a, b, idesc_s, ks > 0 ? 1u : 0u);
+                    }
                 }
-                ptx::tc_commit(ptx::smem_addr(&s_full[j % 2]));
+                ptx::tc_commit(ptx::smem_addr(&s_full[sbuf(j)]));
             };
             // O += P(j) V(j) (the softmax has written P(j))
             auto issue_pv = [&](int j) {
@@ -1284,7 +1303,7 @@ prefix_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
                     const uint64_t b = ptx::smem_desc_sw128(vb + kt * 16 * 128, Cfg::kKVRegionBytes, 1024);
                     // tokens 16kt.. of P: unit u's hi pairs at u*HTK, lo pairs HTK/2 on
                     const int u = kt * 16 / HTK;
-                    const uint32_t a_hi = tmem + (j % 2) * TT + u * HTK + (kt * 16 % HTK) / 2;
+                    const uint32_t a_hi = tmem + sbuf(j) * TT + u * HTK + (kt * 16 % HTK) / 2;
                     ptx::tc_mma_f16_ts(acc, a_hi, b, idesc_o, keep);
                     ptx::tc_mma_f16_ts(acc, a_hi + HTK / 2, b, idesc_o, 1u);
                 }
@@ -1292,21 +1311,21 @@ prefix_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
                 ptx::tc_commit(ptx::smem_addr(&empty_bar[j % NS]));
             };
             if constexpr (ONE) {
-                // With a 2-stage ring, S(j+2) often waits for its copy: one thread
-                // issues both kinds as their inputs become ready, so a product
-                // whose P is written never queues behind it.  S(j) may start once
-                // P V(j-2), the last reader of its buffer, is issued (the tensor
-                // core runs them in order).
+                // One thread issues both kinds as their inputs become ready, so
+                // a product whose P is written never queues behind an S whose
+                // copy is in flight.  S(j) may start once P V(j-1), the last
+                // reader of the one S/P buffer, is issued (the tensor core runs
+                // them in order).
                 int next_s = 0, next_pv = 0;
                 uint64_t t_last = ptx::globaltimer();
                 while (ok && next_pv < ntiles) {
                     bool moved = false;
                     if (next_pv < next_s &&
-                        ptx::mbar_try_wait(ptx::smem_addr(&p_ready[next_pv % 2]), (next_pv / 2) & 1)) {
+                        ptx::mbar_try_wait(ptx::smem_addr(&p_ready[sbuf(next_pv)]), sphase(next_pv))) {
                         issue_pv(next_pv++);
                         moved = true;
                     }
-                    if (next_s < ntiles && next_s < next_pv + 2 &&
+                    if (next_s < ntiles && next_s < next_pv + NSB &&
                         ptx::mbar_try_wait(ptx::smem_addr(&full_bar[next_s % NS]), (next_s / NS) & 1)) {
                         issue_s(next_s++);
                         moved = true;
@@ -1331,7 +1350,7 @@ prefix_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
                     if (ok) issue_s(j);
                 }
                 for (int j = 0; j < ntiles && ok; ++j) {
-                    if (!wait_phase(ptx::smem_addr(&p_ready[j % 2]), (j / 2) & 1, abort_flag,
+                    if (!wait_phase(ptx::smem_addr(&p_ready[sbuf(j)]), sphase(j), abort_flag,
                                     p.err_flag)) {
                         ok = false;
                         break;
@@ -1356,10 +1375,21 @@ prefix_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
         constexpr int HB = HT / kStageTokens;         // 16-token boxes per thread
         // this thread's tokens of every tile: unit `unit` of HT tokens
         const int unit = PAIR ? dcopy : MODE == 2 ? 0 : half;
-        // This thread's half of its row of Q into shared memory (16-byte chunk
-        // c of a 128-byte row lands at chunk c ^ (row % 8): the 128-byte
-        // swizzle of the MMA operand).
-        {
+        const uint32_t lane_base = (uint32_t)(32 * (warp % 4)) << 16;
+        if constexpr (ONE) {
+            // This thread's row of Q into its tensor-memory lane, dims 2c and
+            // 2c+1 in column kColQ + c (the A operand layout of S = Q K^T).
+            static_assert(QV % 8 == 0, "whole 32-column stores");
+#pragma unroll
+            for (int h = 0; h < QV / 8; ++h)
+                ptx::tmem_st32(tmem + lane_base + Cfg::kColQ + h * 32,
+                               *reinterpret_cast<const uint32_t(*)[32]>(qv + h * 8));
+            ptx::tc_fence_before_sync();
+            ptx::mbar_arrive(ptx::smem_addr(q_ready));
+        } else {
+            // This thread's half of its row of Q into shared memory (16-byte
+            // chunk c of a 128-byte row lands at chunk c ^ (row % 8): the
+            // 128-byte swizzle of the MMA operand).
 #pragma unroll
             for (int k = 0; k < QV; ++k) {
                 const int c = half * QV + k;
@@ -1369,13 +1399,12 @@ prefix_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
             ptx::fence_proxy_async_smem();
             ptx::mbar_arrive(ptx::smem_addr(q_ready));
         }
-        const uint32_t lane_base = (uint32_t)(32 * (warp % 4)) << 16;
         const uint32_t col_o = (half && !ONE) ? Cfg::kColOb : Cfg::kColOa;  // this thread's accumulator
         float m_ref = -INFINITY;  // reference max of this half's P (log2 domain)
         float l = 0.f;
         bool ok = true;
         for (int j = 0; j < ntiles; ++j) {
-            if (!warp_wait_phase(ptx::smem_addr(&s_full[j % 2]), (j / 2) & 1, abort_flag,
+            if (!warp_wait_phase(ptx::smem_addr(&s_full[sbuf(j)]), sphase(j), abort_flag,
                                  p.err_flag)) {
                 ok = false;
                 break;
@@ -1384,7 +1413,7 @@ prefix_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
             uint32_t sv[HT];
 #pragma unroll
             for (int h = 0; h < HT / 32; ++h)
-                ptx::tmem_ld32(tmem + lane_base + (j % 2) * TT + unit * HT + h * 32,
+                ptx::tmem_ld32(tmem + lane_base + sbuf(j) * TT + unit * HT + h * 32,
                                *reinterpret_cast<uint32_t(*)[32]>(sv + h * 32));
             const int tile0 = t_begin + j * TT;
             const int h0 = tile0 + unit * HT;  // first token of this thread's unit
@@ -1468,7 +1497,7 @@ prefix_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
                     split_hi_lo(sc[2 * e], sc[2 * e + 1], pv[e], pv[HT / 2 + e], T());
 #pragma unroll
                 for (int h = 0; h < HT / 32; ++h)
-                    ptx::tmem_st32(tmem + lane_base + (j % 2) * TT + unit * HT + h * 32,
+                    ptx::tmem_st32(tmem + lane_base + sbuf(j) * TT + unit * HT + h * 32,
                                    *reinterpret_cast<const uint32_t(*)[32]>(pv + h * 32));
                 if constexpr (PAIR) {
                     // The other copy's half of this lane (S values no thread reads)
@@ -1476,7 +1505,7 @@ prefix_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
                     uint32_t z[HT];
 #pragma unroll
                     for (int e = 0; e < HT; ++e) z[e] = 0u;
-                    ptx::tmem_st32(tmem + lane_base + (j % 2) * TT + (1 - dcopy) * HT, z);
+                    ptx::tmem_st32(tmem + lane_base + sbuf(j) * TT + (1 - dcopy) * HT, z);
                 }
             }
             // V rows of tokens that were not loaded hold stale or uninitialised
@@ -1496,7 +1525,7 @@ prefix_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
             }
             ptx::fence_proxy_async_smem();
             ptx::tc_fence_before_sync();
-            ptx::mbar_arrive(ptx::smem_addr(&p_ready[j % 2]));
+            ptx::mbar_arrive(ptx::smem_addr(&p_ready[sbuf(j)]));
         }
         if (ok && ntiles > 0)
             ok = warp_wait_phase(ptx::smem_addr(&o_done[(ntiles - 1) % 2]), ((ntiles - 1) / 2) & 1,
@@ -1939,7 +1968,7 @@ template <typename T, int D, int MODE = 0>
 static cudaError_t launch_prefix_t(const CUtensorMap& mk, const CUtensorMap& mv,
                                    const PrefixParams& p, dim3 grid, cudaStream_t stream) {
     auto kern = prefix_kernel<T, D, MODE>;
-    using Cfg = PrefixTile<D, MODE != 0 ? 2 : kPrefixStages, MODE != 0>;
+    using Cfg = PrefixTile<D, MODE != 0 ? mq_stages<D>() : kPrefixStages, MODE != 0>;
     static std::once_flag once;
     static cudaError_t attr_err = cudaSuccess;
     std::call_once(once, [&] {
