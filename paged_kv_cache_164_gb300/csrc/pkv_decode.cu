@@ -1038,8 +1038,9 @@ __device__ void plan_cta(const PlanParams& p, int* scratch) {
 // and r + 64), written as partial slots 2 * partition and 2 * partition + 1.
 // MODE 2: up to 128 query rows, one softmax thread per row taking all 64
 // tokens of each tile, one accumulator.
-// MODES 1 and 2 run four softmax warps, 256 tensor-memory columns and a
-// 2-stage ring: two CTAs share an SM, so one's start and per-tile chain
+// MODES 1 and 2 run four softmax warps and 256 tensor-memory columns (one S/P
+// buffer, Q as the A operand of S, one accumulator) and a ring of the shared
+// memory left: two CTAs share an SM, so one's start and per-tile chain
 // overlap the other's.
 template <typename T, int D, int MODE = 0>
 __global__ void __launch_bounds__((MODE != 0 ? 4 : kPrefixSoftmaxWarps) * 32 + 64, MODE != 0 ? 2 : 1)
