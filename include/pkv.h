@@ -317,10 +317,12 @@ pkv_status pkv_decode_attention_prefix_shared(
  * (sequence, KV head) (q_len * num_q_heads / num_kv_heads: verifying a few
  * drafted tokens, or a small GQA group) the decode kernel serves them as it
  * serves the heads of a GQA group, streaming the context once at the HBM
- * rate, with per-row causal limits on the last positions.  With more rows the
- * products run on the tensor cores (tcgen05, 128 rows per CTA, accumulators
- * in tensor memory).  Either way the context is split into partitions whose
- * partials are merged by log-sum-exp as in pkv_merge.
+ * rate, with per-row causal limits on the last positions; up to twice as many
+ * rows take two adjacent CTAs that read the context together (the second
+ * copy mostly from L2).  With more rows the products run on the tensor cores
+ * (tcgen05, 128 rows per CTA, accumulators in tensor memory).  Either way the
+ * context is split into partitions whose partials are merged by log-sum-exp
+ * as in pkv_merge.
  */
 size_t pkv_multi_query_workspace_size(int num_seqs, int q_len, int num_q_heads, int num_kv_heads,
                                       int head_dim, int block_size, int max_context_len);

@@ -396,8 +396,8 @@ def decode_attention_prefix_shared(q: torch.Tensor, k_cache: torch.Tensor, v_cac
 def multi_query_plan(num_seqs: int, q_len: int, num_q_heads: int, num_kv_heads: int,
                      head_dim: int, block_size: int, max_context_len: int) -> tuple:
     """(kernel, context partitions) of a ``multi_query_attention`` call on the
-    current device: kernel "decode" (at most ``pkv_max_group_size()``, 16, query
-    rows per sequence and KV head) or "tcgen05"."""
+    current device: kernel "decode" (at most twice ``pkv_max_group_size()``, 32,
+    query rows per sequence and KV head) or "tcgen05"."""
     parts = ctypes.c_int(0)
     r = load().pkv_multi_query_plan(num_seqs, q_len, num_q_heads, num_kv_heads, head_dim,
                                     block_size, max_context_len, ctypes.byref(parts))

@@ -95,6 +95,7 @@ struct DecodeParams {
     float scale_log2;    // scale * log2(e) (times the K scale of an E4M3 cache)
     float v_scale;       // value of one V unit: 1, or the V scale of an E4M3 cache
     int q_len;           // > 0 (multi-query): columns are (query token, head), causal
+    int row_blocks;      // multi-query: CTAs per (sequence, KV head), NT * 8 rows each
 };
 
 // Context length of sequence b as the kernels use it: negative or too long
@@ -390,9 +391,12 @@ __device__ __forceinline__ void stage_update(uint32_t kbase, uint32_t vbase, int
 
 // NT = number of 8-column groups (1: up to 8 query rows, 2: up to 16); F8:
 // E4M3 cache codes.  MQ: multi-query, the columns are the (query token i,
-// query head) rows of a chunk of q_len tokens (i * group + head in group), and
-// column i sees positions < n - q_len + 1 + i; only the stages that reach past
-// n - q_len + 1 apply the per-column limits.
+// query head) rows of a chunk of q_len tokens (row i * group + head in group),
+// and row i sees positions < n - q_len + 1 + i; only the stages that reach
+// past the first limit of the CTA's rows apply the per-column limits.  With
+// row_blocks > 1 the rows of a (sequence, KV head) are split over adjacent
+// CTAs of NT * 8 rows each, which read the same context at the same time (the
+// second copy mostly from L2).
 template <typename T, int D, int NT, bool F8 = false, bool MQ = false>
 __global__ void __launch_bounds__(kThreads, (F8 && NT == 1) ? 4 : 3)
 decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
@@ -436,10 +440,12 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
         // partitions run before any second one, so sequences that share physical
         // blocks (a common prompt prefix) read them close together in time and
         // the repeats hit in L2.
-        g = blockIdx.x;
+        g = MQ ? blockIdx.x / p.row_blocks : blockIdx.x;
         b = blockIdx.y;
         split = blockIdx.z;
     }
+    // MQ: the CTA's first row of the (sequence, KV head)'s q_len * group rows
+    const int col0 = MQ ? (int)(blockIdx.x % p.row_blocks) * (NT * 8) : 0;
 
     const int cap = min(p.max_blocks_per_seq * bs, p.max_context_len);
     const int n_raw = __ldg(p.context_lens + b);
@@ -590,7 +596,7 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
         // each k-step (for an E4M3 cache, dims 4tq.. and 4tq+2.., the K fragments'
         // order).  A column is a head of the group, or (MQ) a (query token, head).
         uint32_t qb[NT][KSTEPS][2];
-        const int ncols = MQ ? p.q_len * p.group : p.group;
+        const int ncols = MQ ? min(NT * 8, p.q_len * p.group - col0) : p.group;
         // the first row of the CTA's block of q: head g*group of the sequence (MQ:
         // of its first query token)
         const T* qbase = static_cast<const T*>(p.q) +
@@ -600,7 +606,7 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
             const int col = nt * 8 + gq;
             // rows of q after the first: the column's head, or (MQ) its query
             // token's rows of all heads plus its head
-            const int cc = MQ && col >= ncols ? 0 : col;
+            const int cc = MQ ? col0 + (col >= ncols ? 0 : col) : col;
             const int off = MQ ? (cc / p.group) * p.num_q_heads + cc % p.group : col;
             const uint32_t* qrow = reinterpret_cast<const uint32_t*>(qbase + off * D);
 #pragma unroll
@@ -633,8 +639,9 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
             for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
                 for (int k = 0; k < 2; ++k)
-                    lim[nt][k] = max(0, n - p.q_len + 1 + (nt * 8 + 2 * tq + k) / p.group);
-            causal0 = n - p.q_len + 1;
+                    lim[nt][k] =
+                        max(0, n - p.q_len + 1 + (col0 + nt * 8 + 2 * tq + k) / p.group);
+            causal0 = n - p.q_len + 1 + col0 / p.group;
         }
 
         for (int i = warp; i < nstages; i += kConsumerWarps) {
@@ -707,7 +714,7 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
 
         // Per-column combine factors, once per column: c_w = e^(m_w - m*) / L with
         // L = sum_w e^(m_w - m*) l_w, and the column's log-sum-exp.
-        const int G = MQ ? p.q_len * p.group : p.group;
+        const int G = MQ ? min(NT * 8, p.q_len * p.group - col0) : p.group;
         float* sm_f = sm_l + kConsumerWarps * HP;   // [HP][warps]
         float* sm_lse = sm_f + HP * kConsumerWarps; // [HP]
         if (tid < G) {
@@ -747,8 +754,8 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
             // (row of q, query head) of the column: rows of q are sequences, or
             // (sequence, query token) with MQ
             const int64_t orow =
-                MQ ? ((int64_t)b * p.q_len + h / p.group) * p.num_q_heads + g * p.group +
-                         h % p.group
+                MQ ? ((int64_t)b * p.q_len + (col0 + h) / p.group) * p.num_q_heads +
+                         g * p.group + (col0 + h) % p.group
                    : (int64_t)b * p.num_q_heads + (g * G + h);
             if (direct) {
                 T* out = static_cast<T*>(p.out) + orow * D + j;
@@ -793,7 +800,7 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
 // this tile's softmax.  A half's reference max is raised (and its O rescaled in
 // tensor memory) only when its running max exceeds it by more than 2^8; P
 // stays below 256 and the final normalisation uses the same references, so
-// the result is the same softmax.  Multi-query calls with more than 16 rows per
+// the result is the same softmax.  Multi-query calls with more than 32 rows per
 // (sequence, KV head) use the same kernel in MODES 1 and 2 (one softmax thread
 // per tensor-memory lane, two CTAs an SM; see prefix_kernel); smaller ones run
 // on the decode kernel.
@@ -1787,11 +1794,12 @@ static pkv_status check_shapes(int num_seqs, int num_q_heads, int num_kv_heads, 
 // Partitions: whole 16-token stages, whatever the page size; the automatic
 // plan sizes them from 256 to 1024 tokens by an estimate of the time (see the
 // loop).  ctas_per_sm: the decode kernel's resident CTAs an SM (3, or 4 for
-// the E4M3 kernel at one 8-column group).
+// the E4M3 kernel at one 8-column group); unit_mult: CTAs per (sequence, KV
+// head) and partition (the multi-query row blocks).
 constexpr double kCtaStartTokens = 384.0;  // a CTA's fixed start, in tokens streamed
 static pkv_status make_plan(int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
                             int block_size, int max_context_len, int num_splits, Plan* plan,
-                            int ctas_per_sm = 3) {
+                            int ctas_per_sm = 3, int unit_mult = 1) {
     pkv_status st = check_shapes(num_seqs, num_q_heads, num_kv_heads, head_dim, block_size,
                                  max_context_len, num_splits);
     if (st != PKV_OK) return st;
@@ -1815,7 +1823,7 @@ static pkv_status make_plan(int num_seqs, int num_q_heads, int num_kv_heads, int
         // starts: measured on the Llama-70B layer (32 x 4096 tokens, GQA-8),
         // 5 partitions (2.8 waves) ran at 89.6 % of peak, the 7 of a
         // fill-the-last-wave rule (3.9 waves) at 86.9 %.
-        const int64_t units = (int64_t)std::max(1, num_seqs) * num_kv_heads;
+        const int64_t units = (int64_t)std::max(1, num_seqs) * num_kv_heads * unit_mult;
         const double slots = (double)ctas_per_sm * sms;
         const int min_chunk = 256 / kStageTokens, max_chunk = std::min(1024 / kStageTokens, cap_stages);
         const int lo = std::max(1, (max_stages + max_chunk - 1) / max_chunk);
@@ -1933,7 +1941,8 @@ static cudaError_t launch_decode(const CUtensorMap& mk, const CUtensorMap& mv,
                 : launch_decode_t<T, 128, 1, false>(mk, mv, p, grid, stream);
 }
 
-// Multi-query rows on the decode kernel: q_len * group <= 16 columns.
+// Multi-query rows on the decode kernel: up to 16 columns per CTA (two
+// 8-column groups whenever the rows need more than one CTA).
 template <typename T>
 static cudaError_t launch_decode_mq(const CUtensorMap& mk, const CUtensorMap& mv,
                                     const DecodeParams& p, int head_dim, dim3 grid,
@@ -2046,14 +2055,18 @@ static pkv_status make_prefix_plan(int num_seqs, int num_q_heads, int num_kv_hea
     return PKV_OK;
 }
 
-// Plan of a multi-query call.  At most kMaxGroup (query token, query head)
-// rows per (sequence, KV head) (speculative verification of a few tokens, a
-// small GQA group or MHA): the decode kernel with those rows as its columns,
-// planned like a decode.  More rows: 128-row tiles per (sequence, KV head) on
-// the tensor-core kernel; the context in partitions of whole 64-token tiles,
-// as many as give about one CTA per SM, at most kMaxChunkPages pages each.
+// Plan of a multi-query call.  At most 2 * kMaxGroup (query token, query
+// head) rows per (sequence, KV head) (speculative verification of a few
+// tokens, a small GQA group or MHA): the decode kernel with those rows as its
+// columns, in one CTA of up to kMaxGroup rows or two adjacent ones that read
+// the same context together, planned like a decode.  More rows: 128-row
+// tiles per (sequence, KV head) on the tensor-core kernel; the context in
+// partitions of whole 64-token tiles, as many as give about one CTA per SM,
+// at most kMaxChunkPages pages each.
+constexpr int kMqDecodeRowBlocks = 2;
 struct MultiQueryPlan {
     bool on_decode;  // the decode kernel's multi-query form
+    int row_blocks;  // on the decode kernel: CTAs per (sequence, KV head)
     int chunk;
     int parts;
     int row_tiles;
@@ -2075,11 +2088,13 @@ static pkv_status make_mq_plan(int num_seqs, int q_len, int num_q_heads, int num
     if ((int64_t)num_seqs * num_kv_heads > 65535 || mp->row_tiles > 65535 ||
         (int64_t)num_seqs * q_len > 65535)
         return PKV_ERR_UNSUPPORTED;
-    mp->on_decode = rows <= kMaxGroup;
+    mp->on_decode = rows <= kMqDecodeRowBlocks * kMaxGroup;
+    mp->row_blocks = (int)((rows + kMaxGroup - 1) / kMaxGroup);
+    if ((int64_t)num_kv_heads * mp->row_blocks > INT_MAX) return PKV_ERR_UNSUPPORTED;
     if (mp->on_decode) {
         Plan dp;
         st = make_plan(num_seqs, num_q_heads, num_kv_heads, head_dim, block_size,
-                       max_context_len, 0, &dp);
+                       max_context_len, 0, &dp, 3, mp->row_blocks);
         if (st != PKV_OK) return st;
         mp->dup = false;
         mp->chunk = dp.chunk_tokens;
@@ -2602,6 +2617,7 @@ extern "C" pkv_status pkv_multi_query_attention(
         p.num_kv_heads = num_kv_heads;
         p.max_context_len = max_context_len;
         p.q_len = q_len;
+        p.row_blocks = mq.row_blocks;
         p.hnd = hnd;
         p.scale_log2 = scale * kLog2e;
         p.v_scale = 1.f;
@@ -2609,7 +2625,8 @@ extern "C" pkv_status pkv_multi_query_attention(
             p.partial_o = partial_o;
             p.partial_lse = partial_lse;
         }
-        const dim3 grid(num_kv_heads, num_seqs, mq.parts);
+        // a (sequence, KV head)'s row blocks are adjacent CTAs
+        const dim3 grid(num_kv_heads * mq.row_blocks, num_seqs, mq.parts);
         e = dtype == PKV_FP16 ? launch_decode_mq<__half>(mk, mv, p, head_dim, grid, s)
                               : launch_decode_mq<__nv_bfloat16>(mk, mv, p, head_dim, grid, s);
         if (e != cudaSuccess) {

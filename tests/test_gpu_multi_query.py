@@ -36,17 +36,25 @@ CASES = {
                                 max_len_cap=2688, seed=66),
     "gqa8_q9_rows72": dict(name="c3", q_len=9, num_seqs=3, lengths=("uniform", 60, 900),
                            max_len_cap=960, seed=67),
-    # At most 16 (query token, head) rows per (sequence, KV head) run on the
-    # decode kernel (rows as its columns): one and two 8-column groups, one
-    # partition (direct output) and several (partials + merge); 17 rows are
-    # the tensor-core kernel's again.
+    # At most 32 (query token, head) rows per (sequence, KV head) run on the
+    # decode kernel (rows as its columns): one and two 8-column groups, one and
+    # two row blocks (CTAs) per (sequence, KV head), one partition (direct
+    # output) and several (partials + merge); 33 rows are the tensor-core
+    # kernel's again.
     "mha_q4_split_merge": dict(name="c2", q_len=4, num_seqs=3, num_q_heads=4, num_kv_heads=4,
                                lengths=("uniform", 1500, 4000), max_len_cap=4096, seed=68),
     "gqa8_q2_rows16": dict(name="c3", q_len=2, num_seqs=3, lengths=("uniform", 100, 1800),
                            max_len_cap=1856, seed=69),
     "gqa2_q8_fp16_d64_rows16": dict(name="c1", q_len=8),
-    "mha_q17_rows17": dict(name="c2", q_len=17, num_seqs=2, num_q_heads=4, num_kv_heads=4,
-                           lengths=("uniform", 30, 400), max_len_cap=448, seed=70),
+    "mha_q17_rows17_two_blocks": dict(name="c2", q_len=17, num_seqs=2, num_q_heads=4,
+                                      num_kv_heads=4, lengths=("uniform", 30, 400),
+                                      max_len_cap=448, seed=70),
+    "gqa8_q3_rows24": dict(name="c3", q_len=3, num_seqs=3, lengths=("uniform", 100, 1800),
+                           max_len_cap=1856, seed=71),
+    "gqa8_q4_rows32_split": dict(name="c3", q_len=4, num_seqs=2, lengths=("uniform", 2500, 4000),
+                                 max_len_cap=4096, seed=72),
+    "mha_q33_rows33": dict(name="c2", q_len=33, num_seqs=2, num_q_heads=4, num_kv_heads=4,
+                           lengths=("uniform", 40, 400), max_len_cap=448, seed=73),
 }
 
 
@@ -158,11 +166,14 @@ def test_full_size_llama7b_layer_four_token_verify_sampled():
 
 
 def test_rows_per_kv_head_choose_the_kernel():
-    """Up to 16 (query token, head) rows per (sequence, KV head) go to the decode
-    kernel, planned like a decode; more go to the tensor-core kernel."""
+    """Up to 32 (query token, head) rows per (sequence, KV head) go to the decode
+    kernel (one CTA per 16 rows), planned like a decode; more go to the
+    tensor-core kernel."""
     kernel, parts = pkv.multi_query_plan(64, 4, 32, 32, 128, 16, 4096)
     assert kernel == "decode"
     assert parts == pkv.decode_num_splits(64, 32, 32, 128, 16, 4096)
     assert pkv.multi_query_plan(32, 2, 64, 8, 128, 16, 4096)[0] == "decode"    # 16 rows
-    assert pkv.multi_query_plan(32, 3, 64, 8, 128, 16, 4096)[0] == "tcgen05"   # 24 rows
-    assert pkv.multi_query_plan(2, 17, 4, 4, 128, 16, 448)[0] == "tcgen05"     # 17 rows
+    assert pkv.multi_query_plan(32, 3, 64, 8, 128, 16, 4096)[0] == "decode"    # 24 rows
+    assert pkv.multi_query_plan(32, 4, 64, 8, 128, 16, 4096)[0] == "decode"    # 32 rows
+    assert pkv.multi_query_plan(32, 5, 64, 8, 128, 16, 4096)[0] == "tcgen05"   # 40 rows
+    assert pkv.multi_query_plan(2, 33, 4, 4, 128, 16, 448)[0] == "tcgen05"     # 33 rows
