@@ -94,7 +94,7 @@ pkv_status pkv_append(const void* k_new, const void* v_new, void* k_cache, void*
  * Bytes of device workspace pkv_decode_attention (and pkv_decode_attention_fp8)
  * needs for these arguments on the current device (the split-K plan depends on
  * the device's SM count; the automatic plan picks, among partitions of 256 to
- * 1024 tokens, the count with the least estimated time: waves of resident CTAs,
+ * 2048 tokens, the count with the least estimated time: waves of resident CTAs,
  * rounded up, times the partition's tokens plus a fixed per-CTA start; the
  * E4M3 kernel, with more resident CTAs per SM, may pick another count, and
  * this size covers both).  Returns 0 when no workspace is needed and SIZE_MAX

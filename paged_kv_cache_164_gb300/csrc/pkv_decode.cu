@@ -45,7 +45,7 @@ namespace pkv {
 constexpr int kStageTokens = 16;      // tokens per pipeline stage
 constexpr int kConsumerWarps = 4;
 constexpr int kThreads = (kConsumerWarps + 1) * 32;
-constexpr int kMaxChunkPages = 64;    // pages per partition (block-table slice in smem)
+constexpr int kMaxChunkPages = 128;   // pages per partition (block-table slice in smem)
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s per wait before giving up
 
 // Shared-memory geometry of a decode stage: K then V of 16 tokens, as 128-byte
@@ -465,10 +465,11 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
     // pages a partition can touch: it may start and end mid-page
     const int max_pages = min(p.max_blocks_per_seq - page0, (p.chunk_tokens + bs - 1) / bs + 1);
     const int32_t* row = p.block_tables + (int64_t)b * p.max_blocks_per_seq + page0;
-    int blk_r[3] = {-1, -1, -1};
+    int blk_r[5] = {-1, -1, -1, -1, -1};  // up to 160 pages: kMaxChunkPages + 1
+    static_assert(kMaxChunkPages + 1 <= 5 * 32, "the producer lanes hold the table slice");
     if (warp == kConsumerWarps) {
 #pragma unroll
-        for (int r = 0; r < 3; ++r)
+        for (int r = 0; r < 5; ++r)
             if (lane + 32 * r < max_pages) blk_r[r] = __ldg(row + lane + 32 * r);
     }
     if ((n_raw < 0 || n_raw > cap || (MQ && n_raw < p.q_len)) && split == 0 && g == 0 &&
@@ -515,7 +516,7 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
         // Keep this partition's slice of the block table, validating each id.
         const int npages = t_end > t_begin ? (t_end + bs - 1) / bs - page0 : 0;
 #pragma unroll
-        for (int r = 0; r < 3; ++r) {
+        for (int r = 0; r < 5; ++r) {
             const int i = lane + 32 * r;
             if (i < npages) {
                 int blk = blk_r[r];
@@ -1792,7 +1793,7 @@ static pkv_status check_shapes(int num_seqs, int num_q_heads, int num_kv_heads, 
 }
 
 // Partitions: whole 16-token stages, whatever the page size; the automatic
-// plan sizes them from 256 to 1024 tokens by an estimate of the time (see the
+// plan sizes them from 256 to 2048 tokens by an estimate of the time (see the
 // loop).  ctas_per_sm: the decode kernel's resident CTAs an SM (3, or 4 for
 // the E4M3 kernel at one 8-column group); unit_mult: CTAs per (sequence, KV
 // head) and partition (the multi-query row blocks).
@@ -1812,7 +1813,7 @@ static pkv_status make_plan(int num_seqs, int num_q_heads, int num_kv_heads, int
     if (num_splits == 0) {
         const int sms = current_sm_count();
         if (sms <= 0) return PKV_ERR_CUDA;
-        // From 256 to 1024 tokens.  Equal-length CTAs (at the longest
+        // From 256 to 2048 tokens.  Equal-length CTAs (at the longest
         // context) run in waves of resident CTAs; every wave costs its
         // partition's tokens plus a CTA's fixed start (context length and
         // block-table reads, the first copy round trip), kCtaStartTokens in
@@ -1822,10 +1823,11 @@ static pkv_status make_plan(int num_seqs, int num_q_heads, int num_kv_heads, int
         // an SM still draw most of its bandwidth), more waves cost their
         // starts: measured on the Llama-70B layer (32 x 4096 tokens, GQA-8),
         // 5 partitions (2.8 waves) ran at 89.6 % of peak, the 7 of a
-        // fill-the-last-wave rule (3.9 waves) at 86.9 %.
+        // fill-the-last-wave rule (3.9 waves) at 86.9 %; allowing partitions
+        // of up to 2048 tokens (3 partitions, 1.7 waves) 91.7 %.
         const int64_t units = (int64_t)std::max(1, num_seqs) * num_kv_heads * unit_mult;
         const double slots = (double)ctas_per_sm * sms;
-        const int min_chunk = 256 / kStageTokens, max_chunk = std::min(1024 / kStageTokens, cap_stages);
+        const int min_chunk = 256 / kStageTokens, max_chunk = std::min(2048 / kStageTokens, cap_stages);
         const int lo = std::max(1, (max_stages + max_chunk - 1) / max_chunk);
         const int hi = std::max(lo, std::min(PKV_MAX_SPLITS, (max_stages + min_chunk - 1) / min_chunk));
         double best = 0.0;
