@@ -1830,19 +1830,30 @@ static pkv_status make_plan(int num_seqs, int num_q_heads, int num_kv_heads, int
         const int min_chunk = 256 / kStageTokens, max_chunk = std::min(2048 / kStageTokens, cap_stages);
         const int lo = std::max(1, (max_stages + max_chunk - 1) / max_chunk);
         const int hi = std::max(lo, std::min(PKV_MAX_SPLITS, (max_stages + min_chunk - 1) / min_chunk));
-        double best = 0.0;
+        // A count whose CTAs do not fill one wave leaves resident slots idle
+        // with nothing to come: it is taken only when no count fills one (the
+        // E4M3 Llama-70B layer: 2 partitions of 2048 tokens, 0.84 waves, 62.4 %
+        // against 66.8 % for 4).
+        double best = 0.0, best_fill = 0.0;
+        int chunk_fill = 0;
         chunk_stages = (max_stages + lo - 1) / lo;
         for (int s = lo; s <= hi; ++s) {
             const int cs = (max_stages + s - 1) / s;
             const int splits = (max_stages + cs - 1) / cs;
             if (splits != s) continue;  // the same partition as a smaller count
-            const double waves = std::ceil((double)units * splits / slots);
+            const double ctas = (double)units * splits;
+            const double waves = std::ceil(ctas / slots);
             const double cost = waves * (cs * kStageTokens + kCtaStartTokens);
             if (s == lo || cost < best - 1e-9) {
                 best = cost;
                 chunk_stages = cs;
             }
+            if (ctas >= slots && (chunk_fill == 0 || cost < best_fill - 1e-9)) {
+                best_fill = cost;
+                chunk_fill = cs;
+            }
         }
+        if (chunk_fill > 0) chunk_stages = chunk_fill;
     } else {
         chunk_stages = (max_stages + num_splits - 1) / num_splits;
     }
