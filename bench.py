@@ -55,14 +55,14 @@ WORKLOAD_TEXT = {
 # measured on (digest of csrc/), else reported as null.
 NCU_TRAFFIC = {
     # ncu --metrics dram__bytes_read.sum,dram__bytes_write.sum -k regex:decode_kernel -s 4 -c 1
-    "c2": {"digest": "ea0ec0baec519fd4", "splits": 4, "shared": False,
-           "bytes": 2312624640 + 4707584},
-    "c3": {"digest": "ea0ec0baec519fd4", "splits": 5, "shared": False,
-           "bytes": 537496576 + 4721920},
+    "c2": {"digest": "19dbfe7793078903", "splits": 2, "shared": False,
+           "bytes": 2312578048 + 3610112},
+    "c3": {"digest": "19dbfe7793078903", "splits": 3, "shared": False,
+           "bytes": 537488128 + 4089856},
     # shared-prefix path: decode_kernel (suffixes) + prefix_kernel (-k regex:prefix_kernel
     # -s 2 -c 1); the merge kernel's few MB are not included
-    "c5": {"digest": "ea0ec0baec519fd4", "splits": 16, "shared": True,
-           "bytes": (1531712512 + 5743616) + (35797760 + 87296)},
+    "c5": {"digest": "19dbfe7793078903", "splits": 8, "shared": True,
+           "bytes": (1531689216 + 5015552) + (35768320 + 57600)},
 }
 
 
