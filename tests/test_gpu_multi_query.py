@@ -55,6 +55,9 @@ CASES = {
                                  max_len_cap=4096, seed=72),
     "mha_q33_rows33": dict(name="c2", q_len=33, num_seqs=2, num_q_heads=4, num_kv_heads=4,
                            lengths=("uniform", 40, 400), max_len_cap=448, seed=73),
+    "gqa4_d64_bs32_q6_rows24": dict(name="c5_bs32", q_len=6, num_seqs=4, head_dim=64,
+                                    lengths=("uniform", 30, 2500), max_len_cap=2560,
+                                    shared_prefix_groups=0, seed=74),
 }
 
 
