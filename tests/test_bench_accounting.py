@@ -1,0 +1,63 @@
+"""The bench's algorithmic byte counts (the roofline numerator) against closed forms.
+
+The KV bytes of one attention layer are 2 (K and V) x tokens x H_kv x d x
+bytes per element ([inference] "KV Cache 的显存计算": 2·L·H·d·S·B·bytes, here
+for one layer); queries and outputs add 2 x B x q_len x H_q x d x 2, the block
+table 4 bytes per page read and the context lengths 4 bytes per sequence.  With
+shared prefixes the prefix pages count once per group (unique physical slots),
+which these tests compute from the group metadata instead of the block tables.
+"""
+import pytest
+import torch
+
+import bench
+from workloads import make_workload
+
+
+def _closed_form(w, q_len, kv_bytes, unique_tokens):
+    s = w.spec
+    lens = w.context_lens.long()
+    pages = int(((lens + s.block_size - 1) // s.block_size).sum())
+    kv = 2 * unique_tokens * s.num_kv_heads * s.head_dim * kv_bytes
+    qo = 2 * s.num_seqs * q_len * s.num_q_heads * s.head_dim * 2
+    return kv, kv + qo + 4 * pages + 4 * s.num_seqs
+
+
+@pytest.mark.parametrize("q_len,kv_bytes", [(1, 2), (4, 2), (1, 1)])
+def test_plain_workload_counts_every_context_token_once(q_len, kv_bytes):
+    w = make_workload("c1", with_values=False)
+    tokens = int(w.context_lens.sum())
+    kv, decode = _closed_form(w, q_len, kv_bytes, tokens)
+    got = bench.step_bytes(w, q_len, kv_bytes)
+    assert got["kv_unique"] == kv
+    assert got["decode"] == decode
+    assert got["decode_logical"] == decode  # nothing shared: logical == unique
+    s = w.spec
+    assert got["flops"] == 4 * tokens * q_len * s.num_q_heads * s.head_dim
+    assert got["tokens"] == s.num_seqs * q_len
+
+
+def test_uniform_contexts_match_the_kv_size_formula():
+    # every sequence at the same length L: KV = 2 * B * L * H_kv * d * 2
+    w = make_workload("c3", with_values=False, num_seqs=4, lengths=("const", 1000),
+                      max_len_cap=1024)
+    s = w.spec
+    assert torch.all(w.context_lens == 1000)
+    got = bench.step_bytes(w)
+    assert got["kv_unique"] == 2 * s.num_seqs * 1000 * s.num_kv_heads * s.head_dim * 2
+
+
+def test_shared_prefix_pages_count_once_per_group():
+    w = make_workload("c5", with_values=False, num_seqs=8, shared_prefix_groups=2,
+                      lengths=("prefix_lognormal", 256, 64, 1.0, 1024), max_len_cap=1024)
+    gs = w.group_start.long().tolist()
+    gp = w.group_prefix_len.long().tolist()
+    lens = w.context_lens.long().tolist()
+    prefix_once = sum(gp)
+    suffixes = sum(lens[b] - gp[g] for g in range(len(gp)) for b in range(gs[g], gs[g + 1]))
+    kv, decode = _closed_form(w, 1, 2, prefix_once + suffixes)
+    got = bench.step_bytes(w)
+    assert got["kv_unique"] == kv
+    assert got["decode"] == decode
+    logical_kv = 2 * sum(lens) * w.spec.num_kv_heads * w.spec.head_dim * 2
+    assert got["decode_logical"] - got["decode"] == logical_kv - kv > 0
