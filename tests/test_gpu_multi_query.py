@@ -180,3 +180,18 @@ def test_rows_per_kv_head_choose_the_kernel():
     assert pkv.multi_query_plan(32, 4, 64, 8, 128, 16, 4096)[0] == "decode"    # 32 rows
     assert pkv.multi_query_plan(32, 5, 64, 8, 128, 16, 4096)[0] == "tcgen05"   # 40 rows
     assert pkv.multi_query_plan(2, 33, 4, 4, 128, 16, 448)[0] == "tcgen05"     # 33 rows
+
+
+@pytest.mark.parametrize("key", ["mha_q4_split_merge", "spec_verify_gqa8_bf16"])  # decode / tcgen05
+def test_empty_context_gives_zero_rows_and_is_flagged(key):
+    w, q_len = _make(key)
+    kc, vc = _appended(w)
+    q = make_queries(w, q_len, seed=17)
+    cl = w.context_lens.clone()
+    cl[0] = 0
+    flag = pkv.new_error_flag("cuda")
+    out = pkv.multi_query_attention(q, w.k_cache, w.v_cache, w.block_tables, cl,
+                                    w.max_context_len, scale=w.scale, err_flag=flag)
+    assert pkv.check_error(flag) & pkv.EFLAG_CONTEXT_LEN
+    assert torch.count_nonzero(out[0]) == 0
+    assert_attention_close(out[1:], _expect(w, q, kc, vc, cl.cpu().numpy())[1:], key + " n=0")
