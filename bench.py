@@ -3,15 +3,19 @@
 
 A step is one pass of the whole hot path over one batch: append each
 sequence's new K/V token through ``slot_mapping``, then decode attention over
-the paged cache (with the split-K log-sum-exp merge when the plan splits).
+the paged cache (with the split-K log-sum-exp merge when the plan splits; for
+workloads whose sequences share prefix blocks, the shared-prefix decode).
 Inputs are seeded synthetic caches (see ``workloads``) already resident in
-HBM; the KV cache of every workload is larger than the 129 MB L2, so no L2
-flush is needed between steps.
+HBM.  Every workload's KV cache is larger than the 129 MB L2, and consecutive
+calls alternate between two copies of it, so no call finds the previous
+call's lines in L2 and no flush is needed between steps.
 
 Prints ONE JSON line on rank 0.  ``value`` is achieved HBM bandwidth over the
 step's algorithmic bytes (K+V of every context token, counted once per
 physical slot, + Q + O + block-table entries + context lengths + the append's
-reads and writes), in GB/s, summed over ranks.
+reads and writes), in GB/s, summed over ranks.  Without ``--config`` the
+headline is the long-context layer (c4, the largest single-GPU workload) and
+``per_config`` holds the same measurements for c2, c3, c5 and c5_bs32.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--config c2]
   python bench.py --impl reference ...   # the fp64 CPU oracle on the same workload
@@ -275,7 +279,8 @@ def run_reference(args):
     import torch
     from workloads import make_queries, make_workload
     dev = "cuda" if torch.cuda.is_available() else "cpu"
-    w = make_workload(args.config, device=dev)
+    name = args.config or HEADLINE_CONFIG
+    w = make_workload(name, device=dev)
     if args.q_len > 0:
         w.q = make_queries(w, args.q_len, seed=w.spec.seed + 101)
     w = w.to("cpu")
@@ -297,7 +302,7 @@ def run_reference(args):
             "ms_per_step": round(1e3 * statistics.median(secs_all), 3) if secs_all else None,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": "f64", "data": "synthetic",
-            "config": {"workload": args.config, "description": WORKLOAD_TEXT[args.config],
+            "config": {"workload": name, "description": WORKLOAD_TEXT[name],
                        "q_len": max(1, args.q_len)},
             "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": threads,
                              "kind": "oracle", "sample": desc},
@@ -306,29 +311,28 @@ def run_reference(args):
     print(json.dumps(line), flush=True)
 
 
-def run_gpu(args):
+HEADLINE_CONFIG = "c4"
+PER_CONFIGS = ("c2", "c3", "c5", "c5_bs32")
+# Copies of the KV cache that consecutive calls alternate between, so that no
+# call finds the previous call's lines in L2 (each copy is far larger than L2).
+KV_COPIES = 2
+
+
+def _measure(name, args, device, rank, ws, cpu_seconds):
+    """Builds workload ``name`` on ``device`` and times its step, its decode
+    call, its append and its end-to-end step; returns the numbers (timings
+    already reduced over ranks) and the JSON fields that describe them."""
     import torch
-    import torch.distributed as dist
 
     import paged_kv_cache_164_gb300 as pkv
-    from workloads import make_queries, make_workload, to_head_major
-
-    ws, rank, local = _dist_env()
-    if ws > 1:
-        torch.cuda.set_device(local)
-        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
-    device = torch.device("cuda", local if ws > 1 else 0)
-    torch.cuda.set_device(device)
-    pkv.load()
+    from workloads import SPECS, make_queries, make_workload, to_head_major
 
     # --block-size: the workload with another page size
     overrides = {"block_size": args.block_size} if args.block_size else {}
     if ws > 1:  # an independent replica per rank
-        from workloads import SPECS
-        w = make_workload(args.config, device=device, seed=SPECS[args.config].seed + 1000 * rank,
-                          **overrides)
+        w = make_workload(name, device=device, seed=SPECS[name].seed + 1000 * rank, **overrides)
     else:
-        w = make_workload(args.config, device=device, **overrides)
+        w = make_workload(name, device=device, **overrides)
     layout = args.layout
     if layout == "hnd":  # the same values in the head-major page layout
         w.k_cache = to_head_major(w.k_cache)
@@ -341,6 +345,7 @@ def run_gpu(args):
         w.q = make_queries(w, args.q_len, seed=s.seed + 101)
     # --kv fp8: the cache as E4M3 codes with one scale for K and one for V
     fp8 = args.kv == "fp8"
+    k_scale = v_scale = 1.0
     if fp8:
         if mq or args.fused or s.shared_prefix_groups and args.prefix_sharing:
             raise SystemExit("--kv fp8 times the plain decode path only "
@@ -351,6 +356,9 @@ def run_gpu(args):
             torch.float8_e4m3fn).view(torch.uint8)
         w.v_cache = (w.v_cache.float() / v_scale).clamp(-448, 448).to(
             torch.float8_e4m3fn).view(torch.uint8)
+    caches = [(w.k_cache, w.v_cache)]
+    for _ in range(KV_COPIES - 1):
+        caches.append((w.k_cache.clone(), w.v_cache.clone()))
     nbytes = step_bytes(w, args.q_len if mq else 1, 1 if fp8 else 2)
     mcl = w.max_context_len
     # Workloads whose sequences share prefix blocks use the shared-prefix decode
@@ -360,8 +368,8 @@ def run_gpu(args):
     max_group_size, max_prefix_len = w.max_group_size, w.max_prefix_len
     splits = pkv.decode_num_splits(s.num_seqs, s.num_q_heads, s.num_kv_heads, s.head_dim,
                                    s.block_size, mcl, args.splits, kv=args.kv)
+    mq_kernel, mq_parts = None, 0
     if mq:
-        # at most 16 query rows per (sequence, KV head): the decode kernel
         mq_kernel, mq_parts = pkv.multi_query_plan(s.num_seqs, args.q_len, s.num_q_heads,
                                                    s.num_kv_heads, s.head_dim, s.block_size, mcl)
         ws_bytes = pkv.multi_query_workspace_size(s.num_seqs, args.q_len, s.num_q_heads,
@@ -385,117 +393,108 @@ def run_gpu(args):
     else:
         launches_per_step = (4 if shared else (1 if fused else 2) + (1 if splits > 1 else 0))
 
-    def decode_call(q, block_tables, context_lens, out=out):
+    def decode_call(c, q, block_tables, context_lens, out=out):
+        kc, vc = caches[c]
         if fp8:
-            pkv.decode_attention_fp8(q, w.k_cache, w.v_cache, block_tables, context_lens, mcl,
+            pkv.decode_attention_fp8(q, kc, vc, block_tables, context_lens, mcl,
                                      k_scale, v_scale, scale=w.scale, num_splits=args.splits,
                                      out=out, workspace=workspace, err_flag=flag, layout=layout)
         elif mq:
-            pkv.multi_query_attention(q, w.k_cache, w.v_cache, block_tables, context_lens, mcl,
+            pkv.multi_query_attention(q, kc, vc, block_tables, context_lens, mcl,
                                       scale=w.scale, out=out, workspace=workspace, err_flag=flag,
                                       layout=layout)
         elif shared:
             pkv.decode_attention_prefix_shared(
-                q, w.k_cache, w.v_cache, block_tables, context_lens, mcl, w.group_start,
+                q, kc, vc, block_tables, context_lens, mcl, w.group_start,
                 w.group_prefix_len, max_group_size, max_prefix_len, scale=w.scale, out=out,
                 workspace=workspace, err_flag=flag, layout=layout)
         else:
-            pkv.decode_attention(q, w.k_cache, w.v_cache, block_tables, context_lens, mcl,
+            pkv.decode_attention(q, kc, vc, block_tables, context_lens, mcl,
                                  scale=w.scale, num_splits=args.splits, out=out,
                                  workspace=workspace, err_flag=flag, layout=layout)
 
-    def append_call(k_new, v_new, slot_mapping):
+    def append_call(c, k_new, v_new, slot_mapping):
+        kc, vc = caches[c]
         if fp8:
-            pkv.append_fp8(k_new, v_new, w.k_cache, w.v_cache, slot_mapping, k_scale, v_scale,
+            pkv.append_fp8(k_new, v_new, kc, vc, slot_mapping, k_scale, v_scale,
                            err_flag=flag, layout=layout)
         else:
-            pkv.append(k_new, v_new, w.k_cache, w.v_cache, slot_mapping, err_flag=flag,
-                       layout=layout)
+            pkv.append(k_new, v_new, kc, vc, slot_mapping, err_flag=flag, layout=layout)
 
-    def step():
+    def step(c):
         if fused:
-            pkv.append_decode_attention(w.q, w.k_new, w.v_new, w.k_cache, w.v_cache,
+            kc, vc = caches[c]
+            pkv.append_decode_attention(w.q, w.k_new, w.v_new, kc, vc,
                                         w.block_tables, w.context_lens, mcl, scale=w.scale,
                                         num_splits=args.splits, out=out, workspace=workspace,
                                         err_flag=flag, layout=layout)
             return
-        append_call(w.k_new, w.v_new, w.slot_mapping)
-        decode_call(w.q, w.block_tables, w.context_lens)
+        append_call(c, w.k_new, w.v_new, w.slot_mapping)
+        decode_call(c, w.q, w.block_tables, w.context_lens)
 
-    for _ in range(args.warmup):
-        step()
+    for i in range(args.warmup):
+        step(i % KV_COPIES)
     if pkv.check_error(flag) != 0:
-        raise RuntimeError("device error flag set during warm-up")
+        raise RuntimeError(f"{name}: device error flag set during warm-up")
 
     stream = torch.cuda.current_stream(device)
 
-    def decode_only():
-        decode_call(w.q, w.block_tables, w.context_lens)
+    def timed(fn, count):
+        """ms per call of fn(i) over `count` calls back to back, with CUDA events
+        on the launching stream and a synchronise on both sides."""
+        t0 = torch.cuda.Event(enable_timing=True)
+        t1 = torch.cuda.Event(enable_timing=True)
+        barrier(device)
+        torch.cuda.synchronize(device)
+        t0.record(stream)
+        for i in range(count):
+            fn(i)
+        t1.record(stream)
+        torch.cuda.synchronize(device)
+        return t0.elapsed_time(t1) / count
 
     # Timed region: K whole steps back to back (the library chains its kernels
     # with programmatic dependent launch, so no event sits between them).
-    sampler = ClockSampler(device.index) if rank == 0 else None
-    if sampler:
-        sampler.wait_first()
-    e0 = torch.cuda.Event(enable_timing=True)
-    e1 = torch.cuda.Event(enable_timing=True)
-    run_steps = None
+    run_step = lambda i: step(i % KV_COPIES)  # noqa: E731
     if args.graph:
-        # one step captured in a CUDA graph (the library's set-up ran in the
-        # warm-up above), replayed K times: one graph launch per step
-        side = torch.cuda.Stream(device)
-        side.wait_stream(stream)
-        with torch.cuda.stream(side):
-            step()
-        stream.wait_stream(side)
-        graph = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(graph):
-            step()
-        graph.replay()
+        # one step per cache copy captured in a CUDA graph (the library's
+        # set-up ran in the warm-up above), replayed in turn: one graph launch
+        # per step
+        graphs = []
+        for c in range(KV_COPIES):
+            side = torch.cuda.Stream(device)
+            side.wait_stream(stream)
+            with torch.cuda.stream(side):
+                step(c)
+            stream.wait_stream(side)
+            graph = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(graph):
+                step(c)
+            graph.replay()
+            graphs.append(graph)
         torch.cuda.synchronize(device)
-        run_steps = graph.replay
-    barrier(device)
-    torch.cuda.synchronize(device)
+        run_step = lambda i: graphs[i % KV_COPIES].replay()  # noqa: E731
     t_begin = time.time()
-    e0.record(stream)
-    for _ in range(args.steps):
-        (run_steps or step)()
-    e1.record(stream)
-    torch.cuda.synchronize(device)
+    ms_local = timed(run_step, args.steps)
     t_end = time.time()
-    barrier(device)
-    if sampler:
-        sampler.stop()
-    total_ms = e0.elapsed_time(e1)
     # The dominant kernel alone: K decode calls back to back (decode kernel and,
     # when the plan splits, its merge), for the roofline.
-    for _ in range(3):
-        decode_only()
-    d0 = torch.cuda.Event(enable_timing=True)
-    d1 = torch.cuda.Event(enable_timing=True)
-    d0.record(stream)
-    for _ in range(args.steps):
-        decode_only()
-    d1.record(stream)
-    torch.cuda.synchronize(device)
-    decode_ms = d0.elapsed_time(d1) / args.steps
+    for i in range(3):
+        decode_call(i % KV_COPIES, w.q, w.block_tables, w.context_lens)
+    decode_ms = timed(lambda i: decode_call(i % KV_COPIES, w.q, w.block_tables, w.context_lens),
+                      args.steps)
     # The append alone (the scatter of the step's new K/V rows), timed the same way.
-    for _ in range(3):
-        append_call(w.k_new, w.v_new, w.slot_mapping)
-    a0 = torch.cuda.Event(enable_timing=True)
-    a1 = torch.cuda.Event(enable_timing=True)
-    a0.record(stream)
-    for _ in range(args.steps):
-        append_call(w.k_new, w.v_new, w.slot_mapping)
-    a1.record(stream)
-    torch.cuda.synchronize(device)
-    append_ms = a0.elapsed_time(a1) / args.steps
-    ms_local = total_ms / args.steps
+    for i in range(3):
+        append_call(i % KV_COPIES, w.k_new, w.v_new, w.slot_mapping)
+    append_ms = timed(lambda i: append_call(i % KV_COPIES, w.k_new, w.v_new, w.slot_mapping),
+                      args.steps)
     ms_step = reduce_over_ranks(ms_local, "max", device)
+    decode_ms = reduce_over_ranks(decode_ms, "max", device)
+    append_ms = reduce_over_ranks(append_ms, "max", device)
     bytes_all = reduce_over_ranks(float(nbytes["step"]), "sum", device)
     tokens_all = reduce_over_ranks(float(nbytes["tokens"]), "sum", device)
     if pkv.check_error(flag) != 0:
-        raise RuntimeError("device error flag set during the timed steps")
+        raise RuntimeError(f"{name}: device error flag set during the timed steps")
 
     # ---- end to end through the public API: pinned host inputs -> device -> host output
     # Every step copies its inputs from pinned host memory and its output back.
@@ -516,7 +515,8 @@ def run_gpu(args):
         for k in names:
             t = srcs[k]
             nb = t.numel() * t.element_size()
-            host_buf[sidx][offs[k]:offs[k] + nb].copy_(t.contiguous().view(-1).view(torch.uint8).cpu())
+            host_buf[sidx][offs[k]:offs[k] + nb].copy_(
+                t.contiguous().view(-1).view(torch.uint8).cpu())
             v[k] = dev_buf[sidx][offs[k]:offs[k] + nb].view(t.dtype).view(t.shape)
         views.append(v)
     outs = [torch.empty_like(out) for _ in range(2)]
@@ -532,7 +532,8 @@ def run_gpu(args):
     state = {"i": 0}
 
     def e2e_step():
-        sidx = state["i"] % 2
+        i = state["i"]
+        sidx = i % 2
         state["i"] += 1
         h2d_stream.wait_event(in_free[sidx])      # the step that last read this buffer is done
         with torch.cuda.stream(h2d_stream):
@@ -541,8 +542,8 @@ def run_gpu(args):
         stream.wait_event(in_ready[sidx])
         stream.wait_event(out_free[sidx])          # this output buffer's copy-out is done
         v = views[sidx]
-        append_call(v["k_new"], v["v_new"], v["slot_mapping"])
-        decode_call(v["q"], v["block_tables"], v["context_lens"], out=outs[sidx])
+        append_call(i % KV_COPIES, v["k_new"], v["v_new"], v["slot_mapping"])
+        decode_call(i % KV_COPIES, v["q"], v["block_tables"], v["context_lens"], out=outs[sidx])
         in_free[sidx].record(stream)
         done[sidx].record(stream)
         d2h_stream.wait_event(done[sidx])
@@ -569,10 +570,95 @@ def run_gpu(args):
     e2e_drain()
     e1.record(stream)
     torch.cuda.synchronize(device)
+    t_loops_end = time.time()
     e2e_ms = reduce_over_ranks(e0.elapsed_time(e1) / args.steps, "max", device)
     last = (state["i"] - 1) % 2
     if not torch.equal(out_h[last].to(device), out):
-        raise RuntimeError("end-to-end output differs from the device output")
+        raise RuntimeError(f"{name}: end-to-end output differs from the device output")
+
+    traffic = None
+    rec = NCU_TRAFFIC.get(name)
+    if rec and rec.get("digest") == _kernel_digest() and rec.get("splits") == splits and \
+            rec.get("shared") == shared and not mq and layout == "nhd" and not args.block_size \
+            and not fp8:
+        traffic = rec["bytes"]
+
+    cpu = None
+    if rank == 0 and cpu_seconds > 0:
+        w_host = w.to("cpu")
+        gbs, secs, desc, threads, _ = oracle_sample_rate(w_host, cpu_seconds)
+        cpu = {"value": round(gbs, 4), "unit": "GB/s", "cores": threads, "kind": "oracle",
+               "sample": desc, "seconds": round(secs, 3)}
+        del w_host
+
+    peak, _ = _peaks()
+    value = bytes_all / (ms_step * 1e-3) / 1e9
+    decode_gbs = nbytes["decode"] / (decode_ms * 1e-3) / 1e9
+    kernel = (("prefix_kernel in multi-query mode (tcgen05) + merge_kernel"
+               if mq_kernel == "tcgen05" else
+               "decode_kernel in multi-query mode" + (" + merge_kernel" if mq_parts > 1 else ""))
+              if mq else
+              "prefix_kernel (with the plan CTA) + decode_kernel + merge_kernel"
+              if shared else "decode_kernel + merge_kernel")
+    config = {"workload": name, "description": WORKLOAD_TEXT[name],
+              "num_seqs": s.num_seqs, "num_q_heads": s.num_q_heads,
+              "num_kv_heads": s.num_kv_heads, "head_dim": s.head_dim,
+              "block_size": s.block_size, "context_tokens": int(w.context_lens.sum()),
+              "max_context_len": mcl, "num_splits": mq_parts if mq else splits,
+              "accumulate": "fp32", "shared_prefix_decode": shared,
+              "q_len": args.q_len if mq else 1,
+              "fused_append": fused, "cuda_graph": bool(args.graph),
+              "layout": layout, "kv_cache": "e4m3" if fp8 else s.dtype,
+              "kv_bytes_unique": nbytes["kv_unique"],
+              "decode_bytes_per_step": nbytes["decode"],
+              "decode_bytes_logical": nbytes["decode_logical"],
+              "append_bytes_per_step": nbytes["append"],
+              "l2": f"no flush: the KV cache ({nbytes['kv_unique'] / 1e9:.2f} GB) is larger than "
+                    f"the 129 MB L2, and consecutive calls alternate between {KV_COPIES} copies "
+                    "of it, so no call finds the previous call's lines in L2",
+              "parallelism": f"replicas x{ws}" if ws > 1 else "1 GPU"}
+    return {
+        "name": name, "ms_step": ms_step, "value": value, "decode_ms": decode_ms,
+        "append_ms": append_ms, "e2e_ms": e2e_ms, "bytes_all": bytes_all,
+        "tokens_all": tokens_all, "nbytes": nbytes, "decode_gbs": decode_gbs, "peak": peak,
+        "traffic": traffic, "kernel": kernel, "cpu": cpu, "config": config, "h2d": h2d,
+        "d2h": d2h, "launches": launches_per_step * args.steps, "t_begin": t_begin,
+        "t_end": t_end, "t_loops_end": t_loops_end,
+        "dtype": f"e4m3 KV, {s.dtype} q" if fp8 else s.dtype,
+    }
+
+
+def run_gpu(args):
+    import torch
+    import torch.distributed as dist
+
+    import paged_kv_cache_164_gb300 as pkv
+
+    ws, rank, local = _dist_env()
+    if ws > 1:
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    device = torch.device("cuda", local if ws > 1 else 0)
+    torch.cuda.set_device(device)
+    pkv.load()
+
+    # Without --config: the headline on the largest single-GPU workload (the
+    # long-context layer) and a line for each of the other workloads.
+    if args.config:
+        names = [args.config]
+    else:
+        names = [HEADLINE_CONFIG] + ([] if args.no_per_config else list(PER_CONFIGS))
+    sampler = ClockSampler(device.index, period_ms=50) if rank == 0 else None
+    if sampler:
+        sampler.wait_first()
+    results = []
+    for i, name in enumerate(names):
+        secs = (args.cpu_seconds if i == 0 else args.cpu_seconds_per_config) \
+            if args.cpu_baseline else 0.0
+        results.append(_measure(name, args, device, rank, ws, secs))
+        torch.cuda.empty_cache()
+    if sampler:
+        sampler.stop()
 
     if rank != 0:
         if ws > 1:
@@ -580,69 +666,59 @@ def run_gpu(args):
         return
 
     peak, peak_src = _peaks()
-    value = bytes_all / (ms_step * 1e-3) / 1e9
-    decode_gbs = nbytes["decode"] / (decode_ms * 1e-3) / 1e9
-    clocks = sampler.summary(t_begin, t_end) if sampler else None
-    traffic = None
-    rec = NCU_TRAFFIC.get(args.config)
-    if rec and rec.get("digest") == _kernel_digest() and rec.get("splits") == splits and \
-            rec.get("shared") == shared and not mq and layout == "nhd" and not args.block_size \
-            and not fp8:
-        traffic = rec["bytes"]
+    head = results[0]
 
-    cpu = None
-    if args.cpu_baseline:
-        w_host = w.to("cpu")
-        gbs, secs, desc, threads, _ = oracle_sample_rate(w_host, args.cpu_seconds)
-        cpu = {"value": round(gbs, 4), "unit": "GB/s", "cores": threads, "kind": "oracle",
-               "sample": desc, "seconds": round(secs, 3)}
+    def e2e_of(r):
+        return {"value": round(r["bytes_all"] / (r["e2e_ms"] * 1e-3) / 1e9, 2), "unit": "GB/s",
+                "ms_per_step": round(r["e2e_ms"], 5), "h2d_bytes_per_step": r["h2d"],
+                "d2h_bytes_per_step": r["d2h"]}
 
+    def roofline_of(r):
+        return {"bound": "hbm", "achieved": round(r["decode_gbs"], 2), "peak": peak,
+                "unit": "GB/s", "frac": round(r["decode_gbs"] / peak, 4),
+                "traffic": r["traffic"],
+                "kernel": r["kernel"] + " (one attention call, back to back)",
+                "peak_source": f"{peak_src} hbm_gbs"}
+
+    per_config = {}
+    for r in results[1:]:
+        per_config[r["name"]] = {
+            "value": round(r["value"], 2), "unit": "GB/s",
+            "pct_of_peak": round(100.0 * r["value"] / (peak * ws), 2),
+            "ms_per_step": round(r["ms_step"], 5),
+            "tokens_per_s": round(r["tokens_all"] / (r["ms_step"] * 1e-3), 1),
+            "decode_ms": round(r["decode_ms"], 5), "append_ms": round(r["append_ms"], 5),
+            "roofline": roofline_of(r), "e2e": e2e_of(r), "cpu_baseline": r["cpu"],
+            "gpu_launches": r["launches"], "dtype": r["dtype"], "config": r["config"],
+            "clocks": sampler.summary(r["t_begin"], r["t_end"]) if sampler else None,
+        }
+
+    e2e = e2e_of(head)
+    e2e["copies"] = ("per step: inputs packed in one pinned buffer, one H2D copy into one of two "
+                     "device staging buffers on a copy stream (overlapping the previous step's "
+                     "compute), output D2H on a second stream")
     line = {
-        "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": ws,
-        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 5),
+        "metric": METRIC, "value": round(head["value"], 2), "unit": "GB/s", "n_gpus": ws,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(head["ms_step"], 5),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": f"e4m3 KV, {s.dtype} q" if fp8 else s.dtype, "data": "synthetic",
-        "config": {"workload": args.config, "description": WORKLOAD_TEXT[args.config],
-                   "num_seqs": s.num_seqs, "num_q_heads": s.num_q_heads,
-                   "num_kv_heads": s.num_kv_heads, "head_dim": s.head_dim,
-                   "block_size": s.block_size, "context_tokens": int(w.context_lens.sum()),
-                   "max_context_len": mcl, "num_splits": mq_parts if mq else splits, "accumulate": "fp32",
-                   "shared_prefix_decode": shared,
-                   "q_len": args.q_len if mq else 1,
-                   "fused_append": fused, "cuda_graph": bool(args.graph),
-                   "layout": layout, "kv_cache": "e4m3" if fp8 else s.dtype,
-                   "kv_bytes_unique": nbytes["kv_unique"],
-                   "decode_bytes_per_step": nbytes["decode"],
-                   "decode_bytes_logical": nbytes["decode_logical"],
-                   "append_bytes_per_step": nbytes["append"],
-                   "l2": "no flush: KV inputs larger than the 129 MB L2",
-                   "parallelism": f"replicas x{ws}" if ws > 1 else "1 GPU"},
-        "pct_of_peak": round(100.0 * value / (peak * ws), 2),
-        "tokens_per_s": round(tokens_all / (ms_step * 1e-3), 1),
-        "decode_ms": round(decode_ms, 5),
-        "append_ms": round(append_ms, 5),
-        "append_gbs": round(nbytes["append"] / (append_ms * 1e-3) / 1e9, 2),
-        "roofline": {"bound": "hbm", "achieved": round(decode_gbs, 2), "peak": peak,
-                     "unit": "GB/s", "frac": round(decode_gbs / peak, 4),
-                     "traffic": traffic,
-                     "kernel": (("prefix_kernel in multi-query mode (tcgen05) + merge_kernel"
-                                 if mq_kernel == "tcgen05" else
-                                 "decode_kernel in multi-query mode"
-                                 + (" + merge_kernel" if mq_parts > 1 else "")) if mq
-                                else "prefix_kernel (with the plan CTA) + decode_kernel + merge_kernel"
-                                if shared else "decode_kernel + merge_kernel")
-                     + " (one attention call, back to back)",
-                     "peak_source": f"{peak_src} hbm_gbs"},
-        "cpu_baseline": cpu,
-        "e2e": {"value": round(bytes_all / (e2e_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
-                "ms_per_step": round(e2e_ms, 5), "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": d2h,
-                "copies": "per step: inputs packed in one pinned buffer, one H2D copy into one "
-                          "of two device staging buffers on a copy stream (overlapping the "
-                          "previous step's compute), output D2H on a second stream"},
-        "gpu_launches": launches_per_step * args.steps,
-        "clocks": clocks,
+        "dtype": head["dtype"], "data": "synthetic",
+        "config": head["config"],
+        "pct_of_peak": round(100.0 * head["value"] / (peak * ws), 2),
+        "tokens_per_s": round(head["tokens_all"] / (head["ms_step"] * 1e-3), 1),
+        "decode_ms": round(head["decode_ms"], 5),
+        "append_ms": round(head["append_ms"], 5),
+        "append_gbs": round(head["nbytes"]["append"] / (head["append_ms"] * 1e-3) / 1e9, 2),
+        "roofline": roofline_of(head),
+        "cpu_baseline": head["cpu"],
+        "e2e": e2e,
+        "gpu_launches": head["launches"],
+        "clocks": sampler.summary(head["t_begin"], head["t_end"]) if sampler else None,
+        "clocks_all_timed_loops": (sampler.summary(results[0]["t_begin"],
+                                                   results[-1]["t_loops_end"])
+                                   if sampler else None),
     }
+    if per_config:
+        line["per_config"] = per_config
     print(json.dumps(line), flush=True)
     if ws > 1:
         dist.destroy_process_group()
@@ -654,7 +730,11 @@ def main(argv=None):
     ap.add_argument("--steps", type=int, default=300)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["mine", "reference"], default="mine")
-    ap.add_argument("--config", default="c2", choices=sorted(WORKLOAD_TEXT))
+    ap.add_argument("--config", default=None, choices=sorted(WORKLOAD_TEXT),
+                    help="one workload only (default: the long-context layer c4 as the "
+                         "headline, plus a per_config line for c2, c3, c5 and c5_bs32)")
+    ap.add_argument("--no-per-config", action="store_true",
+                    help="without --config: the headline workload only")
     ap.add_argument("--splits", type=int, default=0, help="KV partitions (0 = automatic)")
     ap.add_argument("--kv", choices=["16bit", "fp8"], default="16bit",
                     help="cache element type: the workload's 16-bit type or E4M3 codes")
@@ -670,7 +750,10 @@ def main(argv=None):
     ap.add_argument("--q-len", type=int, default=0,
                     help="query tokens per sequence for causal multi-query attention "
                          "(0 = single-token decode)")
-    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--cpu-seconds", type=float, default=8.0,
+                    help="oracle time for the headline's cpu_baseline")
+    ap.add_argument("--cpu-seconds-per-config", type=float, default=3.0,
+                    help="oracle time for each per_config cpu_baseline")
     ap.add_argument("--no-cpu-baseline", dest="cpu_baseline", action="store_false")
     ap.add_argument("--no-prefix-sharing", dest="prefix_sharing", action="store_false",
                     help="decode shared-prefix workloads with the plain path")

@@ -232,16 +232,21 @@ pkv_status pkv_append_decode_attention(void* out, const void* q, const void* k_n
  *
  *   - The array is reserved on every GPU that loads the library and stays
  *     reserved until the process exits.
- *   - The first call on each device (with that device current) looks up the
- *     array's device address; make that first call before any stream capture.
+ *   - The array's device address belongs to one CUDA context.  The first
+ *     call in each context (for most programs the device's primary context,
+ *     so once per device) looks the address up with that context current and
+ *     remembers it under the context's id; make that first call before any
+ *     stream capture.  A context destroyed and replaced (cudaDeviceReset)
+ *     gets a new id, so its successor looks the address up again.
  *   - All calls share the one array, which keeps the previous call's contents.
  *     The kernels overwrite every scratch entry they read, so nothing has to be
  *     cleared, but calls that may run at the same time on the GPU (for
  *     example on two streams without ordering between them) race on it and
  *     corrupt each other's results.  Order them on one stream.
  *   - Returns PKV_ERR_WORKSPACE, launching nothing, when the split plan for
- *     these arguments needs more than PKV_NOALLOC_SCRATCH_BYTES; pass a
- *     smaller num_splits, or use pkv_decode_attention.
+ *     these arguments (the plan pkv_decode_attention makes for a 16-bit
+ *     cache) needs more than PKV_NOALLOC_SCRATCH_BYTES; pass a smaller
+ *     num_splits, or use pkv_decode_attention.
  */
 #define PKV_NOALLOC_SCRATCH_BYTES (8u << 20)
 
@@ -404,6 +409,15 @@ const char* pkv_status_string(pkv_status status);
 
 /* Number of query heads one CTA of the decode kernel serves at most. */
 int pkv_max_group_size(void);
+
+/*
+ * 1 when the library was compiled with -DPKV_DEBUG, else 0.  A debug build
+ * fills every shared-memory ring slot of the decode and tensor-core kernels
+ * with NaN bytes at the start and again whenever its stage is released, so a
+ * read of a slot whose copy has not landed (or of a stage already released)
+ * shows up as NaN in the output.  Slower; for testing only.
+ */
+int pkv_debug_build(void);
 
 #ifdef __cplusplus
 }

@@ -88,6 +88,8 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.pkv_status_string.argtypes = [i]
     lib.pkv_status_string.restype = ctypes.c_char_p
     lib.pkv_max_group_size.argtypes = []
+    lib.pkv_debug_build.argtypes = []
+    lib.pkv_debug_build.restype = i
     lib.pkv_selftest_wait_timeout.argtypes = [p, ctypes.c_ulonglong, p]
     for name in ("pkv_append", "pkv_decode_attention", "pkv_decode_attention_noalloc",
                  "pkv_append_decode_attention", "pkv_append_fp8", "pkv_decode_attention_fp8",
@@ -468,9 +470,10 @@ def decode_attention_noalloc(q: torch.Tensor, k_cache: torch.Tensor, v_cache: to
     Same result, but the split-K scratch is a fixed 8 MiB array inside the
     library (reserved per GPU for the life of the process) and the caller
     passes ``out``, so the call allocates nothing.  Calls share that array:
-    keep calls that use it ordered on one stream.  Make the first call on each
-    device before any stream capture.  Plans needing more scratch than the
-    array holds are rejected (PKV_ERR_WORKSPACE); ask for fewer splits then.
+    keep calls that use it ordered on one stream.  The first call in each CUDA
+    context (normally once per device) looks the array's address up; make it
+    before any stream capture.  Plans needing more scratch than the array
+    holds are rejected (PKV_ERR_WORKSPACE); ask for fewer splits then.
     """
     lib = load()
     b, h_q, d = q.shape

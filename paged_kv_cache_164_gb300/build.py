@@ -20,6 +20,8 @@ CSRC = os.path.join(HERE, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 OUT_DIR = os.path.join(HERE, "_build")
 LIB = os.path.join(OUT_DIR, "libpkv.so")
+# The NaN-sentinel debug build (-DPKV_DEBUG), kept apart from the normal one.
+DEBUG_DIR = os.path.join(HERE, "_build_debug")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-I", INCLUDE,
               "-I", CSRC, "--expt-relaxed-constexpr"]
@@ -36,8 +38,9 @@ def _sources():
     return sorted(glob.glob(os.path.join(CSRC, "*.cu")))
 
 
-def _inputs_digest() -> str:
+def _inputs_digest(flags) -> str:
     h = hashlib.sha256()
+    h.update(" ".join(flags).encode())
     files = _sources() + sorted(glob.glob(os.path.join(CSRC, "*.cuh"))) + \
         [os.path.join(INCLUDE, "pkv.h"), os.path.abspath(__file__)]
     for f in files:
@@ -47,20 +50,26 @@ def _inputs_digest() -> str:
     return h.hexdigest()
 
 
-def build(force: bool = False, verbose: bool = False) -> str:
-    """Compiles and links the library unless an up-to-date build exists."""
-    digest = _inputs_digest()
-    stamp = os.path.join(OUT_DIR, "stamp")
-    if not force and os.path.exists(LIB) and os.path.exists(stamp):
+def build(force: bool = False, verbose: bool = False, debug: bool = False) -> str:
+    """Compiles and links the library unless an up-to-date build exists.
+
+    ``debug``: the -DPKV_DEBUG build (NaN-filled ring slots), in its own
+    directory.  PKV_NVCC_EXTRA adds flags to either build.
+    """
+    extra = os.environ.get("PKV_NVCC_EXTRA", "").split() + (["-DPKV_DEBUG"] if debug else [])
+    out_dir = DEBUG_DIR if debug else OUT_DIR
+    lib = os.path.join(out_dir, "libpkv.so")
+    digest = _inputs_digest(extra)
+    stamp = os.path.join(out_dir, "stamp")
+    if not force and os.path.exists(lib) and os.path.exists(stamp):
         with open(stamp) as f:
             if f.read().strip() == digest:
-                return LIB
-    os.makedirs(OUT_DIR, exist_ok=True)
+                return lib
+    os.makedirs(out_dir, exist_ok=True)
     nvcc = _nvcc()
-    extra = os.environ.get("PKV_NVCC_EXTRA", "").split()
 
     def compile_one(src):
-        obj = os.path.join(OUT_DIR, os.path.basename(src)[:-3] + ".o")
+        obj = os.path.join(out_dir, os.path.basename(src)[:-3] + ".o")
         cmd = [nvcc, *ARCH, *NVCC_FLAGS, *extra, "-c", src, "-o", obj]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
@@ -71,16 +80,17 @@ def build(force: bool = False, verbose: bool = False) -> str:
 
     with concurrent.futures.ThreadPoolExecutor(max_workers=os.cpu_count() or 4) as ex:
         objs = list(ex.map(compile_one, _sources()))
-    tmp = LIB + f".tmp{os.getpid()}"
+    tmp = lib + f".tmp{os.getpid()}"
     cmd = [nvcc, *ARCH, "-shared", "-cudart", "static", "-o", tmp, *objs]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
-    os.replace(tmp, LIB)
+    os.replace(tmp, lib)
     with open(stamp, "w") as f:
         f.write(digest)
-    return LIB
+    return lib
 
 
 if __name__ == "__main__":
-    print(build(force="--force" in sys.argv, verbose="-v" in sys.argv))
+    print(build(force="--force" in sys.argv, verbose="-v" in sys.argv,
+                debug="--debug" in sys.argv))

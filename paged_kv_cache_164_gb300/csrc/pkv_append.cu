@@ -243,6 +243,14 @@ extern "C" const char* pkv_status_string(pkv_status status) {
 
 extern "C" int pkv_max_group_size(void) { return kMaxGroup; }
 
+extern "C" int pkv_debug_build(void) {
+#ifdef PKV_DEBUG
+    return 1;
+#else
+    return 0;
+#endif
+}
+
 extern "C" pkv_status pkv_append_fp8(const void* k_new, const void* v_new, void* k_cache,
                                      void* v_cache, const int64_t* slot_mapping, int num_tokens,
                                      int num_blocks, int block_size, int num_kv_heads,

@@ -73,4 +73,11 @@ inline bool take_layout(pkv_dtype& dtype) {
 
 constexpr int kMaxGroup = 16;  // query heads per KV head served by one CTA
 
+// Workspace bytes the 16-bit decode (pkv_decode_attention) plans for these
+// arguments on the current device: the same plan decode_impl makes, not the
+// larger of the 16-bit and E4M3 plans pkv_decode_workspace_size reports.
+pkv_status decode_workspace_16bit(int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
+                                  int block_size, int max_context_len, int num_splits,
+                                  size_t* bytes);
+
 }  // namespace pkv

@@ -156,6 +156,21 @@ __device__ __forceinline__ bool wait_phase(uint32_t bar, uint32_t parity, volati
     }
 }
 
+#ifdef PKV_DEBUG
+// Debug builds (-DPKV_DEBUG) fill ring slots with all-ones bytes, a NaN in
+// fp16, bf16 and E4M3 alike, whenever their contents stop being valid: the
+// whole ring at the start, and each slot when its stage is released.  A read
+// of a slot whose copy has not landed, or of a stage already released, then
+// turns the output to NaN instead of passing unnoticed.  `lanes` threads
+// (lane index `lane`) share the fill; each makes its writes visible to the
+// async proxy, which writes the slot next.
+__device__ __forceinline__ void poison_smem(uint8_t* base, int bytes, int lane, int lanes) {
+    for (int i = lane; i < bytes / 16; i += lanes)
+        reinterpret_cast<uint4*>(base)[i] = make_uint4(~0u, ~0u, ~0u, ~0u);
+    ptx::fence_proxy_async_smem();
+}
+#endif
+
 // Two E4M3 codes (the first in the low byte) as a pair of T, exactly: every
 // E4M3 value is an fp16 (and a bf16) value.
 __device__ __forceinline__ uint32_t e4m3x2_to(uint32_t v, __half) {
@@ -532,6 +547,9 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
             ptx::prefetch_tensormap(&tm_v);
         }
     }
+#ifdef PKV_DEBUG
+    poison_smem(ring, Cfg::kRingBytes, tid, kThreads);
+#endif
     __syncthreads();
 
     const uint32_t ring_addr = ptx::smem_addr(ring);
@@ -664,6 +682,10 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
                                                       p.scale_log2, lane);
             }
             __syncwarp();
+#ifdef PKV_DEBUG
+            poison_smem(ring + slot * Cfg::kStageBytes, Cfg::kStageBytes, lane, 32);
+            __syncwarp();
+#endif
             if (lane == 0) ptx::mbar_arrive(ptx::smem_addr(&empty_bar[slot]));
         }
     }
@@ -1206,6 +1228,9 @@ prefix_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
         ptx::tmem_alloc(ptx::smem_addr(tmem_slot), Cfg::kTmemCols);
         ptx::tmem_relinquish_alloc_permit();
     }
+#ifdef PKV_DEBUG
+    poison_smem(ring, NS * Cfg::kStageBytes, tid, (SW + 2) * 32);
+#endif
     ptx::tc_fence_before_sync();
     __syncthreads();
     ptx::tc_fence_after_sync();
@@ -1239,6 +1264,15 @@ prefix_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
             if (j >= NS && !warp_wait_phase(ptx::smem_addr(&empty_bar[slot]), ((j / NS) - 1) & 1,
                                             abort_flag, p.err_flag))
                 break;
+#ifdef PKV_DEBUG
+            // the tensor core has finished reading the slot: nothing may read it again
+            // before this tile's copies land
+            if (j >= NS) {
+                ptx::tc_fence_after_sync();
+                poison_smem(ring + slot * Cfg::kStageBytes, Cfg::kStageBytes, lane, 32);
+                __syncwarp();
+            }
+#endif
             const uint32_t kdst = ring_addr + slot * Cfg::kStageBytes;
             const uint32_t fb = ptx::smem_addr(&full_bar[slot]);
             const int tok0 = t_begin + j * TT + bx * kStageTokens;
@@ -2138,6 +2172,16 @@ static pkv_status make_mq_plan(int num_seqs, int q_len, int num_q_heads, int num
     mp->workspace_bytes =
         (size_t)num_seqs * q_len * num_q_heads * mp->slots * (head_dim + 1) * sizeof(float) + 256;
     return PKV_OK;
+}
+
+pkv_status decode_workspace_16bit(int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
+                                  int block_size, int max_context_len, int num_splits,
+                                  size_t* bytes) {
+    Plan plan;
+    const pkv_status st = make_plan(num_seqs, num_q_heads, num_kv_heads, head_dim, block_size,
+                                    max_context_len, num_splits, &plan);
+    if (st == PKV_OK) *bytes = plan.workspace_bytes;
+    return st;
 }
 
 }  // namespace pkv

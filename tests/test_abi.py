@@ -143,3 +143,16 @@ def test_binding_refuses_cpu_tensors(lib):
     k = torch.zeros(4, 16, 2, 64, dtype=torch.float16)
     with pytest.raises(ValueError, match="CUDA"):
         pkv.append(k[:1, 0], k[:1, 0], k, k, torch.zeros(1, dtype=torch.int64))
+
+
+def test_library_sources_allocate_no_device_memory():
+    # The library allocates nothing on the device: the caller passes every
+    # buffer (and the no-alloc entry point uses a static array).  No source of
+    # the library names an allocating runtime or driver call.
+    csrc = os.path.join(os.path.dirname(os.path.dirname(__file__)), "paged_kv_cache_164_gb300",
+                        "csrc")
+    banned = re.compile(r"\b(cudaMalloc\w*|cudaFree\w*|cuMemAlloc\w*|cuMemFree\w*|"
+                        r"cudaMallocAsync|cudaMemPool\w*|cuMemCreate)\b")
+    for name in sorted(os.listdir(csrc)):
+        text = open(os.path.join(csrc, name)).read()
+        assert not banned.search(text), f"{name} names {banned.search(text).group(0)}"
