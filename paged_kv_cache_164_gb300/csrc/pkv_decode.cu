@@ -888,6 +888,11 @@ struct PrefixParams {
     PlanParams plan;
 };
 
+// Pages of a tensor-core kernel partition (its block-table slice in shared
+// memory): multi-query partitions of up to 4096 tokens at 16-token pages,
+// one per (sequence, KV head) on a 4096-token context, measured faster than
+// two of 2048 (Llama-70B layer, 8 query tokens: 54.9 -> 60.4 % of peak).
+constexpr int kPrefixMaxChunkPages = 256;
 constexpr int kPrefixTileRows = 128;     // query rows per CTA (MMA M)
 constexpr int kPrefixTileTokens = 64;    // tokens per tile (N of S, K of O)
 constexpr int kPrefixStages = 4;
@@ -914,7 +919,7 @@ struct PrefixTile {
     // full[stages], empty[stages], s_full[2], p_ready[2], o_done[2], q_ready, drain
     static constexpr int kBarriers = 2 * NSTG + 8;
     static constexpr int kSmemBytes = 1024 + kQBytes + NSTG * kStageBytes + kXchBytes +
-                                      kBarriers * 8 + (kMaxChunkPages + 1) * 4 + 64;
+                                      kBarriers * 8 + (kPrefixMaxChunkPages + 1) * 4 + 64;
     // S0, S1 (64 columns each; P of the tile overwrites its S as hi/lo 16-bit
     // pairs), O_a, O_b (D columns each).  ONE_ACC: one S/P buffer, Q as 16-bit
     // pairs (D/2 columns) where S1 would be, and only O_a.
@@ -1107,9 +1112,9 @@ prefix_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
     uint64_t* q_ready = o_done + 2;
     uint64_t* drain = q_ready + 1;
     int* table = reinterpret_cast<int*>(bars + Cfg::kBarriers);
-    volatile int* abort_flag = table + kMaxChunkPages + 1;
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(table + kMaxChunkPages + 2);
-    int* warp_lim = table + kMaxChunkPages + 3;  // [SW]
+    volatile int* abort_flag = table + kPrefixMaxChunkPages + 1;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(table + kPrefixMaxChunkPages + 2);
+    int* warp_lim = table + kPrefixMaxChunkPages + 3;  // [SW]
 
     const int rt = blockIdx.x;                     // tile of 128 query rows
     const int g = blockIdx.y % p.num_kv_heads;     // KV head
@@ -1925,9 +1930,55 @@ static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 // tokens x 1 block.  Head major [num_blocks][H_kv][block_size][D]: dims D,
 // block_size, H_kv, num_blocks; box 64 dims x 16 tokens x 1 head x 1 block.
 // 128-byte swizzle either way, so a box lands as 16 rows of 128 bytes.
+//
+// Encoded maps are remembered (a few dozen, the oldest replaced first): a map
+// is a pure function of its arguments (the base address and the geometry), so
+// a remembered map stays right whatever happens to the memory behind it, and
+// the calls of a decode loop over the same caches skip the encoding.
+struct CacheMapKey {
+    const void* base;
+    int dtype, num_blocks, block_size, num_kv_heads, head_dim;
+    bool hnd, f8;
+    bool operator==(const CacheMapKey& o) const {
+        return base == o.base && dtype == o.dtype && num_blocks == o.num_blocks &&
+               block_size == o.block_size && num_kv_heads == o.num_kv_heads &&
+               head_dim == o.head_dim && hnd == o.hnd && f8 == o.f8;
+    }
+};
+constexpr int kCacheMapEntries = 32;
+static std::mutex g_map_mutex;
+static CacheMapKey g_map_keys[kCacheMapEntries];
+static CUtensorMap g_maps[kCacheMapEntries];
+static int g_map_count = 0, g_map_next = 0;
+
+static bool encode_cache_map(CUtensorMap* map, const void* base, pkv_dtype dtype, int num_blocks,
+                             int block_size, int num_kv_heads, int head_dim, bool hnd, bool f8);
+
 static bool make_cache_map(CUtensorMap* map, const void* base, pkv_dtype dtype, int num_blocks,
                            int block_size, int num_kv_heads, int head_dim, bool hnd,
                            bool f8 = false) {
+    const CacheMapKey key{base, (int)dtype, num_blocks, block_size, num_kv_heads, head_dim, hnd, f8};
+    {
+        std::lock_guard<std::mutex> lock(g_map_mutex);
+        for (int i = 0; i < g_map_count; ++i)
+            if (g_map_keys[i] == key) {
+                *map = g_maps[i];
+                return true;
+            }
+    }
+    if (!encode_cache_map(map, base, dtype, num_blocks, block_size, num_kv_heads, head_dim, hnd,
+                          f8))
+        return false;
+    std::lock_guard<std::mutex> lock(g_map_mutex);
+    const int i = g_map_count < kCacheMapEntries ? g_map_count++ : g_map_next;
+    g_map_next = (i + 1) % kCacheMapEntries;
+    g_map_keys[i] = key;
+    g_maps[i] = *map;
+    return true;
+}
+
+static bool encode_cache_map(CUtensorMap* map, const void* base, pkv_dtype dtype, int num_blocks,
+                             int block_size, int num_kv_heads, int head_dim, bool hnd, bool f8) {
     PFN_cuTensorMapEncodeTiled_v12000 fn = encode_fn();
     if (fn == nullptr) return false;
     const cuuint64_t e = f8 ? 1 : 2;
@@ -2109,7 +2160,7 @@ static pkv_status make_prefix_plan(int num_seqs, int num_q_heads, int num_kv_hea
 // the same context together, planned like a decode.  More rows: 128-row
 // tiles per (sequence, KV head) on the tensor-core kernel; the context in
 // partitions of whole 64-token tiles, as many as give about one CTA per SM,
-// at most kMaxChunkPages pages each.
+// at most kPrefixMaxChunkPages pages each.
 constexpr int kMqDecodeRowBlocks = 2;
 struct MultiQueryPlan {
     bool on_decode;  // the decode kernel's multi-query form
@@ -2161,7 +2212,7 @@ static pkv_status make_mq_plan(int num_seqs, int q_len, int num_q_heads, int num
     const int64_t want = std::max<int64_t>(
         1, (int64_t)sms * (mp->dup ? kMqDupCtasPerSm : ctas_per_sm_of_mode(kMqFullMode)) / units);
     const int tiles = std::max(1, (max_context_len + kPrefixTileTokens - 1) / kPrefixTileTokens);
-    const int max_tiles = kMaxChunkPages * block_size / kPrefixTileTokens;
+    const int max_tiles = kPrefixMaxChunkPages * block_size / kPrefixTileTokens;
     const int chunk_tiles =
         (int)std::min<int64_t>(max_tiles, std::max<int64_t>(1, (tiles + want - 1) / want));
     mp->chunk = chunk_tiles * kPrefixTileTokens;
