@@ -58,6 +58,14 @@ CASES = {
     "gqa4_d64_bs32_q6_rows24": dict(name="c5_bs32", q_len=6, num_seqs=4, head_dim=64,
                                     lengths=("uniform", 30, 2500), max_len_cap=2560,
                                     shared_prefix_groups=0, seed=74),
+    # many ragged units (some shorter than one tile) at 32-token pages; long
+    # contexts split into many partitions and merged; fp16 MHA with 20 rows
+    "gqa8_q3_many_ragged_bs32": dict(name="c3", q_len=3, num_seqs=12, block_size=32,
+                                     lengths=("uniform", 3, 3000), max_len_cap=3008, seed=75),
+    "gqa8_q6_long_merged": dict(name="c3", q_len=6, num_seqs=2,
+                                lengths=("uniform", 20000, 40000), max_len_cap=40000, seed=76),
+    "mha_fp16_q20_rows20": dict(name="c2", q_len=20, num_seqs=3, num_q_heads=4, num_kv_heads=4,
+                                lengths=("uniform", 20, 1500), max_len_cap=1536, seed=77),
 }
 
 
