@@ -347,7 +347,7 @@ def _measure(name, args, device, rank, ws, cpu_seconds):
     fp8 = args.kv == "fp8"
     k_scale = v_scale = 1.0
     if fp8:
-        if mq or args.fused or s.shared_prefix_groups and args.prefix_sharing:
+        if mq or s.shared_prefix_groups and args.prefix_sharing:
             raise SystemExit("--kv fp8 times the plain decode path only "
                              "(add --no-prefix-sharing for shared-prefix workloads)")
         k_scale = float(w.k_cache.float().abs().max()) / 448.0
@@ -386,8 +386,10 @@ def _measure(name, args, device, rank, ws, cpu_seconds):
     flag = pkv.new_error_flag(device)
     # append, decode, merge when split; the shared-prefix path: append, prefix
     # (with the plan as one of its CTAs), decode, merge
-    # --fused: the append is done by the decode kernel (plain path only)
-    fused = args.fused and not mq and not shared
+    # The step's append is done by the decode kernel itself
+    # (pkv_append_decode_attention) on the plain 16-bit path; --unfused times
+    # the two calls (pkv_append, then pkv_decode_attention) instead.
+    fused = args.fused and not mq and not shared and not fp8
     if mq:
         launches_per_step = 2 + (1 if mq_kernel == "tcgen05" or mq_parts > 1 else 0)
     else:
@@ -501,7 +503,9 @@ def _measure(name, args, device, rank, ws, cpu_seconds):
     # As a serving loop would: the inputs travel as one packed copy into one of
     # two device staging buffers on a copy stream, so step i+1's inputs move
     # while step i computes, and step i's output returns on another stream.
-    names = ("q", "k_new", "v_new", "slot_mapping", "block_tables", "context_lens")
+    # (the fused step derives each new token's slot itself: no slot mapping)
+    names = ("q", "k_new", "v_new") + (() if fused else ("slot_mapping",)) + \
+        ("block_tables", "context_lens")
     srcs = {k: getattr(w, k) for k in names}
     offs, total = {}, 0
     for k in names:
@@ -542,8 +546,16 @@ def _measure(name, args, device, rank, ws, cpu_seconds):
         stream.wait_event(in_ready[sidx])
         stream.wait_event(out_free[sidx])          # this output buffer's copy-out is done
         v = views[sidx]
-        append_call(i % KV_COPIES, v["k_new"], v["v_new"], v["slot_mapping"])
-        decode_call(i % KV_COPIES, v["q"], v["block_tables"], v["context_lens"], out=outs[sidx])
+        if fused:
+            kc, vc = caches[i % KV_COPIES]
+            pkv.append_decode_attention(v["q"], v["k_new"], v["v_new"], kc, vc,
+                                        v["block_tables"], v["context_lens"], mcl,
+                                        scale=w.scale, num_splits=args.splits, out=outs[sidx],
+                                        workspace=workspace, err_flag=flag, layout=layout)
+        else:
+            append_call(i % KV_COPIES, v["k_new"], v["v_new"], v["slot_mapping"])
+            decode_call(i % KV_COPIES, v["q"], v["block_tables"], v["context_lens"],
+                        out=outs[sidx])
         in_free[sidx].record(stream)
         done[sidx].record(stream)
         d2h_stream.wait_event(done[sidx])
@@ -743,8 +755,10 @@ def main(argv=None):
                          "[blocks][H_kv][bs][d]")
     ap.add_argument("--block-size", type=int, default=0,
                     help="tokens per page (0 = the workload's own)")
-    ap.add_argument("--fused", action="store_true",
-                    help="append inside the decode launch (pkv_append_decode_attention)")
+    ap.add_argument("--unfused", dest="fused", action="store_false",
+                    help="time the step as two calls, pkv_append then the decode, instead of "
+                         "the decode launch appending the new tokens itself "
+                         "(pkv_append_decode_attention, the default on the plain 16-bit path)")
     ap.add_argument("--graph", action="store_true",
                     help="time replays of one step captured in a CUDA graph")
     ap.add_argument("--q-len", type=int, default=0,
