@@ -58,15 +58,19 @@ WORKLOAD_TEXT = {
 # (profiles/), keyed by workload; valid only for the kernel sources they were
 # measured on (digest of csrc/), else reported as null.
 NCU_TRAFFIC = {
-    # ncu --metrics dram__bytes_read.sum,dram__bytes_write.sum -k regex:decode_kernel -s 4 -c 1
-    "c2": {"digest": "19dbfe7793078903", "splits": 2, "shared": False,
-           "bytes": 2312578048 + 3610112},
-    "c3": {"digest": "19dbfe7793078903", "splits": 3, "shared": False,
-           "bytes": 537488128 + 4089856},
-    # shared-prefix path: decode_kernel (suffixes) + prefix_kernel (-k regex:prefix_kernel
-    # -s 2 -c 1); the merge kernel's few MB are not included
-    "c5": {"digest": "19dbfe7793078903", "splits": 8, "shared": True,
-           "bytes": (1531689216 + 5015552) + (35768320 + 57600)},
+    # ncu --metrics dram__bytes_read.sum,dram__bytes_write.sum,gpu__time_duration.sum
+    #     --clock-control none -k regex:decode_kernel -s 4 -c 1 (the fused default step)
+    "c4": {"digest": "94d3ffb64ff791f9", "splits": 64, "shared": False, "fused": True,
+           "bytes": 2818481408 + 7712256},
+    "c2": {"digest": "94d3ffb64ff791f9", "splits": 2, "shared": False, "fused": True,
+           "bytes": 2312643840 + 4651264},
+    "c3": {"digest": "94d3ffb64ff791f9", "splits": 3, "shared": False, "fused": True,
+           "bytes": 537483264 + 4017920},
+    # shared-prefix path: decode_kernel (suffixes) + prefix_kernel
+    # (-k regex:"decode_kernel|prefix_kernel" -s 8 -c 2); the merge kernel's few MB
+    # are not included
+    "c5": {"digest": "94d3ffb64ff791f9", "splits": 8, "shared": True, "fused": False,
+           "bytes": (1531841024 + 3346176) + (35771392 + 68608)},
 }
 
 
@@ -591,8 +595,8 @@ def _measure(name, args, device, rank, ws, cpu_seconds):
     traffic = None
     rec = NCU_TRAFFIC.get(name)
     if rec and rec.get("digest") == _kernel_digest() and rec.get("splits") == splits and \
-            rec.get("shared") == shared and not mq and layout == "nhd" and not args.block_size \
-            and not fp8:
+            rec.get("shared") == shared and rec.get("fused") == fused and not mq and \
+            layout == "nhd" and not args.block_size and not fp8:
         traffic = rec["bytes"]
 
     cpu = None
