@@ -694,7 +694,10 @@ def run_gpu(args):
                 "unit": "GB/s", "frac": round(r["decode_gbs"] / peak, 4),
                 "traffic": r["traffic"],
                 "kernel": r["kernel"] + " (one attention call, back to back)",
-                "peak_source": f"{peak_src} hbm_gbs"}
+                "peak_source": f"{peak_src} hbm_gbs",
+                "peak_kind": "a device-to-device copy (half reads, half writes); this path "
+                             "only reads (KV, q) and writes little, so a call can read a few "
+                             "percent above it"}
 
     per_config = {}
     for r in results[1:]:
