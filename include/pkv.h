@@ -285,6 +285,22 @@ pkv_status pkv_decode_attention_noalloc(void* out, const void* q, const void* k_
  *                     (still the correct result)
  * The precondition that members' tables hold the group's prefix blocks is not
  * checked: the prefix is read from the first member's table.
+ *
+ * Streams: the call queues a plan on `stream`, then runs the prefix kernel on a
+ * second stream of the library's own (one per CUDA context, made on the
+ * context's first such call, highest priority), forked from `stream` after the
+ * plan by an event and joined back before the call returns, so that the
+ * prefix and the suffix decode run at the same time.  Work queued on `stream`
+ * before the call is complete before either starts, and work queued after it
+ * sees the whole result, as with a single-stream call; the fork and join are
+ * ordinary event records and waits, so the call can be captured in a CUDA
+ * graph (make the first call in each context outside the capture, since it
+ * creates the stream and its events).  Calls from several host threads are
+ * serialised on the host around the fork and join.  When the side stream cannot
+ * be had (no current context id, more than 64 contexts), the prefix kernel runs
+ * on `stream` between the plan and the decode.  There is no separate merge
+ * launch: the CTA that writes the last partial of a (sequence, KV head) merges
+ * it, counting down a per-unit count that the plan sets in the workspace.
  */
 size_t pkv_prefix_shared_workspace_size(int num_seqs, int num_q_heads, int num_kv_heads,
                                         int head_dim, int block_size, int max_context_len,

@@ -80,4 +80,10 @@ pkv_status decode_workspace_16bit(int num_seqs, int num_q_heads, int num_kv_head
                                   int block_size, int max_context_len, int num_splits,
                                   size_t* bytes);
 
+// Id of the CUDA context current to this thread (the one the launches use);
+// false when none is current yet or the driver cannot say.  cuCtxGetId never
+// reuses an id within a process, so per-context state keyed by it cannot be
+// served to a context that replaced a destroyed one.
+bool current_context_id(unsigned long long* id);
+
 }  // namespace pkv

@@ -96,6 +96,9 @@ struct DecodeParams {
     float v_scale;       // value of one V unit: 1, or the V scale of an E4M3 cache
     int q_len;           // > 0 (multi-query): columns are (query token, head), causal
     int row_blocks;      // multi-query: CTAs per (sequence, KV head), NT * 8 rows each
+    // nullable (shared-prefix calls): per unit (sequence, KV head), the partials
+    // still to be written; the CTA that writes a unit's last one merges its rows
+    int* unit_left;
 };
 
 // Context length of sequence b as the kernels use it: negative or too long
@@ -402,6 +405,133 @@ __device__ __forceinline__ void stage_update(uint32_t kbase, uint32_t vbase, int
         v_pass(std::true_type{});
     else
         v_pass(std::false_type{});
+}
+
+// Merge of split partials (log-sum-exp rule): one warp per (row of q, query
+// head), four rows per CTA.  Each lane owns float4 columns of the head (lane,
+// lane + 32, ...) and weighs every partition itself: w_p = e^(lse_p - m*),
+// out = sum_p w_p O_p / sum_p w_p; m* and sum_p w_p come from lane-strided
+// sums and shuffles.  No shared memory and no CTA barrier: rows are short,
+// and the merge of a call is a few thousand of them.  With context_lens given
+// (the decode path), a sequence whose context fitted a single partition was
+// written by the decode kernel and is skipped, and only the partitions that
+// hold tokens are read.  Multi-query rows (q_len > 0) are merged from the
+// partitions of their sequence's context; with mq_direct (the decode kernel's
+// multi-query form) a context that fitted one partition was written directly
+// and is skipped.  Without context_lens (pkv_merge), every row merges all
+// num_splits partials.
+struct MergeParams {
+    void* out;
+    const float* partial_o;
+    const float* partial_lse;
+    const int32_t* context_lens;  // nullable
+    const int2* seq_info;         // nullable: shared-prefix tokens and prefix partials per sequence
+    int num_q_heads;
+    int num_kv_heads;
+    int group;                    // query heads per KV head
+    int num_splits;
+    int head_dim;                 // a multiple of 4, at most 512
+    int chunk_tokens;
+    int cap;                      // context clamp, as in the decode kernel
+    int q_len;                    // > 0: multi-query rows (sequence, query token)
+    int mq_slots;                 // multi-query: partial slots per context partition (1 or 2)
+    bool mq_direct;               // multi-query partials of the decode kernel (single ones direct)
+    int64_t rows;                 // (row of q, query head) pairs
+};
+
+constexpr int kMergeRowsPerCta = 4;
+constexpr int kMergeThreads = kMergeRowsPerCta * 32;
+constexpr int kMergeMaxHeadDim = 512;
+
+// One row's merge, by one warp (lane = its lane).  The partials are read
+// through L2 (ld.global.cg): the kernels that merge a unit's rows as soon as
+// its last partial is written read what other CTAs of the same launch, or of
+// a launch running beside it, have just written.
+template <typename T>
+__device__ __forceinline__ void merge_row(const MergeParams& p, int64_t row, int lane) {
+    const int b = (int)(row / p.num_q_heads);  // row of q: a sequence, or (sequence, query token)
+    int ns = p.num_splits;
+    if (p.q_len > 0) {
+        // multi-query partials: the partitions of the sequence's context
+        const int n = clamped_len(__ldg(p.context_lens + b / p.q_len), p.cap);
+        if (p.mq_direct) {
+            ns = suffix_partitions(n, 0, p.chunk_tokens);
+            if (ns <= 1) return;  // written directly by the decode kernel
+        } else {
+            ns = (n + p.chunk_tokens - 1) / p.chunk_tokens * p.mq_slots;
+        }
+    } else if (p.context_lens != nullptr) {
+        int start = 0, slot0 = 0;
+        if (p.seq_info != nullptr) {
+            const int2 si = __ldcg(p.seq_info + b);
+            start = si.x;
+            slot0 = si.y;
+        }
+        const int n = clamped_len(__ldg(p.context_lens + b), p.cap);
+        ns = slot0 + suffix_partitions(max(0, n - start), slot0, p.chunk_tokens);
+        if (slot0 == 0 && ns <= 1) return;  // written directly by the decode kernel
+    }
+    const float* lse = p.partial_lse + row * p.num_splits;
+    // m* = max_p lse_p and 1 / sum_p e^(lse_p - m*)
+    float mx = -INFINITY;
+    for (int sp = lane; sp < ns; sp += 32) mx = fmaxf(mx, __ldcg(lse + sp));
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+    float den = 0.f;
+    if (mx != -INFINITY)
+        for (int sp = lane; sp < ns; sp += 32) {
+            const float ls = __ldcg(lse + sp);
+            if (ls != -INFINITY) den += exp2f((ls - mx) * kLog2e);
+        }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) den += __shfl_xor_sync(0xffffffffu, den, off);
+    const float inv = den > 0.f ? 1.f / den : 0.f;
+    const int cols = p.head_dim / 4;
+    const float* po = p.partial_o + row * p.num_splits * p.head_dim;
+    T* out = static_cast<T*>(p.out) + row * p.head_dim;
+    // Lane-owned float4 columns c = lane + 32k.  Weights come 32 partitions at
+    // a time, one per lane, and reach the other lanes by shuffles; each lane
+    // reads its columns of kMergeBatch partials before it adds any of them, so
+    // the partials' reads overlap instead of waiting on one another.  A zero
+    // weight (an empty partition, whose O may hold anything) adds nothing.
+    constexpr int kMergeBatch = 8;
+    for (int k = 0; 32 * k < cols; ++k) {
+        const int c = lane + 32 * k;
+        const bool col_ok = c < cols;
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (mx != -INFINITY)
+            for (int s0 = 0; s0 < ns; s0 += 32) {
+                const int sl = s0 + lane;
+                const float ls = sl < ns ? __ldcg(lse + sl) : -INFINITY;
+                const float wl = ls == -INFINITY ? 0.f : exp2f((ls - mx) * kLog2e);
+                const int nb = min(32, ns - s0);
+                for (int u0 = 0; u0 < nb; u0 += kMergeBatch) {
+                    float4 v[kMergeBatch];
+#pragma unroll
+                    for (int u = 0; u < kMergeBatch; ++u)
+                        v[u] = (col_ok && u0 + u < nb)
+                                   ? __ldcg(reinterpret_cast<const float4*>(
+                                         po + (int64_t)(s0 + u0 + u) * p.head_dim + c * 4))
+                                   : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+                    for (int u = 0; u < kMergeBatch; ++u) {
+                        const float wgt = __shfl_sync(0xffffffffu, wl, u0 + u);
+                        if (wgt != 0.f) {
+                            acc.x = fmaf(wgt, v[u].x, acc.x);
+                            acc.y = fmaf(wgt, v[u].y, acc.y);
+                            acc.z = fmaf(wgt, v[u].z, acc.z);
+                            acc.w = fmaf(wgt, v[u].w, acc.w);
+                        }
+                    }
+                }
+            }
+        if (col_ok) {
+            uint2 packed;
+            packed.x = pack2(acc.x * inv, acc.y * inv, T());
+            packed.y = pack2(acc.z * inv, acc.w * inv, T());
+            *reinterpret_cast<uint2*>(out + c * 4) = packed;
+        }
+    }
 }
 
 // NT = number of 8-column groups (1: up to 8 query rows, 2: up to 16); F8:
@@ -793,6 +923,36 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
             }
         }
     }
+
+    // Shared-prefix calls (16-bit caches, one query per sequence): the CTA
+    // that writes the last of a unit's partials (prefix partitions and suffix
+    // partitions alike) merges the unit's rows.
+    if (!MQ && !F8 && p.unit_left != nullptr && !direct) {
+        __threadfence();  // this thread's partials, before the count below
+        __syncthreads();
+        int* last = table;  // the table slice is not read after the main loop
+        if (tid == 0)
+            *last = atomicAdd(p.unit_left + (int64_t)b * p.num_kv_heads + g, -1) == 1;
+        __syncthreads();
+        if (*last) {
+            __threadfence();
+            MergeParams mp = {};
+            mp.out = p.out;
+            mp.partial_o = p.partial_o;
+            mp.partial_lse = p.partial_lse;
+            mp.context_lens = p.context_lens;
+            mp.seq_info = p.seq_info;
+            mp.num_q_heads = p.num_q_heads;
+            mp.num_kv_heads = p.num_kv_heads;
+            mp.group = p.group;
+            mp.num_splits = p.num_splits;
+            mp.head_dim = D;
+            mp.chunk_tokens = p.chunk_tokens;
+            mp.cap = cap;
+            for (int h = warp; h < p.group; h += kThreads / 32)
+                merge_row<T>(mp, (int64_t)b * p.num_q_heads + g * p.group + h, lane);
+        }
+    }
 }
 
 // ---------------------------------------------------------------------------
@@ -832,12 +992,16 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
 // Shared-prefix decode: the plan
 // ---------------------------------------------------------------------------
 // One CTA writes, for every sequence, its (shared-prefix tokens, prefix
-// partials) record and the compact list of the suffix partitions that hold
-// tokens, unit by unit ((sequence, KV head) pairs, KV head fastest).  The
-// decode grid is sized for the longest sequence; with the list, only real
-// partitions get a CTA and the rest of the grid exits at once.  The plan runs
-// as an extra CTA of the prefix kernel's launch (it needs nothing the prefix
-// CTAs compute), so it costs neither a launch nor a serial step.
+// partials) record, the compact list of the suffix partitions that hold
+// tokens, unit by unit ((sequence, KV head) pairs, KV head fastest), and each
+// unit's count of partials to come.  The decode grid is sized for the longest
+// sequence; with the list, only real partitions get a CTA and the rest of the
+// grid exits at once.  The plan is a launch of its own on the caller's stream,
+// ahead of both the suffix decode and the prefix kernel (which runs beside the
+// decode on a second stream), so neither waits for the other.
+
+constexpr int kPlanThreads = 1024;
+constexpr int kPlanStagedGroups = 4096;
 
 struct PlanParams {
     const int32_t* context_lens;
@@ -846,6 +1010,7 @@ struct PlanParams {
     int2* seq_info;   // [B] out
     int2* items;      // out: (unit, partition)
     int* item_count;  // out
+    int* unit_left;   // out: per unit, the partials (prefix and suffix) still to be written
     int32_t* err_flag;
     int num_seqs;
     int num_kv_heads;
@@ -857,6 +1022,7 @@ struct PlanParams {
     int prefix_chunk;
     int chunk_tokens;
     int cap;
+    int group;        // query heads per KV head
 };
 
 struct PrefixParams {
@@ -884,8 +1050,12 @@ struct PrefixParams {
     int q_len;            // 0: shared prefixes; > 0: multi-query (q_len query tokens per sequence)
     bool hnd;             // head-major cache layout
     float scale_log2;
-    bool with_plan;       // grid z slice 0 is the plan (its CTA (0, 0, 0)); partitions follow
-    PlanParams plan;
+    // Shared prefixes (MODE 0): the CTA that writes the last partial of a unit
+    // (sequence, KV head) merges the unit's rows into out; nullable.
+    int* unit_left;
+    void* out;
+    const int2* seq_info;
+    int suffix_chunk;     // tokens per suffix partition
 };
 
 // Pages of a tensor-core kernel partition (its block-table slice in shared
@@ -989,50 +1159,71 @@ __device__ __forceinline__ void split_hi_lo(float p0, float p1, uint32_t& hi, ui
     lo = pack2(p0 - back.x, p1 - back.y, __half());
 }
 
-// The plan, run by one CTA of any width (a multiple of 32, at most 1024).
-// scratch: 33 ints of shared memory.
-__device__ void plan_cta(const PlanParams& p, int* scratch) {
-    int* warp_sum = scratch;  // [32] exclusive prefix of the warp totals
-    int* base = scratch + 32;
+// The plan of a shared-prefix call, one CTA.  Every
+// KV head of a sequence has the same suffix partitions, so one block-wide
+// scan over the sequences' partition counts places all the units: unit
+// (b, g) starts at H_kv * (partitions of the sequences before b) + g * c_b.
+// The group bounds are read into shared memory first (when there are at most
+// kPlanStagedGroups groups), so each sequence's search of them costs no
+// round trips to memory.
+__global__ void __launch_bounds__(kPlanThreads) plan_kernel(const PlanParams p) {
+    __shared__ int s_start[kPlanStagedGroups + 1];
+    __shared__ int s_plen[kPlanStagedGroups];
+    __shared__ int warp_sum[kPlanThreads / 32];  // exclusive prefix of the warp totals
+    __shared__ int s_base;
     const int tid = threadIdx.x;
     const int lane = tid & 31;
     const int warp = tid >> 5;
-    const int nthreads = blockDim.x;
-    const int nwarps = nthreads >> 5;
+    constexpr int kWarps = kPlanThreads / 32;
+    ptx::launch_dependents();
+    ptx::grid_dependency_wait();  // lengths and groups may come from the previous kernel
 
-    // 1. per-sequence prefix records (a search of group_start)
-    for (int b = tid; b < p.num_seqs; b += nthreads) {
-        int2 info = make_int2(0, 0);
-        if (p.num_groups > 0) {
-            int lo = 0, hi = p.num_groups - 1;  // last group with group_start <= b
-            while (lo < hi) {
-                const int mid = (lo + hi + 1) >> 1;
-                if (p.group_start[mid] <= b) lo = mid; else hi = mid - 1;
-            }
-            int first, last, plen;
-            if (group_valid(p.group_start, p.group_prefix_len, lo, p.num_seqs, p.max_group_size,
-                            p.max_prefix_len, p.block_size, p.max_blocks_per_seq, first, last,
-                            plen) &&
-                first <= b && b < last)
-                info = make_int2(plen, (plen + p.prefix_chunk - 1) / p.prefix_chunk);
-            else
-                flag_error(p.err_flag, PKV_EFLAG_GROUP);
-        }
-        p.seq_info[b] = info;
+    // the first sequences' lengths, read while the group bounds are staged
+    int n_raw = tid < p.num_seqs ? __ldg(p.context_lens + tid) : 0;
+    const bool staged = p.num_groups > 0 && p.num_groups <= kPlanStagedGroups;
+    if (staged) {
+        for (int i = tid; i <= p.num_groups; i += kPlanThreads) s_start[i] = p.group_start[i];
+        for (int i = tid; i < p.num_groups; i += kPlanThreads) s_plen[i] = p.group_prefix_len[i];
     }
-    if (tid == 0) *base = 0;
+    const int32_t* gs = staged ? s_start : p.group_start;
+    const int32_t* gp = staged ? s_plen : p.group_prefix_len;
+    if (tid == 0) s_base = 0;
     __syncthreads();
 
-    // 2. the suffix partitions with tokens, unit by unit (block-wide scans)
-    const int units = p.num_seqs * p.num_kv_heads;
-    for (int u0 = 0; u0 < units; u0 += nthreads) {
-        const int u = u0 + tid;
-        int cnt = 0;
-        if (u < units) {
-            const int b = u / p.num_kv_heads;
-            const int2 info = p.seq_info[b];
-            const int n = clamped_len(p.context_lens[b], p.cap);
+    for (int b0 = 0; b0 < p.num_seqs; b0 += kPlanThreads) {
+        const int b = b0 + tid;
+        int cnt = 0;  // suffix partitions with tokens, per KV head of sequence b
+        const int n_next =
+            b + kPlanThreads < p.num_seqs ? __ldg(p.context_lens + b + kPlanThreads) : 0;
+        if (b < p.num_seqs) {
+            // the sequence's (shared-prefix tokens, prefix partials) record, and
+            // the prefix CTAs its rows meet: every prefix partition of each
+            // 128-row tile that holds one of them
+            int2 info = make_int2(0, 0);
+            int tiles = 0;
+            if (p.num_groups > 0) {
+                int lo = 0, hi = p.num_groups - 1;  // last group with group_start <= b
+                while (lo < hi) {
+                    const int mid = (lo + hi + 1) >> 1;
+                    if (gs[mid] <= b) lo = mid; else hi = mid - 1;
+                }
+                int first, last, plen;
+                if (group_valid(gs, gp, lo, p.num_seqs, p.max_group_size, p.max_prefix_len,
+                                p.block_size, p.max_blocks_per_seq, first, last, plen) &&
+                    first <= b && b < last) {
+                    info = make_int2(plen, (plen + p.prefix_chunk - 1) / p.prefix_chunk);
+                    const int r0 = (b - first) * p.group;
+                    tiles = (r0 + p.group - 1) / kPrefixTileRows - r0 / kPrefixTileRows + 1;
+                } else {
+                    flag_error(p.err_flag, PKV_EFLAG_GROUP);
+                }
+            }
+            p.seq_info[b] = info;
+            const int n = clamped_len(n_raw, p.cap);
             cnt = suffix_partitions(max(0, n - info.x), info.y, p.chunk_tokens);
+            const int left = info.y * tiles + cnt;
+            for (int g = 0; g < p.num_kv_heads; ++g)
+                p.unit_left[(int64_t)b * p.num_kv_heads + g] = left;
         }
         int incl = cnt;  // inclusive warp scan
 #pragma unroll
@@ -1043,23 +1234,29 @@ __device__ void plan_cta(const PlanParams& p, int* scratch) {
         if (lane == 31) warp_sum[warp] = incl;
         __syncthreads();
         if (warp == 0) {
-            const int w = lane < nwarps ? warp_sum[lane] : 0;
+            const int w = lane < kWarps ? warp_sum[lane] : 0;
             int wi = w;
 #pragma unroll
             for (int off = 1; off < 32; off <<= 1) {
                 const int v = __shfl_up_sync(0xffffffffu, wi, off);
                 if (lane >= off) wi += v;
             }
-            if (lane < nwarps) warp_sum[lane] = wi - w;
+            if (lane < kWarps) warp_sum[lane] = wi - w;
         }
         __syncthreads();
-        const int pos = *base + warp_sum[warp] + incl - cnt;
-        for (int j = 0; j < cnt; ++j) p.items[pos + j] = make_int2(u, j);
+        const int before = s_base + warp_sum[warp] + incl - cnt;  // partitions of sequences < b
+        if (b < p.num_seqs && cnt > 0) {
+            int2* dst = p.items + (int64_t)p.num_kv_heads * before;
+            for (int g = 0; g < p.num_kv_heads; ++g)
+                for (int j = 0; j < cnt; ++j)
+                    dst[g * cnt + j] = make_int2(b * p.num_kv_heads + g, j);
+        }
         __syncthreads();
-        if (tid == nthreads - 1) *base = pos + cnt;
+        if (tid == kPlanThreads - 1) s_base = before + cnt;
         __syncthreads();
+        n_raw = n_next;
     }
-    if (tid == 0) *p.item_count = *base;
+    if (tid == 0) *p.item_count = s_base * p.num_kv_heads;
 }
 
 // MODE 0: up to 128 query rows, two softmax threads per row (token halves),
@@ -1119,7 +1316,7 @@ prefix_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
     const int rt = blockIdx.x;                     // tile of 128 query rows
     const int g = blockIdx.y % p.num_kv_heads;     // KV head
     const int grp = blockIdx.y / p.num_kv_heads;   // group (shared prefix) or sequence (multi-query)
-    const int part = blockIdx.z - (p.with_plan ? 1 : 0);  // partition of the tokens
+    const int part = blockIdx.z;                   // partition of the tokens
     const int tid = threadIdx.x;
     const int warp = tid >> 5;
     const int lane = tid & 31;
@@ -1128,11 +1325,6 @@ prefix_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
 
     ptx::launch_dependents();
     ptx::grid_dependency_wait();
-
-    if (part < 0) {  // the plan slice
-        if (blockIdx.x == 0 && blockIdx.y == 0) plan_cta(p.plan, reinterpret_cast<int*>(smem));
-        return;
-    }
 
     // The CTA's query rows and tokens.  Shared prefix (q_len == 0): row r is
     // query head g*group + r % group of member first + r / group of group grp,
@@ -1657,6 +1849,7 @@ prefix_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
         }
     }
 
+    if (MODE == 0 && p.unit_left != nullptr) __threadfence();  // partials, before the counts
     ptx::tc_fence_before_sync();
     __syncthreads();
     if (warp == (SW + 1)) {
@@ -1664,43 +1857,48 @@ prefix_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
         ptx::tc_fence_after_sync();
         ptx::tmem_dealloc(tmem, Cfg::kTmemCols);
     }
+
+    // Shared prefixes: the tile's rows are one contribution to each of its
+    // members' units; the CTA that makes a unit's last contribution merges the
+    // unit's rows (the plan counted P partitions x the tiles a member's rows
+    // span, plus the member's suffix partitions).
+    if constexpr (MODE == 0) {
+        if (p.unit_left != nullptr && !*abort_flag) {
+            int* list = table;  // the table slice is not read after the main loop
+            const int m_lo = row0 / p.group;
+            const int m_hi = (min(rows, row0 + kPrefixTileRows) - 1) / p.group;
+            if (tid == 0) list[0] = 0;
+            __syncthreads();
+            if (tid <= m_hi - m_lo) {
+                const int seq = first + m_lo + tid;
+                if (atomicAdd(p.unit_left + (int64_t)seq * p.num_kv_heads + g, -1) == 1)
+                    list[1 + atomicAdd(&list[0], 1)] = seq;
+            }
+            __syncthreads();
+            const int nm = list[0];
+            if (nm > 0) {
+                __threadfence();
+                MergeParams mp = {};
+                mp.out = p.out;
+                mp.partial_o = p.partial_o;
+                mp.partial_lse = p.partial_lse;
+                mp.context_lens = p.context_lens;
+                mp.seq_info = p.seq_info;
+                mp.num_q_heads = p.num_q_heads;
+                mp.num_kv_heads = p.num_kv_heads;
+                mp.group = p.group;
+                mp.num_splits = p.num_splits;
+                mp.head_dim = D;
+                mp.chunk_tokens = p.suffix_chunk;
+                mp.cap = p.cap;
+                for (int k = warp; k < nm * p.group; k += (SW + 2))
+                    merge_row<T>(mp, (int64_t)list[1 + k / p.group] * p.num_q_heads +
+                                         g * p.group + k % p.group,
+                                 lane);
+            }
+        }
+    }
 }
-
-// Merge of split partials (log-sum-exp rule): one warp per (row of q, query
-// head), four rows per CTA.  Each lane owns float4 columns of the head (lane,
-// lane + 32, ...) and weighs every partition itself: w_p = e^(lse_p - m*),
-// out = sum_p w_p O_p / sum_p w_p; m* and sum_p w_p come from lane-strided
-// sums and shuffles.  No shared memory and no CTA barrier: rows are short,
-// and the merge of a call is a few thousand of them.  With context_lens given
-// (the decode path), a sequence whose context fitted a single partition was
-// written by the decode kernel and is skipped, and only the partitions that
-// hold tokens are read.  Multi-query rows (q_len > 0) are merged from the
-// partitions of their sequence's context; with mq_direct (the decode kernel's
-// multi-query form) a context that fitted one partition was written directly
-// and is skipped.  Without context_lens (pkv_merge), every row merges all
-// num_splits partials.
-struct MergeParams {
-    void* out;
-    const float* partial_o;
-    const float* partial_lse;
-    const int32_t* context_lens;  // nullable
-    const int2* seq_info;         // nullable: shared-prefix tokens and prefix partials per sequence
-    int num_q_heads;
-    int num_kv_heads;
-    int group;                    // query heads per KV head
-    int num_splits;
-    int head_dim;                 // a multiple of 4, at most 512
-    int chunk_tokens;
-    int cap;                      // context clamp, as in the decode kernel
-    int q_len;                    // > 0: multi-query rows (sequence, query token)
-    int mq_slots;                 // multi-query: partial slots per context partition (1 or 2)
-    bool mq_direct;               // multi-query partials of the decode kernel (single ones direct)
-    int64_t rows;                 // (row of q, query head) pairs
-};
-
-constexpr int kMergeRowsPerCta = 4;
-constexpr int kMergeThreads = kMergeRowsPerCta * 32;
-constexpr int kMergeMaxHeadDim = 512;
 
 template <typename T>
 __global__ void __launch_bounds__(kMergeThreads)
@@ -1710,67 +1908,7 @@ merge_kernel(const MergeParams p) {
     ptx::launch_dependents();
     ptx::grid_dependency_wait();
     if (row >= p.rows) return;
-    const int b = (int)(row / p.num_q_heads);  // row of q: a sequence, or (sequence, query token)
-    int ns = p.num_splits;
-    if (p.q_len > 0) {
-        // multi-query partials: the partitions of the sequence's context
-        const int n = clamped_len(__ldg(p.context_lens + b / p.q_len), p.cap);
-        if (p.mq_direct) {
-            ns = suffix_partitions(n, 0, p.chunk_tokens);
-            if (ns <= 1) return;  // written directly by the decode kernel
-        } else {
-            ns = (n + p.chunk_tokens - 1) / p.chunk_tokens * p.mq_slots;
-        }
-    } else if (p.context_lens != nullptr) {
-        int start = 0, slot0 = 0;
-        if (p.seq_info != nullptr) {
-            const int2 si = __ldcg(p.seq_info + b);
-            start = si.x;
-            slot0 = si.y;
-        }
-        const int n = clamped_len(__ldg(p.context_lens + b), p.cap);
-        ns = slot0 + suffix_partitions(max(0, n - start), slot0, p.chunk_tokens);
-        if (slot0 == 0 && ns <= 1) return;  // written directly by the decode kernel
-    }
-    const float* lse = p.partial_lse + row * p.num_splits;
-    // m* = max_p lse_p and 1 / sum_p e^(lse_p - m*)
-    float mx = -INFINITY;
-    for (int sp = lane; sp < ns; sp += 32) mx = fmaxf(mx, lse[sp]);
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
-    float den = 0.f;
-    if (mx != -INFINITY)
-        for (int sp = lane; sp < ns; sp += 32) {
-            const float ls = lse[sp];
-            if (ls != -INFINITY) den += exp2f((ls - mx) * kLog2e);
-        }
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) den += __shfl_xor_sync(0xffffffffu, den, off);
-    const float inv = den > 0.f ? 1.f / den : 0.f;
-    const int cols = p.head_dim / 4;
-    const float* po = p.partial_o + row * p.num_splits * p.head_dim;
-    T* out = static_cast<T*>(p.out) + row * p.head_dim;
-#pragma unroll
-    for (int k = 0; k < kMergeMaxHeadDim / 128; ++k) {
-        const int c = lane + 32 * k;
-        if (c >= cols) break;
-        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-        if (mx != -INFINITY)
-            for (int sp = 0; sp < ns; ++sp) {
-                const float ls = lse[sp];
-                if (ls == -INFINITY) continue;  // an empty partition may hold anything
-                const float wgt = exp2f((ls - mx) * kLog2e);
-                const float4 v = *reinterpret_cast<const float4*>(po + (int64_t)sp * p.head_dim + c * 4);
-                acc.x = fmaf(wgt, v.x, acc.x);
-                acc.y = fmaf(wgt, v.y, acc.y);
-                acc.z = fmaf(wgt, v.z, acc.z);
-                acc.w = fmaf(wgt, v.w, acc.w);
-            }
-        uint2 packed;
-        packed.x = pack2(acc.x * inv, acc.y * inv, T());
-        packed.y = pack2(acc.z * inv, acc.w * inv, T());
-        *reinterpret_cast<uint2*>(out + c * 4) = packed;
-    }
+    merge_row<T>(p, row, lane);
 }
 
 // Self-test of the bounded wait: one warp waits on a barrier phase that
@@ -1809,6 +1947,51 @@ static int current_sm_count() {
     }
     cache[dev].store(v, std::memory_order_relaxed);
     return v;
+}
+
+// The stream on which a shared-prefix call runs its prefix kernel beside the
+// suffix decode on the caller's stream, with the events that fork it from the
+// caller's stream and join it back: one set per CUDA context, made on the
+// context's first such call and kept for the life of the process.  It has the
+// highest priority the device offers, so that the prefix CTAs (one an SM)
+// are placed first when both grids wait for SMs.  The mutex is held from the
+// fork to the join, so calls from several host threads never see one
+// another's event records.
+struct SideStream {
+    unsigned long long ctx_id;
+    cudaStream_t stream;
+    cudaEvent_t fork, join;
+};
+constexpr int kMaxSideStreams = 64;
+static std::mutex g_side_mutex;
+static SideStream g_side[kMaxSideStreams];
+static int g_side_count = 0;
+
+// The current context's side stream, made if need be; nullptr when there is
+// none to be had (no context id, more contexts than entries, or the runtime
+// refused), in which case the caller runs the prefix on its own stream.
+// Call with g_side_mutex held.
+static const SideStream* side_stream_locked() {
+    unsigned long long id = 0;
+    if (!current_context_id(&id)) return nullptr;
+    for (int i = 0; i < g_side_count; ++i)
+        if (g_side[i].ctx_id == id) return &g_side[i];
+    if (g_side_count == kMaxSideStreams) return nullptr;
+    SideStream e = {id, nullptr, nullptr, nullptr};
+    int least = 0, greatest = 0;
+    if (cudaDeviceGetStreamPriorityRange(&least, &greatest) != cudaSuccess ||
+        cudaStreamCreateWithPriority(&e.stream, cudaStreamNonBlocking, greatest) != cudaSuccess ||
+        cudaEventCreateWithFlags(&e.fork, cudaEventDisableTiming) != cudaSuccess ||
+        cudaEventCreateWithFlags(&e.join, cudaEventDisableTiming) != cudaSuccess) {
+        cudaGetLastError();
+        if (e.join) cudaEventDestroy(e.join);
+        if (e.fork) cudaEventDestroy(e.fork);
+        if (e.stream) cudaStreamDestroy(e.stream);
+        cudaGetLastError();
+        return nullptr;
+    }
+    g_side[g_side_count] = e;
+    return &g_side[g_side_count++];
 }
 
 struct Plan {
@@ -2109,8 +2292,11 @@ constexpr int kMqDupCtasPerSm = ctas_per_sm_of_mode(kMqDupMode);
 
 // Plan of a shared-prefix call: the suffixes planned like a plain decode; the
 // prefix in partitions of whole 64-token tiles, as many as give about one
-// prefix CTA (128 query rows) per SM, at most kMaxChunkPages pages each; per
-// (sequence, query head) the prefix partials first, then the suffix partials.
+// prefix CTA (128 query rows) per kPrefixSmShare SMs, at most kMaxChunkPages
+// pages each; per (sequence, query head) the prefix partials first, then the
+// suffix partials.  The prefix kernel runs beside the suffix decode, so it
+// takes only part of the GPU and the decode keeps the rest.
+constexpr int kPrefixSmShare = 2;
 struct PrefixPlan {
     Plan suffix;
     int prefix_chunk;
@@ -2135,7 +2321,8 @@ static pkv_status make_prefix_plan(int num_seqs, int num_q_heads, int num_kv_hea
     const int sms = current_sm_count();
     if (sms <= 0) return PKV_ERR_CUDA;
     const int64_t units = std::max<int64_t>(1, (int64_t)num_groups * num_kv_heads * pp->row_tiles);
-    const int64_t want = std::max<int64_t>(1, (int64_t)sms * ctas_per_sm_of_mode(kPrefixMode) / units);
+    const int64_t want = std::max<int64_t>(
+        1, (int64_t)sms * ctas_per_sm_of_mode(kPrefixMode) / (kPrefixSmShare * units));
     const int tiles = (max_prefix_len + kPrefixTileTokens - 1) / kPrefixTileTokens;
     const int max_tiles = kMaxChunkPages * block_size / kPrefixTileTokens;
     const int chunk_tiles =
@@ -2147,9 +2334,10 @@ static pkv_status make_prefix_plan(int num_seqs, int num_q_heads, int num_kv_hea
     if (pp->total_splits > PKV_MAX_SPLITS) return PKV_ERR_UNSUPPORTED;
     const size_t partial_floats = (size_t)num_seqs * num_q_heads * pp->total_splits * (head_dim + 1);
     const size_t items = (size_t)num_seqs * num_kv_heads * pp->suffix.num_splits;
-    // partials | per-sequence records | work list | its length
+    // partials | per-sequence records | work list | its length | per-unit counts
     pp->workspace_bytes = ((partial_floats * sizeof(float) + 15) & ~size_t(15)) +
-                          (size_t)num_seqs * sizeof(int2) + items * sizeof(int2) + 16 + 256;
+                          (size_t)num_seqs * sizeof(int2) + items * sizeof(int2) + 16 +
+                          (size_t)num_seqs * num_kv_heads * sizeof(int) + 256;
     return PKV_OK;
 }
 
@@ -2529,11 +2717,12 @@ extern "C" pkv_status pkv_decode_attention_prefix_shared(
     const int64_t num_items = (int64_t)num_seqs * num_kv_heads * pp.suffix.num_splits;
     int2* items = seq_info + num_seqs;
     int* item_count = reinterpret_cast<int*>(items + num_items);
+    int* unit_left = item_count + 4;
     const int cap = std::min(max_blocks_per_seq * block_size, max_context_len);
     cudaStream_t s = (cudaStream_t)stream;
 
     // every sequence's prefix record and the list of suffix partitions with
-    // tokens: the plan, run by the prefix launch's extra CTA
+    // tokens: the plan
     PlanParams pl = {};
     pl.context_lens = context_lens;
     pl.group_start = group_start;
@@ -2552,8 +2741,11 @@ extern "C" pkv_status pkv_decode_attention_prefix_shared(
     pl.prefix_chunk = pp.prefix_chunk;
     pl.chunk_tokens = pp.suffix.chunk_tokens;
     pl.cap = cap;
+    pl.unit_left = unit_left;
+    pl.group = num_q_heads / num_kv_heads;
 
-    // 1. the plan and the prefix partials of every group (tcgen05)
+    // the prefix partials of every group (tcgen05); the last contribution to
+    // a unit merges it
     PrefixParams pr = {};
     pr.q = q;
     pr.block_tables = block_tables;
@@ -2578,22 +2770,13 @@ extern "C" pkv_status pkv_decode_attention_prefix_shared(
     pr.cap = cap;
     pr.hnd = hnd;
     pr.scale_log2 = scale * kLog2e;
-    pr.with_plan = true;
-    pr.plan = pl;
-    const dim3 pgrid(pp.row_tiles, std::max(1, num_groups * num_kv_heads), pp.prefix_parts + 1);
-    cudaError_t e;
-    if (head_dim == 64)
-        e = dtype == PKV_FP16 ? launch_prefix_t<__half, 64, kPrefixMode>(mk, mv, pr, pgrid, s)
-                              : launch_prefix_t<__nv_bfloat16, 64, kPrefixMode>(mk, mv, pr, pgrid, s);
-    else
-        e = dtype == PKV_FP16 ? launch_prefix_t<__half, 128, kPrefixMode>(mk, mv, pr, pgrid, s)
-                              : launch_prefix_t<__nv_bfloat16, 128, kPrefixMode>(mk, mv, pr, pgrid, s);
-    if (e != cudaSuccess) {
-        cudaGetLastError();
-        return PKV_ERR_CUDA;
-    }
+    pr.unit_left = unit_left;
+    pr.out = out;
+    pr.seq_info = seq_info;
+    pr.suffix_chunk = pp.suffix.chunk_tokens;
 
-    // 2. suffix partials (or the whole answer for sequences without a prefix)
+    // suffix partials (or the whole answer for sequences without a prefix),
+    // CTA x taking the plan's item x
     DecodeParams p = {};
     p.out = out;
     p.q = q;
@@ -2617,30 +2800,61 @@ extern "C" pkv_status pkv_decode_attention_prefix_shared(
     p.hnd = hnd;
     p.scale_log2 = scale * kLog2e;
     p.v_scale = 1.f;
-    const dim3 grid((unsigned)num_items);
-    e = dtype == PKV_FP16 ? launch_decode<__half>(mk, mv, p, head_dim, grid, s)
-                          : launch_decode<__nv_bfloat16>(mk, mv, p, head_dim, grid, s);
-    if (e != cudaSuccess) {
-        cudaGetLastError();
-        return PKV_ERR_CUDA;
-    }
+    p.unit_left = unit_left;
 
-    // 3. merge
-    MergeParams mp = {};
-    mp.out = out;
-    mp.partial_o = partial_o;
-    mp.partial_lse = partial_lse;
-    mp.context_lens = context_lens;
-    mp.seq_info = seq_info;
-    mp.num_q_heads = num_q_heads;
-    mp.num_kv_heads = num_kv_heads;
-    mp.group = num_q_heads / num_kv_heads;
-    mp.num_splits = pp.total_splits;
-    mp.head_dim = head_dim;
-    mp.chunk_tokens = pp.suffix.chunk_tokens;
-    mp.cap = cap;
-    e = dtype == PKV_FP16 ? launch_merge<__half>(mp, num_q_heads, num_seqs, s)
-                          : launch_merge<__nv_bfloat16>(mp, num_q_heads, num_seqs, s);
+    auto launch_prefix = [&](cudaStream_t st) {
+        const dim3 pgrid(pp.row_tiles, std::max(1, num_groups * num_kv_heads),
+                         std::max(1, pp.prefix_parts));
+        if (head_dim == 64)
+            return dtype == PKV_FP16 ? launch_prefix_t<__half, 64, kPrefixMode>(mk, mv, pr, pgrid, st)
+                                     : launch_prefix_t<__nv_bfloat16, 64, kPrefixMode>(mk, mv, pr, pgrid, st);
+        return dtype == PKV_FP16 ? launch_prefix_t<__half, 128, kPrefixMode>(mk, mv, pr, pgrid, st)
+                                 : launch_prefix_t<__nv_bfloat16, 128, kPrefixMode>(mk, mv, pr, pgrid, st);
+    };
+    auto launch_plan = [&](cudaStream_t st) {
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(1);
+        cfg.blockDim = dim3(kPlanThreads);
+        cfg.stream = st;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        return cudaLaunchKernelEx(&cfg, plan_kernel, pl);
+    };
+    auto launch_suffix = [&](cudaStream_t st) {
+        const dim3 grid((unsigned)num_items);
+        return dtype == PKV_FP16 ? launch_decode<__half>(mk, mv, p, head_dim, grid, st)
+                                 : launch_decode<__nv_bfloat16>(mk, mv, p, head_dim, grid, st);
+    };
+
+    // 1. the plan; 2. the prefix kernel on the side stream, forked from the
+    // caller's stream after the plan, and the suffix decode on the caller's
+    // stream at the same time; the caller's stream then waits for the prefix.
+    // Whichever kernel writes a unit's last partial merges it, so no merge
+    // launch follows.  Without a side stream, the prefix runs after the plan
+    // on the caller's stream, then the decode.
+    cudaError_t e = launch_plan(s);
+    if (e == cudaSuccess) {
+        std::lock_guard<std::mutex> lock(g_side_mutex);
+        const SideStream* side = pp.prefix_parts > 0 ? side_stream_locked() : nullptr;
+        if (side != nullptr) {
+            e = cudaEventRecord(side->fork, s);
+            if (e == cudaSuccess) e = cudaStreamWaitEvent(side->stream, side->fork, 0);
+            if (e == cudaSuccess) e = launch_prefix(side->stream);
+            // the join is queued even if a launch failed, so the side stream
+            // never runs ahead of the caller's later work
+            const cudaError_t r = cudaEventRecord(side->join, side->stream);
+            if (e == cudaSuccess) e = r;
+            if (e == cudaSuccess) e = launch_suffix(s);
+            const cudaError_t w = cudaStreamWaitEvent(s, side->join, 0);
+            if (e == cudaSuccess) e = w;
+        } else {
+            if (pp.prefix_parts > 0) e = launch_prefix(s);
+            if (e == cudaSuccess) e = launch_suffix(s);
+        }
+    }
     if (e != cudaSuccess) {
         cudaGetLastError();
         return PKV_ERR_CUDA;

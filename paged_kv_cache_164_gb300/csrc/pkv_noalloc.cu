@@ -52,9 +52,7 @@ static const CtxFns& ctx_fns() {
     return fns;
 }
 
-// Id of the context current to this thread (the one the launches use); false
-// when none is current yet or the driver cannot say.
-static bool current_context_id(unsigned long long* id) {
+bool current_context_id(unsigned long long* id) {
     const CtxFns& f = ctx_fns();
     if (f.get_current == nullptr || f.get_id == nullptr) return false;
     CUcontext ctx = nullptr;

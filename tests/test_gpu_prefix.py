@@ -46,6 +46,15 @@ CASES = {
     "1100_groups_of_one": dict(name="c3", num_seqs=1100, num_q_heads=4, num_kv_heads=2, head_dim=64,
                                lengths=("prefix_lognormal", 16, 20, 0.5, 80), max_len_cap=96,
                                shared_prefix_groups=1100, pool="free_list", seed=53),
+    # GQA group of 6: members' rows straddle the 128-row tiles of the prefix kernel
+    # (member 21: rows 126-131), so such a unit gets contributions from two tiles
+    "gqa6_rows_straddle_tiles": dict(name="c3", num_seqs=45, num_q_heads=12, num_kv_heads=2,
+                                     head_dim=128, lengths=("prefix_lognormal", 160, 40, 1.0, 300),
+                                     max_len_cap=320, shared_prefix_groups=1, seed=61),
+    # more groups than the plan keeps in shared memory (4096): their bounds are read in place
+    "4200_groups_of_one": dict(name="c3", num_seqs=4200, num_q_heads=2, num_kv_heads=1, head_dim=64,
+                               lengths=("prefix_lognormal", 16, 10, 0.5, 48), max_len_cap=64,
+                               shared_prefix_groups=4200, pool="free_list", seed=59),
 }
 
 
@@ -94,6 +103,23 @@ def test_member_shorter_than_the_prefix_is_masked():
     assert_attention_close(out, expect, "short members")
 
 
+def test_members_without_suffix_are_merged_by_the_prefix_kernel():
+    # Every member of group 0 ends exactly at the shared prefix: no suffix
+    # partition exists, so the prefix CTAs write each unit's last partial and
+    # must merge it themselves.
+    w = _make("bs32_g4_4groups")
+    pkv.append(w.k_new, w.v_new, w.k_cache, w.v_cache, w.slot_mapping)
+    cl = w.context_lens.clone()
+    g0, g1 = int(w.group_start[0]), int(w.group_start[1])
+    cl[g0:g1] = int(w.group_prefix_len[0])
+    w.context_lens = cl
+    expect, _, _ = oracle_after_append(w)
+    flag = pkv.new_error_flag("cuda")
+    out = _run(w, append=False, flag=flag)
+    assert pkv.check_error(flag) == 0
+    assert_attention_close(out, expect, "no suffixes")
+
+
 def test_malformed_group_is_flagged_and_still_correct():
     w = _make("bs32_g4_4groups")
     expect, _, _ = oracle_after_append(w)
@@ -118,3 +144,35 @@ def test_full_size_shared_prefix_sampled(name):
     plain = pkv.decode_attention(w.q, w.k_cache, w.v_cache, w.block_tables, w.context_lens,
                                  w.max_context_len, scale=w.scale)
     assert torch.allclose(out.float(), plain.float(), atol=2e-3, rtol=1e-2)
+
+
+def test_prefix_waits_for_work_queued_before_the_call():
+    # The prefix kernel runs on a stream of the library's own; it must start only
+    # after everything queued on the caller's stream before the call.  Here the
+    # caller's stream spins for a while and then rewrites q: a prefix that did
+    # not wait would attend with the old q.
+    w = _make("bs16_g4_2groups")
+    pkv.append(w.k_new, w.v_new, w.k_cache, w.v_cache, w.slot_mapping)
+    torch.manual_seed(5)
+    q_new = torch.randn_like(w.q, dtype=torch.float32).to(w.q.dtype)
+    torch.cuda.synchronize()
+    torch.cuda._sleep(20_000_000)
+    w.q.copy_(q_new)
+    out = _run(w, append=False)
+    expect, _, _ = oracle_after_append(w)   # the oracle reads the new q
+    assert_attention_close(out, expect, "prefix after queued work")
+
+
+def test_caller_stream_work_after_the_call_sees_the_prefix():
+    # Work the caller queues after the call (here a copy of the output) must see
+    # the prefix partials merged, on the caller's own non-default stream.
+    w = _make("bs32_g4_4groups")
+    expect, _, _ = oracle_after_append(w)
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        out = _run(w)
+        copy = out.clone()
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    assert_attention_close(copy, expect, "caller stream")
