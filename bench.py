@@ -60,17 +60,17 @@ WORKLOAD_TEXT = {
 NCU_TRAFFIC = {
     # ncu --metrics dram__bytes_read.sum,dram__bytes_write.sum,gpu__time_duration.sum
     #     --clock-control none -k regex:decode_kernel -s 4 -c 1 (the fused default step)
-    "c4": {"digest": "94d3ffb64ff791f9", "splits": 64, "shared": False, "fused": True,
-           "bytes": 2818481408 + 7712256},
-    "c2": {"digest": "94d3ffb64ff791f9", "splits": 2, "shared": False, "fused": True,
-           "bytes": 2312643840 + 4651264},
-    "c3": {"digest": "94d3ffb64ff791f9", "splits": 3, "shared": False, "fused": True,
-           "bytes": 537483264 + 4017920},
-    # shared-prefix path: decode_kernel (suffixes) + prefix_kernel
-    # (-k regex:"decode_kernel|prefix_kernel" -s 8 -c 2); the merge kernel's few MB
-    # are not included
-    "c5": {"digest": "94d3ffb64ff791f9", "splits": 8, "shared": True, "fused": False,
-           "bytes": (1531841024 + 3346176) + (35771392 + 68608)},
+    "c4": {"digest": "ebf1c529cd793cc9", "splits": 64, "shared": False, "fused": True,
+           "bytes": 2818491904 + 7860992},
+    "c2": {"digest": "ebf1c529cd793cc9", "splits": 2, "shared": False, "fused": True,
+           "bytes": 2312603392 + 4647680},
+    "c3": {"digest": "ebf1c529cd793cc9", "splits": 3, "shared": False, "fused": True,
+           "bytes": 537501184 + 3979520},
+    # shared-prefix path: decode_kernel (suffixes, and the merge of each unit by
+    # its last CTA; -k regex:decode_kernel -s 4 -c 1) + prefix_kernel
+    # (-k regex:prefix_kernel -s 2 -c 1); the plan kernel's few KB are not included
+    "c5": {"digest": "ebf1c529cd793cc9", "splits": 8, "shared": True, "fused": False,
+           "bytes": (1536187904 + 5140992) + (35748864 + 13824)},
 }
 
 
@@ -388,8 +388,8 @@ def _measure(name, args, device, rank, ws, cpu_seconds):
     workspace = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device=device)
     out = torch.empty_like(w.q)
     flag = pkv.new_error_flag(device)
-    # append, decode, merge when split; the shared-prefix path: append, prefix
-    # (with the plan as one of its CTAs), decode, merge
+    # append, decode, merge when split; the shared-prefix path: append, plan,
+    # prefix (second stream) and decode (no merge launch)
     # The step's append is done by the decode kernel itself
     # (pkv_append_decode_attention) on the plain 16-bit path; --unfused times
     # the two calls (pkv_append, then pkv_decode_attention) instead.
@@ -614,7 +614,8 @@ def _measure(name, args, device, rank, ws, cpu_seconds):
                if mq_kernel == "tcgen05" else
                "decode_kernel in multi-query mode" + (" + merge_kernel" if mq_parts > 1 else ""))
               if mq else
-              "prefix_kernel (with the plan CTA) + decode_kernel + merge_kernel"
+              "plan_kernel, then prefix_kernel (on a second stream) beside decode_kernel "
+              "(each unit merged by its last CTA)"
               if shared else "decode_kernel + merge_kernel")
     config = {"workload": name, "description": WORKLOAD_TEXT[name],
               "num_seqs": s.num_seqs, "num_q_heads": s.num_q_heads,

@@ -264,6 +264,12 @@ __device__ __forceinline__ void stage_update(uint32_t kbase, uint32_t vbase, int
 #pragma unroll
             for (int c = 0; c < 4; ++c) s[nt][c] += s2[nt][c];
     } else {
+        // odd k-steps accumulate apart (s2): two dependent MMA chains, not one
+        float s2[NT][4];
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+            for (int c = 0; c < 4; ++c) s2[nt][c] = 0.f;
 #pragma unroll
         for (int ks = 0; ks < KSTEPS; ++ks) {
             const int chunk = ks * 2 + k_csel;
@@ -273,8 +279,12 @@ __device__ __forceinline__ void stage_update(uint32_t kbase, uint32_t vbase, int
             ptx::ldmatrix_x4(a, addr);
 #pragma unroll
             for (int nt = 0; nt < NT; ++nt)
-                ptx::mma_16816<T>(s[nt], a, qb[nt][ks][0], qb[nt][ks][1]);
+                ptx::mma_16816<T>((ks & 1) ? s2[nt] : s[nt], a, qb[nt][ks][0], qb[nt][ks][1]);
         }
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+            for (int c = 0; c < 4; ++c) s[nt][c] += s2[nt][c];
     }
 
     // Online softmax in base 2.  s[nt][0]: (token gq, column 2tq), [1]: (gq, 2tq+1),
