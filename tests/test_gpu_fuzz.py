@@ -34,15 +34,19 @@ def draw_case(i: int) -> dict:
                 num_q_heads=h_kv * group, dtype=str(rng.choice(["fp16", "bf16"])),
                 layout=str(rng.choice(["nhd", "hnd"])), splits=int(rng.choice([0, 0, 1, 2, 3, 5, 8])),
                 q_len=int(rng.integers(2, 13)) if mode == "multi_query" else 1,
-                zero_len=False)
+                zero_len=False, no_suffix=False)
     if mode == "prefix_shared":
         groups = int(rng.integers(1, 3))
-        per = int(rng.integers(1, 4))
+        # sometimes groups of many members: several 128-row tiles of the prefix
+        # kernel, members whose rows straddle two tiles when the group is 3 or 5
+        per = int(rng.choice([1, 2, 3, 30, 44]))
         prefix = bs * int(rng.integers(1, max(2, 640 // bs)))
         cap = prefix + int(rng.integers(64, 1200))
         case.update(num_seqs=groups * per, shared_prefix_groups=groups,
                     lengths=("prefix_lognormal", prefix, int(rng.integers(16, 400)), 1.0, cap),
-                    max_len_cap=cap)
+                    max_len_cap=cap,
+                    # the first group's members end at the prefix: no suffix partitions
+                    no_suffix=bool(rng.random() < 0.3))
         return case
     b = int(rng.integers(1, 6))
     edges = [1, bs, bs + 1, 2 * bs - 1, 15, 16, 17]
@@ -79,6 +83,10 @@ def test_random_case_matches_oracle(i):
     if case["zero_len"]:
         cl[0] = 0
         cl_h[0] = 0
+    if case["no_suffix"]:
+        g0, g1 = int(w.group_start[0]), int(w.group_start[1])
+        cl[g0:g1] = int(w.group_prefix_len[0])
+        cl_h[g0:g1] = int(w.group_prefix_len[0])
     layout = case["layout"]
     k_dev, v_dev = w.k_cache, w.v_cache
     if layout == "hnd":
@@ -135,5 +143,12 @@ def test_cases_cover_the_space():
         assert {c[key] for c in cases} == want, key
     assert {c["num_q_heads"] // c["num_kv_heads"] for c in cases} >= {1, 2, 8, 16}
     assert any(c["zero_len"] for c in cases)
+    pre = [c for c in cases if c["mode"] == "prefix_shared"]
+    assert any(c["no_suffix"] for c in pre)
+    # a group of more than one 128-row tile whose GQA group does not divide 128
+    per_group = [(c["num_seqs"] // c["shared_prefix_groups"], c["num_q_heads"] // c["num_kv_heads"])
+                 for c in pre]
+    assert any(m * g > 128 and 128 % g for m, g in per_group)
+    assert any(m * g > 128 for m, g in per_group)
     lens = [n for c in cases if c["lengths"][0] == "fixed" for n in c["lengths"][1]]
     assert 1 in lens and 16 in lens and 17 in lens
