@@ -363,6 +363,9 @@ def decode_attention_prefix_shared(q: torch.Tensor, k_cache: torch.Tensor, v_cac
     group_start int32 [G+1] and group_prefix_len int32 [G] (device) describe
     contiguous groups of sequences whose first group_prefix_len[p] tokens are
     the same physical blocks; each group's prefix is read once for all members.
+    Inside the call the prefix kernel runs on a second stream of the library's
+    own, forked from ``stream`` and joined back to it before the call returns,
+    so work queued on ``stream`` before and after is ordered as usual.
     """
     lib = load()
     b, h_q, d = q.shape
