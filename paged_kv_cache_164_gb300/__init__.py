@@ -223,7 +223,9 @@ def decode_attention(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tens
     dt = k_cache.dtype
     if out is None:
         out = torch.empty_like(q)
-    need = workspace_size(b, h_q, h_kv, d, bs, max_context_len, num_splits)
+    # a given workspace is checked against the plan by the library itself
+    need = workspace_size(b, h_q, h_kv, d, bs, max_context_len, num_splits) \
+        if workspace is None else 0
     if workspace is None and need > 0:
         workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
     ws_ptr = ctypes.c_void_p(0) if workspace is None else _dev(workspace, "workspace")
@@ -261,7 +263,9 @@ def append_decode_attention(q: torch.Tensor, k_new: torch.Tensor, v_new: torch.T
     dt = k_cache.dtype
     if out is None:
         out = torch.empty_like(q)
-    need = workspace_size(b, h_q, h_kv, d, bs, max_context_len, num_splits)
+    # a given workspace is checked against the plan by the library itself
+    need = workspace_size(b, h_q, h_kv, d, bs, max_context_len, num_splits) \
+        if workspace is None else 0
     if workspace is None and need > 0:
         workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
     ws_ptr = ctypes.c_void_p(0) if workspace is None else _dev(workspace, "workspace")
@@ -321,7 +325,9 @@ def decode_attention_fp8(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.
         scale = 1.0 / math.sqrt(d)
     if out is None:
         out = torch.empty_like(q)
-    need = workspace_size(b, h_q, h_kv, d, bs, max_context_len, num_splits)
+    # a given workspace is checked against the plan by the library itself
+    need = workspace_size(b, h_q, h_kv, d, bs, max_context_len, num_splits) \
+        if workspace is None else 0
     if workspace is None and need > 0:
         workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
     ws_ptr = ctypes.c_void_p(0) if workspace is None else _dev(workspace, "workspace")
@@ -380,9 +386,9 @@ def decode_attention_prefix_shared(q: torch.Tensor, k_cache: torch.Tensor, v_cac
     dt = k_cache.dtype
     if out is None:
         out = torch.empty_like(q)
-    need = prefix_shared_workspace_size(b, h_q, h_kv, d, bs, max_context_len, ng, max_group_size,
-                                        max_prefix_len)
-    if workspace is None:
+    if workspace is None:  # a given workspace is checked by the library itself
+        need = prefix_shared_workspace_size(b, h_q, h_kv, d, bs, max_context_len, ng,
+                                            max_group_size, max_prefix_len)
         workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
     st = lib.pkv_decode_attention_prefix_shared(
         _dev(out, "out", dt), _dev(q, "q", dt), _dev(k_cache, "k_cache", dt),
@@ -445,8 +451,8 @@ def multi_query_attention(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch
     dt = k_cache.dtype
     if out is None:
         out = torch.empty_like(q)
-    need = multi_query_workspace_size(b, q_len, h_q, h_kv, d, bs, max_context_len)
-    if workspace is None:
+    if workspace is None:  # a given workspace is checked by the library itself
+        need = multi_query_workspace_size(b, q_len, h_q, h_kv, d, bs, max_context_len)
         workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
     st = lib.pkv_multi_query_attention(
         _dev(out, "out", dt), _dev(q, "q", dt), _dev(k_cache, "k_cache", dt),
