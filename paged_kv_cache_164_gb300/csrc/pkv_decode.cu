@@ -67,6 +67,17 @@ struct Tile {
                                       (kMaxChunkPages + 1) * 4 + 16;
 };
 
+// Shared-memory q tile of the two-group (NT = 2) 16-bit kernels: the CTA's
+// 16 query columns x D dims, rows of D * 2 bytes with the 16-byte chunks
+// XOR-swizzled by the row (column) index mod 8, plus alignment slack.  Each
+// k-step's B fragments come from it by one ldmatrix just before the S^T
+// products, instead of 32 registers a thread holding q all along: that took
+// the GQA-16 kernel's register spills to none and the multi-query one's from
+// 100 to 32 bytes (Llama-70B layer verifying 4 tokens, 32 rows: 54.9 -> 57.8 %
+// of peak; 17 rows on the Llama-7B layer 63.4 -> 67.0 %).
+template <int D, int NT, bool F8>
+constexpr int q_tile_bytes() { return (NT == 2 && !F8) ? 128 + NT * 8 * D * 2 : 0; }
+
 struct DecodeParams {
     void* out;
     const void* q;
@@ -205,13 +216,13 @@ __device__ __forceinline__ uint32_t e4m3x2_to(uint32_t v, __nv_bfloat16) {
 // dims they make the A operand with the rows of each 16-dim block permuted
 // (row r <- dim 2r for r < 8, dim 2(r-8)+1 for r >= 8): o comes out in that
 // order.
-template <typename T, int D, int NT, bool ROW_LIMITS, bool F8 = false>
+template <typename T, int D, int NT, bool ROW_LIMITS, bool F8 = false, bool QS = false>
 __device__ __forceinline__ void stage_update(uint32_t kbase, uint32_t vbase, int nvalid, int tok0,
                                              const int (&lim)[NT][2],
                                              const uint32_t (&qb)[NT][D / 16][2],
                                              float (&o)[NT][D / 16][4], float (&m0)[NT],
                                              float (&m1)[NT], float (&l0)[NT], float (&l1)[NT],
-                                             float scale_log2, int lane) {
+                                             float scale_log2, int lane, uint32_t qaddr = 0) {
     constexpr int KSTEPS = D / 16;
     constexpr int kRegionBytes = kStageTokens * 128;
     const int gq = lane >> 2;
@@ -277,9 +288,20 @@ __device__ __forceinline__ void stage_update(uint32_t kbase, uint32_t vbase, int
                 kbase + (chunk >> 3) * kRegionBytes + k_tok * 128 + (((chunk & 7) ^ r8) << 4);
             uint32_t a[4];
             ptx::ldmatrix_x4(a, addr);
+            if constexpr (QS) {
+                static_assert(NT == 2, "the q tile serves two 8-column groups");
+                // matrices (group 0, dims 16ks..+7), (0, +8..15), (1, ..), (1, ..):
+                // lane's row = column (mi >> 1) * 8 + r8, chunk 2ks + (mi & 1)
+                uint32_t qf[4];
+                ptx::ldmatrix_x4(qf, qaddr + ((mi >> 1) * 8 + r8) * (D * 2) +
+                                         (((2 * ks + (mi & 1)) ^ r8) << 4));
+                ptx::mma_16816<T>((ks & 1) ? s2[0] : s[0], a, qf[0], qf[1]);
+                ptx::mma_16816<T>((ks & 1) ? s2[1] : s[1], a, qf[2], qf[3]);
+            } else {
 #pragma unroll
-            for (int nt = 0; nt < NT; ++nt)
-                ptx::mma_16816<T>((ks & 1) ? s2[nt] : s[nt], a, qb[nt][ks][0], qb[nt][ks][1]);
+                for (int nt = 0; nt < NT; ++nt)
+                    ptx::mma_16816<T>((ks & 1) ? s2[nt] : s[nt], a, qb[nt][ks][0], qb[nt][ks][1]);
+            }
         }
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt)
@@ -568,6 +590,9 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
     uint64_t* empty_bar = full_bar + S;
     int* table = reinterpret_cast<int*>(empty_bar + S);
     volatile int* abort_flag = table + kMaxChunkPages + 1;
+    constexpr bool QS = q_tile_bytes<D, NT, F8>() > 0;
+    uint8_t* q_tile = reinterpret_cast<uint8_t*>(
+        (reinterpret_cast<uintptr_t>(table + kMaxChunkPages + 5) + 127) & ~uintptr_t(127));
 
     const int tid = threadIdx.x;
     const int warp = tid >> 5;
@@ -690,6 +715,22 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
 #ifdef PKV_DEBUG
     poison_smem(ring, Cfg::kRingBytes, tid, kThreads);
 #endif
+    if constexpr (QS) {
+        // the CTA's query columns (zero rows past the ones in use)
+        const int ncols_q = MQ ? min(NT * 8, p.q_len * p.group - col0) : p.group;
+        const T* qb0 = static_cast<const T*>(p.q) +
+                       ((int64_t)b * (MQ ? p.q_len : 1) * p.num_q_heads + g * p.group) * D;
+        for (int idx = tid; idx < NT * 8 * (D / 8); idx += kThreads) {
+            const int col = idx / (D / 8), chunk = idx % (D / 8);
+            uint4 v = make_uint4(0u, 0u, 0u, 0u);
+            if (col < ncols_q) {
+                const int cc = MQ ? col0 + col : col;
+                const int off = MQ ? (cc / p.group) * p.num_q_heads + cc % p.group : col;
+                v = __ldg(reinterpret_cast<const uint4*>(qb0 + (int64_t)off * D) + chunk);
+            }
+            *reinterpret_cast<uint4*>(q_tile + col * (D * 2) + ((chunk ^ (col & 7)) << 4)) = v;
+        }
+    }
     __syncthreads();
 
     const uint32_t ring_addr = ptx::smem_addr(ring);
@@ -773,8 +814,12 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
                 const bool ok = col < ncols;
                 const int d0 = F8 ? ks * 16 + 4 * tq : ks * 16 + 2 * tq;
                 const int d1 = F8 ? d0 + 2 : d0 + 8;
-                qb[nt][ks][0] = ok ? __ldg(qrow + d0 / 2) : 0u;
-                qb[nt][ks][1] = ok ? __ldg(qrow + d1 / 2) : 0u;
+                if constexpr (!QS) {
+                    qb[nt][ks][0] = ok ? __ldg(qrow + d0 / 2) : 0u;
+                    qb[nt][ks][1] = ok ? __ldg(qrow + d1 / 2) : 0u;
+                } else {
+                    qb[nt][ks][0] = qb[nt][ks][1] = 0u;
+                }
             }
             m0[nt] = m1[nt] = -INFINITY;
             l0[nt] = l1[nt] = 0.f;
@@ -812,14 +857,15 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
             const int nvalid = blk >= 0 ? min(kStageTokens, t_end - tok0) : 0;
             if (nvalid > 0) {
                 const uint32_t kbase = ring_addr + slot * Cfg::kStageBytes;
+                const uint32_t qaddr = ptx::smem_addr(q_tile);
                 if (MQ && tok0 + kStageTokens > causal0)
-                    stage_update<T, D, NT, true, F8>(kbase, kbase + Cfg::kHalfBytes, nvalid, tok0,
-                                                     lim, qb, o, m0, m1, l0, l1, p.scale_log2,
-                                                     lane);
+                    stage_update<T, D, NT, true, F8, QS>(kbase, kbase + Cfg::kHalfBytes, nvalid,
+                                                         tok0, lim, qb, o, m0, m1, l0, l1,
+                                                         p.scale_log2, lane, qaddr);
                 else
-                    stage_update<T, D, NT, false, F8>(kbase, kbase + Cfg::kHalfBytes, nvalid, 0,
-                                                      no_limit, qb, o, m0, m1, l0, l1,
-                                                      p.scale_log2, lane);
+                    stage_update<T, D, NT, false, F8, QS>(kbase, kbase + Cfg::kHalfBytes, nvalid,
+                                                          0, no_limit, qb, o, m0, m1, l0, l1,
+                                                          p.scale_log2, lane, qaddr);
             }
             __syncwarp();
 #ifdef PKV_DEBUG
@@ -2200,13 +2246,13 @@ static cudaError_t launch_decode_t(const CUtensorMap& mk, const CUtensorMap& mv,
     static cudaError_t attr_err = cudaSuccess;
     std::call_once(once, [&] {
         attr_err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                        Tile<D, F8>::kSmemBytes);
+                                        Tile<D, F8>::kSmemBytes + q_tile_bytes<D, NT, F8>());
     });
     if (attr_err != cudaSuccess) return attr_err;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = grid;
     cfg.blockDim = dim3(kThreads);
-    cfg.dynamicSmemBytes = Tile<D, F8>::kSmemBytes;
+    cfg.dynamicSmemBytes = Tile<D, F8>::kSmemBytes + q_tile_bytes<D, NT, F8>();
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
