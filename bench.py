@@ -60,17 +60,17 @@ WORKLOAD_TEXT = {
 NCU_TRAFFIC = {
     # ncu --metrics dram__bytes_read.sum,dram__bytes_write.sum,gpu__time_duration.sum
     #     --clock-control none -k regex:decode_kernel -s 4 -c 1 (the fused default step)
-    "c4": {"digest": "ebf1c529cd793cc9", "splits": 64, "shared": False, "fused": True,
-           "bytes": 2818491904 + 7860992},
-    "c2": {"digest": "ebf1c529cd793cc9", "splits": 2, "shared": False, "fused": True,
-           "bytes": 2312603392 + 4647680},
-    "c3": {"digest": "ebf1c529cd793cc9", "splits": 3, "shared": False, "fused": True,
-           "bytes": 537501184 + 3979520},
+    "c4": {"digest": "0835a9a67be948cb", "splits": 64, "shared": False, "fused": True,
+           "bytes": 2818606592 + 7824640},
+    "c2": {"digest": "0835a9a67be948cb", "splits": 2, "shared": False, "fused": True,
+           "bytes": 2312613120 + 4626432},
+    "c3": {"digest": "0835a9a67be948cb", "splits": 3, "shared": False, "fused": True,
+           "bytes": 537499136 + 4073728},
     # shared-prefix path: decode_kernel (suffixes, and the merge of each unit by
     # its last CTA; -k regex:decode_kernel -s 4 -c 1) + prefix_kernel
     # (-k regex:prefix_kernel -s 2 -c 1); the plan kernel's few KB are not included
-    "c5": {"digest": "ebf1c529cd793cc9", "splits": 8, "shared": True, "fused": False,
-           "bytes": (1536187904 + 5140992) + (35748864 + 13824)},
+    "c5": {"digest": "0835a9a67be948cb", "splits": 8, "shared": True, "fused": False,
+           "bytes": (1536162816 + 5147904) + (35748352 + 15872)},
 }
 
 
