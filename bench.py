@@ -71,6 +71,8 @@ NCU_TRAFFIC = {
     # (-k regex:prefix_kernel -s 2 -c 1); the plan kernel's few KB are not included
     "c5": {"digest": "0835a9a67be948cb", "splits": 8, "shared": True, "fused": False,
            "bytes": (1536162816 + 5147904) + (35748352 + 15872)},
+    "c5_bs32": {"digest": "0835a9a67be948cb", "splits": 8, "shared": True, "fused": False,
+                "bytes": (1536127744 + 4915968) + (35748608 + 10496)},
 }
 
 
