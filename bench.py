@@ -393,9 +393,9 @@ def _measure(name, args, device, rank, ws, cpu_seconds):
     # append, decode, merge when split; the shared-prefix path: append, plan,
     # prefix (second stream) and decode (no merge launch)
     # The step's append is done by the decode kernel itself
-    # (pkv_append_decode_attention) on the plain 16-bit path; --unfused times
-    # the two calls (pkv_append, then pkv_decode_attention) instead.
-    fused = args.fused and not mq and not shared and not fp8
+    # (pkv_append_decode_attention, or its E4M3 form) on the plain path;
+    # --unfused times the two calls (the append, then the decode) instead.
+    fused = args.fused and not mq and not shared
     if mq:
         launches_per_step = 2 + (1 if mq_kernel == "tcgen05" or mq_parts > 1 else 0)
     else:
@@ -429,13 +429,21 @@ def _measure(name, args, device, rank, ws, cpu_seconds):
         else:
             pkv.append(k_new, v_new, kc, vc, slot_mapping, err_flag=flag, layout=layout)
 
+    def fused_call(c, q, k_new, v_new, block_tables, context_lens, out=out):
+        kc, vc = caches[c]
+        if fp8:
+            pkv.append_decode_attention_fp8(q, k_new, v_new, kc, vc, block_tables, context_lens,
+                                            mcl, k_scale, v_scale, scale=w.scale,
+                                            num_splits=args.splits, out=out,
+                                            workspace=workspace, err_flag=flag, layout=layout)
+        else:
+            pkv.append_decode_attention(q, k_new, v_new, kc, vc, block_tables, context_lens,
+                                        mcl, scale=w.scale, num_splits=args.splits, out=out,
+                                        workspace=workspace, err_flag=flag, layout=layout)
+
     def step(c):
         if fused:
-            kc, vc = caches[c]
-            pkv.append_decode_attention(w.q, w.k_new, w.v_new, kc, vc,
-                                        w.block_tables, w.context_lens, mcl, scale=w.scale,
-                                        num_splits=args.splits, out=out, workspace=workspace,
-                                        err_flag=flag, layout=layout)
+            fused_call(c, w.q, w.k_new, w.v_new, w.block_tables, w.context_lens)
             return
         append_call(c, w.k_new, w.v_new, w.slot_mapping)
         decode_call(c, w.q, w.block_tables, w.context_lens)
@@ -553,11 +561,8 @@ def _measure(name, args, device, rank, ws, cpu_seconds):
         stream.wait_event(out_free[sidx])          # this output buffer's copy-out is done
         v = views[sidx]
         if fused:
-            kc, vc = caches[i % KV_COPIES]
-            pkv.append_decode_attention(v["q"], v["k_new"], v["v_new"], kc, vc,
-                                        v["block_tables"], v["context_lens"], mcl,
-                                        scale=w.scale, num_splits=args.splits, out=outs[sidx],
-                                        workspace=workspace, err_flag=flag, layout=layout)
+            fused_call(i % KV_COPIES, v["q"], v["k_new"], v["v_new"], v["block_tables"],
+                       v["context_lens"], out=outs[sidx])
         else:
             append_call(i % KV_COPIES, v["k_new"], v["v_new"], v["slot_mapping"])
             decode_call(i % KV_COPIES, v["q"], v["block_tables"], v["context_lens"],

@@ -218,6 +218,29 @@ pkv_status pkv_append_decode_attention(void* out, const void* q, const void* k_n
                                        int32_t* err_flag, void* stream);
 
 /*
+ * The same one-launch step over E4M3 caches ([vllm-06] 3.3 FP8 inference;
+ * 2.2, the KV-cache write fused with quantisation): the result, and the cache
+ * after the call, are those of pkv_append_fp8 with slot_mapping[b] = the slot
+ * of position context_lens[b] - 1 of sequence b, followed by
+ * pkv_decode_attention_fp8.  The new rows are quantised exactly as
+ * pkv_append_fp8 does (the same codes, bit for bit).
+ *
+ *   k_new, v_new  [num_seqs][num_kv_heads][head_dim], dtype (fp16 or bf16)
+ *   k_cache, v_cache  uint8 E4M3 codes, written at those slots (private pages)
+ *   k_scale, v_scale, other arguments as for pkv_decode_attention_fp8
+ */
+pkv_status pkv_append_decode_attention_fp8(void* out, const void* q, const void* k_new,
+                                           const void* v_new, void* k_cache, void* v_cache,
+                                           const int32_t* block_tables, int max_blocks_per_seq,
+                                           const int32_t* context_lens, int max_context_len,
+                                           int num_seqs, int num_blocks, int block_size,
+                                           int num_q_heads, int num_kv_heads, int head_dim,
+                                           float scale, float k_scale, float v_scale,
+                                           int num_splits, void* workspace,
+                                           size_t workspace_bytes, pkv_dtype dtype,
+                                           int32_t* err_flag, void* stream);
+
+/*
  * Decode attention for callers that cannot allocate device memory.
  *
  * The paper has no counterpart to this call; it exists for integration.  Some

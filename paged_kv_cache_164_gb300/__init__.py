@@ -68,6 +68,8 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
                                          i, p, p]
     lib.pkv_append_decode_attention.argtypes = [p, p, p, p, p, p, p, i, p, i, i, i, i, i, i, i,
                                                 f, i, p, sz, i, p, p]
+    lib.pkv_append_decode_attention_fp8.argtypes = [p, p, p, p, p, p, p, i, p, i, i, i, i, i, i,
+                                                    i, f, f, f, i, p, sz, i, p, p]
     lib.pkv_append_fp8.argtypes = [p, p, p, p, p, i, i, i, i, i, f, f, i, p, p]
     lib.pkv_decode_attention_fp8.argtypes = [p, p, p, p, p, i, p, i, i, i, i, i, i, i, f, f, f, i,
                                              p, sz, i, p, p]
@@ -92,7 +94,8 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.pkv_debug_build.restype = i
     lib.pkv_selftest_wait_timeout.argtypes = [p, ctypes.c_ulonglong, p]
     for name in ("pkv_append", "pkv_decode_attention", "pkv_decode_attention_noalloc",
-                 "pkv_append_decode_attention", "pkv_append_fp8", "pkv_decode_attention_fp8",
+                 "pkv_append_decode_attention", "pkv_append_decode_attention_fp8",
+                 "pkv_append_fp8", "pkv_decode_attention_fp8",
                  "pkv_decode_attention_prefix_shared", "pkv_multi_query_attention",
                  "pkv_merge", "pkv_gather", "pkv_selftest_wait_timeout",
                  "pkv_check_error", "pkv_max_group_size", "pkv_multi_query_plan"):
@@ -340,6 +343,49 @@ def decode_attention_fp8(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.
         float(v_scale), int(num_splits), ws_ptr, ws_bytes, _kv_code(q, layout),
         _opt(err_flag, "err_flag"), _stream(stream, q.device))
     _check(st, "pkv_decode_attention_fp8")
+    return out
+
+
+def append_decode_attention_fp8(q: torch.Tensor, k_new: torch.Tensor, v_new: torch.Tensor,
+                                k_cache: torch.Tensor, v_cache: torch.Tensor,
+                                block_tables: torch.Tensor, context_lens: torch.Tensor,
+                                max_context_len: int, k_scale: float, v_scale: float,
+                                scale: Optional[float] = None, num_splits: int = 0,
+                                out: Optional[torch.Tensor] = None,
+                                workspace: Optional[torch.Tensor] = None,
+                                err_flag: Optional[torch.Tensor] = None, stream=None,
+                                layout: str = "nhd") -> torch.Tensor:
+    """``append_decode_attention`` over uint8 E4M3 caches: sequence b's new token
+    is quantised as ``append_fp8`` does and written at position context_lens[b] - 1,
+    then ``decode_attention_fp8`` runs over the updated cache; head_dim 128."""
+    lib = load()
+    if k_cache.dtype != torch.uint8 or v_cache.dtype != torch.uint8:
+        raise TypeError("E4M3 caches are uint8 tensors of codes")
+    b, h_q, d = q.shape
+    nb, bs, h_kv, d2 = _cache_dims(k_cache, layout)
+    if d2 != d or v_cache.shape != k_cache.shape or block_tables.dim() != 2 or \
+            block_tables.shape[0] != b or context_lens.shape != (b,) or \
+            k_new.shape != (b, h_kv, d) or v_new.shape != (b, h_kv, d):
+        raise ValueError("inconsistent fp8 append-decode shapes")
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    if out is None:
+        out = torch.empty_like(q)
+    # a given workspace is checked against the plan by the library itself
+    need = workspace_size(b, h_q, h_kv, d, bs, max_context_len, num_splits) \
+        if workspace is None else 0
+    if workspace is None and need > 0:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    ws_ptr = ctypes.c_void_p(0) if workspace is None else _dev(workspace, "workspace")
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    st = lib.pkv_append_decode_attention_fp8(
+        _dev(out, "out", q.dtype), _dev(q, "q"), _dev(k_new, "k_new", q.dtype),
+        _dev(v_new, "v_new", q.dtype), _dev(k_cache, "k_cache"), _dev(v_cache, "v_cache"),
+        _dev(block_tables, "block_tables", torch.int32), block_tables.shape[1],
+        _dev(context_lens, "context_lens", torch.int32), int(max_context_len), b, nb, bs, h_q,
+        h_kv, d, float(scale), float(k_scale), float(v_scale), int(num_splits), ws_ptr,
+        ws_bytes, _kv_code(q, layout), _opt(err_flag, "err_flag"), _stream(stream, q.device))
+    _check(st, "pkv_append_decode_attention_fp8")
     return out
 
 

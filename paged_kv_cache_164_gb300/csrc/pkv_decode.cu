@@ -87,6 +87,7 @@ struct DecodeParams {
     float* partial_lse;  // [B][H_q][num_splits]
     const void* k_new;     // nullable: fused append of one new token per sequence ([B][H_kv][D])
     const void* v_new;
+    float k_scale;         // E4M3 cache: the fused append stores E4M3(k / k_scale) (v: v_scale)
     void* k_cache;         // the caches, for the fused append's stores
     void* v_cache;
     const int2* seq_info;  // nullable: per sequence (shared-prefix tokens, prefix partials written)
@@ -666,7 +667,9 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
     // Fused append: the one CTA of (sequence, KV head) whose partition holds the
     // last position n-1 first stores the new token's K and V rows of this KV
     // head into that position's slot, then orders the stores before its own
-    // TMA reads (no other CTA reads that position).
+    // TMA reads (no other CTA reads that position).  An E4M3 cache stores the
+    // codes pkv_append_fp8 would: E4M3(x / scale), the quotient rounded to fp32
+    // and then to the nearest E4M3 value (ties to even), saturating at +-448.
     if (p.k_new != nullptr && n_raw == n && n > 0 && t_begin <= n - 1 && n - 1 < t_end &&
         warp < kConsumerWarps && tid < 2 * (D / 8)) {
         const int pos = n - 1;
@@ -679,7 +682,23 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ 
                 (p.hnd ? ((int64_t)blk * p.num_kv_heads + g) * bs + pos % bs
                        : ((int64_t)blk * bs + pos % bs) * p.num_kv_heads + g) * (D / 8) + c;
             const uint4 v = __ldg(static_cast<const uint4*>(is_v ? p.v_new : p.k_new) + src);
-            static_cast<uint4*>(is_v ? p.v_cache : p.k_cache)[dst] = v;
+            if constexpr (F8) {
+                // eight 16-bit elements in, eight one-byte codes out
+                const float sc = is_v ? p.v_scale : p.k_scale;
+                const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+                uint32_t codes[2] = {0u, 0u};
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const float2 x = pair_to_float2(w[j], T());
+                    const float2 f = make_float2(__fdiv_rn(x.x, sc), __fdiv_rn(x.y, sc));
+                    const uint32_t two = __nv_cvt_float2_to_fp8x2(f, __NV_SATFINITE, __NV_E4M3);
+                    codes[j / 2] |= two << (16 * (j % 2));
+                }
+                static_cast<uint2*>(is_v ? p.v_cache : p.k_cache)[dst] =
+                    make_uint2(codes[0], codes[1]);
+            } else {
+                static_cast<uint4*>(is_v ? p.v_cache : p.k_cache)[dst] = v;
+            }
             ptx::fence_proxy_async_global();
         }
     }
@@ -2545,7 +2564,7 @@ static pkv_status decode_impl(void* out, const void* q, const void* k_new, const
     if ((k_new == nullptr) != (v_new == nullptr) ||
         (k_new != nullptr && (!aligned16(k_new) || !aligned16(v_new))))
         return PKV_ERR_INVALID_ARG;
-    if (f8 && (head_dim != 128 || k_new != nullptr)) return PKV_ERR_UNSUPPORTED;
+    if (f8 && head_dim != 128) return PKV_ERR_UNSUPPORTED;
     if (f8 && (!std::isfinite(k_scale) || !std::isfinite(v_scale) || k_scale <= 0.f ||
                v_scale <= 0.f))
         return PKV_ERR_INVALID_ARG;
@@ -2589,6 +2608,7 @@ static pkv_status decode_impl(void* out, const void* q, const void* k_new, const
     p.item_count = nullptr;
     p.k_new = k_new;
     p.v_new = v_new;
+    p.k_scale = k_scale;
     p.k_cache = k_cache;
     p.v_cache = v_cache;
     p.hnd = hnd;
@@ -2671,6 +2691,22 @@ extern "C" pkv_status pkv_append_decode_attention(
                        context_lens, max_context_len, num_seqs, num_blocks, block_size,
                        num_q_heads, num_kv_heads, head_dim, scale, num_splits, workspace,
                        workspace_bytes, dtype, err_flag, stream);
+}
+
+extern "C" pkv_status pkv_append_decode_attention_fp8(
+    void* out, const void* q, const void* k_new, const void* v_new, void* k_cache, void* v_cache,
+    const int32_t* block_tables, int max_blocks_per_seq, const int32_t* context_lens,
+    int max_context_len, int num_seqs, int num_blocks, int block_size, int num_q_heads,
+    int num_kv_heads, int head_dim, float scale, float k_scale, float v_scale, int num_splits,
+    void* workspace, size_t workspace_bytes, pkv_dtype dtype, int32_t* err_flag, void* stream) {
+    const pkv_status st = check_shapes(num_seqs, num_q_heads, num_kv_heads, head_dim, block_size,
+                                       max_context_len, num_splits);
+    if (st != PKV_OK) return st;
+    if (num_seqs > 0 && (k_new == nullptr || v_new == nullptr)) return PKV_ERR_INVALID_ARG;
+    return decode_impl(out, q, k_new, v_new, k_cache, v_cache, block_tables, max_blocks_per_seq,
+                       context_lens, max_context_len, num_seqs, num_blocks, block_size,
+                       num_q_heads, num_kv_heads, head_dim, scale, num_splits, workspace,
+                       workspace_bytes, dtype, err_flag, stream, true, k_scale, v_scale);
 }
 
 extern "C" pkv_status pkv_merge(void* out, const float* partial_o, const float* partial_lse,

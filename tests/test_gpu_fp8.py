@@ -147,3 +147,37 @@ def test_fp8_decode_subnormal_codes(dtype):
                                          w.block_tables.cpu().numpy(), w.context_lens.cpu().numpy(),
                                          1.0 / np.sqrt(s.head_dim), k_scale, v_scale, dtype)
     assert_attention_close(out, expect, f"subnormal codes {dtype}")
+
+
+@pytest.mark.parametrize("layout", ["nhd", "hnd"])
+@pytest.mark.parametrize("splits", [0, 3])
+@pytest.mark.parametrize("key", sorted(CASES))
+def test_fused_fp8_append_decode_matches_oracle_and_separate_append(key, splits, layout):
+    # One launch: the decode kernel quantises each sequence's new token into the
+    # slot of position n-1 (the same codes the oracle's quantiser gives, bit for
+    # bit) and attends over the updated E4M3 cache.
+    k_scale, v_scale = 5.0 / 448, 4.5 / 448
+    case = dict(CASES[key])
+    name = case.pop("name")
+    w = make_workload(name, device="cuda", poison=True, **case)
+    k0 = oracle.encode_e4m3(w.k_cache.float().cpu().numpy() / np.float32(k_scale))
+    v0 = oracle.encode_e4m3(w.v_cache.float().cpu().numpy() / np.float32(v_scale))
+    kq, vq = k0.copy(), v0.copy()
+    assert oracle.append_fp8(kq, vq, bits(w.k_new), bits(w.v_new), w.slot_mapping.cpu().numpy(),
+                             k_scale, v_scale, w.spec.dtype) == 0
+    expect = oracle.decode_attention_fp8(bits(w.q), kq, vq, w.block_tables.cpu().numpy(),
+                                         w.context_lens.cpu().numpy(), w.scale, k_scale, v_scale,
+                                         w.spec.dtype)
+    kc, vc = torch.from_numpy(k0).cuda(), torch.from_numpy(v0).cuda()
+    if layout == "hnd":
+        kc, vc = to_head_major(kc), to_head_major(vc)
+    flag = pkv.new_error_flag("cuda")
+    out = pkv.append_decode_attention_fp8(w.q, w.k_new, w.v_new, kc, vc, w.block_tables,
+                                          w.context_lens, w.max_context_len, k_scale, v_scale,
+                                          scale=w.scale, num_splits=splits, err_flag=flag,
+                                          layout=layout)
+    assert pkv.check_error(flag) == 0
+    if layout == "hnd":
+        kc, vc = kc.permute(0, 2, 1, 3).contiguous(), vc.permute(0, 2, 1, 3).contiguous()
+    assert np.array_equal(kc.cpu().numpy(), kq) and np.array_equal(vc.cpu().numpy(), vq)
+    assert_attention_close(out, expect, f"{key} splits={splits} {layout}")

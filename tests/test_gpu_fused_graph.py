@@ -210,3 +210,33 @@ def test_graph_of_e4m3_append_then_decode_replays_like_eager():
                                         w.context_lens, w._mcl, k_scale, v_scale, scale=w.scale,
                                         out=w._out, workspace=w._ws)
     _graph_vs_eager(make, step)
+
+
+def test_graph_of_fused_e4m3_step_replays_like_eager():
+    import numpy as np
+
+    import oracle
+    k_scale, v_scale = 5.0 / 448, 4.5 / 448
+
+    def make():
+        w = make_workload("c3", device="cuda", num_seqs=4, lengths=("uniform", 100, 900),
+                          max_len_cap=960, seed=77)
+        s = w.spec
+        w.k_cache = torch.from_numpy(oracle.encode_e4m3(
+            w.k_cache.float().cpu().numpy() / np.float32(k_scale))).cuda()
+        w.v_cache = torch.from_numpy(oracle.encode_e4m3(
+            w.v_cache.float().cpu().numpy() / np.float32(v_scale))).cuda()
+        w._mcl = w.max_context_len
+        w._ws = torch.empty(max(16, pkv.workspace_size(s.num_seqs, s.num_q_heads,
+                                                       s.num_kv_heads, s.head_dim, s.block_size,
+                                                       w._mcl, 0)),
+                            dtype=torch.uint8, device="cuda")
+        w._out = torch.empty_like(w.q)
+        return w
+
+    def step(w):
+        return pkv.append_decode_attention_fp8(w.q, w.k_new, w.v_new, w.k_cache, w.v_cache,
+                                               w.block_tables, w.context_lens, w._mcl, k_scale,
+                                               v_scale, scale=w.scale, out=w._out,
+                                               workspace=w._ws)
+    _graph_vs_eager(make, step)
