@@ -60,19 +60,19 @@ WORKLOAD_TEXT = {
 NCU_TRAFFIC = {
     # ncu --metrics dram__bytes_read.sum,dram__bytes_write.sum,gpu__time_duration.sum
     #     --clock-control none -k regex:decode_kernel -s 4 -c 1 (the fused default step)
-    "c4": {"digest": "0835a9a67be948cb", "splits": 64, "shared": False, "fused": True,
-           "bytes": 2818606592 + 7824640},
-    "c2": {"digest": "0835a9a67be948cb", "splits": 2, "shared": False, "fused": True,
-           "bytes": 2312613120 + 4626432},
-    "c3": {"digest": "0835a9a67be948cb", "splits": 3, "shared": False, "fused": True,
-           "bytes": 537499136 + 4073728},
+    "c4": {"digest": "09423fd81f92c1df", "splits": 64, "shared": False, "fused": True,
+           "bytes": 2818685952 + 8013568},
+    "c2": {"digest": "09423fd81f92c1df", "splits": 2, "shared": False, "fused": True,
+           "bytes": 2312810240 + 4622592},
+    "c3": {"digest": "09423fd81f92c1df", "splits": 3, "shared": False, "fused": True,
+           "bytes": 537497344 + 4061184},
     # shared-prefix path: decode_kernel (suffixes, and the merge of each unit by
     # its last CTA; -k regex:decode_kernel -s 4 -c 1) + prefix_kernel
     # (-k regex:prefix_kernel -s 2 -c 1); the plan kernel's few KB are not included
-    "c5": {"digest": "0835a9a67be948cb", "splits": 8, "shared": True, "fused": False,
-           "bytes": (1536162816 + 5147904) + (35748352 + 15872)},
-    "c5_bs32": {"digest": "0835a9a67be948cb", "splits": 8, "shared": True, "fused": False,
-                "bytes": (1536127744 + 4915968) + (35748608 + 10496)},
+    "c5": {"digest": "09423fd81f92c1df", "splits": 8, "shared": True, "fused": False,
+           "bytes": (1536196096 + 5471744) + (35749120 + 12032)},
+    "c5_bs32": {"digest": "09423fd81f92c1df", "splits": 8, "shared": True, "fused": False,
+                "bytes": (1536193280 + 5236736) + (35747840 + 15872)},
 }
 
 
