@@ -60,19 +60,19 @@ WORKLOAD_TEXT = {
 NCU_TRAFFIC = {
     # ncu --metrics dram__bytes_read.sum,dram__bytes_write.sum,gpu__time_duration.sum
     #     --clock-control none -k regex:decode_kernel -s 4 -c 1 (the fused default step)
-    "c4": {"digest": "09423fd81f92c1df", "splits": 64, "shared": False, "fused": True,
-           "bytes": 2818685952 + 8013568},
-    "c2": {"digest": "09423fd81f92c1df", "splits": 2, "shared": False, "fused": True,
-           "bytes": 2312810240 + 4622592},
-    "c3": {"digest": "09423fd81f92c1df", "splits": 3, "shared": False, "fused": True,
-           "bytes": 537497344 + 4061184},
+    "c4": {"digest": "cf3422a1a4f3f93b", "splits": 64, "shared": False, "fused": True,
+           "bytes": 2818488320 + 7384064},
+    "c2": {"digest": "cf3422a1a4f3f93b", "splits": 2, "shared": False, "fused": True,
+           "bytes": 2312607744 + 4360192},
+    "c3": {"digest": "cf3422a1a4f3f93b", "splits": 3, "shared": False, "fused": True,
+           "bytes": 537545984 + 4047872},
     # shared-prefix path: decode_kernel (suffixes, and the merge of each unit by
     # its last CTA; -k regex:decode_kernel -s 4 -c 1) + prefix_kernel
     # (-k regex:prefix_kernel -s 2 -c 1); the plan kernel's few KB are not included
-    "c5": {"digest": "09423fd81f92c1df", "splits": 8, "shared": True, "fused": False,
-           "bytes": (1536196096 + 5471744) + (35749120 + 12032)},
-    "c5_bs32": {"digest": "09423fd81f92c1df", "splits": 8, "shared": True, "fused": False,
-                "bytes": (1536193280 + 5236736) + (35747840 + 15872)},
+    "c5": {"digest": "cf3422a1a4f3f93b", "splits": 8, "shared": True, "fused": False,
+           "bytes": (1536165632 + 5141504) + (35748096 + 16640)},
+    "c5_bs32": {"digest": "cf3422a1a4f3f93b", "splits": 8, "shared": True, "fused": False,
+                "bytes": (1536079616 + 5253632) + (35749120 + 9216)},
 }
 
 
@@ -372,6 +372,10 @@ def _measure(name, args, device, rank, ws, cpu_seconds):
     shared = s.shared_prefix_groups > 0 and args.prefix_sharing and not mq
     # Host-side bounds of the group metadata, read once (each read syncs the device).
     max_group_size, max_prefix_len = w.max_group_size, w.max_prefix_len
+    if shared and args.splits:
+        # the shared-prefix call plans its own suffix partitions
+        raise SystemExit("--splits does not apply to the shared-prefix step "
+                         "(add --no-prefix-sharing to time the plain path)")
     splits = pkv.decode_num_splits(s.num_seqs, s.num_q_heads, s.num_kv_heads, s.head_dim,
                                    s.block_size, mcl, args.splits, kv=args.kv)
     mq_kernel, mq_parts = None, 0

@@ -90,6 +90,43 @@ def test_group_sizes_and_head_dims(group, d):
     assert_attention_close(_run(w), expect, f"G={group} d={d}")
 
 
+@pytest.mark.parametrize("dtype", ["bf16", "fp16"])
+@pytest.mark.parametrize("group", [8, 16])
+@pytest.mark.parametrize("rise", [0.075, 0.117, 0.225, -0.075])
+def test_scores_rising_across_stages(rise, group, dtype):
+    """Scores that climb (or fall) steadily along the context by about `rise`
+    (base 2) per token.  A consumer warp of the decode kernel takes every fourth
+    16-token stage, so its consecutive stages lie 64 tokens apart: 0.117 raises
+    the maximum between them by ~7.5, just under the 2^8 the running softmax
+    reference tolerates (kept, exponentials up to ~2^7.5), 0.225 by ~14.4 (the
+    reference moves every time), 0.075 by ~4.8 (it moves every second time); the
+    partitions of each split count start their own.  K is nonzero in dim 0 only
+    and the ramp is centred on the context, so every score is one exact product
+    of at most ~80 in magnitude and the comparison measures the softmax, not
+    fp32 summation of large logits."""
+    lens = (600, 333)
+    w = make_workload("c3", num_seqs=2, num_q_heads=2 * group, num_kv_heads=2, head_dim=128,
+                      dtype=dtype, lengths=("fixed", lens), max_len_cap=608,
+                      pool="free_list", pool_slack=0.1, seed=7 + group, device="cuda",
+                      poison=True)
+    bs = w.spec.block_size
+    # head h's base-2 score of token t: rise * (1 + h / 256) * (t - n / 2)
+    h = torch.arange(w.q.shape[1], device="cuda", dtype=torch.float32)
+    w.q[:, :, 0] = (1.0 + h / 256.0)[None, :].to(w.q.dtype)
+    unit = 1.0 / (w.scale * math.log2(math.e))
+    for b, n in enumerate(lens):
+        t = torch.arange(n, device="cuda")
+        kv = torch.zeros(n, w.k_cache.shape[2], w.k_cache.shape[3], device="cuda")
+        kv[:, :, 0] = (rise * (t.float() - n / 2) * unit)[:, None]
+        blk = w.block_tables[b, t // bs].long()
+        w.k_cache[blk[:-1], (t % bs)[:-1]] = kv[:-1].to(w.k_cache.dtype)
+        w.k_new[b] = kv[-1].to(w.k_new.dtype)
+    expect, _, _ = oracle_after_append(w)
+    for splits in (0, 1, 3):
+        assert_attention_close(_run(w, splits), expect,
+                               f"rise={rise} G={group} {dtype} splits={splits}")
+
+
 def test_context_len_zero_gives_zeros():
     w = _make("mha_ragged")
     expect, _, _ = oracle_after_append(w)
