@@ -353,9 +353,6 @@ def _measure(name, args, device, rank, ws, cpu_seconds):
     fp8 = args.kv == "fp8"
     k_scale = v_scale = 1.0
     if fp8:
-        if mq or s.shared_prefix_groups and args.prefix_sharing:
-            raise SystemExit("--kv fp8 times the plain decode path only "
-                             "(add --no-prefix-sharing for shared-prefix workloads)")
         k_scale = float(w.k_cache.float().abs().max()) / 448.0
         v_scale = float(w.v_cache.float().abs().max()) / 448.0
         w.k_cache = (w.k_cache.float() / k_scale).clamp(-448, 448).to(
@@ -372,10 +369,6 @@ def _measure(name, args, device, rank, ws, cpu_seconds):
     shared = s.shared_prefix_groups > 0 and args.prefix_sharing and not mq
     # Host-side bounds of the group metadata, read once (each read syncs the device).
     max_group_size, max_prefix_len = w.max_group_size, w.max_prefix_len
-    if shared and args.splits:
-        # the shared-prefix call plans its own suffix partitions
-        raise SystemExit("--splits does not apply to the shared-prefix step "
-                         "(add --no-prefix-sharing to time the plain path)")
     splits = pkv.decode_num_splits(s.num_seqs, s.num_q_heads, s.num_kv_heads, s.head_dim,
                                    s.block_size, mcl, args.splits, kv=args.kv)
     mq_kernel, mq_parts = None, 0
@@ -670,12 +663,7 @@ def run_gpu(args):
     torch.cuda.set_device(device)
     pkv.load()
 
-    # Without --config: the headline on the largest single-GPU workload (the
-    # long-context layer) and a line for each of the other workloads.
-    if args.config:
-        names = [args.config]
-    else:
-        names = [HEADLINE_CONFIG] + ([] if args.no_per_config else list(PER_CONFIGS))
+    names = config_names(args)
     sampler = ClockSampler(device.index, period_ms=50) if rank == 0 else None
     if sampler:
         sampler.wait_first()
@@ -755,6 +743,33 @@ def run_gpu(args):
         dist.destroy_process_group()
 
 
+def config_names(args):
+    """The workloads one run measures: without --config, the headline on the
+    largest single-GPU workload (the long-context layer) and a line for each of
+    the other workloads."""
+    if args.config:
+        return [args.config]
+    return [HEADLINE_CONFIG] + ([] if args.no_per_config else list(PER_CONFIGS))
+
+
+def check_args(args, ap):
+    """Refuses, before any GPU work, the flag combinations a step cannot honour."""
+    from workloads import SPECS
+
+    for name in config_names(args):
+        shared = SPECS[name].shared_prefix_groups > 0 and args.prefix_sharing and args.q_len == 0
+        if args.kv == "fp8" and (args.q_len > 0 or shared):
+            ap.error(f"{name}: --kv fp8 times the plain decode path only "
+                     "(add --no-prefix-sharing for shared-prefix workloads)")
+        if args.splits and shared:
+            # the shared-prefix call plans its own suffix partitions
+            ap.error(f"{name}: --splits does not apply to the shared-prefix step "
+                     "(add --no-prefix-sharing to time the plain path)")
+        if args.splits and args.q_len > 0:
+            ap.error("--splits does not apply to the multi-query step "
+                     "(it plans its own context partitions)")
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -793,6 +808,7 @@ def main(argv=None):
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("at least 3 warm-up steps")
+    check_args(args, ap)
     if args.impl == "reference":
         run_reference(args)
     else:

@@ -61,3 +61,48 @@ def test_shared_prefix_pages_count_once_per_group():
     assert got["decode"] == decode
     logical_kv = 2 * sum(lens) * w.spec.num_kv_heads * w.spec.head_dim * 2
     assert got["decode_logical"] - got["decode"] == logical_kv - kv > 0
+
+
+@pytest.mark.parametrize("argv,what", [
+    (["--config", "c5", "--splits", "4"], "--splits does not apply"),
+    (["--config", "c5_bs32", "--splits", "12"], "--splits does not apply"),
+    (["--splits", "4"], "--splits does not apply"),  # the default run includes c5
+    (["--config", "c5", "--kv", "fp8"], "--kv fp8 times the plain decode path only"),
+    (["--config", "c3", "--kv", "fp8", "--q-len", "4"], "--kv fp8 times the plain decode path only"),
+    (["--config", "c3", "--q-len", "4", "--splits", "2"], "--splits does not apply to the multi-query"),
+])
+def test_bench_refuses_flags_a_step_cannot_honour(argv, what, capsys):
+    """Refused on the host before any GPU work, so a line is never labelled with
+    a split count or cache type that the timed step did not use."""
+    with pytest.raises(SystemExit) as e:
+        bench.main(argv)
+    assert e.value.code == 2
+    assert what in capsys.readouterr().err
+
+
+@pytest.mark.parametrize("argv", [
+    ["--config", "c5", "--splits", "4", "--no-prefix-sharing"],
+    ["--config", "c3", "--splits", "4"],
+    ["--config", "c3", "--kv", "fp8"],
+    ["--config", "c5", "--kv", "fp8", "--no-prefix-sharing"],
+    ["--config", "c5", "--q-len", "4"],
+])
+def test_bench_accepts_flags_the_step_honours(argv):
+    args = _parse(argv)  # main() checks the flags before it would start the run
+    assert args.config == argv[1]
+
+
+def _parse(argv):
+    """bench.main's parsing and checks, with the run itself replaced."""
+    captured = {}
+
+    def fake_run(args):
+        captured["args"] = args
+
+    old_gpu, old_ref = bench.run_gpu, bench.run_reference
+    bench.run_gpu = bench.run_reference = fake_run
+    try:
+        bench.main(argv)
+    finally:
+        bench.run_gpu, bench.run_reference = old_gpu, old_ref
+    return captured["args"]
