@@ -156,3 +156,29 @@ def test_library_sources_allocate_no_device_memory():
     for name in sorted(os.listdir(csrc)):
         text = open(os.path.join(csrc, name)).read()
         assert not banned.search(text), f"{name} names {banned.search(text).group(0)}"
+
+
+def _append_decode_fp8(lib, **kw):
+    fake = ctypes.c_void_p(1 << 20)  # 16-byte aligned, never dereferenced: the call rejects first
+    a = dict(out=fake, q=fake, kn=fake, vn=fake, k=fake, v=fake, bt=fake, mb=4, cl=fake, mcl=64,
+             B=2, nb=8, bs=16, hq=16, hkv=2, d=128, scale=0.088, ks=0.01, vs=0.02, splits=0,
+             ws=NULL, wsb=0, dt=1, err=NULL, stream=NULL)
+    a.update(kw)
+    return lib.pkv_append_decode_attention_fp8(
+        a["out"], a["q"], a["kn"], a["vn"], a["k"], a["v"], a["bt"], a["mb"], a["cl"], a["mcl"],
+        a["B"], a["nb"], a["bs"], a["hq"], a["hkv"], a["d"], a["scale"], a["ks"], a["vs"],
+        a["splits"], a["ws"], a["wsb"], a["dt"], a["err"], a["stream"])
+
+
+def test_append_decode_fp8_rejects_bad_arguments_without_launching(lib):
+    assert _append_decode_fp8(lib, kn=NULL) == 1          # the new tokens are required
+    assert _append_decode_fp8(lib, vn=NULL) == 1
+    assert _append_decode_fp8(lib, out=NULL) == 1
+    assert _append_decode_fp8(lib, d=64, hq=4) == 2       # an E4M3 stage row holds 128 dims
+    for bad in (0.0, -1.0, float("inf"), float("nan")):
+        assert _append_decode_fp8(lib, ks=bad) == 1       # scales positive and finite
+        assert _append_decode_fp8(lib, vs=bad) == 1
+    assert _append_decode_fp8(lib, dt=3) == 1             # fp16 or bf16 activations only
+    assert _append_decode_fp8(lib, hq=5) == 1             # heads not a multiple of the KV heads
+    assert _append_decode_fp8(lib, bs=8) == 2             # unsupported page size
+    assert _append_decode_fp8(lib, B=0, kn=NULL, vn=NULL) == 0  # empty batch is a no-op
