@@ -98,9 +98,10 @@ def test_scores_rising_across_stages(rise, group, dtype):
     (base 2) per token.  A consumer warp of the decode kernel takes every fourth
     16-token stage, so its consecutive stages lie 64 tokens apart: 0.117 raises
     the maximum between them by ~7.5, just under the 2^8 the running softmax
-    reference tolerates (kept, exponentials up to ~2^7.5), 0.225 by ~14.4 (the
-    reference moves every time), 0.075 by ~4.8 (it moves every second time); the
-    partitions of each split count start their own.  K is nonzero in dim 0 only
+    reference tolerates (kept for one step with exponentials up to ~2^7.5, then
+    moved), 0.075 by ~4.8 (kept, then moved, with exponentials up to ~2^4.8),
+    0.225 by ~14.4 (moved every time); the partitions of each split count start
+    their own.  K is nonzero in dim 0 only
     and the ramp is centred on the context, so every score is one exact product
     of at most ~80 in magnitude and the comparison measures the softmax, not
     fp32 summation of large logits."""
