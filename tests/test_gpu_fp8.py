@@ -181,3 +181,36 @@ def test_fused_fp8_append_decode_matches_oracle_and_separate_append(key, splits,
         kc, vc = kc.permute(0, 2, 1, 3).contiguous(), vc.permute(0, 2, 1, 3).contiguous()
     assert np.array_equal(kc.cpu().numpy(), kq) and np.array_equal(vc.cpu().numpy(), vq)
     assert_attention_close(out, expect, f"{key} splits={splits} {layout}")
+
+
+def test_fused_fp8_full_size_llama70b_layer_sampled():
+    # The E4M3 step the benchmark times on the Llama-70B layer (one fused launch,
+    # automatic plan): every new token's codes bit for bit, sampled outputs
+    # against the oracle.
+    w = make_workload("c3", device="cuda", with_values=False)
+    s = w.spec
+    kc = make_fp8_codes((w.num_blocks, s.block_size, s.num_kv_heads, s.head_dim), seed=195,
+                        device="cuda")
+    vc = make_fp8_codes(kc.shape, seed=196, device="cuda")
+    g = torch.Generator(device="cuda").manual_seed(197)
+    q, k_new, v_new = (torch.randn(shape, generator=g, device="cuda", dtype=torch.float32)
+                       .to(torch.bfloat16)
+                       for shape in ((s.num_seqs, s.num_q_heads, s.head_dim),
+                                     (s.num_seqs, s.num_kv_heads, s.head_dim),
+                                     (s.num_seqs, s.num_kv_heads, s.head_dim)))
+    k_scale, v_scale = 4.0 / 448, 3.5 / 448
+    kq, vq = kc.cpu().numpy(), vc.cpu().numpy()
+    assert oracle.append_fp8(kq, vq, bits(k_new), bits(v_new), w.slot_mapping.cpu().numpy(),
+                             k_scale, v_scale, "bf16") == 0
+    flag = pkv.new_error_flag("cuda")
+    out = pkv.append_decode_attention_fp8(q, k_new, v_new, kc, vc, w.block_tables,
+                                          w.context_lens, w.max_context_len, k_scale, v_scale,
+                                          err_flag=flag)
+    assert pkv.check_error(flag) == 0
+    assert np.array_equal(kc.cpu().numpy(), kq) and np.array_equal(vc.cpu().numpy(), vq)
+    seqs = np.array([0, 17, 31])
+    expect = oracle.decode_attention_fp8(bits(q)[seqs], kq, vq, w.block_tables.cpu().numpy()[seqs],
+                                         w.context_lens.cpu().numpy()[seqs],
+                                         1.0 / np.sqrt(s.head_dim), k_scale, v_scale, "bf16")
+    assert_attention_close(out[torch.as_tensor(seqs, device="cuda")], expect, "c3 fp8 fused")
+    assert torch.isfinite(out).all()
