@@ -207,6 +207,31 @@ def test_full_size_sampled(name):
     assert float(out.abs().max()) <= float(w.v_cache.abs().max()) * (1 + 2**-7)
 
 
+@pytest.mark.parametrize("name", ["c2", "c3", "c4"])
+def test_full_size_fused_step_sampled(name):
+    """The 16-bit step the benchmark times on the plain-path workloads: one fused
+    append + decode launch with the automatic plan.  Every new token lands in
+    its slot bit for bit; sampled outputs match the oracle."""
+    w = make_workload(name, device="cuda")
+    seqs = np.arange(w.spec.num_seqs)
+    if FULL[name] < w.spec.num_seqs:
+        seqs = np.sort(np.random.default_rng(4321).choice(w.spec.num_seqs, size=FULL[name],
+                                                          replace=False))
+    expect, kc_expect, vc_expect = oracle_after_append(w, seqs)
+    flag = pkv.new_error_flag("cuda")
+    out = pkv.append_decode_attention(w.q, w.k_new, w.v_new, w.k_cache, w.v_cache,
+                                      w.block_tables, w.context_lens, w.max_context_len,
+                                      scale=w.scale, err_flag=flag)
+    assert pkv.check_error(flag) == 0
+    h, d = w.spec.num_kv_heads, w.spec.head_dim
+    slots = w.slot_mapping.cpu().numpy()
+    for cache, host in ((w.k_cache, kc_expect), (w.v_cache, vc_expect)):
+        got = bits(cache.view(-1, h, d)[w.slot_mapping])
+        assert np.array_equal(got, host.reshape(-1, h, d)[slots])
+    assert_attention_close(out[torch.as_tensor(seqs, device="cuda")], expect, f"{name} fused")
+    assert torch.isfinite(out).all()
+
+
 def test_long_context_plan_uses_at_least_four_partitions():
     w = make_workload("c4", with_values=False)
     s = w.spec
