@@ -214,3 +214,31 @@ def test_fused_fp8_full_size_llama70b_layer_sampled():
                                          1.0 / np.sqrt(s.head_dim), k_scale, v_scale, "bf16")
     assert_attention_close(out[torch.as_tensor(seqs, device="cuda")], expect, "c3 fp8 fused")
     assert torch.isfinite(out).all()
+
+
+def test_fused_fp8_append_skips_and_flags_a_bad_last_block():
+    # A sequence whose last block id is out of range: flagged, its new token
+    # not stored, every other sequence's token stored as usual.
+    k_scale, v_scale = 5.0 / 448, 4.5 / 448
+    case = dict(CASES["gqa8_bf16"])
+    name = case.pop("name")
+    w = make_workload(name, device="cuda", **case)
+    kc = torch.from_numpy(oracle.encode_e4m3(w.k_cache.float().cpu().numpy() /
+                                             np.float32(k_scale))).cuda()
+    vc = torch.from_numpy(oracle.encode_e4m3(w.v_cache.float().cpu().numpy() /
+                                             np.float32(v_scale))).cuda()
+    before = kc.clone()
+    bt = w.block_tables.clone()
+    b, bs = 2, w.spec.block_size
+    n = int(w.context_lens[b])
+    bt[b, (n - 1) // bs] = w.num_blocks + 5   # out of range
+    flag = pkv.new_error_flag("cuda")
+    pkv.append_decode_attention_fp8(w.q, w.k_new, w.v_new, kc, vc, bt, w.context_lens,
+                                    w.max_context_len, k_scale, v_scale, scale=w.scale,
+                                    err_flag=flag)
+    assert pkv.check_error(flag) & pkv.EFLAG_BLOCK_ID
+    changed = (kc != before).any(dim=3).any(dim=2)
+    slots = w.slot_mapping.cpu().tolist()
+    expect_changed = {(s // bs, s % bs) for i, s in enumerate(slots) if i != b}
+    got_changed = {tuple(x) for x in torch.nonzero(changed).cpu().tolist()}
+    assert got_changed <= expect_changed
