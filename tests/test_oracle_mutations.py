@@ -6,7 +6,12 @@ max subtraction, a dropped token, a missing normalisation, a wrong fp16
 exponent bias or a wrong bf16 shift — compiled into a temporary directory.
 The same independent references the pin tests use (library conversion, dense
 torch attention, the dominant-key closed form) must reject every mutant, while
-the unmodified source passes them.
+the unmodified source passes them.  The E4M3 functions get their own mutants
+(exponent bias, subnormal scale, ties away from even, saturation losing its
+sign, the append's scales, the attention's scales), rejected by references that
+do not use them: torch's float8_e4m3fn type, tie and saturation codes worked out
+from the format, an independent quantising scatter, and dense torch attention
+over values the torch type dequantises.
 """
 import os
 import subprocess
@@ -18,7 +23,7 @@ import torch
 import oracle
 from oracle import build as oracle_build
 from oracle.reference import load_library
-from workloads import bits, make_workload
+from workloads import bits, make_append_case, make_workload
 
 from test_oracle_pins import SMALL_CASES, _dense_torch, _make
 
@@ -98,3 +103,106 @@ def test_mutant_is_caught(tmp_path, source, name):
     mutated = source.replace(old, new, 1)
     assert mutated != source
     assert _fails_a_pin(_compile(tmp_path, name, mutated)), f"pins miss mutant {name}"
+
+
+# ---------------------------------------------------------------- E4M3 (FP8) functions
+
+E4M3_MUTANTS = {
+    "e4m3_exponent_bias": ("ldexp((double)(8 + frac), expo - 10)",
+                           "ldexp((double)(8 + frac), expo - 11)"),
+    "e4m3_subnormal_scale": ("ldexp((double)frac, -9)", "ldexp((double)frac, -10)"),
+    "e4m3_ties_away_from_even": ("return fmod(f, 2.0) == 0.0 ? f : f + 1.0;", "return f + 1.0;"),
+    "e4m3_saturation_drops_sign": ("if (a >= 448.0) return sign | 0x7E;",
+                                   "if (a >= 448.0) return 0x7E;"),
+    "fp8_append_unscaled": ("k_cache[dst + j] = encode_e4m3(kx / k_scale);",
+                            "k_cache[dst + j] = encode_e4m3(kx);"),
+    "fp8_append_v_with_k_scale": ("v_cache[dst + j] = encode_e4m3(vx / v_scale);",
+                                  "v_cache[dst + j] = encode_e4m3(vx / k_scale);"),
+    "fp8_attention_k_unscaled": ("dot += qd[j] * (decode_e4m3(kt[j]) * k_scale);",
+                                 "dot += qd[j] * decode_e4m3(kt[j]);"),
+    "fp8_attention_v_unscaled": ("o[j] += w * (decode_e4m3(vt[j]) * v_scale);",
+                                 "o[j] += w * decode_e4m3(vt[j]);"),
+}
+
+
+def _lib_e4m3(x: torch.Tensor) -> torch.Tensor:
+    """The library's E4M3 codes of x (round to nearest even; x within +-448)."""
+    return x.clamp(-448, 448).to(torch.float8_e4m3fn).view(torch.uint8)
+
+
+def _fails_an_e4m3_pin(lib) -> bool:
+    """True if the library's E4M3 functions disagree with a reference that does
+    not use them: torch's float8_e4m3fn type, the tie / saturation codes worked
+    out from the format, an independent quantising scatter, and dense torch
+    attention over values the torch type dequantises."""
+    codes = np.arange(256, dtype=np.uint8)
+    ref = torch.from_numpy(codes).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    got = oracle.decode_e4m3(codes, lib=lib)
+    fin = np.isfinite(ref)
+    if not np.array_equal(got[fin], ref[fin]) or not np.isnan(got[~fin]).all():
+        return True
+    g = torch.Generator().manual_seed(6)
+    x = torch.randn(50000, generator=g) * torch.exp2(
+        torch.randint(-12, 9, (50000,), generator=g).float())
+    x = x.clamp(-448, 448)
+    if not np.array_equal(oracle.encode_e4m3(x.numpy(), lib=lib), _lib_e4m3(x).numpy()):
+        return True
+    # ties to the even code, the subnormal tie, saturation with its sign
+    worked = {1.0625: 0x38, 1.1875: 0x3A, 3 * 2.0 ** -10: 0x02, 470.0: 0x7E, -1.0e6: 0xFE}
+    enc = oracle.encode_e4m3(np.array(list(worked), dtype=np.float32), lib=lib)
+    if list(enc) != list(worked.values()):
+        return True
+    # quantising append against an independent scatter
+    c = make_append_case(40, 8, 16, 2, 32, "bf16", seed=11)
+    slots = c["slot_mapping"].numpy()
+    k_scale, v_scale = 0.0123, 0.0311
+    kc = np.full((8, 16, 2, 32), 0x5A, dtype=np.uint8)
+    vc = kc.copy()
+    if oracle.append_fp8(kc, vc, bits(c["k_new"]), bits(c["v_new"]), slots, k_scale, v_scale,
+                         "bf16", lib=lib) != 0:
+        return True
+    ks = torch.full((8 * 16, 2, 32), 0x5A, dtype=torch.uint8)
+    vs = ks.clone()
+    for i, s in enumerate(slots):
+        if s >= 0:
+            ks[s] = _lib_e4m3(c["k_new"][i].float() / torch.tensor(k_scale))
+            vs[s] = _lib_e4m3(c["v_new"][i].float() / torch.tensor(v_scale))
+    if not (np.array_equal(kc.reshape(-1, 2, 32), ks.numpy()) and
+            np.array_equal(vc.reshape(-1, 2, 32), vs.numpy())):
+        return True
+    # attention over an E4M3 cache against dense torch attention
+    w = make_workload("c3", num_seqs=2, num_q_heads=4, num_kv_heads=2, head_dim=32,
+                      lengths=("uniform", 5, 60), max_len_cap=64, seed=19)
+    k_scale, v_scale = 5.0 / 448, 4.0 / 448
+    kq = _lib_e4m3(w.k_cache.float() / k_scale)
+    vq = _lib_e4m3(w.v_cache.float() / v_scale)
+    bt, cl = w.block_tables.numpy(), w.context_lens.numpy()
+    got = oracle.decode_attention_fp8(bits(w.q), kq.numpy(), vq.numpy(), bt, cl, w.scale,
+                                      k_scale, v_scale, w.spec.dtype, lib=lib)
+    kd = kq.view(torch.float8_e4m3fn).to(torch.float64) * k_scale
+    vd = vq.view(torch.float8_e4m3fn).to(torch.float64) * v_scale
+    qd = w.q.to(torch.float64)
+    bs = w.spec.block_size
+    for b in range(2):
+        n = int(cl[b])
+        t = torch.arange(n)
+        blk = torch.from_numpy(bt[b]).long()[t // bs]
+        for h in range(4):
+            k = kd[blk, t % bs, h // 2]
+            v = vd[blk, t % bs, h // 2]
+            ref = torch.softmax(qd[b, h] @ k.T * w.scale, dim=0) @ v
+            if not np.allclose(got[b, h], ref.numpy(), rtol=1e-12, atol=1e-14):
+                return True
+    return False
+
+
+def test_unmodified_source_passes_the_e4m3_pins(tmp_path, source):
+    assert not _fails_an_e4m3_pin(_compile(tmp_path, "original_e4m3", source))
+
+
+@pytest.mark.parametrize("name", sorted(E4M3_MUTANTS))
+def test_e4m3_mutant_is_caught(tmp_path, source, name):
+    old, new = E4M3_MUTANTS[name]
+    assert source.count(old) == 1, f"mutation site for {name} not found once"
+    mutated = source.replace(old, new)
+    assert _fails_an_e4m3_pin(_compile(tmp_path, name, mutated)), f"pins miss mutant {name}"
