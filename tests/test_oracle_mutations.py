@@ -11,7 +11,10 @@ the unmodified source passes them.  The E4M3 functions get their own mutants
 sign, the append's scales, the attention's scales), rejected by references that
 do not use them: torch's float8_e4m3fn type, tie and saturation codes worked out
 from the format, an independent quantising scatter, and dense torch attention
-over values the torch type dequantises.
+over values the torch type dequantises.  The multi-query (causal) function,
+plain Python over the decode oracle, is mutated in copies of its source (a
+limit one short, the causal order reversed, rows paired with the wrong
+sequences' tables) and must fail the causal brute force.
 """
 import os
 import subprocess
@@ -23,7 +26,7 @@ import torch
 import oracle
 from oracle import build as oracle_build
 from oracle.reference import load_library
-from workloads import bits, make_append_case, make_workload
+from workloads import bits, make_append_case, make_queries, make_workload
 
 from test_oracle_pins import SMALL_CASES, _dense_torch, _make
 
@@ -206,3 +209,65 @@ def test_e4m3_mutant_is_caught(tmp_path, source, name):
     assert source.count(old) == 1, f"mutation site for {name} not found once"
     mutated = source.replace(old, new)
     assert _fails_an_e4m3_pin(_compile(tmp_path, name, mutated)), f"pins miss mutant {name}"
+
+
+# ---------------------------------------------------------------- multi-query (causal) attention
+
+MQ_MUTANTS = {
+    "mq_limit_one_short": ("cl[:, None] - q_len + 1 + np.arange(q_len)",
+                           "cl[:, None] - q_len + np.arange(q_len)"),
+    "mq_causal_order_reversed": ("np.arange(q_len)[None, :]", "np.arange(q_len)[::-1][None, :]"),
+    "mq_tables_tiled": ("np.repeat(np.asarray(block_tables), q_len, axis=0)",
+                        "np.tile(np.asarray(block_tables), (q_len, 1))"),
+}
+
+
+def _mq_function(src: str):
+    """The oracle's multi_query_attention compiled from `src`, in its module's namespace."""
+    import oracle.reference as ref
+    ns = dict(ref.__dict__)
+    exec(compile(src, "mutant", "exec"), ns)
+    return ns["multi_query_attention"]
+
+
+def _fails_the_causal_pin(mq) -> bool:
+    """True if `mq` disagrees with the causal brute force of the pin tests on two
+    sequences with their own tables and four query tokens."""
+    from test_oracle_pins import _causal_brute_force
+    w = make_workload("c1")
+    s = w.spec
+    q_len = 4
+    q = make_queries(w, q_len, seed=3)
+    kc, vc = bits(w.k_cache), bits(w.v_cache)
+    bt, cl = w.block_tables.numpy(), w.context_lens.numpy()
+    try:
+        got = mq(bits(q), kc, vc, bt, cl, w.scale, s.dtype)
+    except ValueError:
+        return True
+    qv = oracle.decode_values(bits(q), s.dtype)
+    group = s.num_q_heads // s.num_kv_heads
+    for b in range(s.num_seqs):
+        n = int(cl[b])
+        for h in range(s.num_q_heads):
+            k, v = oracle.gather_kv(kc, vc, bt, n, b, h // group)
+            ref = _causal_brute_force(qv[b, :, h], oracle.decode_values(k, s.dtype),
+                                      oracle.decode_values(v, s.dtype), n, w.scale)
+            if not np.allclose(got[b, :, h], ref, rtol=1e-12, atol=1e-13):
+                return True
+    return False
+
+
+def test_unmodified_multi_query_passes_the_causal_pin():
+    import inspect
+    import oracle.reference as ref
+    assert not _fails_the_causal_pin(_mq_function(inspect.getsource(ref.multi_query_attention)))
+
+
+@pytest.mark.parametrize("name", sorted(MQ_MUTANTS))
+def test_multi_query_mutant_is_caught(name):
+    import inspect
+    import oracle.reference as ref
+    src = inspect.getsource(ref.multi_query_attention)
+    old, new = MQ_MUTANTS[name]
+    assert src.count(old) == 1, f"mutation site for {name} not found once"
+    assert _fails_the_causal_pin(_mq_function(src.replace(old, new))), f"pin misses {name}"
