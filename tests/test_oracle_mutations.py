@@ -14,8 +14,13 @@ from the format, an independent quantising scatter, and dense torch attention
 over values the torch type dequantises.  The multi-query (causal) function,
 plain Python over the decode oracle, is mutated in copies of its source (a
 limit one short, the causal order reversed, rows paired with the wrong
-sequences' tables) and must fail the causal brute force.
+sequences' tables) and must fail the causal brute force.  The pages' combine
+and the log-sum-exp merge (plain Python too) are mutated the same way (the
+segment scales dropped from L*, unweighted partials, empty splits weighted,
+base-2 weights of natural-log lse, no final division) and must fail the
+split / merge pins.
 """
+import math
 import os
 import subprocess
 
@@ -271,3 +276,84 @@ def test_multi_query_mutant_is_caught(name):
     old, new = MQ_MUTANTS[name]
     assert src.count(old) == 1, f"mutation site for {name} not found once"
     assert _fails_the_causal_pin(_mq_function(src.replace(old, new))), f"pin misses {name}"
+
+
+# ---------------------------------------------------------------- combine and log-sum-exp merge
+
+MERGE_MUTANTS = {
+    "combine_drops_segment_scales_in_sum": ("l_star = np.sum(scale_i * l_sum)",
+                                            "l_star = np.sum(l_sum)"),
+    "combine_unweighted_partials": ("(scale_i * (l_sum / l_star))[:, None] * o",
+                                    "(l_sum / l_star)[:, None] * o"),
+    "merge_empty_split_weighted": (
+        "w = np.where(np.isfinite(pl), np.exp(np.where(np.isfinite(pl), pl, 0.0) - safe_star), 0.0)",
+        "w = np.exp(np.where(np.isfinite(pl), pl, 0.0) - safe_star)"),
+    "merge_base_two_weights": ("np.exp(np.where(np.isfinite(pl), pl, 0.0) - safe_star)",
+                               "np.exp2(np.where(np.isfinite(pl), pl, 0.0) - safe_star)"),
+    "merge_unnormalised": ("num / np.where(den > 0, den, 1.0)", "num"),
+}
+
+
+def _merge_source() -> str:
+    import inspect
+    import oracle.reference as ref
+    return "\n\n".join(inspect.getsource(f) for f in (ref.combine_result, ref.merge_lse,
+                                                        ref.decode_attention_pagewise))
+
+
+def _merge_functions(src: str):
+    """combine_result, merge_lse and decode_attention_pagewise compiled from `src`
+    in a copy of their module's namespace (so the pagewise decode calls the
+    combine compiled here)."""
+    import oracle.reference as ref
+    ns = dict(ref.__dict__)
+    exec(compile(src, "mutant", "exec"), ns)
+    return ns["combine_result"], ns["merge_lse"], ns["decode_attention_pagewise"]
+
+
+def _fails_a_merge_pin(combine, merge, pagewise) -> bool:
+    """True if the functions disagree with the pins of the split / merge tests:
+    the pages' per-page decode and random splits equal the single pass, and the
+    merge's worked edge cases."""
+    from test_oracle_pins import SMALL_CASES, _make, _np, _oracle
+    for case in SMALL_CASES:
+        w = _make(case)
+        got = pagewise(_np(w.q), _np(w.k_cache), _np(w.v_cache), w.block_tables.numpy(),
+                       w.context_lens.numpy(), w.scale)
+        if not np.allclose(got, _oracle(w), rtol=0, atol=1e-13):
+            return True
+    w = _make(SMALL_CASES[2])
+    rng = np.random.default_rng(0)
+    kc, vc = _np(w.k_cache), _np(w.v_cache)
+    full = _oracle(w)
+    group = w.spec.num_q_heads // w.spec.num_kv_heads
+    for b in range(w.spec.num_seqs):
+        n = int(w.context_lens[b])
+        for h in range(w.spec.num_q_heads):
+            k, v = oracle.gather_kv(kc, vc, w.block_tables.numpy(), n, b, h // group)
+            cuts = sorted(rng.choice(np.arange(1, n), size=5, replace=False).tolist())
+            bounds = [0] + cuts + [n]
+            bounds.insert(2, bounds[2])  # an empty segment in the middle
+            o, l_sum, m = oracle.segment_partials(_np(w.q)[b, h], k, v, bounds, w.scale)
+            if not np.allclose(combine(o, l_sum, m), full[b, h], rtol=0, atol=1e-13):
+                return True
+            lse = np.where(np.isfinite(m), m + np.log(np.where(l_sum > 0, l_sum, 1.0)), -np.inf)
+            if not np.allclose(merge(o, lse), full[b, h], rtol=0, atol=1e-13):
+                return True
+    o = np.array([[1.0, 2.0], [3.0, 4.0]])
+    edge = [([-np.inf, -np.inf], [0.0, 0.0]), ([-np.inf, 0.3], [3.0, 4.0]),
+            ([0.0, 0.0], [2.0, 3.0]), ([math.log(3.0), 0.0], [1.5, 2.5])]
+    return any(not np.allclose(merge(o, np.array(lse)), out, rtol=1e-15, atol=0)
+               for lse, out in edge)
+
+
+def test_unmodified_merge_functions_pass_the_merge_pins():
+    assert not _fails_a_merge_pin(*_merge_functions(_merge_source()))
+
+
+@pytest.mark.parametrize("name", sorted(MERGE_MUTANTS))
+def test_merge_mutant_is_caught(name):
+    src = _merge_source()
+    old, new = MERGE_MUTANTS[name]
+    assert src.count(old) == 1, f"mutation site for {name} not found once"
+    assert _fails_a_merge_pin(*_merge_functions(src.replace(old, new))), f"pins miss {name}"
