@@ -110,14 +110,14 @@ def kv_cache_bytes(num_layers: int, num_kv_heads: int, head_dim: int, seq_len: i
 # ---------------------------------------------------------------------------
 
 def append(k_cache: np.ndarray, v_cache: np.ndarray, k_new: np.ndarray, v_new: np.ndarray,
-           slot_mapping: np.ndarray) -> int:
+           slot_mapping: np.ndarray, lib: ctypes.CDLL = None) -> int:
     """Host scatter, in place: token i goes to block slot//bs, offset slot%bs; slot < 0 skips.
 
     Caches are uint16 [num_blocks, block_size, num_kv_heads, head_dim]; k_new and
     v_new are uint16 [num_tokens, num_kv_heads, head_dim]; slot_mapping is int64.
     Returns 0, or -2 if some slot lies beyond the pool (that token is skipped).
     (inference.html, KVCachePool.write_tokens; tutorial chapter 12,
-    PagedKVCache.update.)
+    PagedKVCache.update.)  ``lib`` selects another build of the C oracle.
     """
     for a in (k_cache, v_cache):
         if a.dtype != np.uint16 or not a.flags.c_contiguous:
@@ -126,7 +126,7 @@ def append(k_cache: np.ndarray, v_cache: np.ndarray, k_new: np.ndarray, v_new: n
     k_new = _bits(k_new)
     v_new = _bits(v_new)
     slots = np.ascontiguousarray(slot_mapping, dtype=np.int64)
-    return int(_lib().oracle_append(_ptr(k_cache), _ptr(v_cache), _ptr(k_new), _ptr(v_new),
+    return int((lib or _lib()).oracle_append(_ptr(k_cache), _ptr(v_cache), _ptr(k_new), _ptr(v_new),
                                     _ptr(slots), int(slots.size), num_blocks, block_size,
                                     h_kv, d))
 

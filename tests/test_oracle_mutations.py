@@ -18,7 +18,11 @@ sequences' tables) and must fail the causal brute force.  The pages' combine
 and the log-sum-exp merge (plain Python too) are mutated the same way (the
 segment scales dropped from L*, unweighted partials, empty splits weighted,
 base-2 weights of natural-log lse, no final division) and must fail the
-split / merge pins.
+split / merge pins.  The append scatter (C) and the block-table gather (Python)
+get mutants too (V rows from the new K rows, the in-block offset dropped, block
+and offset exchanged; the page index shifted by a token, V read from the K
+cache, always the first KV head), rejected by the independent scatter and by
+the pages' block-table example plus dense attention over gathered rows.
 """
 import math
 import os
@@ -357,3 +361,123 @@ def test_merge_mutant_is_caught(name):
     old, new = MERGE_MUTANTS[name]
     assert src.count(old) == 1, f"mutation site for {name} not found once"
     assert _fails_a_merge_pin(*_merge_functions(src.replace(old, new))), f"pins miss {name}"
+
+
+# ---------------------------------------------------------------- append scatter and gather
+
+APPEND_MUTANTS = {
+    "append_v_from_k_new": ("memcpy(v_cache + dst, v_new + (int64_t)i * row",
+                            "memcpy(v_cache + dst, k_new + (int64_t)i * row"),
+    "append_offset_dropped": ("int64_t dst = (blk * block_size + off) * row;",
+                              "int64_t dst = (blk * block_size) * row;"),
+    "append_block_as_offset": ("int64_t dst = (blk * block_size + off) * row;",
+                               "int64_t dst = (off * block_size + blk % block_size) * row;"),
+}
+
+GATHER_MUTANTS = {
+    "gather_page_shifted": ("blk = block_tables[seq, t // bs]",
+                            "blk = block_tables[seq, (t + 1) // bs]"),
+    "gather_v_from_k_cache": ("v_cache[blk, off, kv_head, :]", "k_cache[blk, off, kv_head, :]"),
+    "gather_first_kv_head": ("k_cache[blk, off, kv_head, :]", "k_cache[blk, off, 0, :]"),
+}
+
+
+def _fails_the_append_pin(lib) -> bool:
+    """The append pin: an independent numpy scatter, and untouched slots keep the
+    sentinel (every mutant keeps its writes inside the pool)."""
+    for dtype in ("fp16", "bf16"):
+        c = make_append_case(300, 40, 16, 4, 64, dtype, seed=5)
+        kc, vc = bits(c["k_cache"]).copy(), bits(c["v_cache"]).copy()
+        slots = c["slot_mapping"].numpy()
+        if oracle.append(kc, vc, bits(c["k_new"]), bits(c["v_new"]), slots, lib=lib) != 0:
+            return True
+        ek, ev = bits(c["k_cache"]).copy(), bits(c["v_cache"]).copy()
+        keep = slots >= 0
+        ek.reshape(-1, 4, 64)[slots[keep]] = bits(c["k_new"])[keep]
+        ev.reshape(-1, 4, 64)[slots[keep]] = bits(c["v_new"])[keep]
+        if not (np.array_equal(kc, ek) and np.array_equal(vc, ev)):
+            return True
+    return False
+
+
+def test_unmodified_append_passes_its_pin(tmp_path, source):
+    assert not _fails_the_append_pin(_compile(tmp_path, "original_append", source))
+
+
+@pytest.mark.parametrize("name", sorted(APPEND_MUTANTS))
+def test_append_mutant_is_caught(tmp_path, source, name):
+    old, new = APPEND_MUTANTS[name]
+    assert source.count(old) == 1, f"mutation site for {name} not found once"
+    lib = _compile(tmp_path, name, source.replace(old, new))
+    assert _fails_the_append_pin(lib), f"pin misses mutant {name}"
+
+
+def _gather_function(src: str):
+    import oracle.reference as ref
+    ns = dict(ref.__dict__)
+    exec(compile(src, "mutant", "exec"), ns)
+    return ns["gather_kv"]
+
+
+def _fails_a_gather_pin(gather) -> bool:
+    """The gather pins: the pages' block-table worked example (golden file), and
+    on a two-KV-head workload with its own K and V, the rows the decode
+    definition reads (the oracle's dense attention over gathered rows equals its
+    paged attention)."""
+    from test_oracle_pins import GOLDEN, _make, _np, _oracle
+    table, bs = {}, None
+    with open(os.path.join(GOLDEN, "block_table_example.txt")) as f:
+        for line in f:
+            p = line.split()
+            if not p or p[0].startswith("#"):
+                continue
+            if p[0] == "block_size":
+                bs = int(p[1])
+                continue
+            table.setdefault(int(p[0]), {})[int(p[1])] = int(p[2])
+    cache = np.zeros((8, bs, 1, 2), dtype=np.int32)
+    cache[:, :, 0, 0] = np.arange(8)[:, None]
+    cache[:, :, 0, 1] = np.arange(bs)[None, :]
+    tables = np.full((2, 3), -1, dtype=np.int32)
+    for req, m in table.items():
+        for logical, phys in m.items():
+            tables[req - 1, logical] = phys
+    try:
+        k, _ = gather(cache, cache, tables, 3 * bs, 0, 0)
+    except IndexError:
+        return True
+    if k[:, 0].tolist() != [5] * bs + [7] * bs + [2] * bs or \
+            k[:, 1].tolist() != list(range(bs)) * 3:
+        return True
+    w = _make(dict(name="c3", num_seqs=2, num_q_heads=4, num_kv_heads=2, head_dim=32,
+                   lengths=("uniform", 20, 90), max_len_cap=96, pool="free_list", seed=23))
+    paged = _oracle(w)
+    q, kc, vc = _np(w.q), _np(w.k_cache), _np(w.v_cache)
+    for b in range(2):
+        n = int(w.context_lens[b])
+        for h in range(4):
+            try:
+                k, v = gather(kc, vc, w.block_tables.numpy(), n, b, h // 2)
+            except IndexError:
+                return True
+            s = torch.from_numpy(q[b, h] @ k.T * w.scale)
+            dense = (torch.softmax(s, dim=0) @ torch.from_numpy(v)).numpy()
+            if not np.allclose(dense, paged[b, h], rtol=1e-12, atol=1e-13):
+                return True
+    return False
+
+
+def test_unmodified_gather_passes_its_pins():
+    import inspect
+    import oracle.reference as ref
+    assert not _fails_a_gather_pin(_gather_function(inspect.getsource(ref.gather_kv)))
+
+
+@pytest.mark.parametrize("name", sorted(GATHER_MUTANTS))
+def test_gather_mutant_is_caught(name):
+    import inspect
+    import oracle.reference as ref
+    src = inspect.getsource(ref.gather_kv)
+    old, new = GATHER_MUTANTS[name]
+    assert src.count(old) == 1, f"mutation site for {name} not found once"
+    assert _fails_a_gather_pin(_gather_function(src.replace(old, new))), f"pins miss {name}"
