@@ -290,8 +290,9 @@ def run_reference(args):
     if args.q_len > 0:
         w.q = make_queries(w, args.q_len, seed=w.spec.seed + 101)
     w = w.to("cpu")
-    # about 150 s of oracle work in all, whatever the step count (0.2 to 10 s a step)
-    per_step = max(0.2, min(10.0, 150.0 / max(1, args.steps + args.warmup)))
+    # about --ref-seconds (150 s) of oracle work in all, whatever the step count
+    # (0.2 to 10 s a step)
+    per_step = max(0.2, min(10.0, args.ref_seconds / max(1, args.steps + args.warmup)))
     inputs = oracle_inputs(w)
     seqs = None
     for _ in range(args.warmup):
@@ -800,6 +801,8 @@ def main(argv=None):
                          "(0 = single-token decode)")
     ap.add_argument("--cpu-seconds", type=float, default=8.0,
                     help="oracle time for the headline's cpu_baseline")
+    ap.add_argument("--ref-seconds", type=float, default=150.0,
+                    help="oracle work in all for --impl reference (seconds)")
     ap.add_argument("--cpu-seconds-per-config", type=float, default=3.0,
                     help="oracle time for each per_config cpu_baseline")
     ap.add_argument("--no-cpu-baseline", dest="cpu_baseline", action="store_false")

@@ -106,3 +106,29 @@ def _parse(argv):
     finally:
         bench.run_gpu, bench.run_reference = old_gpu, old_ref
     return captured["args"]
+
+
+def test_reference_arm_prints_the_contract_line():
+    """The oracle arm (`--impl reference`) runs on the host cores and prints one
+    JSON line with the keys the driver reads, on the arm's own metric and unit.
+    It runs in a process of its own: the oracle's OpenMP threads must not live on
+    in this one, whose later tests fork."""
+    import json
+    import os
+    import subprocess
+    import sys
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    r = subprocess.run([sys.executable, os.path.join(root, "bench.py"), "--impl", "reference",
+                        "--config", "c1", "--steps", "3", "--warmup", "3", "--ref-seconds", "2"],
+                       capture_output=True, text=True, timeout=600, cwd=root)
+    assert r.returncode == 0, r.stderr[-2000:]
+    d = json.loads(r.stdout.strip().splitlines()[-1])
+    for key in ("metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step",
+                "higher_is_better", "scaling", "vs_baseline", "dtype", "data", "config",
+                "cpu_baseline", "e2e"):
+        assert key in d, key
+    assert d["impl"] == "reference" and d["steps"] == 3 and d["warmup"] == 3
+    assert d["unit"] == "GB/s" and d["higher_is_better"] is True and d["value"] > 0
+    assert d["config"]["workload"] == "c1"
+    assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["value"] == d["value"]
+    assert d["e2e"]["value"] == d["value"] and d["e2e"]["h2d_bytes_per_step"] == 0
